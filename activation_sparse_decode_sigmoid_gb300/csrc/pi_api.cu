@@ -1,0 +1,628 @@
+// Host side of libpi: contexts, layer loading, launch planning and the C ABI
+// declared in include/pi.h.  All compute happens in the kernels of
+// pi_step_*.cu and pi_load.cu; this file validates arguments, owns device
+// memory and plans the shared-memory layout of each launch.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "pi.h"
+#include "pi_kernels.h"
+
+using pi::LayerDev;
+using pi::StepParams;
+
+namespace {
+
+struct LayerSlot {
+    bool loaded = false;
+    pi_layer_desc desc{};
+    LayerDev dev{};
+    std::vector<void *> bufs;
+};
+
+int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+} // namespace
+
+struct pi_ctx {
+    int device = 0;
+    cudaStream_t stream = nullptr;
+    int max_layers = 0, max_batch = 0;
+    int G = 0;          // SMs = CTAs of the persistent kernels
+    int smem_optin = 0; // dynamic shared memory limit per CTA
+    std::vector<LayerSlot> layers;
+    LayerDev *d_layers = nullptr;
+    // workspace
+    float *h = nullptr;
+    int32_t *loc_list = nullptr;
+    int32_t *loc_cnt = nullptr;
+    float *partial = nullptr;
+    int *ctl = nullptr; // [0..1] grid barrier, [2] status, [3] abort
+    // trace
+    float *tr_x = nullptr;
+    void *tr_xhat = nullptr;
+    int32_t *tr_idx = nullptr;
+    int32_t *tr_cnt = nullptr;
+    unsigned long long wait_ns = 2000000000ull;
+    int bar_extra = 0;
+    std::string err;
+};
+
+namespace {
+
+pi_status fail(pi_ctx *c, pi_status code, const char *fmt, ...)
+{
+    if (c) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        c->err = buf;
+    }
+    return code;
+}
+
+#define CU(call)                                                                                        \
+    do {                                                                                                \
+        cudaError_t e_ = (call);                                                                        \
+        if (e_ != cudaSuccess)                                                                          \
+            return fail(c, e_ == cudaErrorMemoryAllocation ? PI_ERR_OOM : PI_ERR_CUDA, "%s: %s (%s:%d)", \
+                        #call, cudaGetErrorString(e_), __FILE__, __LINE__);                            \
+    } while (0)
+
+void free_layer(LayerSlot &s)
+{
+    for (void *p : s.bufs) cudaFree(p);
+    s.bufs.clear();
+    s.loaded = false;
+    s.dev = LayerDev{};
+}
+
+bool valid_dtype16(int dt) { return dt == PI_F16 || dt == PI_BF16; }
+
+pi_status check_desc(pi_ctx *c, const pi_layer_desc *d)
+{
+    if (!d) return fail(c, PI_ERR_ARG, "desc is NULL");
+    if (d->act != PI_RELU && d->act != PI_REGLU) return fail(c, PI_ERR_ARG, "act %d invalid", d->act);
+    if (!valid_dtype16(d->act_dtype)) return fail(c, PI_ERR_ARG, "act_dtype %d invalid", d->act_dtype);
+    if (d->w_dtype != d->act_dtype && !(d->w_dtype == PI_Q4_0 && d->act_dtype == PI_F16))
+        return fail(c, PI_ERR_ARG, "w_dtype %d with act_dtype %d unsupported", d->w_dtype, d->act_dtype);
+    if (d->d_model < 8 || d->d_model > pi::kMaxD || d->d_model % 8)
+        return fail(c, PI_ERR_SHAPE, "d_model %d outside [8, %d] or not a multiple of 8", d->d_model, pi::kMaxD);
+    if (d->w_dtype == PI_Q4_0 && d->d_model % 32)
+        return fail(c, PI_ERR_SHAPE, "Q4_0 needs d_model %% 32 == 0 (got %d)", d->d_model);
+    if (d->d_ffn < 1 || d->d_ffn > pi::kMaxN) return fail(c, PI_ERR_SHAPE, "d_ffn %d outside [1, %d]", d->d_ffn, pi::kMaxN);
+    if (d->rank < 8 || d->rank > pi::kMaxRank || d->rank % 8)
+        return fail(c, PI_ERR_SHAPE, "rank %d outside [8, %d] or not a multiple of 8", d->rank, pi::kMaxRank);
+    return PI_OK;
+}
+
+pi_status dev_alloc(pi_ctx *c, LayerSlot &s, void **out, size_t bytes)
+{
+    void *p = nullptr;
+    CU(cudaMalloc(&p, bytes < 16 ? 16 : bytes));
+    s.bufs.push_back(p);
+    *out = p;
+    return PI_OK;
+}
+
+// The stack = slots 0..L-1, all loaded, same d_model / act_dtype / weight kind.
+pi_status stack_layers(pi_ctx *c, int *L_out)
+{
+    int L = 0;
+    while (L < c->max_layers && c->layers[L].loaded) ++L;
+    if (L == 0) return fail(c, PI_ERR_NOT_LOADED, "no layer loaded in slot 0");
+    for (int l = L; l < c->max_layers; ++l)
+        if (c->layers[l].loaded) return fail(c, PI_ERR_NOT_LOADED, "slot %d empty but slot %d loaded", L, l);
+    const pi_layer_desc &d0 = c->layers[0].desc;
+    for (int l = 1; l < L; ++l) {
+        const pi_layer_desc &d = c->layers[l].desc;
+        if (d.d_model != d0.d_model || d.act_dtype != d0.act_dtype || (d.w_dtype == PI_Q4_0) != (d0.w_dtype == PI_Q4_0))
+            return fail(c, PI_ERR_UNSUPPORTED, "layer %d differs from layer 0 in d_model, act_dtype or weight kind", l);
+    }
+    *L_out = L;
+    return PI_OK;
+}
+
+// Shared-memory plan of one launch of the step kernel.
+pi_status plan(pi_ctx *c, StepParams &p, int l0, int L, int B, int mode, int *tgf_out)
+{
+    const pi_layer_desc &d0 = c->layers[l0].desc;
+    const int d = d0.d_model, G = c->G;
+    int rmax = 0, nmax = 0, nbmax = 0;
+    for (int l = l0; l < l0 + L; ++l) {
+        const LayerSlot &s = c->layers[l];
+        rmax = std::max(rmax, s.desc.rank);
+        nmax = std::max(nmax, s.desc.d_ffn);
+        nbmax = std::max(nbmax, (s.desc.act == PI_REGLU ? 3 : 2) * s.dev.rowB);
+    }
+    const bool pred = (mode & (pi::M_PREDICT | pi::M_COUNTS)) != 0;
+    const bool ffn = (mode & pi::M_FFN) != 0;
+    const int tgf = B == 1 ? 1 : 4;
+    p.d = d;
+    p.B = B;
+    p.tg = std::min(B, tgf);
+    p.slotB = pred ? 16384 : 0;
+    const int xs = round_up(p.tg * d * 2, 128);
+    p.lcap = (nmax + G - 1) / G + 2;
+    const int words = (nmax + 31) / 32;
+    p.wcap = (words + G - 1) / G + 1;
+    p.rcap = std::max((rmax + G - 1) / G + 1, p.wcap * 32);
+    const int misc_bound = pi::misc_layout(8, 16, p.lcap, G, p.wcap, p.rcap, tgf).total;
+    const int budget = c->smem_optin - misc_bound - xs;
+    int nss = pred ? 6 : 0, nsd = 0, dslot = 0, dyn = 0;
+    if (ffn) {
+        dslot = round_up(std::max(nbmax, 24576), 128);
+        for (;;) {
+            nsd = (budget - nss * p.slotB) / dslot;
+            if (nsd >= 3 || nss <= 2 || !pred) break;
+            --nss;
+        }
+        if (nsd < 2)
+            return fail(c, PI_ERR_UNSUPPORTED, "a neuron (%d bytes) does not fit two pipeline stages", nbmax);
+        nsd = std::min(nsd, 16);
+        dyn = nsd * dslot;
+    }
+    if (pred) {
+        const int hrow = rmax * 4;
+        if (!ffn) {
+            const int fit = std::max(1, (budget - 2 * p.slotB) / hrow);
+            dyn = round_up(std::min(std::min(B, 16), fit) * hrow, 128);
+        }
+        while (nss > 2 && nss * p.slotB + dyn > budget) --nss;
+        if (nss * p.slotB + dyn > budget) return fail(c, PI_ERR_UNSUPPORTED, "predictor does not fit shared memory");
+        p.tgB = std::max(1, std::min(B, dyn / hrow));
+    } else {
+        p.tgB = 1;
+    }
+    p.nss = nss;
+    p.nsd = nsd;
+    p.dslotB = dslot;
+    p.off_dyn = nss * p.slotB;
+    p.off_xs = p.off_dyn + dyn;
+    p.off_misc = p.off_xs + xs;
+    p.smem_bytes = p.off_misc + pi::misc_layout(nss, nsd, p.lcap, G, p.wcap, p.rcap, tgf).total;
+    if (p.smem_bytes > c->smem_optin) return fail(c, PI_ERR_UNSUPPORTED, "plan needs %d bytes of shared memory", p.smem_bytes);
+    *tgf_out = tgf;
+    return PI_OK;
+}
+
+pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
+{
+    int tgf = 1;
+    pi_status st = plan(c, p, l0, L, B, mode, &tgf);
+    if (st) return st;
+    p.layers = c->d_layers + l0;
+    p.L = L;
+    p.mode = mode;
+    p.h = c->h;
+    p.loc_list = c->loc_list;
+    p.loc_cnt = c->loc_cnt;
+    p.partial = c->partial;
+    p.bar = reinterpret_cast<unsigned *>(c->ctl);
+    p.status = c->ctl + 2;
+    p.abort_flag = c->ctl + 3;
+    p.wait_ns = c->wait_ns;
+    p.bar_extra = c->bar_extra;
+    const pi_layer_desc &d0 = c->layers[l0].desc;
+    cudaError_t e;
+    if (d0.w_dtype == PI_Q4_0) e = pi::launch_step_q4(p, tgf, c->G, c->stream);
+    else if (d0.act_dtype == PI_BF16) e = pi::launch_step_bf16(p, tgf, c->G, c->stream);
+    else e = pi::launch_step_f16(p, tgf, c->G, c->stream);
+    if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "step kernel launch: %s", cudaGetErrorString(e));
+    return PI_OK;
+}
+
+pi_status check_layer(pi_ctx *c, int layer)
+{
+    if (layer < 0 || layer >= c->max_layers) return fail(c, PI_ERR_ARG, "layer %d outside [0, %d)", layer, c->max_layers);
+    if (!c->layers[layer].loaded) return fail(c, PI_ERR_NOT_LOADED, "layer %d not loaded", layer);
+    return PI_OK;
+}
+
+pi_status check_batch(pi_ctx *c, int B)
+{
+    if (B < 1 || B > c->max_batch) return fail(c, PI_ERR_ARG, "batch %d outside [1, %d]", B, c->max_batch);
+    return PI_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_layers, int32_t max_batch)
+{
+    if (!out) return PI_ERR_ARG;
+    *out = nullptr;
+    if (max_layers < 1 || max_layers > 4096 || max_batch < 1 || max_batch > pi::kMaxBatch) return PI_ERR_ARG;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return PI_ERR_CUDA;
+    DeviceGuard g(device);
+    pi_ctx *c = new pi_ctx();
+    c->device = device;
+    c->stream = (cudaStream_t)stream;
+    c->max_layers = max_layers;
+    c->max_batch = max_batch;
+    c->layers.resize(max_layers);
+    int coop = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&c->G, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    if (e != cudaSuccess || !coop) {
+        delete c;
+        return PI_ERR_CUDA;
+    }
+    size_t need[] = {sizeof(LayerDev) * (size_t)max_layers,
+                     sizeof(float) * (size_t)max_batch * pi::kMaxRank,
+                     sizeof(int32_t) * (size_t)pi::kMaxN,
+                     sizeof(int32_t) * (size_t)c->G,
+                     sizeof(float) * (size_t)c->G * max_batch * pi::kMaxD,
+                     sizeof(int) * 64};
+    void *ptrs[6] = {};
+    for (int i = 0; i < 6 && e == cudaSuccess; ++i) e = cudaMalloc(&ptrs[i], need[i]);
+    if (e == cudaSuccess) e = cudaMemset(ptrs[0], 0, need[0]);
+    if (e == cudaSuccess) e = cudaMemset(ptrs[5], 0, need[5]);
+    if (e != cudaSuccess) {
+        for (void *p : ptrs) cudaFree(p);
+        delete c;
+        return e == cudaErrorMemoryAllocation ? PI_ERR_OOM : PI_ERR_CUDA;
+    }
+    c->d_layers = (LayerDev *)ptrs[0];
+    c->h = (float *)ptrs[1];
+    c->loc_list = (int32_t *)ptrs[2];
+    c->loc_cnt = (int32_t *)ptrs[3];
+    c->partial = (float *)ptrs[4];
+    c->ctl = (int *)ptrs[5];
+    *out = c;
+    return PI_OK;
+}
+
+pi_status pi_destroy(pi_ctx *c)
+{
+    if (!c) return PI_ERR_ARG;
+    {
+        DeviceGuard g(c->device);
+        cudaStreamSynchronize(c->stream);
+        for (LayerSlot &s : c->layers) free_layer(s);
+        cudaFree(c->d_layers);
+        cudaFree(c->h);
+        cudaFree(c->loc_list);
+        cudaFree(c->loc_cnt);
+        cudaFree(c->partial);
+        cudaFree(c->ctl);
+    }
+    delete c;
+    return PI_OK;
+}
+
+pi_status pi_set_stream(pi_ctx *c, void *stream)
+{
+    if (!c) return PI_ERR_ARG;
+    c->stream = (cudaStream_t)stream;
+    return PI_OK;
+}
+
+pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, const pi_layer_weights *w,
+                        const int32_t *perm)
+{
+    if (!c) return PI_ERR_ARG;
+    if (layer < 0 || layer >= c->max_layers) return fail(c, PI_ERR_ARG, "layer %d outside [0, %d)", layer, c->max_layers);
+    pi_status st = check_desc(c, desc);
+    if (st) return st;
+    if (!w || !w->w_up || !w->w_down || !w->p_w1 || !w->p_w2) return fail(c, PI_ERR_ARG, "missing weight pointer");
+    if (desc->act == PI_REGLU && !w->w_gate) return fail(c, PI_ERR_ARG, "ReGLU needs w_gate");
+    const int d = desc->d_model, n = desc->d_ffn, r = desc->rank;
+    if (perm) {
+        std::vector<char> seen(n, 0);
+        for (int i = 0; i < n; ++i) {
+            if (perm[i] < 0 || perm[i] >= n || seen[perm[i]]) return fail(c, PI_ERR_ARG, "perm is not a permutation of 0..%d", n - 1);
+            seen[perm[i]] = 1;
+        }
+    }
+    DeviceGuard g(c->device);
+    CU(cudaStreamSynchronize(c->stream));
+    LayerSlot &s = c->layers[layer];
+    free_layer(s);
+    const bool q4 = desc->w_dtype == PI_Q4_0;
+    const bool reglu = desc->act == PI_REGLU;
+    const int scB = q4 ? round_up((d / 32) * 2, 16) : 0;
+    const int rowB = q4 ? scB + d / 2 : 2 * d;
+    const size_t srcRow = q4 ? (size_t)(d / 32) * 18 : (size_t)2 * d; // bytes of a source FFN row
+    LayerDev &L = s.dev;
+    L.d = d;
+    L.n = n;
+    L.r = r;
+    L.act = desc->act;
+    L.q4 = q4;
+    L.rowB = rowB;
+    L.scB = scB;
+    void *pw1 = nullptr, *pb1 = nullptr, *pw2 = nullptr, *pb2 = nullptr, *pup = nullptr, *pgate = nullptr,
+         *pdn = nullptr, *pb = nullptr, *pbd = nullptr;
+#define ALLOC(ptr, bytes)                                 \
+    do {                                                  \
+        pi_status s_ = dev_alloc(c, s, &(ptr), (bytes)); \
+        if (s_) {                                         \
+            free_layer(s);                                \
+            return s_;                                    \
+        }                                                 \
+    } while (0)
+    ALLOC(pw1, (size_t)r * d * 2);
+    ALLOC(pb1, (size_t)r * 2);
+    ALLOC(pw2, (size_t)n * r * 2);
+    ALLOC(pb2, (size_t)n * 2);
+    ALLOC(pup, (size_t)n * rowB);
+    if (reglu) ALLOC(pgate, (size_t)n * rowB);
+    ALLOC(pdn, (size_t)n * rowB);
+    ALLOC(pb, (size_t)n * 2);
+    ALLOC(pbd, (size_t)d * 2);
+#undef ALLOC
+    // staging of host sources and of the permutation
+    std::vector<void *> tmp;
+    auto cleanup = [&]() {
+        for (void *p : tmp) cudaFree(p);
+    };
+    auto src = [&](const void *p, size_t bytes, const void **out) -> pi_status {
+        if (!p) {
+            *out = nullptr;
+            return PI_OK;
+        }
+        if (w->on_device) {
+            *out = p;
+            return PI_OK;
+        }
+        void *dptr = nullptr;
+        cudaError_t e = cudaMalloc(&dptr, bytes);
+        if (e != cudaSuccess) return fail(c, PI_ERR_OOM, "staging %zu bytes: %s", bytes, cudaGetErrorString(e));
+        tmp.push_back(dptr);
+        e = cudaMemcpy(dptr, p, bytes, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "staging copy: %s", cudaGetErrorString(e));
+        *out = dptr;
+        return PI_OK;
+    };
+    const void *s_up, *s_gate, *s_b, *s_dn, *s_bd, *s_w1, *s_b1, *s_w2, *s_b2;
+    int32_t *dperm = nullptr;
+    pi_status rc = PI_OK;
+    if (!rc) rc = src(w->w_up, n * srcRow, &s_up);
+    if (!rc) rc = src(w->w_gate, n * srcRow, &s_gate);
+    if (!rc) rc = src(w->b, (size_t)n * 2, &s_b);
+    if (!rc) rc = src(w->w_down, q4 ? n * srcRow : (size_t)d * n * 2, &s_dn);
+    if (!rc) rc = src(w->b_down, (size_t)d * 2, &s_bd);
+    if (!rc) rc = src(w->p_w1, (size_t)r * d * 2, &s_w1);
+    if (!rc) rc = src(w->p_b1, (size_t)r * 2, &s_b1);
+    if (!rc) rc = src(w->p_w2, (size_t)n * r * 2, &s_w2);
+    if (!rc) rc = src(w->p_b2, (size_t)n * 2, &s_b2);
+    if (!rc && perm) {
+        cudaError_t e = cudaMalloc((void **)&dperm, (size_t)n * 4);
+        if (e == cudaSuccess) {
+            tmp.push_back(dperm);
+            e = cudaMemcpy(dperm, perm, (size_t)n * 4, cudaMemcpyHostToDevice);
+        }
+        if (e != cudaSuccess) rc = fail(c, PI_ERR_CUDA, "perm staging: %s", cudaGetErrorString(e));
+    }
+    cudaStream_t st0 = c->stream;
+    cudaError_t e = cudaSuccess;
+    auto chk = [&](cudaError_t x) {
+        if (e == cudaSuccess) e = x;
+    };
+    if (!rc) {
+        if (q4) {
+            chk(pi::launch_q4_split((const uint8_t *)s_up, (uint8_t *)pup, dperm, n, d, scB, st0));
+            if (reglu) chk(pi::launch_q4_split((const uint8_t *)s_gate, (uint8_t *)pgate, dperm, n, d, scB, st0));
+            chk(pi::launch_q4_split((const uint8_t *)s_dn, (uint8_t *)pdn, dperm, n, d, scB, st0));
+        } else {
+            chk(pi::launch_permute_rows(s_up, pup, dperm, n, (size_t)rowB, st0));
+            if (reglu) chk(pi::launch_permute_rows(s_gate, pgate, dperm, n, (size_t)rowB, st0));
+            chk(pi::launch_transpose_permute16((const uint16_t *)s_dn, (uint16_t *)pdn, dperm, d, n, st0));
+        }
+        if (s_b) chk(pi::launch_permute16((const uint16_t *)s_b, (uint16_t *)pb, dperm, n, st0));
+        else chk(cudaMemsetAsync(pb, 0, (size_t)n * 2, st0));
+        chk(cudaMemcpyAsync(pw1, s_w1, (size_t)r * d * 2, cudaMemcpyDeviceToDevice, st0));
+        if (s_b1) chk(cudaMemcpyAsync(pb1, s_b1, (size_t)r * 2, cudaMemcpyDeviceToDevice, st0));
+        else chk(cudaMemsetAsync(pb1, 0, (size_t)r * 2, st0));
+        chk(pi::launch_permute_rows(s_w2, pw2, dperm, n, (size_t)r * 2, st0));
+        if (s_b2) chk(pi::launch_permute16((const uint16_t *)s_b2, (uint16_t *)pb2, dperm, n, st0));
+        else chk(cudaMemsetAsync(pb2, 0, (size_t)n * 2, st0));
+        if (s_bd) chk(cudaMemcpyAsync(pbd, s_bd, (size_t)d * 2, cudaMemcpyDeviceToDevice, st0));
+        else chk(cudaMemsetAsync(pbd, 0, (size_t)d * 2, st0));
+        chk(cudaStreamSynchronize(st0));
+        if (e != cudaSuccess) rc = fail(c, PI_ERR_CUDA, "layer load: %s", cudaGetErrorString(e));
+    }
+    cleanup();
+    if (rc) {
+        free_layer(s);
+        return rc;
+    }
+    L.w1 = (const uint16_t *)pw1;
+    L.b1 = (const uint16_t *)pb1;
+    L.w2 = (const uint16_t *)pw2;
+    L.b2 = (const uint16_t *)pb2;
+    L.up = (const uint8_t *)pup;
+    L.gate = (const uint8_t *)pgate;
+    L.dn = (const uint8_t *)pdn;
+    L.b = (const uint16_t *)pb;
+    L.bdown = (const uint16_t *)pbd;
+    e = cudaMemcpy(c->d_layers + layer, &L, sizeof(LayerDev), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        free_layer(s);
+        return fail(c, PI_ERR_CUDA, "layer table: %s", cudaGetErrorString(e));
+    }
+    s.desc = *desc;
+    s.loaded = true;
+    return PI_OK;
+}
+
+pi_status pi_perm_from_counts(const int32_t *counts, int32_t n, int32_t *perm)
+{
+    if (!counts || !perm || n < 1) return PI_ERR_ARG;
+    for (int i = 0; i < n; ++i) perm[i] = i;
+    std::stable_sort(perm, perm + n, [&](int32_t a, int32_t b) { return counts[a] > counts[b]; });
+    return PI_OK;
+}
+
+pi_status pi_layer_counts(pi_ctx *c, int32_t layer, const void *x_hat, int32_t T, int32_t *counts)
+{
+    if (!c) return PI_ERR_ARG;
+    pi_status st = check_layer(c, layer);
+    if (st) return st;
+    if (!x_hat || !counts || T < 1) return fail(c, PI_ERR_ARG, "x_hat/counts NULL or T < 1");
+    DeviceGuard g(c->device);
+    const pi_layer_desc &d = c->layers[layer].desc;
+    CU(cudaMemsetAsync(counts, 0, (size_t)d.d_ffn * 4, c->stream));
+    for (int t0 = 0; t0 < T; t0 += c->max_batch) {
+        StepParams p{};
+        p.xhat_in = (const uint16_t *)x_hat + (size_t)t0 * d.d_model;
+        p.counts_out = counts;
+        st = launch(c, layer, 1, std::min(c->max_batch, T - t0), pi::M_COUNTS, p);
+        if (st) return st;
+    }
+    return PI_OK;
+}
+
+pi_status pi_predict(pi_ctx *c, int32_t layer, const void *x_hat, int32_t B, int32_t *idx, int32_t *count)
+{
+    if (!c) return PI_ERR_ARG;
+    pi_status st = check_layer(c, layer);
+    if (!st) st = check_batch(c, B);
+    if (st) return st;
+    if (!x_hat || !idx || !count) return fail(c, PI_ERR_ARG, "x_hat/idx/count NULL");
+    DeviceGuard g(c->device);
+    StepParams p{};
+    p.xhat_in = (const uint16_t *)x_hat;
+    p.idx_out = idx;
+    p.count_out = count;
+    return launch(c, layer, 1, B, pi::M_PREDICT | pi::M_COMPACT, p);
+}
+
+pi_status pi_sparse_ffn(pi_ctx *c, int32_t layer, const void *x_hat, int32_t B, const int32_t *idx,
+                        const int32_t *count, void *y)
+{
+    if (!c) return PI_ERR_ARG;
+    pi_status st = check_layer(c, layer);
+    if (!st) st = check_batch(c, B);
+    if (st) return st;
+    if (!x_hat || !idx || !count || !y) return fail(c, PI_ERR_ARG, "x_hat/idx/count/y NULL");
+    DeviceGuard g(c->device);
+    StepParams p{};
+    p.xhat_in = (const uint16_t *)x_hat;
+    p.idx_in = idx;
+    p.count_in = count;
+    p.y_out = (uint16_t *)y;
+    return launch(c, layer, 1, B, pi::M_IDX_IN | pi::M_FFN, p);
+}
+
+pi_status pi_dense_ffn(pi_ctx *c, int32_t layer, const void *x_hat, int32_t B, void *y)
+{
+    if (!c) return PI_ERR_ARG;
+    pi_status st = check_layer(c, layer);
+    if (!st) st = check_batch(c, B);
+    if (st) return st;
+    if (!x_hat || !y) return fail(c, PI_ERR_ARG, "x_hat/y NULL");
+    DeviceGuard g(c->device);
+    StepParams p{};
+    p.xhat_in = (const uint16_t *)x_hat;
+    p.y_out = (uint16_t *)y;
+    return launch(c, layer, 1, B, pi::M_DENSE | pi::M_FFN, p);
+}
+
+static pi_status step_common(pi_ctx *c, float *x, int32_t B, int mode)
+{
+    if (!c) return PI_ERR_ARG;
+    pi_status st = check_batch(c, B);
+    if (st) return st;
+    if (!x) return fail(c, PI_ERR_ARG, "x NULL");
+    int L = 0;
+    st = stack_layers(c, &L);
+    if (st) return st;
+    DeviceGuard g(c->device);
+    StepParams p{};
+    p.x = x;
+    p.tr_x = c->tr_x;
+    p.tr_xhat = (uint16_t *)c->tr_xhat;
+    p.tr_idx = c->tr_idx;
+    p.tr_cnt = c->tr_cnt;
+    int nmax = 0;
+    for (int l = 0; l < L; ++l) nmax = std::max(nmax, c->layers[l].desc.d_ffn);
+    p.tr_n = nmax;
+    return launch(c, 0, L, B, mode, p);
+}
+
+pi_status pi_decode_step(pi_ctx *c, float *x, int32_t B)
+{
+    return step_common(c, x, B, pi::M_RMSNORM | pi::M_PREDICT | pi::M_FFN | pi::M_RESID);
+}
+
+pi_status pi_dense_step(pi_ctx *c, float *x, int32_t B)
+{
+    return step_common(c, x, B, pi::M_RMSNORM | pi::M_DENSE | pi::M_FFN | pi::M_RESID);
+}
+
+pi_status pi_set_trace(pi_ctx *c, float *x_trace, void *xhat_trace, int32_t *idx_trace, int32_t *count_trace)
+{
+    if (!c) return PI_ERR_ARG;
+    c->tr_x = x_trace;
+    c->tr_xhat = xhat_trace;
+    c->tr_idx = idx_trace;
+    c->tr_cnt = count_trace;
+    return PI_OK;
+}
+
+pi_status pi_sync_status(pi_ctx *c)
+{
+    if (!c) return PI_ERR_ARG;
+    DeviceGuard g(c->device);
+    cudaError_t e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+    int ctl[4];
+    CU(cudaMemcpy(ctl, c->ctl, sizeof ctl, cudaMemcpyDeviceToHost));
+    if (ctl[2] != 0 || ctl[3] != 0) {
+        CU(cudaMemset(c->ctl, 0, sizeof(int) * 4));
+        const int code = ctl[2] ? ctl[2] : PI_ERR_TIMEOUT;
+        return fail(c, code, code == PI_ERR_TIMEOUT ? "a device-side wait timed out" : "a kernel flagged invalid device data");
+    }
+    return PI_OK;
+}
+
+const char *pi_last_error(pi_ctx *c)
+{
+    if (!c) return "null context";
+    return c->err.c_str();
+}
+
+int32_t pi_grid_size(pi_ctx *c) { return c ? c->G : 0; }
+
+pi_status pi_debug_set_wait_limit(pi_ctx *c, uint64_t ns)
+{
+    if (!c || ns == 0) return PI_ERR_ARG;
+    c->wait_ns = ns;
+    return PI_OK;
+}
+
+pi_status pi_debug_barrier_extra(pi_ctx *c, int32_t extra)
+{
+    if (!c || extra < 0) return PI_ERR_ARG;
+    c->bar_extra = extra;
+    return PI_OK;
+}
+
+} // extern "C"

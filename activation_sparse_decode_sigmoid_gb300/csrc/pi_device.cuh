@@ -1,0 +1,240 @@
+// Device-side building blocks for the sm_103a kernels of libpi: shared-memory
+// mbarriers, bulk (TMA) global->shared copies, bounded waits, the grid
+// barrier of the persistent step kernel, and 16-bit float helpers.
+//
+// Every wait here is bounded by a globaltimer deadline.  A wait that runs out
+// records PI_ERR_TIMEOUT in the device status word, raises the abort flag
+// that every other wait also polls, and returns false; callers then unwind
+// and the kernel exits.  Nothing traps.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pi_kernels.h"
+
+namespace pi {
+
+// ------------------------------------------------------------------ status
+static __device__ __forceinline__ void raise_error(const StepParams &p, int code)
+{
+    atomicCAS(p.status, 0, code);
+    atomicExch(p.abort_flag, 1);
+}
+
+static __device__ __forceinline__ bool aborted(const StepParams &p)
+{
+    return *(volatile int *)p.abort_flag != 0;
+}
+
+static __device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------------------------ shared memory / mbarrier
+static __device__ __forceinline__ uint32_t smem_u32(const void *ptr)
+{
+    return (uint32_t)__cvta_generic_to_shared(ptr);
+}
+
+static __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// make initialised mbarriers visible to the async (TMA) proxy
+static __device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// order this thread's generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy) writes to the same bytes
+static __device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+static __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+static __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+static __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase with the given parity of `bar` has completed.
+static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const StepParams &p)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (aborted(p)) return false;
+        if (globaltimer() - t0 > p.wait_ns) {
+            raise_error(p, PI_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory; completion is counted on `bar`.
+static __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+static __device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// named barrier over the consumer warps only (the producer warps never join)
+static __device__ __forceinline__ void cons_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+
+// ------------------------------------------------------------------ grid barrier
+static __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *ptr)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+static __device__ __forceinline__ void st_release_gpu(unsigned *ptr, unsigned v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+static __device__ __forceinline__ unsigned atom_add_acqrel_gpu(unsigned *ptr, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
+}
+
+// All CTAs of the (co-resident, cooperative) grid meet here.  Called by every
+// consumer thread; the first consumer thread does the global handshake.
+// bar[0] counts arrivals, bar[1] is the generation.  `fail` is the CTA's
+// shared failure word (see wait_cta): a CTA that already failed does not
+// arrive.  Returns false when the kernel must unwind.
+static __device__ __noinline__ bool grid_sync(const StepParams &p, volatile int *fail, volatile int *flag)
+{
+    cons_sync();
+    if (*fail) return false;
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        __threadfence();
+        const unsigned gen = ld_acquire_gpu(p.bar + 1);
+        const unsigned target = gridDim.x + (unsigned)p.bar_extra;
+        const unsigned arrived = atom_add_acqrel_gpu(p.bar, 1u) + 1u;
+        if (arrived == target) {
+            atomicExch(p.bar, 0u);
+            __threadfence();
+            st_release_gpu(p.bar + 1, gen + 1u);
+        } else {
+            const uint64_t t0 = globaltimer();
+            while (ld_acquire_gpu(p.bar + 1) == gen) {
+                if (aborted(p)) { ok = 0; break; }
+                if (globaltimer() - t0 > p.wait_ns) {
+                    raise_error(p, PI_DEV_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+        *flag = ok;
+        if (!ok) *fail = 1;
+    }
+    cons_sync();
+    return *flag != 0;
+}
+
+// Consumer-side wait on an mbarrier phase.  A failed wait (timeout or abort)
+// sets the CTA's shared failure word; the warp then skips the rest of its
+// work but keeps meeting the consumer barriers, after which every consumer
+// thread sees the word and the CTA unwinds as a whole (a warp that left
+// early would leave the others blocked on a named barrier).
+static __device__ __forceinline__ bool wait_cta(uint64_t *bar, uint32_t parity, const StepParams &p, volatile int *fail,
+                                         bool &ok)
+{
+    if (!ok) return false;
+    if (*fail || !mbar_wait(bar, parity, p)) {
+        *fail = 1;
+        ok = false;
+    }
+    return ok;
+}
+
+static __device__ __forceinline__ bool cons_sync_ok(volatile int *fail)
+{
+    cons_sync();
+    return *fail == 0;
+}
+
+// ------------------------------------------------------------------ 16-bit floats
+template <typename T> struct F16T;
+
+template <> struct F16T<__half> {
+    static __device__ __forceinline__ float2 pair(uint32_t u)
+    {
+        __half2 h;
+        memcpy(&h, &u, 4);
+        return __half22float2(h);
+    }
+    static __device__ __forceinline__ float one(uint16_t u) { return __half2float(__ushort_as_half(u)); }
+    static __device__ __forceinline__ uint16_t round(float f) { return __half_as_ushort(__float2half_rn(f)); }
+};
+
+template <> struct F16T<__nv_bfloat16> {
+    static __device__ __forceinline__ float2 pair(uint32_t u)
+    {
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+    }
+    static __device__ __forceinline__ float one(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
+    static __device__ __forceinline__ uint16_t round(float f)
+    {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+    }
+};
+
+// ------------------------------------------------------------------ slices
+static __device__ __forceinline__ int slice_lo(long long total, int c, int G)
+{
+    return (int)((total * (long long)c) / G);
+}
+
+} // namespace pi

@@ -1,0 +1,149 @@
+// Structures shared by the host side of libpi and its kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pi {
+
+// Thread layout of the persistent step kernel: 16 consumer warps, then one
+// producer warp for the static weight stream (predictor W1/W2 slices) and
+// one for the dynamic stream (rows of the predicted neurons).
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 64;
+constexpr int kStaticWarp = kConsumerWarps;
+constexpr int kDynamicWarp = kConsumerWarps + 1;
+
+constexpr int kMaxD = 8192;          // d_model limit (x_hat row fits a 16 KB slot)
+constexpr int kMaxRank = 2048;       // predictor width limit
+constexpr int kMaxN = 65536;         // neurons per layer
+constexpr int kMaxBatch = 64;        // tokens per call
+constexpr int kYSlots = 16;          // output columns a consumer thread owns (d <= 8192)
+constexpr int kMaxNeuronsPerStage = 8;
+constexpr int kPhaseBTokens = 4;     // tokens per inner pass of the W2 dot products
+
+// device status codes (mirror pi.h)
+constexpr int PI_DEV_TIMEOUT = -6;
+constexpr int PI_DEV_FLAG = -7;
+
+// mode bits of one launch of the step kernel
+enum : int {
+    M_RMSNORM = 1,   // x_hat = RMSNorm(x) per layer (else x_hat given)
+    M_PREDICT = 2,   // run the predictor; the FFN list is its union
+    M_IDX_IN = 4,    // FFN list given (idx_in / count_in)
+    M_DENSE = 8,     // FFN list = every neuron
+    M_FFN = 16,      // run the sparse FFN and the merge
+    M_RESID = 32,    // merge into the fp32 residual x (else write y)
+    M_COUNTS = 64,   // predictor: per-neuron selection counts over the tokens
+    M_COMPACT = 128, // predictor: write the ascending idx list + count
+};
+
+struct LayerDev {
+    int d, n, r, act, q4;
+    int rowB;               // bytes of one FFN row (16-bit: 2d; Q4_0: scB + d/2)
+    int scB;                // Q4_0: bytes of the scale part of a row (16-byte padded)
+    int pad;
+    const uint16_t *w1;     // [r][d]
+    const uint16_t *b1;     // [r]
+    const uint16_t *w2;     // [n][r]   rows in physical order
+    const uint16_t *b2;     // [n]
+    const uint8_t *up;      // [n] rows of rowB bytes
+    const uint8_t *gate;    // [n] rows (ReGLU) or null
+    const uint8_t *dn;      // [n] rows of W_down transposed
+    const uint16_t *b;      // [n] up bias (ReLU) / gate bias (ReGLU)
+    const uint16_t *bdown;  // [d]
+};
+
+struct StepParams {
+    const LayerDev *layers; // device array [L]
+    int L, B, mode, d;
+    float *x;               // [B][d] fp32 residual
+    const uint16_t *xhat_in;// [B][d]
+    const int32_t *idx_in;
+    const int32_t *count_in;
+    int32_t *idx_out;
+    int32_t *count_out;
+    uint16_t *y_out;        // [B][d]
+    int32_t *counts_out;    // [n]
+    // workspace
+    float *h;               // [B][r_max]
+    int32_t *loc_list;      // [n_max]
+    int32_t *loc_cnt;       // [G]
+    float *partial;         // [G][B][d]
+    unsigned *bar;          // grid barrier {count, generation}
+    int *status;            // first device error
+    int *abort_flag;
+    // trace
+    float *tr_x;            // [L][B][d]
+    uint16_t *tr_xhat;      // [L][B][d]
+    int32_t *tr_idx;        // [L][tr_n]
+    int32_t *tr_cnt;        // [L]
+    int tr_n;
+    int bar_extra;
+    unsigned long long wait_ns;
+    // shared-memory plan
+    int slotB, nss;         // static ring: bytes per slot, slots
+    int dslotB, nsd;        // dynamic ring: bytes per stage, stages
+    int tg;                 // tokens per x_hat pass (phase A and FFN)
+    int tgB;                // tokens per h pass (phase B)
+    int lcap;               // capacity of the per-CTA neuron list
+    int wcap;               // capacity of the per-CTA mask words
+    int rcap;               // capacity of the per-CTA predictor-bias cache
+    int off_dyn, off_xs, off_misc;
+    int smem_bytes;
+};
+
+// Byte offsets of the small shared-memory objects of the step kernel (the
+// "misc" region).  Computed identically by the host planner and the kernel.
+struct MiscLayout {
+    int bars, info, tmp, slist, sbias, spref, swords, srb, red, total;
+};
+
+__host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, int G, int wcap, int rcap, int tgf)
+{
+    MiscLayout m;
+    int o = 0;
+    m.bars = o;
+    o += (2 * nss + 2 * nsd + 1) * 8;
+    o = (o + 15) & ~15;
+    m.info = o;
+    o += 16 * 4;
+    m.tmp = o;
+    o += 256 * 4;
+    m.slist = o;
+    o += lcap * 4;
+    m.sbias = o;
+    o += lcap * 4;
+    m.spref = o;
+    o += (G + 1) * 4;
+    o = (o + 15) & ~15;
+    m.swords = o;
+    o += wcap * 4;
+    m.srb = o;
+    o += rcap * 4;
+    o = (o + 15) & ~15;
+    m.red = o;
+    o += 2 * kConsumerWarps * kMaxNeuronsPerStage * tgf * 2 * 4;
+    m.total = (o + 127) & ~127;
+    return m;
+}
+
+// Launchers (host side of the kernels), in the step/load translation units.
+// tgf: 1 (single-token kernel) or 4 (up to four tokens per FFN pass)
+cudaError_t launch_step_f16(const StepParams &p, int tgf, int grid, cudaStream_t s);
+cudaError_t launch_step_bf16(const StepParams &p, int tgf, int grid, cudaStream_t s);
+cudaError_t launch_step_q4(const StepParams &p, int tgf, int grid, cudaStream_t s);
+cudaError_t occupancy_step_f16(int tgf, int smem_bytes, int *blocks);
+cudaError_t occupancy_step_bf16(int tgf, int smem_bytes, int *blocks);
+cudaError_t occupancy_step_q4(int tgf, int smem_bytes, int *blocks);
+
+cudaError_t launch_permute_rows(const void *src, void *dst, const int32_t *perm, int rows, size_t rowBytes,
+                                cudaStream_t s);
+cudaError_t launch_transpose_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int d, int n,
+                                       cudaStream_t s);
+cudaError_t launch_q4_split(const uint8_t *src, uint8_t *dst, const int32_t *perm, int n, int d, int scB,
+                            cudaStream_t s);
+cudaError_t launch_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int n, cudaStream_t s);
+
+} // namespace pi

@@ -1,0 +1,114 @@
+// Load-time layout kernels of libpi (not on the timed path).
+//
+// The offline hot/cold placement of the PowerInfer pages (blog.csdn.net
+// QbitAI/IPADS article, "CPU/GPU混合推理设计": neurons are profiled offline and
+// placed by how often they fire) becomes, on one device, a permutation of the
+// neurons: physical neuron i is original neuron perm[i], hot neurons first.
+// These kernels apply it while converting to the layouts the step kernel
+// streams: one contiguous row per neuron for W_up / W_gate / W_down^T, and for
+// Q4_0 rows a 16-byte-aligned run of fp16 scales followed by the nibbles.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pi_kernels.h"
+
+namespace pi {
+
+// dst row i = src row perm[i]; rowBytes is a multiple of 16.
+__global__ void permute_rows_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                    const int32_t *__restrict__ perm, int rows, size_t row16)
+{
+    for (int i = blockIdx.x; i < rows; i += gridDim.x) {
+        const int o = perm ? perm[i] : i;
+        const uint4 *s = src + (size_t)o * row16;
+        uint4 *d = dst + (size_t)i * row16;
+        for (size_t k = threadIdx.x; k < row16; k += blockDim.x) d[k] = s[k];
+    }
+}
+
+// dst [n][d] (row i = physical neuron i) from src [d][n] (column o = original
+// neuron o): dst[i][j] = src[j][perm[i]].  32x32 tiles through shared memory.
+__global__ void transpose_permute16_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
+                                           const int32_t *__restrict__ perm, int d, int n)
+{
+    __shared__ uint16_t tile[32][33];
+    const int i0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+    const int tx = threadIdx.x, ty = threadIdx.y; // 32 x 8
+    for (int yy = ty; yy < 32; yy += 8) {
+        const int i = i0 + tx, j = j0 + yy;
+        if (i < n && j < d) {
+            const int o = perm ? perm[i] : i;
+            tile[yy][tx] = src[(size_t)j * n + o];
+        }
+    }
+    __syncthreads();
+    for (int yy = ty; yy < 32; yy += 8) {
+        const int i = i0 + yy, j = j0 + tx;
+        if (i < n && j < d) dst[(size_t)i * d + j] = tile[tx][yy];
+    }
+}
+
+// Q4_0 rows of 18-byte blocks -> [scales (d/32 fp16, padded to scB bytes)]
+// [nibbles (d/32 x 16 bytes)], rows permuted.  One thread per block.
+__global__ void q4_split_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst,
+                                const int32_t *__restrict__ perm, int n, int nb, int scB)
+{
+    const size_t total = (size_t)n * nb;
+    const size_t rowB = (size_t)scB + (size_t)nb * 16;
+    for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < total; k += (size_t)gridDim.x * blockDim.x) {
+        const int i = (int)(k / nb), b = (int)(k % nb);
+        const int o = perm ? perm[i] : i;
+        const uint8_t *s = src + ((size_t)o * nb + b) * 18;
+        uint8_t *row = dst + (size_t)i * rowB;
+        row[2 * b] = s[0];
+        row[2 * b + 1] = s[1];
+        uint8_t *q = row + scB + (size_t)b * 16;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) q[j] = s[2 + j];
+        if (b == nb - 1) // zero the padding after the last scale
+            for (int z = 2 * nb; z < scB; ++z) row[z] = 0;
+    }
+}
+
+__global__ void permute16_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
+                                 const int32_t *__restrict__ perm, int n)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        dst[i] = src[perm ? perm[i] : i];
+}
+
+cudaError_t launch_permute_rows(const void *src, void *dst, const int32_t *perm, int rows, size_t rowBytes,
+                                cudaStream_t s)
+{
+    if (rows <= 0) return cudaSuccess;
+    const int grid = rows < 65535 ? rows : 65535;
+    permute_rows_kernel<<<grid, 256, 0, s>>>((const uint4 *)src, (uint4 *)dst, perm, rows, rowBytes / 16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int d, int n,
+                                       cudaStream_t s)
+{
+    dim3 grid((n + 31) / 32, (d + 31) / 32), block(32, 8);
+    transpose_permute16_kernel<<<grid, block, 0, s>>>(src, dst, perm, d, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q4_split(const uint8_t *src, uint8_t *dst, const int32_t *perm, int n, int d, int scB,
+                            cudaStream_t s)
+{
+    const int nb = d / 32;
+    const size_t total = (size_t)n * nb;
+    const int grid = (int)((total + 255) / 256 < 65535 ? (total + 255) / 256 : 65535);
+    q4_split_kernel<<<grid, 256, 0, s>>>(src, dst, perm, n, nb, scB);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int n, cudaStream_t s)
+{
+    const int grid = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    permute16_kernel<<<grid, 256, 0, s>>>(src, dst, perm, n);
+    return cudaGetLastError();
+}
+
+} // namespace pi

@@ -1,0 +1,906 @@
+// The persistent step kernel of libpi: activation predictor followed by the
+// neuron-aware sparse FFN, for one layer or a whole stack, in one launch.
+//
+// PowerInfer (blog.csdn.net QbitAI/IPADS article, sections
+// "充分利用模型和硬件特点" and "CPU/GPU混合推理设计"): a small per-layer
+// routing predictor selects the neurons an input activates; only those
+// neurons' rows of W_up (W_gate) and columns of W_down are read; the partial
+// results of the executors are merged.  On GB300 every executor is an SM: the
+// predicted list is split evenly over the SMs, each SM accumulates an fp32
+// partial of the layer output, and a fixed-order split-K reduction merges
+// them into the residual stream.
+//
+// One CTA per SM (cooperative launch), 18 warps:
+//   warps 0..15  consumers: dot products, activations, partial sums, merge;
+//   warp 16      static producer: streams this CTA's slice of the predictor
+//                weights W1 / W2 into a ring of shared-memory slots with bulk
+//                copies (cp.async.bulk + mbarrier).  The stream is known in
+//                advance, so it runs ahead across grid barriers and layers;
+//   warp 17      dynamic producer: once the predicted list is known, streams
+//                the rows (W_up, W_gate, W_down^T) of this CTA's share of the
+//                predicted neurons into a second ring.
+// Per layer (consumers):
+//   A  x_hat = RMSNorm(x) (or given); h = max(CDOT(W1, x_hat) + b1, 0)  -> global
+//   -- grid barrier --
+//   B  z = CDOT(W2, h) + b2 for this CTA's rows; z > 0 sets a bit; the CTA's
+//      ascending local list and its count -> global
+//   -- grid barrier --
+//   C  prefix of the local counts gives the ascending global list; this CTA
+//      takes an equal share of it, streams those neurons' rows, computes
+//      a = act(W_up x_hat + b ...) and accumulates a * W_down^T rows -> fp32
+//      partial [B][d] of this CTA -> global
+//   -- grid barrier --
+//   D  every CTA reduces a slice of the columns over all partials in a fixed
+//      order and adds the result (+ b_down) into x (or writes y)
+//   -- grid barrier (before the next layer reads x) --
+#pragma once
+
+#include "pi_device.cuh"
+
+namespace pi {
+
+// ------------------------------------------------------------------ shared layout
+struct Shm {
+    uint8_t *ring_s, *ring_d, *xs;
+    uint64_t *full_s, *empty_s, *full_d, *empty_d, *lst_full;
+    int *info;      // [16] scalars
+    float *tmp;     // [256] scratch (norm sums, inverses)
+    int *slist;     // [lcap] this CTA's neuron ids (phase C)
+    float *sbias;   // [lcap] their biases
+    int *spref;     // [G+1] prefix of the local counts
+    unsigned *swords; // [wcap] predicted-mask words of this CTA's rows
+    float *srb;     // [rcap] predictor-bias cache of this CTA's rows
+    float *red;     // [2][warps][kMaxNeuronsPerStage][TGF][2] cross-warp dot sums
+};
+
+enum { INFO_FLAG = 0, INFO_NCNT = 1, INFO_FAIL = 2 };
+
+static __device__ __forceinline__ volatile int *fail_word(const Shm &S) { return S.info + INFO_FAIL; }
+
+static __device__ __forceinline__ Shm carve(uint8_t *smem, const StepParams &p, int tgf)
+{
+    Shm s;
+    s.ring_s = smem;
+    s.ring_d = smem + p.off_dyn;
+    s.xs = smem + p.off_xs;
+    const MiscLayout m = misc_layout(p.nss, p.nsd, p.lcap, gridDim.x, p.wcap, p.rcap, tgf);
+    uint8_t *base = smem + p.off_misc;
+    s.full_s = (uint64_t *)(base + m.bars);
+    s.empty_s = s.full_s + p.nss;
+    s.full_d = s.empty_s + p.nss;
+    s.empty_d = s.full_d + p.nsd;
+    s.lst_full = s.empty_d + p.nsd;
+    s.info = (int *)(base + m.info);
+    s.tmp = (float *)(base + m.tmp);
+    s.slist = (int *)(base + m.slist);
+    s.sbias = (float *)(base + m.sbias);
+    s.spref = (int *)(base + m.spref);
+    s.swords = (unsigned *)(base + m.swords);
+    s.srb = (float *)(base + m.srb);
+    s.red = (float *)(base + m.red);
+    return s;
+}
+
+// ------------------------------------------------------------------ slices (shared by producers and consumers)
+struct SliceA {
+    int j0, j1, rps, nst; // W1 rows [j0,j1), rows per slot, stages per token group
+};
+struct SliceB {
+    int i0, i1, rps, nst; // W2 rows [i0,i1) (word aligned), rows per slot, stages per token group
+};
+
+static __device__ __forceinline__ SliceA slice_a(const LayerDev &L, const StepParams &p)
+{
+    SliceA a;
+    a.j0 = slice_lo(L.r, blockIdx.x, gridDim.x);
+    a.j1 = slice_lo(L.r, blockIdx.x + 1, gridDim.x);
+    a.rps = max(1, p.slotB / (L.d * 2));
+    a.nst = (a.j1 - a.j0 + a.rps - 1) / a.rps;
+    return a;
+}
+
+static __device__ __forceinline__ int word_row_start(int n, int c, int G)
+{
+    const int nw = (n + 31) >> 5;
+    return min(n, 32 * slice_lo(nw, c, G));
+}
+
+static __device__ __forceinline__ SliceB slice_b(const LayerDev &L, const StepParams &p)
+{
+    SliceB b;
+    b.i0 = word_row_start(L.n, blockIdx.x, gridDim.x);
+    b.i1 = word_row_start(L.n, blockIdx.x + 1, gridDim.x);
+    b.rps = max(1, p.slotB / (L.r * 2));
+    b.nst = (b.i1 - b.i0 + b.rps - 1) / b.rps;
+    return b;
+}
+
+static __device__ __forceinline__ int neuron_bytes(const LayerDev &L)
+{
+    return (L.gate ? 3 : 2) * L.rowB;
+}
+
+static __device__ __forceinline__ int neurons_per_stage(const LayerDev &L, const StepParams &p)
+{
+    return max(1, min(kMaxNeuronsPerStage, p.dslotB / neuron_bytes(L)));
+}
+
+// ------------------------------------------------------------------ producers
+// Wait (bounded, ignoring the abort flag) until the copies of the last issued
+// stages have landed, so that no bulk copy is in flight when the CTA exits.
+static __device__ void drain(uint64_t *full, uint32_t issued, int nslots, const StepParams &p)
+{
+    const uint32_t first = issued > (uint32_t)nslots ? issued - nslots : 0;
+    for (uint32_t k = first; k < issued; ++k) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(full + (k % nslots), (k / nslots) & 1)) {
+            if (globaltimer() - t0 > 100000000ull) break; // 100 ms: copies land in microseconds
+        }
+    }
+}
+
+static __device__ void static_producer(const StepParams &p, const Shm &S)
+{
+    if (!(p.mode & (M_PREDICT | M_COUNTS)) || p.nss == 0) return;
+    const uint64_t pol = policy_evict_first();
+    uint32_t s = 0;
+    bool ok = true;
+    for (int l = 0; l < p.L && ok; ++l) {
+        const LayerDev &L = p.layers[l];
+        const SliceA A = slice_a(L, p);
+        const SliceB Bs = slice_b(L, p);
+        const int nga = (p.B + p.tg - 1) / p.tg;
+        const int ngb = (p.B + p.tgB - 1) / p.tgB;
+        for (int pass = 0; pass < 2 && ok; ++pass) {
+            const int ng = pass == 0 ? nga : ngb;
+            const int lo = pass == 0 ? A.j0 : Bs.i0;
+            const int hi = pass == 0 ? A.j1 : Bs.i1;
+            const int rps = pass == 0 ? A.rps : Bs.rps;
+            const size_t rowB = pass == 0 ? (size_t)L.d * 2 : (size_t)L.r * 2;
+            const uint8_t *src = (const uint8_t *)(pass == 0 ? L.w1 : L.w2);
+            for (int g = 0; g < ng && ok; ++g) {
+                for (int row = lo; row < hi; row += rps, ++s) {
+                    const int slot = s % p.nss;
+                    if (s >= (uint32_t)p.nss && !mbar_wait(S.empty_s + slot, ((s / p.nss) - 1) & 1, p)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bytes = (uint32_t)(min(rps, hi - row) * rowB);
+                    mbar_arrive_expect_tx(S.full_s + slot, bytes);
+                    bulk_g2s(S.ring_s + (size_t)slot * p.slotB, src + (size_t)row * rowB, bytes, S.full_s + slot, pol);
+                }
+            }
+        }
+    }
+    drain(S.full_s, s, p.nss, p);
+}
+
+static __device__ void dynamic_producer(const StepParams &p, const Shm &S)
+{
+    if (!(p.mode & M_FFN)) return;
+    const uint64_t pol = policy_evict_first();
+    uint32_t sd = 0;
+    for (int l = 0; l < p.L; ++l) {
+        if (!mbar_wait(S.lst_full, l & 1, p)) break;
+        const LayerDev &L = p.layers[l];
+        const int ncnt = S.info[INFO_NCNT];
+        const int nb = neuron_bytes(L);
+        const int npd = neurons_per_stage(L, p);
+        const int ngf = (p.B + p.tg - 1) / p.tg;
+        const size_t rowB = (size_t)L.rowB;
+        bool ok = true;
+        for (int g = 0; g < ngf && ok; ++g) {
+            for (int k = 0; k < ncnt; k += npd, ++sd) {
+                const int slot = sd % p.nsd;
+                if (sd >= (uint32_t)p.nsd && !mbar_wait(S.empty_d + slot, ((sd / p.nsd) - 1) & 1, p)) {
+                    ok = false;
+                    break;
+                }
+                const int nn = min(npd, ncnt - k);
+                uint32_t bytes = 0;
+                for (int j = 0; j < nn; ++j)
+                    if (S.slist[k + j] >= 0) bytes += (uint32_t)nb;
+                mbar_arrive_expect_tx(S.full_d + slot, bytes);
+                uint8_t *dst = S.ring_d + (size_t)slot * p.dslotB;
+                for (int j = 0; j < nn; ++j) {
+                    const int id = S.slist[k + j];
+                    if (id < 0) continue;
+                    uint8_t *o = dst + (size_t)j * nb;
+                    bulk_g2s(o, L.up + (size_t)id * rowB, (uint32_t)rowB, S.full_d + slot, pol);
+                    o += rowB;
+                    if (L.gate) {
+                        bulk_g2s(o, L.gate + (size_t)id * rowB, (uint32_t)rowB, S.full_d + slot, pol);
+                        o += rowB;
+                    }
+                    bulk_g2s(o, L.dn + (size_t)id * rowB, (uint32_t)rowB, S.full_d + slot, pol);
+                }
+            }
+        }
+        if (!ok) break;
+    }
+    drain(S.full_d, sd, p.nsd, p);
+}
+
+// ------------------------------------------------------------------ canonical dot products (CDOT)
+static __device__ __forceinline__ float butterfly_sum(float a)
+{
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, m));
+    return a;
+}
+
+// acc[t] = CDOT(w, x_t) for t < nt (<= NT): w is a 16-bit row of K elements
+// in shared memory, x_t a 16-bit row (xs + t*K) in shared memory.
+template <typename T, int NT>
+static __device__ __forceinline__ void cdot_xhat(const uint8_t *w, const uint8_t *xs, int K, int nt, int lane,
+                                          float (&acc)[NT])
+{
+    using F = F16T<T>;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+    const int nch = K >> 3;
+    for (int ch = lane; ch < nch; ch += 32) {
+        const uint4 wv = *reinterpret_cast<const uint4 *>(w + (size_t)ch * 16);
+        const float2 w0 = F::pair(wv.x), w1 = F::pair(wv.y), w2 = F::pair(wv.z), w3 = F::pair(wv.w);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t < nt) {
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xs + (size_t)t * K * 2 + (size_t)ch * 16);
+                const float2 x0 = F::pair(xv.x), x1 = F::pair(xv.y), x2 = F::pair(xv.z), x3 = F::pair(xv.w);
+                float a = acc[t];
+                a = __fmaf_rn(w0.x, x0.x, a);
+                a = __fmaf_rn(w0.y, x0.y, a);
+                a = __fmaf_rn(w1.x, x1.x, a);
+                a = __fmaf_rn(w1.y, x1.y, a);
+                a = __fmaf_rn(w2.x, x2.x, a);
+                a = __fmaf_rn(w2.y, x2.y, a);
+                a = __fmaf_rn(w3.x, x3.x, a);
+                a = __fmaf_rn(w3.y, x3.y, a);
+                acc[t] = a;
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = butterfly_sum(acc[t]);
+}
+
+// acc[t] = CDOT(w, h_t): w a 16-bit row of K elements, h_t fp32 (hs + t*K).
+template <typename T, int NT>
+static __device__ __forceinline__ void cdot_h(const uint8_t *w, const float *hs, int K, int nt, int lane, float (&acc)[NT])
+{
+    using F = F16T<T>;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+    const int nch = K >> 3;
+    for (int ch = lane; ch < nch; ch += 32) {
+        const uint4 wv = *reinterpret_cast<const uint4 *>(w + (size_t)ch * 16);
+        const float2 w0 = F::pair(wv.x), w1 = F::pair(wv.y), w2 = F::pair(wv.z), w3 = F::pair(wv.w);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t < nt) {
+                const float4 h0 = *reinterpret_cast<const float4 *>(hs + (size_t)t * K + (size_t)ch * 8);
+                const float4 h1 = *reinterpret_cast<const float4 *>(hs + (size_t)t * K + (size_t)ch * 8 + 4);
+                float a = acc[t];
+                a = __fmaf_rn(w0.x, h0.x, a);
+                a = __fmaf_rn(w0.y, h0.y, a);
+                a = __fmaf_rn(w1.x, h0.z, a);
+                a = __fmaf_rn(w1.y, h0.w, a);
+                a = __fmaf_rn(w2.x, h1.x, a);
+                a = __fmaf_rn(w2.y, h1.y, a);
+                a = __fmaf_rn(w3.x, h1.z, a);
+                a = __fmaf_rn(w3.y, h1.w, a);
+                acc[t] = a;
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = butterfly_sum(acc[t]);
+}
+
+// ------------------------------------------------------------------ x_hat staging
+// xs[t][:] = x_hat of tokens t0..t0+nt-1, either RMSNorm of the fp32 residual
+// (fixed reduction order: every CTA computes bit-identical values) or a copy
+// of the caller's x_hat.  CTA 0 also writes the trace.
+template <typename T>
+static __device__ void stage_xhat(const StepParams &p, const Shm &S, int l, int t0, int nt)
+{
+    using F = F16T<T>;
+    const int d = p.d, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint16_t *xs = reinterpret_cast<uint16_t *>(S.xs);
+    if (p.mode & M_RMSNORM) {
+        for (int t = 0; t < nt; ++t) {
+            const float4 *xr = reinterpret_cast<const float4 *>(p.x + (size_t)(t0 + t) * d);
+            float ss = 0.f;
+            for (int k = tid; k < d / 4; k += kConsumerThreads) {
+                const float4 v = __ldcg(xr + k);
+                ss = __fmaf_rn(v.x, v.x, ss);
+                ss = __fmaf_rn(v.y, v.y, ss);
+                ss = __fmaf_rn(v.z, v.z, ss);
+                ss = __fmaf_rn(v.w, v.w, ss);
+            }
+            ss = butterfly_sum(ss);
+            if (lane == 0) S.tmp[warp * 4 + (t & 3)] = ss;
+            if ((t & 3) == 3 || t == nt - 1) {
+                cons_sync();
+                if (tid == 0) {
+                    for (int u = t & ~3; u <= t; ++u) {
+                        float tot = 0.f;
+                        for (int w = 0; w < kConsumerWarps; ++w) tot = __fadd_rn(tot, S.tmp[w * 4 + (u & 3)]);
+                        S.tmp[128 + u] = rsqrtf(__fadd_rn(__fdiv_rn(tot, (float)d), 1e-5f));
+                    }
+                }
+                cons_sync();
+            }
+        }
+        for (int t = 0; t < nt; ++t) {
+            const float inv = S.tmp[128 + t];
+            const float4 *xr = reinterpret_cast<const float4 *>(p.x + (size_t)(t0 + t) * d);
+            for (int k = tid; k < d / 4; k += kConsumerThreads) {
+                const float4 v = __ldcg(xr + k);
+                const uint32_t lo = (uint32_t)F::round(__fmul_rn(v.x, inv)) | ((uint32_t)F::round(__fmul_rn(v.y, inv)) << 16);
+                const uint32_t hi = (uint32_t)F::round(__fmul_rn(v.z, inv)) | ((uint32_t)F::round(__fmul_rn(v.w, inv)) << 16);
+                *reinterpret_cast<uint2 *>(xs + (size_t)t * d + 4 * k) = make_uint2(lo, hi);
+            }
+        }
+    } else {
+        for (int t = 0; t < nt; ++t) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.xhat_in + (size_t)(t0 + t) * d);
+            uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)t * d);
+            for (int k = tid; k < d / 8; k += kConsumerThreads) dst[k] = src[k];
+        }
+    }
+    cons_sync();
+    if (blockIdx.x == 0) {
+        if (p.tr_xhat) {
+            for (int t = 0; t < nt; ++t) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(xs + (size_t)t * d);
+                uint4 *dst = reinterpret_cast<uint4 *>(p.tr_xhat + ((size_t)l * p.B + t0 + t) * d);
+                for (int k = tid; k < d / 8; k += kConsumerThreads) dst[k] = src[k];
+            }
+        }
+        if (p.tr_x && (p.mode & M_RMSNORM)) {
+            for (int t = 0; t < nt; ++t) {
+                const float4 *src = reinterpret_cast<const float4 *>(p.x + (size_t)(t0 + t) * d);
+                float4 *dst = reinterpret_cast<float4 *>(p.tr_x + ((size_t)l * p.B + t0 + t) * d);
+                for (int k = tid; k < d / 4; k += kConsumerThreads) dst[k] = __ldcg(src + k);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ phase A: h = relu(W1 x_hat + b1)
+template <typename T>
+static __device__ bool phase_a(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &ss)
+{
+    using F = F16T<T>;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const SliceA A = slice_a(L, p);
+    bool ok = true;
+    for (int k = tid; k < A.j1 - A.j0; k += kConsumerThreads) S.srb[k] = F::one(L.b1[A.j0 + k]);
+    const int nga = (p.B + p.tg - 1) / p.tg;
+    for (int g = 0; g < nga; ++g) {
+        const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
+        stage_xhat<T>(p, S, l, t0, nt); // ends with cons_sync (covers srb too)
+        for (int k = warp; k < A.nst; k += kConsumerWarps) {
+            const uint32_t s = ss + k;
+            const int slot = s % p.nss;
+            if (!wait_cta(S.full_s + slot, (s / p.nss) & 1, p, fail_word(S), ok)) continue;
+            const uint8_t *base = S.ring_s + (size_t)slot * p.slotB;
+            const int jr0 = A.j0 + k * A.rps, jr1 = min(A.j1, jr0 + A.rps);
+            for (int j = jr0; j < jr1; ++j) {
+                const uint8_t *w = base + (size_t)(j - jr0) * L.d * 2;
+                for (int tt = 0; tt < nt; tt += 4) {
+                    float acc[4];
+                    cdot_xhat<T, 4>(w, S.xs + (size_t)tt * L.d * 2, L.d, min(4, nt - tt), lane, acc);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if (tt + u < nt) {
+                                const float s1 = __fadd_rn(acc[u], S.srb[j - A.j0]);
+                                p.h[(size_t)(t0 + tt + u) * L.r + j] = s1 > 0.f ? s1 : 0.f;
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(S.empty_s + slot);
+        }
+        ss += A.nst;
+        if (!cons_sync_ok(fail_word(S))) return false; // xs is rewritten by the next group
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ phase B: z = W2 h + b2 > 0
+template <typename T>
+static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev &L, uint32_t &ss)
+{
+    using F = F16T<T>;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const SliceB Bs = slice_b(L, p);
+    const int nrows = Bs.i1 - Bs.i0;
+    const int nwords = (nrows + 31) >> 5;
+    for (int k = tid; k < nwords; k += kConsumerThreads) S.swords[k] = 0u;
+    for (int k = tid; k < nrows; k += kConsumerThreads) S.srb[k] = F::one(L.b2[Bs.i0 + k]);
+    float *hs = reinterpret_cast<float *>(S.ring_d);
+    const int ngb = (p.B + p.tgB - 1) / p.tgB;
+    bool ok = true;
+    for (int g = 0; g < ngb; ++g) {
+        const int t0 = g * p.tgB, nt = min(p.tgB, p.B - t0);
+        for (int k = tid; k < nt * L.r / 4; k += kConsumerThreads) {
+            const int t = (4 * k) / L.r, j = (4 * k) % L.r;
+            reinterpret_cast<float4 *>(hs)[k] =
+                __ldcg(reinterpret_cast<const float4 *>(p.h + (size_t)(t0 + t) * L.r + j));
+        }
+        cons_sync();
+        for (int k = warp; k < Bs.nst; k += kConsumerWarps) {
+            const uint32_t s = ss + k;
+            const int slot = s % p.nss;
+            if (!wait_cta(S.full_s + slot, (s / p.nss) & 1, p, fail_word(S), ok)) continue;
+            const uint8_t *base = S.ring_s + (size_t)slot * p.slotB;
+            const int ir0 = Bs.i0 + k * Bs.rps, ir1 = min(Bs.i1, ir0 + Bs.rps);
+            for (int i = ir0; i < ir1; ++i) {
+                const uint8_t *w = base + (size_t)(i - ir0) * L.r * 2;
+                const float b2 = S.srb[i - Bs.i0];
+                int cnt = 0;
+                for (int tt = 0; tt < nt; tt += kPhaseBTokens) {
+                    float acc[kPhaseBTokens];
+                    cdot_h<T, kPhaseBTokens>(w, hs + (size_t)tt * L.r, L.r, min(kPhaseBTokens, nt - tt), lane, acc);
+#pragma unroll
+                    for (int u = 0; u < kPhaseBTokens; ++u)
+                        if (tt + u < nt) cnt += __fadd_rn(acc[u], b2) > 0.f ? 1 : 0;
+                }
+                if (lane == 0 && cnt) {
+                    if (p.mode & M_COUNTS) atomicAdd(p.counts_out + i, cnt);
+                    if (p.mode & M_PREDICT) atomicOr(S.swords + ((i - Bs.i0) >> 5), 1u << ((i - Bs.i0) & 31));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(S.empty_s + slot);
+        }
+        ss += Bs.nst;
+        if (!cons_sync_ok(fail_word(S))) return false; // hs is rewritten by the next group
+    }
+    fence_proxy_async_smem(); // hs bytes are overwritten by bulk copies in phase C
+    if (p.mode & M_PREDICT) {
+        if (warp == 0) {
+            int base = 0;
+            for (int w0 = 0; w0 < nwords; w0 += 32) {
+                const int wi = w0 + lane;
+                const unsigned bits = wi < nwords ? S.swords[wi] : 0u;
+                const int c = __popc(bits);
+                int incl = c;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                int pos = base + incl - c;
+                unsigned b = bits;
+                while (b) {
+                    const int bit = __ffs(b) - 1;
+                    b &= b - 1;
+                    p.loc_list[Bs.i0 + pos++] = Bs.i0 + 32 * wi + bit;
+                }
+                base += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) p.loc_cnt[blockIdx.x] = base;
+        }
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ list resolution
+// This CTA's equal share [s0, s1) of the layer's neuron list -> slist/sbias.
+template <typename T>
+static __device__ void resolve_list(const StepParams &p, const Shm &S, const LayerDev &L, int l)
+{
+    using F = F16T<T>;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x, c = blockIdx.x;
+    int m;
+    if (p.mode & M_PREDICT) {
+        for (int k = tid; k < G; k += kConsumerThreads) S.spref[k + 1] = __ldcg(p.loc_cnt + k);
+        cons_sync();
+        if (warp == 0) {
+            int base = 0;
+            for (int k0 = 0; k0 < G; k0 += 32) {
+                const int k = k0 + lane;
+                const int v = k < G ? S.spref[k + 1] : 0;
+                int incl = v;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += u;
+                }
+                if (k < G) S.spref[k + 1] = base + incl;
+                base += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) S.spref[0] = 0;
+        }
+        cons_sync();
+        m = S.spref[G];
+    } else if (p.mode & M_IDX_IN) {
+        m = *(volatile const int32_t *)p.count_in;
+        if (m < 0 || m > L.n) {
+            if (tid == 0) raise_error(p, PI_DEV_FLAG);
+            m = 0;
+        }
+    } else {
+        m = L.n;
+    }
+    const int s0 = slice_lo(m, c, G), s1 = slice_lo(m, c + 1, G);
+    const int ncnt = s1 - s0;
+    for (int k = tid; k < ncnt; k += kConsumerThreads) {
+        const int pos = s0 + k;
+        int id;
+        if (p.mode & M_PREDICT) {
+            int lo = 0, hi = G - 1; // largest c' with spref[c'] <= pos
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (S.spref[mid] <= pos) lo = mid;
+                else hi = mid - 1;
+            }
+            id = __ldcg(p.loc_list + word_row_start(L.n, lo, G) + (pos - S.spref[lo]));
+        } else if (p.mode & M_IDX_IN) {
+            id = p.idx_in[pos];
+            if (id < 0 || id >= L.n) {
+                raise_error(p, PI_DEV_FLAG);
+                id = -1;
+            }
+        } else {
+            id = pos;
+        }
+        S.slist[k] = id;
+        S.sbias[k] = id >= 0 ? F::one(L.b[id]) : 0.f;
+        if (p.idx_out) p.idx_out[pos] = id;
+        if (p.tr_idx) p.tr_idx[(size_t)l * p.tr_n + pos] = id;
+    }
+    if (tid == 0) {
+        S.info[INFO_NCNT] = ncnt;
+        if (c == 0) {
+            if (p.count_out) *p.count_out = m;
+            if (p.tr_cnt) p.tr_cnt[l] = m;
+        }
+    }
+    cons_sync();
+}
+
+// ------------------------------------------------------------------ phase C: gather FFN
+// Thread `tid` owns output columns: 16-bit rows -> chunks of 8 columns
+// ch = tid and tid + 512 (kYSlots = 16 columns); Q4_0 -> half-block hb = tid
+// (16 columns of block hb/2).
+template <typename T, bool Q4, int TGF>
+static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd, int &rbuf)
+{
+    using F = F16T<T>;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int d = L.d;
+    const int ncnt = S.info[INFO_NCNT];
+    const int nb = neuron_bytes(L);
+    const int npd = neurons_per_stage(L, p);
+    const int nst = (ncnt + npd - 1) / npd;
+    const bool reglu = L.gate != nullptr;
+    const int ngf = (p.B + p.tg - 1) / p.tg;
+    const int nch = d >> 3;     // 16-bit: chunks of 8 columns
+    const int nhb = d >> 4;     // Q4_0: half-blocks of 16 columns
+    bool ok = true;
+    for (int g = 0; g < ngf; ++g) {
+        const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
+        stage_xhat<T>(p, S, l, t0, nt);
+        float y[TGF][kYSlots];
+#pragma unroll
+        for (int t = 0; t < TGF; ++t)
+#pragma unroll
+            for (int e = 0; e < kYSlots; ++e) y[t][e] = 0.f;
+
+        for (int k = 0; k < nst; ++k) {
+            const uint32_t s = sd++;
+            const int slot = s % p.nsd;
+            const bool have = wait_cta(S.full_d + slot, (s / p.nsd) & 1, p, fail_word(S), ok);
+            const uint8_t *stage = S.ring_d + (size_t)slot * p.dslotB;
+            const int nn = have ? min(npd, ncnt - k * npd) : 0;
+            float *red = S.red + (size_t)rbuf * kConsumerWarps * kMaxNeuronsPerStage * TGF * 2;
+            // ---- partial dot products of this thread's columns
+            for (int j = 0; j < nn; ++j) {
+                const uint8_t *up = stage + (size_t)j * nb;
+                const uint8_t *gt = up + L.rowB;
+                float au[TGF], ag[TGF];
+#pragma unroll
+                for (int t = 0; t < TGF; ++t) au[t] = ag[t] = 0.f;
+                if (!Q4) {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int ch = tid + q * kConsumerThreads;
+                        if (ch < nch) {
+                            const uint4 wu = *reinterpret_cast<const uint4 *>(up + (size_t)ch * 16);
+                            uint4 wg = make_uint4(0, 0, 0, 0);
+                            if (reglu) wg = *reinterpret_cast<const uint4 *>(gt + (size_t)ch * 16);
+#pragma unroll
+                            for (int t = 0; t < TGF; ++t) {
+                                if (t < nt) {
+                                    const uint4 xv = *reinterpret_cast<const uint4 *>(S.xs + ((size_t)t * d + ch * 8) * 2);
+                                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                                    const uint32_t uw[4] = {wu.x, wu.y, wu.z, wu.w};
+                                    const uint32_t gw[4] = {wg.x, wg.y, wg.z, wg.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float2 xf = F::pair(xw[e]);
+                                        const float2 uf = F::pair(uw[e]);
+                                        au[t] = fmaf(uf.x, xf.x, au[t]);
+                                        au[t] = fmaf(uf.y, xf.y, au[t]);
+                                        if (reglu) {
+                                            const float2 gf = F::pair(gw[e]);
+                                            ag[t] = fmaf(gf.x, xf.x, ag[t]);
+                                            ag[t] = fmaf(gf.y, xf.y, ag[t]);
+                                        }
+                                    }
+                                }
+                            }
+                        }
+                    }
+                } else {
+                    const int hb = tid;
+                    if (hb < nhb) {
+                        const int blk = hb >> 1, half = hb & 1;
+                        const uint4 qv = *reinterpret_cast<const uint4 *>(up + L.scB + (size_t)blk * 16);
+                        const float su = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(up)[blk]));
+                        uint4 qg = make_uint4(0, 0, 0, 0);
+                        float sg = 0.f;
+                        if (reglu) {
+                            qg = *reinterpret_cast<const uint4 *>(gt + L.scB + (size_t)blk * 16);
+                            sg = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(gt)[blk]));
+                        }
+                        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                        const uint32_t gw[4] = {qg.x, qg.y, qg.z, qg.w};
+                        const int sh = half * 4;
+#pragma unroll
+                        for (int t = 0; t < TGF; ++t) {
+                            if (t < nt) {
+                                const uint8_t *xb = S.xs + ((size_t)t * d + blk * 32 + half * 16) * 2;
+                                const uint4 x0 = *reinterpret_cast<const uint4 *>(xb);
+                                const uint4 x1 = *reinterpret_cast<const uint4 *>(xb + 16);
+                                const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                                float su_acc = 0.f, sg_acc = 0.f;
+#pragma unroll
+                                for (int e = 0; e < 16; e += 2) {
+                                    const float2 xf = F::pair(xw[e >> 1]);
+                                    const int q0 = (int)((qw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8;
+                                    const int q1 = (int)((qw[(e + 1) >> 2] >> (8 * ((e + 1) & 3) + sh)) & 15u) - 8;
+                                    su_acc = fmaf((float)q0, xf.x, su_acc);
+                                    su_acc = fmaf((float)q1, xf.y, su_acc);
+                                    if (reglu) {
+                                        const int g0 = (int)((gw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8;
+                                        const int g1 = (int)((gw[(e + 1) >> 2] >> (8 * ((e + 1) & 3) + sh)) & 15u) - 8;
+                                        sg_acc = fmaf((float)g0, xf.x, sg_acc);
+                                        sg_acc = fmaf((float)g1, xf.y, sg_acc);
+                                    }
+                                }
+                                au[t] = su_acc * su;
+                                ag[t] = sg_acc * sg;
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < TGF; ++t) {
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) {
+                        au[t] += __shfl_xor_sync(0xffffffffu, au[t], o);
+                        if (reglu) ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], o);
+                    }
+                }
+                if (lane == 0) {
+#pragma unroll
+                    for (int t = 0; t < TGF; ++t) {
+                        red[((warp * kMaxNeuronsPerStage + j) * TGF + t) * 2 + 0] = au[t];
+                        red[((warp * kMaxNeuronsPerStage + j) * TGF + t) * 2 + 1] = ag[t];
+                    }
+                }
+            }
+            cons_sync();
+            // ---- activations, then the down-projection rows into this thread's columns
+            for (int j = 0; j < nn; ++j) {
+                const int id = S.slist[k * npd + j];
+                if (id < 0) continue;
+                const float bias = S.sbias[k * npd + j];
+                float a[TGF];
+#pragma unroll
+                for (int t = 0; t < TGF; ++t) {
+                    float u = 0.f, gsum = 0.f;
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        u += red[((w * kMaxNeuronsPerStage + j) * TGF + t) * 2 + 0];
+                        gsum += red[((w * kMaxNeuronsPerStage + j) * TGF + t) * 2 + 1];
+                    }
+                    if (reglu) a[t] = fmaxf(gsum + bias, 0.f) * u;
+                    else a[t] = fmaxf(u + bias, 0.f);
+                }
+                const uint8_t *dn = stage + (size_t)j * nb + (size_t)(reglu ? 2 : 1) * L.rowB;
+                if (!Q4) {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int ch = tid + q * kConsumerThreads;
+                        if (ch < nch) {
+                            const uint4 wv = *reinterpret_cast<const uint4 *>(dn + (size_t)ch * 16);
+                            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 wf = F::pair(ww[e]);
+#pragma unroll
+                                for (int t = 0; t < TGF; ++t) {
+                                    y[t][q * 8 + 2 * e] = fmaf(a[t], wf.x, y[t][q * 8 + 2 * e]);
+                                    y[t][q * 8 + 2 * e + 1] = fmaf(a[t], wf.y, y[t][q * 8 + 2 * e + 1]);
+                                }
+                            }
+                        }
+                    }
+                } else {
+                    const int hb = tid;
+                    if (hb < nhb) {
+                        const int blk = hb >> 1, sh = (hb & 1) * 4;
+                        const uint4 qv = *reinterpret_cast<const uint4 *>(dn + L.scB + (size_t)blk * 16);
+                        const float s = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(dn)[blk]));
+                        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                        float as[TGF];
+#pragma unroll
+                        for (int t = 0; t < TGF; ++t) as[t] = a[t] * s;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float q = (float)((int)((qw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8);
+#pragma unroll
+                            for (int t = 0; t < TGF; ++t) y[t][e] = fmaf(as[t], q, y[t][e]);
+                        }
+                    }
+                }
+            }
+            rbuf ^= 1;
+            __syncwarp();
+            if (have && lane == 0) mbar_arrive(S.empty_d + slot);
+        }
+        // ---- this CTA's fp32 partial of the layer output
+        for (int t = 0; t < nt; ++t) {
+            float *dst = p.partial + ((size_t)blockIdx.x * p.B + t0 + t) * d;
+            if (!Q4) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int ch = tid + q * kConsumerThreads;
+                    if (ch < nch) {
+                        float4 *o = reinterpret_cast<float4 *>(dst + ch * 8);
+#pragma unroll
+                        for (int tt = 0; tt < TGF; ++tt) {
+                            if (tt == t) {
+                                o[0] = make_float4(y[tt][q * 8 + 0], y[tt][q * 8 + 1], y[tt][q * 8 + 2], y[tt][q * 8 + 3]);
+                                o[1] = make_float4(y[tt][q * 8 + 4], y[tt][q * 8 + 5], y[tt][q * 8 + 6], y[tt][q * 8 + 7]);
+                            }
+                        }
+                    }
+                }
+            } else {
+                const int hb = tid;
+                if (hb < nhb) {
+                    float4 *o = reinterpret_cast<float4 *>(dst + (hb >> 1) * 32 + (hb & 1) * 16);
+#pragma unroll
+                    for (int tt = 0; tt < TGF; ++tt) {
+                        if (tt == t) {
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                o[v] = make_float4(y[tt][4 * v], y[tt][4 * v + 1], y[tt][4 * v + 2], y[tt][4 * v + 3]);
+                        }
+                    }
+                }
+            }
+        }
+        if (!cons_sync_ok(fail_word(S))) return false; // xs is rewritten by the next group
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ phase D: merge
+template <typename T>
+static __device__ void phase_d(const StepParams &p, const LayerDev &L)
+{
+    using F = F16T<T>;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x, d = L.d;
+    const int U = p.B * d / 4;
+    const int u0 = slice_lo(U, blockIdx.x, G), u1 = slice_lo(U, blockIdx.x + 1, G);
+    const size_t stride4 = (size_t)p.B * d / 4;
+    const float4 *part = reinterpret_cast<const float4 *>(p.partial);
+    (void)tid;
+    for (int u = u0 + warp; u < u1; u += kConsumerWarps) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int cc = lane; cc < G; cc += 32) {
+            const float4 v = __ldcg(part + (size_t)cc * stride4 + u);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+            acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+            acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+        }
+        if (lane == 0) {
+            const int j = (4 * u) % d;
+            acc.x += F::one(L.bdown[j]);
+            acc.y += F::one(L.bdown[j + 1]);
+            acc.z += F::one(L.bdown[j + 2]);
+            acc.w += F::one(L.bdown[j + 3]);
+            if (p.mode & M_RESID) {
+                float4 *xp = reinterpret_cast<float4 *>(p.x) + u;
+                float4 xv = __ldcg(xp);
+                xv.x += acc.x;
+                xv.y += acc.y;
+                xv.z += acc.z;
+                xv.w += acc.w;
+                __stcg(xp, xv);
+            } else {
+                const uint32_t lo = (uint32_t)F::round(acc.x) | ((uint32_t)F::round(acc.y) << 16);
+                const uint32_t hi = (uint32_t)F::round(acc.z) | ((uint32_t)F::round(acc.w) << 16);
+                reinterpret_cast<uint2 *>(p.y_out)[u] = make_uint2(lo, hi);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <typename T, bool Q4, int TGF>
+__global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const Shm S = carve(smem, p, TGF);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (tid == 0) {
+        for (int i = 0; i < p.nss; ++i) {
+            mbar_init(S.full_s + i, 1);
+            mbar_init(S.empty_s + i, 1);
+        }
+        for (int i = 0; i < p.nsd; ++i) {
+            mbar_init(S.full_d + i, 1);
+            mbar_init(S.empty_d + i, kConsumerWarps);
+        }
+        mbar_init(S.lst_full, 1);
+        fence_barrier_init();
+        S.info[INFO_FAIL] = 0;
+    }
+    __syncthreads();
+    if (aborted(p)) return; // an earlier launch failed and nobody has cleared the state yet
+    if (warp == kStaticWarp) {
+        if ((tid & 31) == 0) static_producer(p, S);
+        return;
+    }
+    if (warp == kDynamicWarp) {
+        if ((tid & 31) == 0) dynamic_producer(p, S);
+        return;
+    }
+    // ---- consumers
+    uint32_t ss = 0, sd = 0;
+    int rbuf = 0;
+    const bool pred = (p.mode & (M_PREDICT | M_COUNTS)) != 0;
+    for (int l = 0; l < p.L; ++l) {
+        const LayerDev L = p.layers[l];
+        if (pred) {
+            if (!phase_a<T>(p, S, L, l, ss)) return;
+            if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
+            if (!phase_b<T>(p, S, L, ss)) return;
+            if (!(p.mode & (M_FFN | M_COMPACT))) continue;
+            if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
+        }
+        if (p.mode & (M_FFN | M_COMPACT)) {
+            resolve_list<T>(p, S, L, l);
+            if (p.mode & M_FFN) {
+                if (threadIdx.x == 0) mbar_arrive(S.lst_full);
+                if (!phase_c<T, Q4, TGF>(p, S, L, l, sd, rbuf)) return;
+                if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
+                phase_d<T>(p, L);
+                if (l + 1 < p.L && !grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
+            }
+        }
+    }
+}
+
+} // namespace pi

@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Benchmark of the predictor -> neuron-aware sparse FFN decode step on GB300.
+
+Default workload: the OPT-30B-shaped ReLU FFN stack in fp16 (48 layers,
+d_model 7168, d_ffn 28672, predictor rank 1024), seeded synthetic Zipf-sparse
+weights drawn on the device, neurons permuted by a 256-token calibration
+profile, batch 1.  One step = one decode token through all 48 layers = one
+launch of the persistent step kernel.  Every step streams ~7.5 GB of distinct
+weights, far more than the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-FFN decode tokens/s (1 GB300) and effective HBM GB/s vs 8 TB/s roofline"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="opt30b_relu_f16")
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=0, help="override the stack depth (0 = the config's)")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-extras", action="store_true", help="skip dense, e2e and CPU legs")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(world, v: float, device) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ peaks, clocks, profiles
+def measured_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        try:
+            sm = [float(r[1]) for r in rows]
+            mx = max(float(r[2]) for r in rows)
+        except ValueError:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        loaded = [s for s in sm if s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "activation_sparse_decode_sigmoid_gb300", "csrc", "*")))
+    for p in files:
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the step kernel from a committed ncu summary,
+    if it was taken on the current kernel sources (else None)."""
+    for p in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        kv = {}
+        with open(p) as f:
+            for line in f:
+                if line.startswith("- ") and ":" in line:
+                    k, v = line[2:].split(":", 1)
+                    kv[k.strip()] = v.strip().strip("`")
+        if kv.get("workload") == workload and kv.get("kernel_source_hash") == kernel_source_hash():
+            try:
+                return float(kv["traffic_bytes_per_launch"])
+            except (KeyError, ValueError):
+                pass
+    return None
+
+
+# ------------------------------------------------------------------ workload
+def algorithmic_bytes(cfg, L, B, counts):
+    """Bytes a step must move: predictor weights + biases, the rows of the
+    active neurons (W_up [+ W_gate] + W_down^T + bias), x_hat / x traffic."""
+    from activation_sparse_decode_sigmoid_gb300 import workload as W
+    d, n, r = cfg.d, cfg.n, cfg.r
+    rows = 3 if cfg.act == W.REGLU else 2
+    row = d * 18 / 32 if cfg.w_dtype == W.Q4_0 else d * 2
+    pred = r * d * 2 + n * r * 2 + (r + n) * 2
+    total = 0.0
+    for m in counts:
+        total += pred + m * (rows * row + 2) + B * d * (2 + 4 + 4)
+    return total
+
+
+def build_stack(cfg, L, B, seed, device, keep_host=()):
+    import numpy as np
+    import torch
+    from activation_sparse_decode_sigmoid_gb300 import pi
+    from activation_sparse_decode_sigmoid_gb300 import workload as W
+
+    ctx = pi.Context(device, max_layers=L, max_batch=max(B, 1))
+    host = {}
+    for l in range(L):
+        lw = W.make_layer_device(cfg, l, seed, torch.device("cuda", device))
+        ctx.load_layer(l, lw)
+        cal = torch.from_numpy(W.calibration_inputs(cfg, l, seed).view(np.int16)).cuda(device)
+        counts = ctx.layer_counts(l, cal).cpu().numpy()
+        perm = pi.pi_perm_from_counts(counts)
+        ctx.load_layer(l, lw, perm)
+        if l in keep_host:
+            host[l] = (W.layer_to_host(lw), perm)
+        del lw, cal
+    torch.cuda.synchronize(device)
+    ctx.check()
+    return ctx, host
+
+
+def cpu_oracle_sample(cfg, L, host_layers, seed, budget_s):
+    """Time the oracle (as it stands, all host cores) on layer-token pairs of
+    the workload until the budget is used; returns tokens/s for the stack."""
+    import numpy as np
+    import oracle as O
+    from activation_sparse_decode_sigmoid_gb300 import workload as W
+
+    threads = O.default_threads()
+    xs = W.xhat_inputs(cfg, 8, seed + 7)
+    times, pairs = [], 0
+    t_start = time.perf_counter()
+    for tok in range(8):
+        for l, (lw, _perm) in host_layers.items():
+            x = xs[tok: tok + 1]
+            t0 = time.perf_counter()
+            res = O.layer_predict(lw, x, threads)
+            idx = O.union(res["mask"])
+            O.masked_ffn(lw, x, idx, threads)
+            times.append(time.perf_counter() - t0)
+            pairs += 1
+            if time.perf_counter() - t_start > budget_s:
+                break
+        if time.perf_counter() - t_start > budget_s:
+            break
+    per_layer = sum(times) / len(times)
+    return {"value": 1.0 / (per_layer * L), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{pairs} (layer, token) pairs of the full-size workload (layers {sorted(host_layers)}), "
+                      f"mean {per_layer:.3f} s per layer, scaled to the {L}-layer stack"}
+
+
+def host_layers_numpy(cfg, layers, seed):
+    from activation_sparse_decode_sigmoid_gb300 import workload as W
+    return {l: (W.make_layer(cfg, l, seed), None) for l in layers}
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args, world, rank):
+    """The oracle on the host cores, same config/metric, bounded per step."""
+    import oracle as O
+    from activation_sparse_decode_sigmoid_gb300 import workload as W
+
+    if rank != 0:
+        return
+    O.build()
+    cfg = W.CONFIGS[args.config]
+    L = args.layers or cfg.L
+    hl = host_layers_numpy(cfg, [0, 1], args.seed)
+    threads = O.default_threads()
+    xs = W.xhat_inputs(cfg, args.steps + args.warmup, args.seed + 7)
+    keys = sorted(hl)
+
+    def step(i):
+        lw = hl[keys[i % len(keys)]][0]
+        x = xs[i: i + 1]
+        res = O.layer_predict(lw, x, threads)
+        O.masked_ffn(lw, x, O.union(res["mask"]), threads)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    per_layer = el / args.steps
+    value = args.batch / (per_layer * L)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_layer * L * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block(cfg, L, args.batch),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step = one (layer, token) pair of the full-size stack, "
+                                   f"timed and scaled by {L} layers"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(cfg, L, B):
+    from activation_sparse_decode_sigmoid_gb300 import workload as W
+    return {"workload": f"{cfg.name}: {L} layers, d_model {cfg.d}, d_ffn {cfg.n}, predictor rank {cfg.r}, "
+                        f"{'ReGLU' if cfg.act == W.REGLU else 'ReLU'}, weights {W.DTYPE_NAMES[cfg.w_dtype]}, "
+                        f"Zipf alpha {cfg.alpha}, mean activation {cfg.rho}",
+            "batch": B, "seq_len": 1, "parallelism": "replicas (one independent stack per GPU)",
+            "l2": "no flush: each step streams the whole stack (GBs) through the 129 MB L2",
+            "seed": 0}
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+    from activation_sparse_decode_sigmoid_gb300 import build as libbuild
+    from activation_sparse_decode_sigmoid_gb300 import pi
+    from activation_sparse_decode_sigmoid_gb300 import workload as W
+
+    libbuild.build()
+    device = local
+    torch.cuda.set_device(device)
+    cfg = W.CONFIGS[args.config]
+    L = args.layers or cfg.L
+    B = args.batch
+    K, Wm = args.steps, args.warmup
+    do_extras = not args.no_extras
+    do_cpu = do_extras and rank == 0 and world == 1
+    ctx, host = build_stack(cfg, L, B, args.seed, device, keep_host=(0, L // 2) if do_cpu else ())
+    d = cfg.d
+    xbuf = torch.from_numpy(W.decode_inputs(cfg, (K + Wm) * B, args.seed)).cuda(device).view(K + Wm, B, d)
+    cnt = torch.zeros((K + Wm, L), dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    clocks = ClockSampler(device) if rank == 0 else None
+    for i in range(Wm):
+        ctx.set_trace(None, None, None, cnt[i])
+        ctx.decode_step(xbuf[i])
+    ctx.check()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    torch.cuda.synchronize(device)
+    barrier(world)
+    if clocks:
+        clocks.mark_start()
+    ev[0].record(stream)
+    for k in range(K):
+        ctx.set_trace(None, None, None, cnt[Wm + k])
+        ctx.decode_step(xbuf[Wm + k])
+        ev[k + 1].record(stream)
+    torch.cuda.synchronize(device)
+    if clocks:
+        clocks.mark_end()
+    barrier(world)
+    st = ctx.sync_status()
+    if st:
+        raise RuntimeError(f"device status {st}: {pi.pi_last_error(ctx.handle)}")
+    ms = ev[0].elapsed_time(ev[K])
+    ms = allreduce_max(world, ms, torch.device("cuda", device))
+    per_launch = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
+    counts = cnt[Wm:].cpu().numpy()  # [K][L] active neurons per layer
+    bytes_per_step = [algorithmic_bytes(cfg, L, B, counts[k]) for k in range(K)]
+    mean_launch_s = statistics.mean(per_launch) / 1e3
+    achieved = statistics.mean(bytes_per_step) / mean_launch_s / 1e9
+    peak, peak_kind = measured_hbm()
+    value = world * K * B / (ms / 1e3)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": W.DTYPE_NAMES[cfg.w_dtype], "data": "synthetic", "config": config_block(cfg, L, B),
+        "effective_hbm_gbs": achieved, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+        "mean_active_neurons_per_layer": float(counts.mean()), "mean_active_fraction": float(counts.mean() / cfg.n),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
+                     "traffic": profiled_traffic(cfg.name + f"/L{L}/B{B}"),
+                     "kernel": "step_kernel (one persistent launch per step)"},
+        "gpu_launches": K,
+    }
+
+    if do_extras:
+        # dense baseline: the same stack, every neuron, same kernel family
+        nd = max(2, min(5, K))
+        xd = xbuf[:nd].clone()
+        ctx.set_trace(None, None, None, None)
+        ctx.dense_step(xd[0])
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(1, nd):
+            ctx.dense_step(xd[i])
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        dense_ms = e0.elapsed_time(e1) / (nd - 1)
+        dense_bytes = L * (cfg.r * d * 2 * 0 + cfg.n * ((3 if cfg.act == W.REGLU else 2) *
+                                                         (d * 18 / 32 if cfg.w_dtype == W.Q4_0 else d * 2) + 2))
+        line["dense_baseline"] = {"tokens_per_s": B / (dense_ms / 1e3), "ms_per_step": dense_ms,
+                                  "effective_hbm_gbs": dense_bytes / (dense_ms / 1e3) / 1e9,
+                                  "what": "same persistent kernel over every neuron, no predictor (cuBLAS-free dense GEMV)"}
+        # end to end through the public API: pinned host input, H2D, step, D2H
+        ne = K
+        xh_in = torch.from_numpy(W.decode_inputs(cfg, ne * B, args.seed + 3)).view(ne, B, d).pin_memory()
+        xh_out = torch.empty_like(xh_in).pin_memory()
+        xdev = torch.empty((B, d), dtype=torch.float32, device=device)
+        for i in range(min(2, ne)):
+            xdev.copy_(xh_in[i], non_blocking=True)
+            ctx.decode_step(xdev)
+            xh_out[i].copy_(xdev, non_blocking=True)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for i in range(ne):
+            xdev.copy_(xh_in[i], non_blocking=True)
+            ctx.decode_step(xdev)
+            xh_out[i].copy_(xdev, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_ms = e0.elapsed_time(e1)
+        e2e_ms = allreduce_max(world, e2e_ms, torch.device("cuda", device))
+        line["e2e"] = {"value": world * ne * B / (e2e_ms / 1e3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": B * d * 4, "d2h_bytes_per_step": B * d * 4}
+        ctx.check()
+    if clocks:
+        line["clocks"] = clocks.stop()
+    if do_cpu:
+        line["cpu_baseline"] = cpu_oracle_sample(cfg, L, host, args.seed, args.cpu_seconds)
+    ctx.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

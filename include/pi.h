@@ -1,0 +1,205 @@
+/*
+ * pi.h -- C ABI of libpi, a GB300 (sm_103a) implementation of the PowerInfer
+ * decode hot path: a per-layer activation predictor followed by a
+ * neuron-aware sparse FFN.
+ *
+ * What the calls compute (PowerInfer: Fast LLM Serving with a Consumer-grade
+ * GPU):
+ *   - blog.csdn.net QbitAI/IPADS article, section "充分利用模型和硬件特点":
+ *     before a layer's FFN runs, a small per-layer routing predictor decides
+ *     which neurons the input activates; only those neurons are computed
+ *     (about 10% of an OPT FFN's neurons suffice).
+ *   - chatpaper.ai abstract: adaptive predictors and neuron-aware sparse
+ *     operators; hot neurons (power-law activation) are kept close to compute.
+ *   - same article, section "CPU/GPU混合推理设计": neurons are placed by an
+ *     offline hot/cold profile, executors compute their share of the
+ *     predicted neurons, and the partial results are merged.  On one GB300 the
+ *     whole model is resident in HBM; the hot/cold split becomes an offline
+ *     neuron permutation (hot neurons first) and the merge is a split-K
+ *     reduction in fp32.
+ *   - de.news.hada.io summary: ReLU / ReGLU activations, Q4_0 INT4 weights.
+ * The pages print no formulas; the readings used (z > 0 for "sigmoid > 0.5",
+ * the canonical fp32 predictor order, Q4_0 block layout, weightless RMSNorm
+ * between layers, union of per-token sets for a batch) are documented with
+ * the calls below.
+ *
+ * Conventions for every call
+ *   - Returns PI_OK (0) or a negative pi_status.  Argument and shape errors
+ *     are detected on the host before anything is launched.  Errors raised
+ *     inside a kernel (a bounded wait that ran out) are written to a device
+ *     status word that pi_sync_status() returns; nothing traps or aborts.
+ *   - Compute calls are asynchronous on the context's current stream
+ *     (pi_set_stream); device buffers passed in must stay valid until the
+ *     stream has reached the call.
+ *   - "dev" pointers are CUDA device pointers, "host" pointers are ordinary
+ *     host memory.  16-bit activations are IEEE binary16 (PI_F16) or bfloat16
+ *     (PI_BF16) bit patterns.
+ *   - Neuron indices are physical: after the layer's neuron permutation.
+ *     perm[i] (as passed to pi_load_layer) is the original id of physical
+ *     neuron i.
+ *   - A context is single-threaded: do not call it from two host threads at
+ *     once.
+ */
+#ifndef PI_H
+#define PI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t pi_status;
+#define PI_OK 0
+#define PI_ERR_ARG (-1)          /* null pointer or invalid enum / count */
+#define PI_ERR_SHAPE (-2)        /* dimension outside the supported range */
+#define PI_ERR_CUDA (-3)         /* a CUDA runtime call failed */
+#define PI_ERR_OOM (-4)          /* device allocation failed */
+#define PI_ERR_NOT_LOADED (-5)   /* layer slot empty, or stack not contiguous */
+#define PI_ERR_TIMEOUT (-6)      /* a bounded device-side wait ran out */
+#define PI_ERR_DEVICE_FLAG (-7)  /* a kernel flagged invalid device data */
+#define PI_ERR_UNSUPPORTED (-8)  /* valid request this build does not serve */
+
+typedef enum { PI_RELU = 0, PI_REGLU = 1 } pi_act;
+typedef enum { PI_F16 = 0, PI_BF16 = 1, PI_Q4_0 = 2 } pi_dtype;
+
+/* Shape and types of one FFN layer and its predictor.
+ *   d_model in [8, 8192], multiple of 8 (of 32 for Q4_0 weights)
+ *   d_ffn   in [1, 65536]      (neurons n)
+ *   rank    in [8, 2048], multiple of 8 (predictor hidden width r)
+ *   act_dtype: PI_F16 or PI_BF16 -- x_hat, predictor weights, biases, y
+ *   w_dtype:   act_dtype, or PI_Q4_0 (only with act_dtype PI_F16) for
+ *              W_up / W_gate / W_down. */
+typedef struct {
+    int32_t d_model, d_ffn, rank;
+    int32_t act;       /* pi_act */
+    int32_t w_dtype;   /* pi_dtype */
+    int32_t act_dtype; /* pi_dtype */
+} pi_layer_desc;
+
+/* Weights of one layer in the model's own layout (original neuron order).
+ *   w_up   [n][d]  row i = neuron i (ReLU: u_i = w_up[i].x + b[i])
+ *   w_gate [n][d]  ReGLU only, else NULL (a_i = max(w_gate[i].x + b[i], 0) * (w_up[i].x))
+ *   b      [n]     bias of the up projection (ReLU) or of the gate (ReGLU); NULL = 0
+ *   w_down [d][n]  column i = neuron i's output vector
+ *   b_down [d]     NULL = 0
+ *   p_w1   [r][d], p_b1 [r] (NULL = 0), p_w2 [n][r], p_b2 [n] (NULL = 0)
+ * Q4_0 weights: w_up / w_gate are [n] rows of d/32 Q4_0 blocks, and w_down is
+ * given TRANSPOSED, as [n] rows of d/32 blocks along d.  A Q4_0 block is 18
+ * bytes: little-endian fp16 scale s, then 16 bytes whose low nibble j is
+ * element j and high nibble j is element j+16; weight = (nibble - 8) * s.
+ * on_device = 1: all pointers are device pointers; 0: host pointers. */
+typedef struct {
+    const void *w_up, *w_gate, *b, *w_down, *b_down;
+    const void *p_w1, *p_b1, *p_w2, *p_b2;
+    int32_t on_device;
+} pi_layer_weights;
+
+typedef struct pi_ctx pi_ctx;
+
+/* Create a context on CUDA device `device`.  `stream` is a cudaStream_t (NULL
+ * = the legacy default stream).  max_layers bounds the layer slots of the
+ * stack, max_batch the tokens per call (1..64).  Allocates the workspace;
+ * layers are allocated by pi_load_layer.  *out receives the context. */
+pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_layers, int32_t max_batch);
+
+/* Free every device buffer of the context (synchronises its stream first). */
+pi_status pi_destroy(pi_ctx *ctx);
+
+/* Make `stream` (a cudaStream_t) the stream of subsequent calls. */
+pi_status pi_set_stream(pi_ctx *ctx, void *stream);
+
+/* Load (or replace) layer slot `layer` (0 <= layer < max_layers).  Copies the
+ * weights into buffers the library owns, applying the neuron permutation
+ * `perm` (host [n], perm[i] = original id of physical neuron i; NULL =
+ * identity; must be a permutation of 0..n-1), transposing W_down into rows of
+ * WdT (one contiguous row per neuron) and splitting Q4_0 rows into separate
+ * scale and nibble arrays.  This is the offline placement step of the
+ * "CPU/GPU混合推理设计" section, mapped to one device: hot neurons first.
+ * Synchronous: returns when the copy is done; the caller keeps its buffers. */
+pi_status pi_load_layer(pi_ctx *ctx, int32_t layer, const pi_layer_desc *desc,
+                        const pi_layer_weights *w, const int32_t *perm);
+
+/* Offline activation profile ("稀疏激活带来的推理局部性": count how often
+ * each neuron is activated over general inputs).  For T calibration inputs
+ * x_hat (dev [T][d], act_dtype), counts[i] (dev int32 [n]) is set to the
+ * number of tokens for which the predictor selects physical neuron i. */
+pi_status pi_layer_counts(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t T, int32_t *counts);
+
+/* Host helper: perm (host [n]) = neurons in descending count order, ties to
+ * the lower id -- the permutation that makes hot neurons contiguous. */
+pi_status pi_perm_from_counts(const int32_t *counts, int32_t n, int32_t *perm);
+
+/* Predictor ("充分利用模型和硬件特点": a small per-layer routing module
+ * predicts the neurons each input activates).  For B tokens x_hat (dev
+ * [B][d], act_dtype):
+ *   h_t = max(CDOT(W1, x_t) + b1, 0)   (fp32, r values, not rounded)
+ *   z_t = CDOT(W2, h_t) + b2           (fp32, n values)
+ *   neuron i is selected for token t iff sigmoid(z) > 0.5, i.e. z > 0
+ *   (so +0, -0 and NaN are not selected).
+ * CDOT is a fixed fp32 order: 32 lanes, lane l accumulates fma over the
+ * 8-element chunks l, l+32, ... in order, then a butterfly add over lane
+ * distances 16, 8, 4, 2, 1; it makes the index list a deterministic function
+ * of the input bytes.
+ * Output: idx (dev int32, capacity n) = ascending physical ids of the union
+ * over the B tokens; *count (dev int32) = its length. */
+pi_status pi_predict(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t B, int32_t *idx, int32_t *count);
+
+/* Neuron-aware sparse FFN on the listed neurons only.  x_hat dev [B][d];
+ * idx dev int32 [*count] physical ids (any order, no duplicates, each in
+ * [0, n)); count dev int32.  Every token uses the whole list.
+ *   a_{t,i} = ReLU:  max(W_up[i].x_t + b_i, 0)
+ *             ReGLU: max(W_gate[i].x_t + b_i, 0) * (W_up[i].x_t)
+ *   y_t = sum_i a_{t,i} W_down[:, i] + b_down        (fp32 accumulate)
+ * y: dev [B][d] act_dtype.  An id outside [0, n) or a count outside [0, n]
+ * sets PI_ERR_DEVICE_FLAG (returned by pi_sync_status) and that entry or the
+ * whole call is skipped. */
+pi_status pi_sparse_ffn(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t B, const int32_t *idx,
+                        const int32_t *count, void *y);
+
+/* The same FFN over every neuron (the dense baseline, no predictor). */
+pi_status pi_dense_ffn(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t B, void *y);
+
+/* One decode step over the loaded stack (slots 0..L-1, all with the same
+ * d_model and act_dtype), in place on the fp32 residual stream x (dev
+ * [B][d]):  for each layer l:
+ *   x_hat = act_dtype(x / sqrt(mean(x^2) + 1e-5))   (weightless RMSNorm)
+ *   idx = predicted union over the B tokens (as pi_predict)
+ *   x += sparse FFN of x_hat on idx (as pi_sparse_ffn, kept in fp32)
+ * One persistent kernel runs the whole stack. */
+pi_status pi_decode_step(pi_ctx *ctx, float *x, int32_t B);
+
+/* The same step with every neuron computed (dense baseline). */
+pi_status pi_dense_step(pi_ctx *ctx, float *x, int32_t B);
+
+/* Optional per-layer trace of pi_decode_step / pi_dense_step, for checking a
+ * stack against a reference layer by layer: x_trace dev fp32 [L][B][d] (the
+ * residual entering each layer), xhat_trace dev [L][B][d] act_dtype,
+ * idx_trace dev int32 [L][n_max] (n_max = largest d_ffn of the stack),
+ * count_trace dev int32 [L].  NULL pointers disable that part. */
+pi_status pi_set_trace(pi_ctx *ctx, float *x_trace, void *xhat_trace, int32_t *idx_trace, int32_t *count_trace);
+
+/* Synchronise the context's stream and return the first device-side error
+ * since the previous call (PI_ERR_TIMEOUT, PI_ERR_DEVICE_FLAG), or a CUDA
+ * error, and clear it. */
+pi_status pi_sync_status(pi_ctx *ctx);
+
+/* Text of the last error on this context (never NULL; owned by the context). */
+const char *pi_last_error(pi_ctx *ctx);
+
+/* Number of SMs the persistent kernels use (one CTA per SM). */
+int32_t pi_grid_size(pi_ctx *ctx);
+
+/* Test hooks.  pi_debug_set_wait_limit: nanoseconds a device-side wait may
+ * spin before it gives up with PI_ERR_TIMEOUT (default 2e9).
+ * pi_debug_barrier_extra: add `extra` phantom arrivals to the grid barrier's
+ * target count, so the next step's barrier can never complete and must time
+ * out (0 restores normal operation). */
+pi_status pi_debug_set_wait_limit(pi_ctx *ctx, uint64_t ns);
+pi_status pi_debug_barrier_extra(pi_ctx *ctx, int32_t extra);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PI_H */

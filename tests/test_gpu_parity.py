@@ -1,0 +1,248 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.  Index lists bit-exact; fp16/bf16 outputs within a max
+relative error of 1e-2 and Q4_0 within 2e-2 (max_k |y-ref| / max(|ref|, rms))."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle as O
+from activation_sparse_decode_sigmoid_gb300 import pi
+from activation_sparse_decode_sigmoid_gb300 import workload as W
+from tests import _gpu as G
+from tests._helpers import max_rel_err, worked_example_layer
+
+pytestmark = pytest.mark.gpu
+
+# small layers spanning several tiles with ragged tails (n not a multiple of
+# 32, d not a multiple of 256), every activation / weight kind
+CFGS = {
+    "relu_f16": W.LayerConfig("relu_f16", 256, 1000, 64, 3, W.RELU, W.F16, W.F16, alpha=0.8, cfg_id=201),
+    "reglu_bf16": W.LayerConfig("reglu_bf16", 264, 777, 32, 3, W.REGLU, W.BF16, W.BF16, alpha=0.7, cfg_id=202),
+    "relu_q4": W.LayerConfig("relu_q4", 512, 640, 64, 3, W.RELU, W.Q4_0, W.F16, alpha=0.9, cfg_id=203),
+    "opt_1layer": W.CONFIGS["opt_1layer_relu_f16"],
+}
+
+
+@pytest.fixture(scope="module")
+def c64():
+    c = G.ctx(max_layers=4, max_batch=64)
+    yield c
+    c.close()
+
+
+def _layer(name, random_bias=True):
+    cfg = CFGS[name]
+    return cfg, W.make_layer(cfg, 0, 0, random_b1=random_bias, random_bdown=random_bias)
+
+
+@pytest.mark.parametrize("name", list(CFGS))
+@pytest.mark.parametrize("B", [1, 3, 8])
+def test_predict_and_sparse_ffn(c64, name, B):
+    cfg, layer = _layer(name)
+    perm = np.random.default_rng(1).permutation(cfg.n).astype(np.int32)
+    c64.load_layer(0, layer, perm)
+    x = W.xhat_inputs(cfg, B, 7)
+    idx, cnt, oidx = G.predict_checked(c64, 0, layer, x, perm)
+    assert oidx.size > 0
+    G.ffn_checked(c64, 0, layer, x, idx, cnt, oidx)
+
+
+@pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4"])
+@pytest.mark.parametrize("B", [1, 2, 7, 9, 64])
+def test_batch_sizes(c64, name, B):
+    cfg, layer = _layer(name)
+    c64.load_layer(0, layer)
+    x = W.xhat_inputs(cfg, B, 11)
+    idx, cnt, oidx = G.predict_checked(c64, 0, layer, x)
+    G.ffn_checked(c64, 0, layer, x, idx, cnt, oidx)
+
+
+@pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4"])
+def test_dense_ffn(c64, name):
+    cfg, layer = _layer(name)
+    c64.load_layer(0, layer)
+    x = W.xhat_inputs(cfg, 4, 3)
+    y = c64.dense_ffn(0, G.dev16(x))
+    c64.check()
+    want = O.masked_ffn(layer, x, np.arange(cfg.n, dtype=np.int32))
+    assert max_rel_err(G.y_to_f64(y, cfg.act_dtype), want) <= G.tol(layer)
+
+
+@pytest.mark.parametrize("name", ["relu_f16", "relu_q4"])
+def test_edge_lists(c64, name):
+    """Empty list -> b_down; full list -> dense; an unordered subset."""
+    t = G.torch()
+    cfg, layer = _layer(name)
+    c64.load_layer(0, layer)
+    x = W.xhat_inputs(cfg, 2, 5)
+    bd = W.from_bits(layer["b_down"], cfg.act_dtype).astype(np.float64)
+    for ids in (np.zeros(0, np.int32), np.arange(cfg.n, dtype=np.int32),
+                np.random.default_rng(2).permutation(cfg.n)[:37].astype(np.int32)):
+        idx = t.from_numpy(np.concatenate([ids, np.zeros(1, np.int32)])).cuda()
+        cnt = t.tensor([ids.size], dtype=t.int32, device="cuda")
+        y = c64.sparse_ffn(0, G.dev16(x), idx, cnt)
+        c64.check()
+        got = G.y_to_f64(y, cfg.act_dtype)
+        want = O.masked_ffn(layer, x, np.sort(ids))
+        if ids.size == 0:
+            assert np.array_equal(got, np.broadcast_to(
+                W.from_bits(W.to_bits(bd.astype(np.float32), cfg.act_dtype), cfg.act_dtype), got.shape))
+        else:
+            assert max_rel_err(got, want) <= G.tol(layer)
+
+
+def test_golden_worked_example_on_gpu(c64):
+    """The {3,4,5} example: predicted set and merged output, exact."""
+    layer, x, exp = worked_example_layer(W.F16)
+    c64.load_layer(0, layer)
+    idx, cnt = c64.predict(0, G.dev16(x))
+    c64.check()
+    assert idx[: int(cnt.item())].cpu().tolist() == exp["predicted"]
+    y = c64.sparse_ffn(0, G.dev16(x), idx, cnt)
+    c64.check()
+    assert G.y_to_f64(y, W.F16)[0].tolist() == exp["y_masked"]
+    yd = c64.dense_ffn(0, G.dev16(x))
+    c64.check()
+    assert G.y_to_f64(yd, W.F16)[0].tolist() == exp["y_dense"]
+
+
+def test_zero_logits_are_inactive(c64):
+    """Integer predictor: every logit is exact, including exact zeros."""
+    cfg = W.LayerConfig("intpred", 64, 200, 16, 1, W.RELU, W.F16, W.F16, alpha=0.8, cfg_id=204)
+    layer = W.make_layer(cfg, 0, 0)
+    rng = np.random.default_rng(3)
+    w1 = rng.integers(-2, 3, (16, 64)).astype(np.float32)
+    w2 = rng.integers(-2, 3, (200, 16)).astype(np.float32)
+    w2[:40] = 0                      # z = b2 = 0 exactly for these rows
+    b2 = rng.integers(-4, 5, 200).astype(np.float32)
+    b2[:40] = 0
+    layer.update(p_w1=W.to_bits(w1, W.F16), p_w2=W.to_bits(w2, W.F16), p_b2=W.to_bits(b2, W.F16), p_b1=None)
+    x = W.to_bits(rng.integers(-2, 3, (3, 64)).astype(np.float32), W.F16)
+    c64.load_layer(0, layer)
+    idx, cnt, oidx = G.predict_checked(c64, 0, layer, x)
+    assert not np.any(idx[: int(cnt.item())].cpu().numpy() < 40)
+
+
+def test_layer_counts_and_calibrated_permutation(c64):
+    t = G.torch()
+    cfg, layer = _layer("relu_f16")
+    c64.load_layer(0, layer)
+    cal = W.calibration_inputs(cfg, 0, 0, T=150)  # > max_batch: several launches
+    counts = c64.layer_counts(0, G.dev16(cal))
+    c64.check()
+    ref = O.layer_predict(layer, cal)["mask"].sum(0).astype(np.int32)
+    assert np.array_equal(counts.cpu().numpy(), ref)
+    perm = pi.pi_perm_from_counts(ref)
+    assert np.array_equal(perm, O.perm_from_counts(ref))
+    c64.load_layer(0, layer, perm)
+    counts2 = c64.layer_counts(0, G.dev16(cal))
+    assert np.array_equal(counts2.cpu().numpy(), ref[perm])  # hot neurons first
+    assert np.all(np.diff(counts2.cpu().numpy()) <= 0)
+    x = W.xhat_inputs(cfg, 1, 9)
+    G.predict_checked(c64, 0, layer, x, perm)
+    del t
+
+
+@pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4"])
+@pytest.mark.parametrize("B", [1, 3])
+@pytest.mark.parametrize("dense", [False, True])
+def test_decode_stack_teacher_forced(name, B, dense):
+    """Three-layer stack, one persistent launch: per layer the oracle consumes
+    the GPU's x_hat (trace) and must give the same list and the same update."""
+    t = G.torch()
+    cfg = CFGS[name]
+    c = G.ctx(max_layers=3, max_batch=8)
+    layers, perms = [], []
+    for l in range(3):
+        lw = W.make_layer(cfg, l, 0, random_b1=True, random_bdown=True)
+        c.load_layer(l, lw)
+        cal = W.calibration_inputs(cfg, l, 0, T=64)
+        perm = pi.pi_perm_from_counts(c.layer_counts(l, G.dev16(cal)).cpu().numpy())
+        c.load_layer(l, lw, perm)
+        layers.append(lw)
+        perms.append(perm)
+    L, d, n = 3, cfg.d, cfg.n
+    x0 = W.decode_inputs(cfg, B, 4)
+    x = t.from_numpy(x0.copy()).cuda()
+    tx = t.zeros((L, B, d), dtype=t.float32, device="cuda")
+    txh = t.zeros((L, B, d), dtype=t.int16, device="cuda")
+    tidx = t.full((L, n), -1, dtype=t.int32, device="cuda")
+    tcnt = t.zeros(L, dtype=t.int32, device="cuda")
+    c.set_trace(tx, txh, tidx, tcnt)
+    (c.dense_step if dense else c.decode_step)(x)
+    c.check()
+    xs = np.concatenate([tx.cpu().numpy(), x.cpu().numpy()[None]], 0).astype(np.float64)
+    assert np.array_equal(xs[0], x0.astype(np.float64))
+    xh = G.host16(txh)
+    for l in range(L):
+        # the GPU's RMSNorm is within one unit in the last place of the fp64 one
+        want = O.rmsnorm(xs[l].astype(np.float32), cfg.act_dtype)
+        assert np.abs(xh[l].astype(np.int32) - want.astype(np.int32)).max() <= 1
+        m = int(tcnt[l].item())
+        gidx = tidx[l, :m].cpu().numpy()
+        if dense:
+            assert m == n and np.array_equal(gidx, np.arange(n))
+            oidx = np.arange(n, dtype=np.int32)
+        else:
+            oidx = O.union(O.layer_predict(layers[l], xh[l])["mask"])
+            assert np.array_equal(np.sort(perms[l][gidx]), oidx)
+        y_ref = O.masked_ffn(layers[l], xh[l], oidx)
+        err = max_rel_err(xs[l + 1] - xs[l], y_ref)
+        assert err <= G.tol(layers[l]), f"layer {l}: {err:.3g}"
+    c.close()
+
+
+def test_timeout_is_reported_and_context_recovers():
+    """A grid barrier that can never complete (one phantom arrival expected)
+    must time out, report PI_ERR_TIMEOUT and leave the context usable."""
+    t = G.torch()
+    cfg, layer = _layer("relu_f16")
+    c = G.ctx(max_layers=1, max_batch=1)
+    c.load_layer(0, layer)
+    x = t.from_numpy(W.decode_inputs(cfg, 1, 0)).cuda()
+    ref = x.clone()
+    c.decode_step(ref)
+    c.check()
+    pi.pi_debug_set_wait_limit(c.handle, 50_000_000)  # 50 ms
+    pi.pi_debug_barrier_extra(c.handle, 1)
+    bad = x.clone()
+    c.decode_step(bad)
+    assert c.sync_status() == pi.PI_ERR_TIMEOUT
+    pi.pi_debug_barrier_extra(c.handle, 0)
+    again = x.clone()
+    c.decode_step(again)
+    c.check()
+    assert t.equal(again, ref)  # deterministic and unaffected by the failed launch
+    c.close()
+
+
+def test_out_of_range_index_is_flagged(c64):
+    t = G.torch()
+    cfg, layer = _layer("relu_f16")
+    c64.load_layer(0, layer)
+    x = G.dev16(W.xhat_inputs(cfg, 1, 0))
+    idx = t.tensor([3, cfg.n + 5, 7], dtype=t.int32, device="cuda")
+    cnt = t.tensor([3], dtype=t.int32, device="cuda")
+    c64.sparse_ffn(0, x, idx, cnt)
+    assert c64.sync_status() == pi.PI_ERR_DEVICE_FLAG
+    cnt_bad = t.tensor([cfg.n + 1], dtype=t.int32, device="cuda")
+    c64.sparse_ffn(0, x, idx, cnt_bad)
+    assert c64.sync_status() == pi.PI_ERR_DEVICE_FLAG
+    ok_idx = t.tensor([3, 7], dtype=t.int32, device="cuda")
+    c64.sparse_ffn(0, x, ok_idx, t.tensor([2], dtype=t.int32, device="cuda"))
+    c64.check()
+
+
+def test_host_side_errors(c64):
+    cfg, layer = _layer("relu_f16")
+    bad = dict(layer, d=260)  # not a multiple of 8
+    with pytest.raises(pi.PiError) as e:
+        c64.load_layer(1, bad)
+    assert e.value.status == pi.PI_ERR_SHAPE
+    with pytest.raises(pi.PiError) as e:
+        c64.load_layer(0, layer, perm=np.zeros(cfg.n, np.int32))
+    assert e.value.status == pi.PI_ERR_ARG
+    with pytest.raises(pi.PiError) as e:
+        pi.pi_predict(c64.handle, 3, None, 1, None, None)
+    assert e.value.status in (pi.PI_ERR_NOT_LOADED, pi.PI_ERR_ARG)
