@@ -105,7 +105,7 @@ __host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, in
     MiscLayout m;
     int o = 0;
     m.bars = o;
-    o += (2 * nss + 2 * nsd + 1) * 8;
+    o += (2 * nss + 2 * nsd + 2) * 8;
     o = (o + 15) & ~15;
     m.info = o;
     o += 16 * 4;

@@ -42,7 +42,7 @@ namespace pi {
 // ------------------------------------------------------------------ shared layout
 struct Shm {
     uint8_t *ring_s, *ring_d, *xs;
-    uint64_t *full_s, *empty_s, *full_d, *empty_d, *lst_full;
+    uint64_t *full_s, *empty_s, *full_d, *empty_d, *lst_full, *lst_free;
     int *info;      // [16] scalars
     float *tmp;     // [256] scratch (norm sums, inverses)
     int *slist;     // [lcap] this CTA's neuron ids (phase C)
@@ -53,7 +53,7 @@ struct Shm {
     float *red;     // [2][warps][kMaxNeuronsPerStage][TGF][2] cross-warp dot sums
 };
 
-enum { INFO_FLAG = 0, INFO_NCNT = 1, INFO_FAIL = 2 };
+enum { INFO_FLAG = 0, INFO_NCNT = 1, INFO_FAIL = 2, INFO_M = 3 };
 
 static __device__ __forceinline__ volatile int *fail_word(const Shm &S) { return S.info + INFO_FAIL; }
 
@@ -70,6 +70,7 @@ static __device__ __forceinline__ Shm carve(uint8_t *smem, const StepParams &p, 
     s.full_d = s.empty_s + p.nss;
     s.empty_d = s.full_d + p.nsd;
     s.lst_full = s.empty_d + p.nsd;
+    s.lst_free = s.lst_full + 1;
     s.info = (int *)(base + m.info);
     s.tmp = (float *)(base + m.tmp);
     s.slist = (int *)(base + m.slist);
@@ -217,6 +218,7 @@ static __device__ void dynamic_producer(const StepParams &p, const Shm &S)
             }
         }
         if (!ok) break;
+        mbar_arrive(S.lst_free); // done reading this layer's list and count
     }
     drain(S.full_d, sd, p.nsd, p);
 }
@@ -381,9 +383,13 @@ static __device__ bool phase_a(const StepParams &p, const Shm &S, const LayerDev
     for (int g = 0; g < nga; ++g) {
         const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
         stage_xhat<T>(p, S, l, t0, nt); // ends with cons_sync (covers srb too)
-        for (int k = warp; k < A.nst; k += kConsumerWarps) {
+        // warp w consumes exactly the stages that land in slot w, so each of
+        // its waits is one phase ahead of what it last saw (a parity wait
+        // cannot tell phases two apart)
+        for (int k = 0; k < A.nst; ++k) {
             const uint32_t s = ss + k;
             const int slot = s % p.nss;
+            if (slot != warp) continue;
             if (!wait_cta(S.full_s + slot, (s / p.nss) & 1, p, fail_word(S), ok)) continue;
             const uint8_t *base = S.ring_s + (size_t)slot * p.slotB;
             const int jr0 = A.j0 + k * A.rps, jr1 = min(A.j1, jr0 + A.rps);
@@ -434,9 +440,10 @@ static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev
                 __ldcg(reinterpret_cast<const float4 *>(p.h + (size_t)(t0 + t) * L.r + j));
         }
         cons_sync();
-        for (int k = warp; k < Bs.nst; k += kConsumerWarps) {
+        for (int k = 0; k < Bs.nst; ++k) { // slot-owned, as in phase A
             const uint32_t s = ss + k;
             const int slot = s % p.nss;
+            if (slot != warp) continue;
             if (!wait_cta(S.full_s + slot, (s / p.nss) & 1, p, fail_word(S), ok)) continue;
             const uint8_t *base = S.ring_s + (size_t)slot * p.slotB;
             const int ir0 = Bs.i0 + k * Bs.rps, ir1 = min(Bs.i1, ir0 + Bs.rps);
@@ -494,11 +501,17 @@ static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev
 // ------------------------------------------------------------------ list resolution
 // This CTA's equal share [s0, s1) of the layer's neuron list -> slist/sbias.
 template <typename T>
-static __device__ void resolve_list(const StepParams &p, const Shm &S, const LayerDev &L, int l)
+static __device__ bool resolve_list(const StepParams &p, const Shm &S, const LayerDev &L, int l)
 {
     using F = F16T<T>;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
+    if ((p.mode & M_FFN) && l > 0) {
+        // the dynamic producer must have finished reading layer l-1's list
+        bool ok = true;
+        wait_cta(S.lst_free, (l - 1) & 1, p, fail_word(S), ok);
+        if (!cons_sync_ok(fail_word(S))) return false;
+    }
     int m;
     if (p.mode & M_PREDICT) {
         for (int k = tid; k < G; k += kConsumerThreads) S.spref[k + 1] = __ldcg(p.loc_cnt + k);
@@ -522,11 +535,16 @@ static __device__ void resolve_list(const StepParams &p, const Shm &S, const Lay
         cons_sync();
         m = S.spref[G];
     } else if (p.mode & M_IDX_IN) {
-        m = *(volatile const int32_t *)p.count_in;
-        if (m < 0 || m > L.n) {
-            if (tid == 0) raise_error(p, PI_DEV_FLAG);
-            m = 0;
+        if (tid == 0) {
+            int v = *(volatile const int32_t *)p.count_in;
+            if (v < 0 || v > L.n) {
+                raise_error(p, PI_DEV_FLAG);
+                v = 0;
+            }
+            S.info[INFO_M] = v;
         }
+        cons_sync(); // one read, broadcast: the slice bounds must agree across warps
+        m = S.info[INFO_M];
     } else {
         m = L.n;
     }
@@ -565,6 +583,7 @@ static __device__ void resolve_list(const StepParams &p, const Shm &S, const Lay
         }
     }
     cons_sync();
+    return true;
 }
 
 // ------------------------------------------------------------------ phase C: gather FFN
@@ -864,11 +883,16 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
             mbar_init(S.empty_d + i, kConsumerWarps);
         }
         mbar_init(S.lst_full, 1);
+        mbar_init(S.lst_free, 1);
         fence_barrier_init();
         S.info[INFO_FAIL] = 0;
+        // An earlier launch failed and nobody has cleared the state yet.  Read
+        // once and broadcast: every warp of the CTA must take the same path,
+        // or the consumer warps that stay would block on a named barrier.
+        S.info[INFO_FLAG] = aborted(p) ? 1 : 0;
     }
     __syncthreads();
-    if (aborted(p)) return; // an earlier launch failed and nobody has cleared the state yet
+    if (S.info[INFO_FLAG]) return;
     if (warp == kStaticWarp) {
         if ((tid & 31) == 0) static_producer(p, S);
         return;
@@ -891,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
             if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
         }
         if (p.mode & (M_FFN | M_COMPACT)) {
-            resolve_list<T>(p, S, L, l);
+            if (!resolve_list<T>(p, S, L, l)) return;
             if (p.mode & M_FFN) {
                 if (threadIdx.x == 0) mbar_arrive(S.lst_full);
                 if (!phase_c<T, Q4, TGF>(p, S, L, l, sd, rbuf)) return;

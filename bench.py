@@ -186,29 +186,6 @@ def algorithmic_bytes(cfg, L, B, counts):
     return total
 
 
-def build_stack(cfg, L, B, seed, device, keep_host=()):
-    import numpy as np
-    import torch
-    from activation_sparse_decode_sigmoid_gb300 import pi
-    from activation_sparse_decode_sigmoid_gb300 import workload as W
-
-    ctx = pi.Context(device, max_layers=L, max_batch=max(B, 1))
-    host = {}
-    for l in range(L):
-        lw = W.make_layer_device(cfg, l, seed, torch.device("cuda", device))
-        ctx.load_layer(l, lw)
-        cal = torch.from_numpy(W.calibration_inputs(cfg, l, seed).view(np.int16)).cuda(device)
-        counts = ctx.layer_counts(l, cal).cpu().numpy()
-        perm = pi.pi_perm_from_counts(counts)
-        ctx.load_layer(l, lw, perm)
-        if l in keep_host:
-            host[l] = (W.layer_to_host(lw), perm)
-        del lw, cal
-    torch.cuda.synchronize(device)
-    ctx.check()
-    return ctx, host
-
-
 def cpu_oracle_sample(cfg, L, host_layers, seed, budget_s):
     """Time the oracle (as it stands, all host cores) on layer-token pairs of
     the workload until the budget is used; returns tokens/s for the stack."""
@@ -313,7 +290,8 @@ def run_ours(args, world, rank, local):
     K, Wm = args.steps, args.warmup
     do_extras = not args.no_extras
     do_cpu = do_extras and rank == 0 and world == 1
-    ctx, host = build_stack(cfg, L, B, args.seed, device, keep_host=(0, L // 2) if do_cpu else ())
+    from activation_sparse_decode_sigmoid_gb300.calibrate import load_synthetic_stack
+    ctx, host = load_synthetic_stack(cfg, L, args.seed, device, max(B, 1), keep_host=(0, L // 2) if do_cpu else ())
     d = cfg.d
     xbuf = torch.from_numpy(W.decode_inputs(cfg, (K + Wm) * B, args.seed)).cuda(device).view(K + Wm, B, d)
     cnt = torch.zeros((K + Wm, L), dtype=torch.int32, device=device)
@@ -378,8 +356,8 @@ def run_ours(args, world, rank, local):
         e1.record(stream)
         torch.cuda.synchronize(device)
         dense_ms = e0.elapsed_time(e1) / (nd - 1)
-        dense_bytes = L * (cfg.r * d * 2 * 0 + cfg.n * ((3 if cfg.act == W.REGLU else 2) *
-                                                         (d * 18 / 32 if cfg.w_dtype == W.Q4_0 else d * 2) + 2))
+        row = d * 18 / 32 if cfg.w_dtype == W.Q4_0 else d * 2
+        dense_bytes = L * cfg.n * ((3 if cfg.act == W.REGLU else 2) * row + 2)
         line["dense_baseline"] = {"tokens_per_s": B / (dense_ms / 1e3), "ms_per_step": dense_ms,
                                   "effective_hbm_gbs": dense_bytes / (dense_ms / 1e3) / 1e9,
                                   "what": "same persistent kernel over every neuron, no predictor (cuBLAS-free dense GEMV)"}

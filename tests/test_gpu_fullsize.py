@@ -1,0 +1,89 @@
+"""GPU parity at the full sizes of the five workloads.
+
+Each full-size layer is drawn on the GPU, calibrated and loaded exactly as the
+benchmark does; the oracle works on the same bytes copied back.  Index lists
+are compared bit-exactly for the whole batch; FFN outputs for every token when
+the batch is small, else for sampled tokens (the oracle computes them one by
+one).  The 48-layer OPT-30B-shaped stack runs in the benchmark's launch
+configuration (one persistent launch per token) and is checked layer by layer
+on sampled layers with teacher forcing from the trace."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle as O
+from activation_sparse_decode_sigmoid_gb300 import workload as W
+from activation_sparse_decode_sigmoid_gb300.calibrate import calibrate_and_load, load_synthetic_stack
+from tests import _gpu as G
+from tests._helpers import max_rel_err
+
+pytestmark = pytest.mark.gpu
+
+FULL = {
+    "opt30b_relu_f16": [1, 3],
+    "llama70b_reglu_bf16": [1, 8],
+    "falcon40b_relu_f16": [4, 16, 32],
+    "falcon40b_relu_q4": [1, 64],
+    "opt_1layer_relu_f16": [1, 8],
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_layer(name):
+    t = G.torch()
+    cfg = W.CONFIGS[name]
+    batches = FULL[name]
+    c = G.ctx(max_layers=1, max_batch=max(batches))
+    dev = t.device("cuda", 0)
+    lw = W.make_layer_device(cfg, 0, 0, dev)
+    cal = t.from_numpy(W.calibration_inputs(cfg, 0, 0).view(np.int16)).to(dev)
+    perm = calibrate_and_load(c, 0, lw, cal)
+    host = W.layer_to_host(lw)
+    del lw
+    for B in batches:
+        x = W.xhat_inputs(cfg, B, 21)
+        idx, cnt, oidx = G.predict_checked(c, 0, host, x, perm)
+        frac = oidx.size / cfg.n
+        assert 0.02 < frac < 0.999, frac
+        y = c.sparse_ffn(0, G.dev16(x), idx, cnt)
+        c.check()
+        got = G.y_to_f64(y, cfg.act_dtype)
+        toks = range(B) if B <= 8 else [0, B // 2, B - 1]
+        for tok in toks:
+            want = O.masked_ffn(host, x[tok: tok + 1], oidx)
+            err = max_rel_err(got[tok: tok + 1], want)
+            assert err <= G.tol(host), f"B={B} token {tok}: {err:.3g}"
+    c.close()
+
+
+def test_full_stack_decode_opt30b_sampled_layers():
+    """48 layers, batch 1, as the benchmark times it."""
+    t = G.torch()
+    cfg = W.CONFIGS["opt30b_relu_f16"]
+    L, d, n = cfg.L, cfg.d, cfg.n
+    sample = (0, L // 2, L - 1)
+    c, host = load_synthetic_stack(cfg, L, 0, 0, 1, keep_host=sample)
+    x0 = W.decode_inputs(cfg, 1, 0)
+    x = t.from_numpy(x0.copy()).cuda()
+    tx = t.zeros((L, 1, d), dtype=t.float32, device="cuda")
+    txh = t.zeros((L, 1, d), dtype=t.int16, device="cuda")
+    tidx = t.full((L, n), -1, dtype=t.int32, device="cuda")
+    tcnt = t.zeros(L, dtype=t.int32, device="cuda")
+    c.set_trace(tx, txh, tidx, tcnt)
+    c.decode_step(x)
+    c.check()
+    xs = np.concatenate([tx.cpu().numpy(), x.cpu().numpy()[None]], 0).astype(np.float64)
+    xh = G.host16(txh)
+    counts = tcnt.cpu().numpy()
+    assert np.all(counts > 0.03 * n) and np.all(counts < 0.3 * n), counts
+    for l in sample:
+        lw, perm = host[l]
+        want = O.rmsnorm(xs[l].astype(np.float32), cfg.act_dtype)
+        assert np.abs(xh[l].astype(np.int32) - want.astype(np.int32)).max() <= 1
+        gidx = tidx[l, : counts[l]].cpu().numpy()
+        oidx = O.union(O.layer_predict(lw, xh[l])["mask"])
+        assert np.array_equal(np.sort(perm[gidx]), oidx), f"layer {l}"
+        err = max_rel_err(xs[l + 1] - xs[l], O.masked_ffn(lw, xh[l], oidx))
+        assert err <= 1e-2, f"layer {l}: {err:.3g}"
+    c.close()

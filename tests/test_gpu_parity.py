@@ -21,6 +21,8 @@ CFGS = {
     "reglu_bf16": W.LayerConfig("reglu_bf16", 264, 777, 32, 3, W.REGLU, W.BF16, W.BF16, alpha=0.7, cfg_id=202),
     "relu_q4": W.LayerConfig("relu_q4", 512, 640, 64, 3, W.RELU, W.Q4_0, W.F16, alpha=0.9, cfg_id=203),
     "opt_1layer": W.CONFIGS["opt_1layer_relu_f16"],
+    # enough W1 / W2 rows per SM that both static-ring passes wrap several times
+    "ring_wrap": W.LayerConfig("ring_wrap", 4096, 12000, 2048, 2, W.RELU, W.F16, W.F16, alpha=0.9, cfg_id=205),
 }
 
 
