@@ -35,7 +35,8 @@ def load_synthetic_stack(cfg: W.LayerConfig, L: int, seed: int, device: int, max
     layers in `keep_host` (for checking against a CPU reference)."""
     import torch
 
-    ctx = pi.Context(device, max_layers=L, max_batch=max_batch)
+    # calibration runs 64 tokens per launch; decode calls use their own batch
+    ctx = pi.Context(device, max_layers=L, max_batch=max(max_batch, 64))
     host = {}
     dev = torch.device("cuda", device)
     for l in range(L):

@@ -65,6 +65,8 @@ struct pi_ctx {
     int32_t *tr_cnt = nullptr;
     unsigned long long wait_ns = 2000000000ull;
     int bar_extra = 0;
+    unsigned long long *timeline = nullptr;
+    int tl_stride = 0;
     std::string err;
 };
 
@@ -225,6 +227,8 @@ pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
     p.abort_flag = c->ctl + 3;
     p.wait_ns = c->wait_ns;
     p.bar_extra = c->bar_extra;
+    p.timeline = c->timeline;
+    p.tl_stride = c->tl_stride;
     const pi_layer_desc &d0 = c->layers[l0].desc;
     cudaError_t e;
     if (d0.w_dtype == PI_Q4_0) e = pi::launch_step_q4(p, tgf, c->G, c->stream);
@@ -615,6 +619,14 @@ pi_status pi_debug_set_wait_limit(pi_ctx *c, uint64_t ns)
 {
     if (!c || ns == 0) return PI_ERR_ARG;
     c->wait_ns = ns;
+    return PI_OK;
+}
+
+pi_status pi_debug_set_timeline(pi_ctx *c, uint64_t *stamps, int32_t per_cta)
+{
+    if (!c || (stamps && per_cta < 1)) return PI_ERR_ARG;
+    c->timeline = (unsigned long long *)stamps;
+    c->tl_stride = stamps ? per_cta : 0;
     return PI_OK;
 }
 

@@ -22,6 +22,7 @@ constexpr int kMaxBatch = 64;        // tokens per call
 constexpr int kYSlots = 16;          // output columns a consumer thread owns (d <= 8192)
 constexpr int kMaxNeuronsPerStage = 8;
 constexpr int kPhaseBTokens = 4;     // tokens per inner pass of the W2 dot products
+constexpr int kTimelineEvents = 9;   // stamps per layer in the debug timeline
 
 // device status codes (mirror pi.h)
 constexpr int PI_DEV_TIMEOUT = -6;
@@ -82,6 +83,8 @@ struct StepParams {
     int tr_n;
     int bar_extra;
     unsigned long long wait_ns;
+    unsigned long long *timeline; // [G][tl_stride] globaltimer stamps (debug)
+    int tl_stride;
     // shared-memory plan
     int slotB, nss;         // static ring: bytes per slot, slots
     int dslotB, nsd;        // dynamic ring: bytes per stage, stages

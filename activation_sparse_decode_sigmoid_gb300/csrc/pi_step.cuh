@@ -57,6 +57,13 @@ enum { INFO_FLAG = 0, INFO_NCNT = 1, INFO_FAIL = 2, INFO_M = 3 };
 
 static __device__ __forceinline__ volatile int *fail_word(const Shm &S) { return S.info + INFO_FAIL; }
 
+// debug timeline: thread 0 of each CTA stamps the globaltimer at phase ends
+__device__ __forceinline__ void mark(const StepParams &p, int ev)
+{
+    if (p.timeline && threadIdx.x == 0 && ev < p.tl_stride)
+        p.timeline[(size_t)blockIdx.x * p.tl_stride + ev] = globaltimer();
+}
+
 static __device__ __forceinline__ Shm carve(uint8_t *smem, const StepParams &p, int tgf)
 {
     Shm s;
@@ -618,6 +625,7 @@ static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev
             const uint32_t s = sd++;
             const int slot = s % p.nsd;
             const bool have = wait_cta(S.full_d + slot, (s / p.nsd) & 1, p, fail_word(S), ok);
+            if (k == 0 && g == 0) mark(p, 1 + l * kTimelineEvents + 8);
             const uint8_t *stage = S.ring_d + (size_t)slot * p.dslotB;
             const int nn = have ? min(npd, ncnt - k * npd) : 0;
             float *red = S.red + (size_t)rbuf * kConsumerWarps * kMaxNeuronsPerStage * TGF * 2;
@@ -905,22 +913,32 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
     uint32_t ss = 0, sd = 0;
     int rbuf = 0;
     const bool pred = (p.mode & (M_PREDICT | M_COUNTS)) != 0;
+    mark(p, 0);
     for (int l = 0; l < p.L; ++l) {
         const LayerDev L = p.layers[l];
+        const int ev = 1 + l * kTimelineEvents;
         if (pred) {
             if (!phase_a<T>(p, S, L, l, ss)) return;
+            mark(p, ev + 0);
             if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
+            mark(p, ev + 1);
             if (!phase_b<T>(p, S, L, ss)) return;
+            mark(p, ev + 2);
             if (!(p.mode & (M_FFN | M_COMPACT))) continue;
             if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
+            mark(p, ev + 3);
         }
         if (p.mode & (M_FFN | M_COMPACT)) {
             if (!resolve_list<T>(p, S, L, l)) return;
+            mark(p, ev + 4);
             if (p.mode & M_FFN) {
                 if (threadIdx.x == 0) mbar_arrive(S.lst_full);
                 if (!phase_c<T, Q4, TGF>(p, S, L, l, sd, rbuf)) return;
+                mark(p, ev + 5);
                 if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
+                mark(p, ev + 6);
                 phase_d<T>(p, L);
+                mark(p, ev + 7);
                 if (l + 1 < p.L && !grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
             }
         }

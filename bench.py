@@ -307,11 +307,13 @@ def run_ours(args, world, rank, local):
     barrier(world)
     if clocks:
         clocks.mark_start()
+    torch.cuda.nvtx.range_push("timed")
     ev[0].record(stream)
     for k in range(K):
         ctx.set_trace(None, None, None, cnt[Wm + k])
         ctx.decode_step(xbuf[Wm + k])
         ev[k + 1].record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(device)
     if clocks:
         clocks.mark_end()

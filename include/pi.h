@@ -191,13 +191,21 @@ const char *pi_last_error(pi_ctx *ctx);
 /* Number of SMs the persistent kernels use (one CTA per SM). */
 int32_t pi_grid_size(pi_ctx *ctx);
 
-/* Test hooks.  pi_debug_set_wait_limit: nanoseconds a device-side wait may
+/* Test and profiling hooks.  pi_debug_set_wait_limit: nanoseconds a device-side wait may
  * spin before it gives up with PI_ERR_TIMEOUT (default 2e9).
  * pi_debug_barrier_extra: add `extra` phantom arrivals to the grid barrier's
  * target count, so the next step's barrier can never complete and must time
  * out (0 restores normal operation). */
 pi_status pi_debug_set_wait_limit(pi_ctx *ctx, uint64_t ns);
 pi_status pi_debug_barrier_extra(pi_ctx *ctx, int32_t extra);
+
+/* Debug timeline: when `stamps` (dev uint64 [grid][per_cta]) is set, thread 0
+ * of every CTA of the step kernel writes %globaltimer (ns) at phase ends:
+ * index 0 = start, then per layer l at 1 + 9*l + k, k = 0 predictor hidden
+ * layer done, 1 its grid barrier, 2 predictor output done, 3 its barrier,
+ * 4 list resolved, 5 FFN done, 6 its barrier, 7 merge done, 8 first FFN
+ * rows landed.  Stamps past per_cta are dropped.  NULL disables. */
+pi_status pi_debug_set_timeline(pi_ctx *ctx, uint64_t *stamps, int32_t per_cta);
 
 #ifdef __cplusplus
 }
