@@ -54,10 +54,10 @@ struct pi_ctx {
     LayerDev *d_layers = nullptr;
     // workspace
     float *h = nullptr;
-    int32_t *loc_list = nullptr;
-    int32_t *loc_cnt = nullptr;
+    uint32_t *bitmap = nullptr;
     float *partial = nullptr;
-    int *ctl = nullptr; // [0..1] grid barrier, [2] status, [3] abort
+    int *ctl = nullptr; // [0..1] grid-barrier counter (u64), [2] status, [3] abort
+    unsigned long long bar_base = 0; // counter value the next launch starts from
     // trace
     float *tr_x = nullptr;
     void *tr_xhat = nullptr;
@@ -147,7 +147,9 @@ pi_status stack_layers(pi_ctx *c, int *L_out)
     return PI_OK;
 }
 
-// Shared-memory plan of one launch of the step kernel.
+// Shared-memory plan of one launch of the step kernel: the ring region is
+// time-shared between the static view (16 KB slots for predictor rows) and
+// the dynamic view (stages holding whole neurons for the FFN phase).
 pi_status plan(pi_ctx *c, StepParams &p, int l0, int L, int B, int mode, int *tgf_out)
 {
     const pi_layer_desc &d0 = c->layers[l0].desc;
@@ -165,46 +167,28 @@ pi_status plan(pi_ctx *c, StepParams &p, int l0, int L, int B, int mode, int *tg
     p.d = d;
     p.B = B;
     p.tg = std::min(B, tgf);
-    p.slotB = pred ? 16384 : 0;
-    const int xs = round_up(p.tg * d * 2, 128);
+    p.tgB = pred ? std::min(B, 4) : 1;
+    const int xsB = round_up(p.tg * d * 2, 128);
+    const int hB = pred ? round_up(p.tgB * rmax * 4, 128) : 0;
     p.lcap = (nmax + G - 1) / G + 2;
     const int words = (nmax + 31) / 32;
     p.wcap = (words + G - 1) / G + 1;
     p.rcap = std::max((rmax + G - 1) / G + 1, p.wcap * 32);
-    const int misc_bound = pi::misc_layout(8, 16, p.lcap, G, p.wcap, p.rcap, tgf).total;
-    const int budget = c->smem_optin - misc_bound - xs;
-    int nss = pred ? 6 : 0, nsd = 0, dslot = 0, dyn = 0;
-    if (ffn) {
-        dslot = round_up(std::max(nbmax, 24576), 128);
-        for (;;) {
-            nsd = (budget - nss * p.slotB) / dslot;
-            if (nsd >= 3 || nss <= 2 || !pred) break;
-            --nss;
-        }
-        if (nsd < 2)
-            return fail(c, PI_ERR_UNSUPPORTED, "a neuron (%d bytes) does not fit two pipeline stages", nbmax);
-        nsd = std::min(nsd, 16);
-        dyn = nsd * dslot;
-    }
-    if (pred) {
-        const int hrow = rmax * 4;
-        if (!ffn) {
-            const int fit = std::max(1, (budget - 2 * p.slotB) / hrow);
-            dyn = round_up(std::min(std::min(B, 16), fit) * hrow, 128);
-        }
-        while (nss > 2 && nss * p.slotB + dyn > budget) --nss;
-        if (nss * p.slotB + dyn > budget) return fail(c, PI_ERR_UNSUPPORTED, "predictor does not fit shared memory");
-        p.tgB = std::max(1, std::min(B, dyn / hrow));
-    } else {
-        p.tgB = 1;
-    }
-    p.nss = nss;
-    p.nsd = nsd;
-    p.dslotB = dslot;
-    p.off_dyn = nss * p.slotB;
-    p.off_xs = p.off_dyn + dyn;
-    p.off_misc = p.off_xs + xs;
-    p.smem_bytes = p.off_misc + pi::misc_layout(nss, nsd, p.lcap, G, p.wcap, p.rcap, tgf).total;
+    const int misc_bound = pi::misc_layout(pi::kConsumerWarps, 16, p.lcap, p.wcap, p.rcap, tgf).total;
+    const int ringB = (c->smem_optin - misc_bound - xsB - hB) / 128 * 128;
+    p.slotB = 16384;
+    p.nss = pred ? std::min(pi::kConsumerWarps, ringB / p.slotB) : 0; // one consumer warp per slot
+    if (pred && p.nss < 2) return fail(c, PI_ERR_UNSUPPORTED, "predictor ring does not fit shared memory");
+    p.dslotB = ffn ? round_up(std::max(nbmax, 24576), 128) : 0;
+    p.nsd = ffn ? std::min(16, ringB / p.dslotB) : 0;
+    if (ffn && p.nsd < 2)
+        return fail(c, PI_ERR_UNSUPPORTED, "a neuron (%d bytes) does not fit two pipeline stages", nbmax);
+    p.ringB = ringB;
+    p.off_h = ringB;
+    p.hB = hB;
+    p.off_xs = p.off_h + hB;
+    p.off_misc = p.off_xs + xsB;
+    p.smem_bytes = p.off_misc + pi::misc_layout(p.nss, p.nsd, p.lcap, p.wcap, p.rcap, tgf).total;
     if (p.smem_bytes > c->smem_optin) return fail(c, PI_ERR_UNSUPPORTED, "plan needs %d bytes of shared memory", p.smem_bytes);
     *tgf_out = tgf;
     return PI_OK;
@@ -219,10 +203,10 @@ pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
     p.L = L;
     p.mode = mode;
     p.h = c->h;
-    p.loc_list = c->loc_list;
-    p.loc_cnt = c->loc_cnt;
+    p.bitmap = c->bitmap;
     p.partial = c->partial;
-    p.bar = reinterpret_cast<unsigned *>(c->ctl);
+    p.bar = reinterpret_cast<unsigned long long *>(c->ctl);
+    p.bar_base = c->bar_base;
     p.status = c->ctl + 2;
     p.abort_flag = c->ctl + 3;
     p.wait_ns = c->wait_ns;
@@ -235,6 +219,8 @@ pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
     else if (d0.act_dtype == PI_BF16) e = pi::launch_step_bf16(p, tgf, c->G, c->stream);
     else e = pi::launch_step_f16(p, tgf, c->G, c->stream);
     if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "step kernel launch: %s", cudaGetErrorString(e));
+    // every CTA arrives once per grid barrier of the launch
+    c->bar_base += (unsigned long long)c->G * (unsigned long long)pi::launch_barriers(mode, L);
     return PI_OK;
 }
 
@@ -279,8 +265,8 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     }
     size_t need[] = {sizeof(LayerDev) * (size_t)max_layers,
                      sizeof(float) * (size_t)max_batch * pi::kMaxRank,
-                     sizeof(int32_t) * (size_t)pi::kMaxN,
-                     sizeof(int32_t) * (size_t)c->G,
+                     sizeof(uint32_t) * (size_t)(pi::kMaxN / 32),
+                     sizeof(int) * 64,
                      sizeof(float) * (size_t)c->G * max_batch * pi::kMaxD,
                      sizeof(int) * 64};
     void *ptrs[6] = {};
@@ -294,8 +280,8 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     }
     c->d_layers = (LayerDev *)ptrs[0];
     c->h = (float *)ptrs[1];
-    c->loc_list = (int32_t *)ptrs[2];
-    c->loc_cnt = (int32_t *)ptrs[3];
+    c->bitmap = (uint32_t *)ptrs[2];
+    cudaFree(ptrs[3]); // (unused slot kept so the allocation list stays aligned with `need`)
     c->partial = (float *)ptrs[4];
     c->ctl = (int *)ptrs[5];
     *out = c;
@@ -311,8 +297,7 @@ pi_status pi_destroy(pi_ctx *c)
         for (LayerSlot &s : c->layers) free_layer(s);
         cudaFree(c->d_layers);
         cudaFree(c->h);
-        cudaFree(c->loc_list);
-        cudaFree(c->loc_cnt);
+        cudaFree(c->bitmap);
         cudaFree(c->partial);
         cudaFree(c->ctl);
     }
@@ -600,7 +585,9 @@ pi_status pi_sync_status(pi_ctx *c)
     int ctl[4];
     CU(cudaMemcpy(ctl, c->ctl, sizeof ctl, cudaMemcpyDeviceToHost));
     if (ctl[2] != 0 || ctl[3] != 0) {
+        // a failed launch leaves the barrier counter wherever its CTAs stopped
         CU(cudaMemset(c->ctl, 0, sizeof(int) * 4));
+        c->bar_base = 0;
         const int code = ctl[2] ? ctl[2] : PI_ERR_TIMEOUT;
         return fail(c, code, code == PI_ERR_TIMEOUT ? "a device-side wait timed out" : "a kernel flagged invalid device data");
     }

@@ -126,61 +126,87 @@ static __device__ __forceinline__ void cons_sync()
 }
 
 // ------------------------------------------------------------------ grid barrier
-static __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *ptr)
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long *ptr)
 {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
     return v;
 }
 
-static __device__ __forceinline__ void st_release_gpu(unsigned *ptr, unsigned v)
+__device__ __forceinline__ void red_release_gpu_add_u64(unsigned long long *ptr, unsigned long long v)
 {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
-}
-
-static __device__ __forceinline__ unsigned atom_add_acqrel_gpu(unsigned *ptr, unsigned v)
-{
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
-    return old;
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
 }
 
 // All CTAs of the (co-resident, cooperative) grid meet here.  Called by every
-// consumer thread; the first consumer thread does the global handshake.
-// bar[0] counts arrivals, bar[1] is the generation.  `fail` is the CTA's
-// shared failure word (see wait_cta): a CTA that already failed does not
-// arrive.  Returns false when the kernel must unwind.
-static __device__ __noinline__ bool grid_sync(const StepParams &p, volatile int *fail, volatile int *flag)
+// consumer thread with the launch-local barrier number k (1, 2, ...); the
+// first consumer thread posts one arrival on a monotonic 64-bit counter and
+// polls it until all G arrivals of barrier k are in (counter >= base + k*G).
+// No reset, no generation word: one release-add and the polls.  `fail` is the
+// CTA's shared failure word (see wait_cta): a CTA that already failed does
+// not arrive.  Returns false when the kernel must unwind.
+static __device__ __noinline__ bool grid_sync(const StepParams &p, volatile int *fail, volatile int *flag,
+                                              int &k)
 {
     cons_sync();
     if (*fail) return false;
+    ++k;
     if (threadIdx.x == 0) {
         int ok = 1;
+        const unsigned long long target =
+            p.bar_base + (unsigned long long)k * (gridDim.x + (unsigned)p.bar_extra);
         __threadfence();
-        const unsigned gen = ld_acquire_gpu(p.bar + 1);
-        const unsigned target = gridDim.x + (unsigned)p.bar_extra;
-        const unsigned arrived = atom_add_acqrel_gpu(p.bar, 1u) + 1u;
-        if (arrived == target) {
-            atomicExch(p.bar, 0u);
-            __threadfence();
-            st_release_gpu(p.bar + 1, gen + 1u);
-        } else {
+        red_release_gpu_add_u64(p.bar, 1ull);
+        if (ld_acquire_gpu_u64(p.bar) < target) {
             const uint64_t t0 = globaltimer();
-            while (ld_acquire_gpu(p.bar + 1) == gen) {
-                if (aborted(p)) { ok = 0; break; }
-                if (globaltimer() - t0 > p.wait_ns) {
-                    raise_error(p, PI_DEV_TIMEOUT);
-                    ok = 0;
-                    break;
+            for (unsigned it = 1;; ++it) {
+                if (ld_acquire_gpu_u64(p.bar) >= target) break;
+                if ((it & 63) == 0) {
+                    if (aborted(p)) { ok = 0; break; }
+                    if (globaltimer() - t0 > p.wait_ns) {
+                        raise_error(p, PI_DEV_TIMEOUT);
+                        ok = 0;
+                        break;
+                    }
                 }
             }
         }
-        __threadfence();
         *flag = ok;
         if (!ok) *fail = 1;
     }
     cons_sync();
     return *flag != 0;
+}
+
+// Bulk prefetch of [src, src+bytes) into L2 (no shared memory, no completion).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes),
+                 "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Wait until the shared counter reaches `target` (bounded; polls the abort flag).
+static __device__ __noinline__ bool wait_counter(volatile int *ctr, int target, const StepParams &p)
+{
+    if (*ctr >= target) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (*ctr >= target) return true;
+        if (aborted(p)) return false;
+        if (globaltimer() - t0 > p.wait_ns) {
+            raise_error(p, PI_DEV_TIMEOUT);
+            return false;
+        }
+        __nanosleep(64);
+    }
 }
 
 // Consumer-side wait on an mbarrier phase.  A failed wait (timeout or abort)

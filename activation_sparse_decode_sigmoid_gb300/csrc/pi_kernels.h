@@ -68,11 +68,11 @@ struct StepParams {
     uint16_t *y_out;        // [B][d]
     int32_t *counts_out;    // [n]
     // workspace
-    float *h;               // [B][r_max]
-    int32_t *loc_list;      // [n_max]
-    int32_t *loc_cnt;       // [G]
-    float *partial;         // [G][B][d]
-    unsigned *bar;          // grid barrier {count, generation}
+    float *h;               // [B][r_max] predictor hidden activations
+    uint32_t *bitmap;       // [ceil(n_max/32)] predicted-mask words (union over tokens)
+    float *partial;         // [G][B][d] split-K partials of the FFN output
+    unsigned long long *bar;// grid barrier: monotonic arrival counter
+    unsigned long long bar_base; // counter value when this launch starts
     int *status;            // first device error
     int *abort_flag;
     // trace
@@ -85,25 +85,43 @@ struct StepParams {
     unsigned long long wait_ns;
     unsigned long long *timeline; // [G][tl_stride] globaltimer stamps (debug)
     int tl_stride;
-    // shared-memory plan
-    int slotB, nss;         // static ring: bytes per slot, slots
-    int dslotB, nsd;        // dynamic ring: bytes per stage, stages
+    // shared-memory plan.  The ring region [0, ringB) is time-shared: during
+    // the predictor phases it is nss static slots of slotB bytes, during the
+    // FFN phase nsd dynamic stages of dslotB bytes.
+    int ringB;
+    int slotB, nss;
+    int dslotB, nsd;
+    int off_h, hB;          // predictor hidden staging (tgB tokens)
+    int off_xs;             // x_hat of tg tokens
+    int off_misc;
     int tg;                 // tokens per x_hat pass (phase A and FFN)
     int tgB;                // tokens per h pass (phase B)
     int lcap;               // capacity of the per-CTA neuron list
     int wcap;               // capacity of the per-CTA mask words
     int rcap;               // capacity of the per-CTA predictor-bias cache
-    int off_dyn, off_xs, off_misc;
     int smem_bytes;
 };
+
+// Number of grid barriers one launch performs (host and kernel agree on it:
+// the host advances the barrier base by G times this after each launch).
+__host__ __device__ inline int launch_barriers(int mode, int L)
+{
+    const bool pred = (mode & (M_PREDICT | M_COUNTS)) != 0;
+    int n = 0;
+    for (int l = 0; l < L; ++l) {
+        if (pred) n += (mode & (M_FFN | M_COMPACT)) ? 2 : 1;
+        if (mode & M_FFN) n += (l + 1 < L) ? 2 : 1;
+    }
+    return n;
+}
 
 // Byte offsets of the small shared-memory objects of the step kernel (the
 // "misc" region).  Computed identically by the host planner and the kernel.
 struct MiscLayout {
-    int bars, info, tmp, slist, sbias, spref, swords, srb, red, total;
+    int bars, info, tmp, slist, sbias, swords, srb, red, total;
 };
 
-__host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, int G, int wcap, int rcap, int tgf)
+__host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, int wcap, int rcap, int tgf)
 {
     MiscLayout m;
     int o = 0;
@@ -118,9 +136,6 @@ __host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, in
     o += lcap * 4;
     m.sbias = o;
     o += lcap * 4;
-    m.spref = o;
-    o += (G + 1) * 4;
-    o = (o + 15) & ~15;
     m.swords = o;
     o += wcap * 4;
     m.srb = o;

@@ -13,19 +13,22 @@
 // One CTA per SM (cooperative launch), 18 warps:
 //   warps 0..15  consumers: dot products, activations, partial sums, merge;
 //   warp 16      static producer: streams this CTA's slice of the predictor
-//                weights W1 / W2 into a ring of shared-memory slots with bulk
-//                copies (cp.async.bulk + mbarrier).  The stream is known in
-//                advance, so it runs ahead across grid barriers and layers;
+//                weights W1 / W2 with bulk copies (cp.async.bulk + mbarrier)
+//                into nss slots of the shared ring, and, once a layer's slice
+//                is issued, prefetches the next layer's slice into L2;
 //   warp 17      dynamic producer: once the predicted list is known, streams
 //                the rows (W_up, W_gate, W_down^T) of this CTA's share of the
-//                predicted neurons into a second ring.
+//                predicted neurons into nsd stages of the same ring.
+// The ring is time-shared: static slots during phases A/B, dynamic stages
+// during phase C (the static producer of the next layer waits until the
+// consumers have finished phase C).
 // Per layer (consumers):
 //   A  x_hat = RMSNorm(x) (or given); h = max(CDOT(W1, x_hat) + b1, 0)  -> global
 //   -- grid barrier --
-//   B  z = CDOT(W2, h) + b2 for this CTA's rows; z > 0 sets a bit; the CTA's
-//      ascending local list and its count -> global
+//   B  z = CDOT(W2, h) + b2 for this CTA's rows; z > 0 sets a bit of the
+//      CTA's mask words -> global bitmap
 //   -- grid barrier --
-//   C  prefix of the local counts gives the ascending global list; this CTA
+//   C  a prefix scan of the bitmap gives the ascending global list; this CTA
 //      takes an equal share of it, streams those neurons' rows, computes
 //      a = act(W_up x_hat + b ...) and accumulates a * W_down^T rows -> fp32
 //      partial [B][d] of this CTA -> global
@@ -41,24 +44,23 @@ namespace pi {
 
 // ------------------------------------------------------------------ shared layout
 struct Shm {
-    uint8_t *ring_s, *ring_d, *xs;
+    uint8_t *ring, *hs, *xs;
     uint64_t *full_s, *empty_s, *full_d, *empty_d, *lst_full, *lst_free;
     int *info;      // [16] scalars
-    float *tmp;     // [256] scratch (norm sums, inverses)
+    float *tmp;     // [256] scratch (norm sums, scan totals)
     int *slist;     // [lcap] this CTA's neuron ids (phase C)
     float *sbias;   // [lcap] their biases
-    int *spref;     // [G+1] prefix of the local counts
     unsigned *swords; // [wcap] predicted-mask words of this CTA's rows
     float *srb;     // [rcap] predictor-bias cache of this CTA's rows
     float *red;     // [2][warps][kMaxNeuronsPerStage][TGF][2] cross-warp dot sums
 };
 
-enum { INFO_FLAG = 0, INFO_NCNT = 1, INFO_FAIL = 2, INFO_M = 3 };
+enum { INFO_FLAG = 0, INFO_NCNT = 1, INFO_FAIL = 2, INFO_M = 3, INFO_REGION = 4 };
 
 static __device__ __forceinline__ volatile int *fail_word(const Shm &S) { return S.info + INFO_FAIL; }
 
 // debug timeline: thread 0 of each CTA stamps the globaltimer at phase ends
-__device__ __forceinline__ void mark(const StepParams &p, int ev)
+static __device__ __forceinline__ void mark(const StepParams &p, int ev)
 {
     if (p.timeline && threadIdx.x == 0 && ev < p.tl_stride)
         p.timeline[(size_t)blockIdx.x * p.tl_stride + ev] = globaltimer();
@@ -67,10 +69,10 @@ __device__ __forceinline__ void mark(const StepParams &p, int ev)
 static __device__ __forceinline__ Shm carve(uint8_t *smem, const StepParams &p, int tgf)
 {
     Shm s;
-    s.ring_s = smem;
-    s.ring_d = smem + p.off_dyn;
+    s.ring = smem;
+    s.hs = smem + p.off_h;
     s.xs = smem + p.off_xs;
-    const MiscLayout m = misc_layout(p.nss, p.nsd, p.lcap, gridDim.x, p.wcap, p.rcap, tgf);
+    const MiscLayout m = misc_layout(p.nss, p.nsd, p.lcap, p.wcap, p.rcap, tgf);
     uint8_t *base = smem + p.off_misc;
     s.full_s = (uint64_t *)(base + m.bars);
     s.empty_s = s.full_s + p.nss;
@@ -82,7 +84,6 @@ static __device__ __forceinline__ Shm carve(uint8_t *smem, const StepParams &p, 
     s.tmp = (float *)(base + m.tmp);
     s.slist = (int *)(base + m.slist);
     s.sbias = (float *)(base + m.sbias);
-    s.spref = (int *)(base + m.spref);
     s.swords = (unsigned *)(base + m.swords);
     s.srb = (float *)(base + m.srb);
     s.red = (float *)(base + m.red);
@@ -136,7 +137,7 @@ static __device__ __forceinline__ int neurons_per_stage(const LayerDev &L, const
 // ------------------------------------------------------------------ producers
 // Wait (bounded, ignoring the abort flag) until the copies of the last issued
 // stages have landed, so that no bulk copy is in flight when the CTA exits.
-static __device__ void drain(uint64_t *full, uint32_t issued, int nslots, const StepParams &p)
+static __device__ void drain(uint64_t *full, uint32_t issued, int nslots)
 {
     const uint32_t first = issued > (uint32_t)nslots ? issued - nslots : 0;
     for (uint32_t k = first; k < issued; ++k) {
@@ -147,13 +148,31 @@ static __device__ void drain(uint64_t *full, uint32_t issued, int nslots, const 
     }
 }
 
+// L2 prefetch of layer l's predictor slice of this CTA (W1 rows, then W2 rows).
+static __device__ void prefetch_predictor(const StepParams &p, int l, uint64_t pol)
+{
+    const LayerDev &L = p.layers[l];
+    const SliceA A = slice_a(L, p);
+    const SliceB Bs = slice_b(L, p);
+    const uint8_t *w1 = (const uint8_t *)L.w1 + (size_t)A.j0 * L.d * 2;
+    const uint8_t *w2 = (const uint8_t *)L.w2 + (size_t)Bs.i0 * L.r * 2;
+    const size_t b1 = (size_t)(A.j1 - A.j0) * L.d * 2, b2 = (size_t)(Bs.i1 - Bs.i0) * L.r * 2;
+    constexpr size_t kChunk = 65536;
+    for (size_t o = 0; o < b1; o += kChunk) bulk_prefetch_l2(w1 + o, (uint32_t)min(kChunk, b1 - o), pol);
+    for (size_t o = 0; o < b2; o += kChunk) bulk_prefetch_l2(w2 + o, (uint32_t)min(kChunk, b2 - o), pol);
+}
+
 static __device__ void static_producer(const StepParams &p, const Shm &S)
 {
     if (!(p.mode & (M_PREDICT | M_COUNTS)) || p.nss == 0) return;
     const uint64_t pol = policy_evict_first();
+    const uint64_t keep = policy_evict_last();
+    const bool ffn = (p.mode & M_FFN) != 0;
     uint32_t s = 0;
     bool ok = true;
     for (int l = 0; l < p.L && ok; ++l) {
+        // the ring holds dynamic stages during phase C of the previous layer
+        if (ffn && l > 0 && !wait_counter(S.info + INFO_REGION, l, p)) break;
         const LayerDev &L = p.layers[l];
         const SliceA A = slice_a(L, p);
         const SliceB Bs = slice_b(L, p);
@@ -175,12 +194,15 @@ static __device__ void static_producer(const StepParams &p, const Shm &S)
                     }
                     const uint32_t bytes = (uint32_t)(min(rps, hi - row) * rowB);
                     mbar_arrive_expect_tx(S.full_s + slot, bytes);
-                    bulk_g2s(S.ring_s + (size_t)slot * p.slotB, src + (size_t)row * rowB, bytes, S.full_s + slot, pol);
+                    bulk_g2s(S.ring + (size_t)slot * p.slotB, src + (size_t)row * rowB, bytes, S.full_s + slot, pol);
                 }
             }
         }
+        // keep HBM busy through the barriers, the merge and the next layer's
+        // first phases: pull the next layer's predictor slice into L2 now
+        if (ok && (p.mode & M_RESID)) prefetch_predictor(p, l + 1 < p.L ? l + 1 : 0, keep);
     }
-    drain(S.full_s, s, p.nss, p);
+    drain(S.full_s, s, p.nss);
 }
 
 static __device__ void dynamic_producer(const StepParams &p, const Shm &S)
@@ -209,7 +231,7 @@ static __device__ void dynamic_producer(const StepParams &p, const Shm &S)
                 for (int j = 0; j < nn; ++j)
                     if (S.slist[k + j] >= 0) bytes += (uint32_t)nb;
                 mbar_arrive_expect_tx(S.full_d + slot, bytes);
-                uint8_t *dst = S.ring_d + (size_t)slot * p.dslotB;
+                uint8_t *dst = S.ring + (size_t)slot * p.dslotB;
                 for (int j = 0; j < nn; ++j) {
                     const int id = S.slist[k + j];
                     if (id < 0) continue;
@@ -227,7 +249,7 @@ static __device__ void dynamic_producer(const StepParams &p, const Shm &S)
         if (!ok) break;
         mbar_arrive(S.lst_free); // done reading this layer's list and count
     }
-    drain(S.full_d, sd, p.nsd, p);
+    drain(S.full_d, sd, p.nsd);
 }
 
 // ------------------------------------------------------------------ canonical dot products (CDOT)
@@ -238,117 +260,120 @@ static __device__ __forceinline__ float butterfly_sum(float a)
     return a;
 }
 
-// acc[t] = CDOT(w, x_t) for t < nt (<= NT): w is a 16-bit row of K elements
-// in shared memory, x_t a 16-bit row (xs + t*K) in shared memory.
-template <typename T, int NT>
-static __device__ __forceinline__ void cdot_xhat(const uint8_t *w, const uint8_t *xs, int K, int nt, int lane,
-                                          float (&acc)[NT])
+// acc[r] = CDOT(w_r, v) for NR rows w_r = w + r*rstride (16-bit, K elements,
+// shared memory) and one vector v: 16-bit (x_hat, VF = false) or fp32 (h,
+// VF = true), in shared memory.  The NR chains are independent: each keeps
+// the canonical per-lane order, they only share the loads of v.
+template <typename T, int NR, bool VF>
+static __device__ __forceinline__ void cdot_rows(const uint8_t *w, size_t rstride, const void *v, int K, int lane,
+                                                 float (&acc)[NR])
 {
     using F = F16T<T>;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+    for (int r = 0; r < NR; ++r) acc[r] = 0.f;
     const int nch = K >> 3;
     for (int ch = lane; ch < nch; ch += 32) {
-        const uint4 wv = *reinterpret_cast<const uint4 *>(w + (size_t)ch * 16);
-        const float2 w0 = F::pair(wv.x), w1 = F::pair(wv.y), w2 = F::pair(wv.z), w3 = F::pair(wv.w);
+        float vv[8];
+        if (VF) {
+            const float4 a = *reinterpret_cast<const float4 *>((const float *)v + (size_t)ch * 8);
+            const float4 b = *reinterpret_cast<const float4 *>((const float *)v + (size_t)ch * 8 + 4);
+            vv[0] = a.x, vv[1] = a.y, vv[2] = a.z, vv[3] = a.w, vv[4] = b.x, vv[5] = b.y, vv[6] = b.z, vv[7] = b.w;
+        } else {
+            const uint4 xv = *reinterpret_cast<const uint4 *>((const uint8_t *)v + (size_t)ch * 16);
+            const float2 x0 = F::pair(xv.x), x1 = F::pair(xv.y), x2 = F::pair(xv.z), x3 = F::pair(xv.w);
+            vv[0] = x0.x, vv[1] = x0.y, vv[2] = x1.x, vv[3] = x1.y, vv[4] = x2.x, vv[5] = x2.y, vv[6] = x3.x, vv[7] = x3.y;
+        }
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            if (t < nt) {
-                const uint4 xv = *reinterpret_cast<const uint4 *>(xs + (size_t)t * K * 2 + (size_t)ch * 16);
-                const float2 x0 = F::pair(xv.x), x1 = F::pair(xv.y), x2 = F::pair(xv.z), x3 = F::pair(xv.w);
-                float a = acc[t];
-                a = __fmaf_rn(w0.x, x0.x, a);
-                a = __fmaf_rn(w0.y, x0.y, a);
-                a = __fmaf_rn(w1.x, x1.x, a);
-                a = __fmaf_rn(w1.y, x1.y, a);
-                a = __fmaf_rn(w2.x, x2.x, a);
-                a = __fmaf_rn(w2.y, x2.y, a);
-                a = __fmaf_rn(w3.x, x3.x, a);
-                a = __fmaf_rn(w3.y, x3.y, a);
-                acc[t] = a;
-            }
+        for (int r = 0; r < NR; ++r) {
+            const uint4 wv = *reinterpret_cast<const uint4 *>(w + r * rstride + (size_t)ch * 16);
+            const float2 w0 = F::pair(wv.x), w1 = F::pair(wv.y), w2 = F::pair(wv.z), w3 = F::pair(wv.w);
+            float a = acc[r];
+            a = __fmaf_rn(w0.x, vv[0], a);
+            a = __fmaf_rn(w0.y, vv[1], a);
+            a = __fmaf_rn(w1.x, vv[2], a);
+            a = __fmaf_rn(w1.y, vv[3], a);
+            a = __fmaf_rn(w2.x, vv[4], a);
+            a = __fmaf_rn(w2.y, vv[5], a);
+            a = __fmaf_rn(w3.x, vv[6], a);
+            a = __fmaf_rn(w3.y, vv[7], a);
+            acc[r] = a;
         }
     }
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = butterfly_sum(acc[t]);
+    for (int r = 0; r < NR; ++r) acc[r] = butterfly_sum(acc[r]);
 }
 
-// acc[t] = CDOT(w, h_t): w a 16-bit row of K elements, h_t fp32 (hs + t*K).
-template <typename T, int NT>
-static __device__ __forceinline__ void cdot_h(const uint8_t *w, const float *hs, int K, int nt, int lane, float (&acc)[NT])
+// Rows [0, nrows) of a static stage (row stride rstride), 4 independent rows
+// at a time, then the remainder one by one; emit(row, acc) gets each CDOT.
+template <typename T, bool VF, typename Emit>
+static __device__ __forceinline__ void stage_rows(const uint8_t *base, size_t rstride, int nrows, const void *v, int K,
+                                                  int lane, Emit emit)
 {
-    using F = F16T<T>;
+    int r = 0;
+    for (; r + 4 <= nrows; r += 4) {
+        float acc[4];
+        cdot_rows<T, 4, VF>(base + (size_t)r * rstride, rstride, v, K, lane, acc);
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-    const int nch = K >> 3;
-    for (int ch = lane; ch < nch; ch += 32) {
-        const uint4 wv = *reinterpret_cast<const uint4 *>(w + (size_t)ch * 16);
-        const float2 w0 = F::pair(wv.x), w1 = F::pair(wv.y), w2 = F::pair(wv.z), w3 = F::pair(wv.w);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            if (t < nt) {
-                const float4 h0 = *reinterpret_cast<const float4 *>(hs + (size_t)t * K + (size_t)ch * 8);
-                const float4 h1 = *reinterpret_cast<const float4 *>(hs + (size_t)t * K + (size_t)ch * 8 + 4);
-                float a = acc[t];
-                a = __fmaf_rn(w0.x, h0.x, a);
-                a = __fmaf_rn(w0.y, h0.y, a);
-                a = __fmaf_rn(w1.x, h0.z, a);
-                a = __fmaf_rn(w1.y, h0.w, a);
-                a = __fmaf_rn(w2.x, h1.x, a);
-                a = __fmaf_rn(w2.y, h1.y, a);
-                a = __fmaf_rn(w3.x, h1.z, a);
-                a = __fmaf_rn(w3.y, h1.w, a);
-                acc[t] = a;
-            }
-        }
+        for (int u = 0; u < 4; ++u) emit(r + u, acc[u]);
     }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = butterfly_sum(acc[t]);
+    for (; r < nrows; ++r) {
+        float acc[1];
+        cdot_rows<T, 1, VF>(base + (size_t)r * rstride, rstride, v, K, lane, acc);
+        emit(r, acc[0]);
+    }
 }
 
 // ------------------------------------------------------------------ x_hat staging
 // xs[t][:] = x_hat of tokens t0..t0+nt-1, either RMSNorm of the fp32 residual
 // (fixed reduction order: every CTA computes bit-identical values) or a copy
-// of the caller's x_hat.  CTA 0 also writes the trace.
+// of the caller's x_hat.  One round trip to L2 per token.  CTA 0 writes the
+// trace.
 template <typename T>
 static __device__ void stage_xhat(const StepParams &p, const Shm &S, int l, int t0, int nt)
 {
     using F = F16T<T>;
     const int d = p.d, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint16_t *xs = reinterpret_cast<uint16_t *>(S.xs);
+    const int n4 = d / 4; // float4 chunks of a row; thread owns k = tid + 512 q, q < 4
     if (p.mode & M_RMSNORM) {
         for (int t = 0; t < nt; ++t) {
             const float4 *xr = reinterpret_cast<const float4 *>(p.x + (size_t)(t0 + t) * d);
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int k = tid + q * kConsumerThreads;
+                v[q] = k < n4 ? __ldcg(xr + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             float ss = 0.f;
-            for (int k = tid; k < d / 4; k += kConsumerThreads) {
-                const float4 v = __ldcg(xr + k);
-                ss = __fmaf_rn(v.x, v.x, ss);
-                ss = __fmaf_rn(v.y, v.y, ss);
-                ss = __fmaf_rn(v.z, v.z, ss);
-                ss = __fmaf_rn(v.w, v.w, ss);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                ss = __fmaf_rn(v[q].x, v[q].x, ss);
+                ss = __fmaf_rn(v[q].y, v[q].y, ss);
+                ss = __fmaf_rn(v[q].z, v[q].z, ss);
+                ss = __fmaf_rn(v[q].w, v[q].w, ss);
             }
             ss = butterfly_sum(ss);
-            if (lane == 0) S.tmp[warp * 4 + (t & 3)] = ss;
-            if ((t & 3) == 3 || t == nt - 1) {
-                cons_sync();
-                if (tid == 0) {
-                    for (int u = t & ~3; u <= t; ++u) {
-                        float tot = 0.f;
-                        for (int w = 0; w < kConsumerWarps; ++w) tot = __fadd_rn(tot, S.tmp[w * 4 + (u & 3)]);
-                        S.tmp[128 + u] = rsqrtf(__fadd_rn(__fdiv_rn(tot, (float)d), 1e-5f));
-                    }
-                }
-                cons_sync();
+            if (lane == 0) S.tmp[warp] = ss;
+            cons_sync();
+            if (tid == 0) {
+                float tot = 0.f;
+                for (int w = 0; w < kConsumerWarps; ++w) tot = __fadd_rn(tot, S.tmp[w]);
+                S.tmp[128] = rsqrtf(__fadd_rn(__fdiv_rn(tot, (float)d), 1e-5f));
             }
-        }
-        for (int t = 0; t < nt; ++t) {
-            const float inv = S.tmp[128 + t];
-            const float4 *xr = reinterpret_cast<const float4 *>(p.x + (size_t)(t0 + t) * d);
-            for (int k = tid; k < d / 4; k += kConsumerThreads) {
-                const float4 v = __ldcg(xr + k);
-                const uint32_t lo = (uint32_t)F::round(__fmul_rn(v.x, inv)) | ((uint32_t)F::round(__fmul_rn(v.y, inv)) << 16);
-                const uint32_t hi = (uint32_t)F::round(__fmul_rn(v.z, inv)) | ((uint32_t)F::round(__fmul_rn(v.w, inv)) << 16);
-                *reinterpret_cast<uint2 *>(xs + (size_t)t * d + 4 * k) = make_uint2(lo, hi);
+            cons_sync();
+            const float inv = S.tmp[128];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int k = tid + q * kConsumerThreads;
+                if (k < n4) {
+                    const uint32_t lo = (uint32_t)F::round(__fmul_rn(v[q].x, inv)) |
+                                        ((uint32_t)F::round(__fmul_rn(v[q].y, inv)) << 16);
+                    const uint32_t hi = (uint32_t)F::round(__fmul_rn(v[q].z, inv)) |
+                                        ((uint32_t)F::round(__fmul_rn(v[q].w, inv)) << 16);
+                    *reinterpret_cast<uint2 *>(xs + (size_t)t * d + 4 * k) = make_uint2(lo, hi);
+                    if (p.tr_x && blockIdx.x == 0)
+                        reinterpret_cast<float4 *>(p.tr_x + ((size_t)l * p.B + t0 + t) * d)[k] = v[q];
+                }
             }
         }
     } else {
@@ -359,25 +384,19 @@ static __device__ void stage_xhat(const StepParams &p, const Shm &S, int l, int 
         }
     }
     cons_sync();
-    if (blockIdx.x == 0) {
-        if (p.tr_xhat) {
-            for (int t = 0; t < nt; ++t) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(xs + (size_t)t * d);
-                uint4 *dst = reinterpret_cast<uint4 *>(p.tr_xhat + ((size_t)l * p.B + t0 + t) * d);
-                for (int k = tid; k < d / 8; k += kConsumerThreads) dst[k] = src[k];
-            }
-        }
-        if (p.tr_x && (p.mode & M_RMSNORM)) {
-            for (int t = 0; t < nt; ++t) {
-                const float4 *src = reinterpret_cast<const float4 *>(p.x + (size_t)(t0 + t) * d);
-                float4 *dst = reinterpret_cast<float4 *>(p.tr_x + ((size_t)l * p.B + t0 + t) * d);
-                for (int k = tid; k < d / 4; k += kConsumerThreads) dst[k] = __ldcg(src + k);
-            }
+    if (p.tr_xhat && blockIdx.x == 0) {
+        for (int t = 0; t < nt; ++t) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(xs + (size_t)t * d);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.tr_xhat + ((size_t)l * p.B + t0 + t) * d);
+            for (int k = tid; k < d / 8; k += kConsumerThreads) dst[k] = src[k];
         }
     }
 }
 
 // ------------------------------------------------------------------ phase A: h = relu(W1 x_hat + b1)
+// Warp w consumes exactly the stages that land in slot w (w < nss), so each of
+// its waits is one phase ahead of what it last saw (a parity wait cannot tell
+// phases two apart).
 template <typename T>
 static __device__ bool phase_a(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &ss)
 {
@@ -390,31 +409,22 @@ static __device__ bool phase_a(const StepParams &p, const Shm &S, const LayerDev
     for (int g = 0; g < nga; ++g) {
         const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
         stage_xhat<T>(p, S, l, t0, nt); // ends with cons_sync (covers srb too)
-        // warp w consumes exactly the stages that land in slot w, so each of
-        // its waits is one phase ahead of what it last saw (a parity wait
-        // cannot tell phases two apart)
         for (int k = 0; k < A.nst; ++k) {
             const uint32_t s = ss + k;
             const int slot = s % p.nss;
             if (slot != warp) continue;
             if (!wait_cta(S.full_s + slot, (s / p.nss) & 1, p, fail_word(S), ok)) continue;
-            const uint8_t *base = S.ring_s + (size_t)slot * p.slotB;
-            const int jr0 = A.j0 + k * A.rps, jr1 = min(A.j1, jr0 + A.rps);
-            for (int j = jr0; j < jr1; ++j) {
-                const uint8_t *w = base + (size_t)(j - jr0) * L.d * 2;
-                for (int tt = 0; tt < nt; tt += 4) {
-                    float acc[4];
-                    cdot_xhat<T, 4>(w, S.xs + (size_t)tt * L.d * 2, L.d, min(4, nt - tt), lane, acc);
-                    if (lane == 0) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            if (tt + u < nt) {
-                                const float s1 = __fadd_rn(acc[u], S.srb[j - A.j0]);
-                                p.h[(size_t)(t0 + tt + u) * L.r + j] = s1 > 0.f ? s1 : 0.f;
-                            }
-                        }
-                    }
-                }
+            const uint8_t *base = S.ring + (size_t)slot * p.slotB;
+            const int jr0 = A.j0 + k * A.rps, nrows = min(A.j1, jr0 + A.rps) - jr0;
+            for (int t = 0; t < nt; ++t) {
+                stage_rows<T, false>(base, (size_t)L.d * 2, nrows, S.xs + (size_t)t * L.d * 2, L.d, lane,
+                                     [&](int r, float acc) {
+                                         if (lane == 0) {
+                                             const int j = jr0 + r;
+                                             const float s1 = __fadd_rn(acc, S.srb[j - A.j0]);
+                                             p.h[(size_t)(t0 + t) * L.r + j] = s1 > 0.f ? s1 : 0.f;
+                                         }
+                                     });
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(S.empty_s + slot);
@@ -436,7 +446,7 @@ static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev
     const int nwords = (nrows + 31) >> 5;
     for (int k = tid; k < nwords; k += kConsumerThreads) S.swords[k] = 0u;
     for (int k = tid; k < nrows; k += kConsumerThreads) S.srb[k] = F::one(L.b2[Bs.i0 + k]);
-    float *hs = reinterpret_cast<float *>(S.ring_d);
+    float *hs = reinterpret_cast<float *>(S.hs);
     const int ngb = (p.B + p.tgB - 1) / p.tgB;
     bool ok = true;
     for (int g = 0; g < ngb; ++g) {
@@ -447,27 +457,31 @@ static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev
                 __ldcg(reinterpret_cast<const float4 *>(p.h + (size_t)(t0 + t) * L.r + j));
         }
         cons_sync();
-        for (int k = 0; k < Bs.nst; ++k) { // slot-owned, as in phase A
+        for (int k = 0; k < Bs.nst; ++k) {
             const uint32_t s = ss + k;
             const int slot = s % p.nss;
             if (slot != warp) continue;
             if (!wait_cta(S.full_s + slot, (s / p.nss) & 1, p, fail_word(S), ok)) continue;
-            const uint8_t *base = S.ring_s + (size_t)slot * p.slotB;
-            const int ir0 = Bs.i0 + k * Bs.rps, ir1 = min(Bs.i1, ir0 + Bs.rps);
-            for (int i = ir0; i < ir1; ++i) {
-                const uint8_t *w = base + (size_t)(i - ir0) * L.r * 2;
-                const float b2 = S.srb[i - Bs.i0];
-                int cnt = 0;
-                for (int tt = 0; tt < nt; tt += kPhaseBTokens) {
-                    float acc[kPhaseBTokens];
-                    cdot_h<T, kPhaseBTokens>(w, hs + (size_t)tt * L.r, L.r, min(kPhaseBTokens, nt - tt), lane, acc);
-#pragma unroll
-                    for (int u = 0; u < kPhaseBTokens; ++u)
-                        if (tt + u < nt) cnt += __fadd_rn(acc[u], b2) > 0.f ? 1 : 0;
+            const uint8_t *base = S.ring + (size_t)slot * p.slotB;
+            const int ir0 = Bs.i0 + k * Bs.rps, nr = min(Bs.i1, ir0 + Bs.rps) - ir0;
+            for (int r0 = 0; r0 < nr; r0 += 32) {
+                const int nrr = min(32, nr - r0);
+                unsigned bits = 0; // bit r: row ir0 + r0 + r selected for some token of the group
+                for (int t = 0; t < nt; ++t) {
+                    stage_rows<T, true>(base + (size_t)r0 * L.r * 2, (size_t)L.r * 2, nrr, hs + (size_t)t * L.r, L.r,
+                                        lane, [&](int r, float acc) {
+                                            if (__fadd_rn(acc, S.srb[ir0 + r0 + r - Bs.i0]) > 0.f) {
+                                                bits |= 1u << r;
+                                                if (lane == 0 && (p.mode & M_COUNTS))
+                                                    atomicAdd(p.counts_out + ir0 + r0 + r, 1);
+                                            }
+                                        });
                 }
-                if (lane == 0 && cnt) {
-                    if (p.mode & M_COUNTS) atomicAdd(p.counts_out + i, cnt);
-                    if (p.mode & M_PREDICT) atomicOr(S.swords + ((i - Bs.i0) >> 5), 1u << ((i - Bs.i0) & 31));
+                if (lane == 0 && (p.mode & M_PREDICT) && bits) {
+                    const int rel = ir0 + r0 - Bs.i0; // rows relative to the word-aligned i0
+                    const int w0 = rel >> 5, sh = rel & 31;
+                    atomicOr(S.swords + w0, bits << sh);
+                    if (sh && (bits >> (32 - sh))) atomicOr(S.swords + w0 + 1, bits >> (32 - sh));
                 }
             }
             __syncwarp();
@@ -476,37 +490,16 @@ static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev
         ss += Bs.nst;
         if (!cons_sync_ok(fail_word(S))) return false; // hs is rewritten by the next group
     }
-    fence_proxy_async_smem(); // hs bytes are overwritten by bulk copies in phase C
-    if (p.mode & M_PREDICT) {
-        if (warp == 0) {
-            int base = 0;
-            for (int w0 = 0; w0 < nwords; w0 += 32) {
-                const int wi = w0 + lane;
-                const unsigned bits = wi < nwords ? S.swords[wi] : 0u;
-                const int c = __popc(bits);
-                int incl = c;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += v;
-                }
-                int pos = base + incl - c;
-                unsigned b = bits;
-                while (b) {
-                    const int bit = __ffs(b) - 1;
-                    b &= b - 1;
-                    p.loc_list[Bs.i0 + pos++] = Bs.i0 + 32 * wi + bit;
-                }
-                base += __shfl_sync(0xffffffffu, incl, 31);
-            }
-            if (lane == 0) p.loc_cnt[blockIdx.x] = base;
-        }
-    }
+    if (p.mode & M_PREDICT)
+        for (int k = tid; k < nwords; k += kConsumerThreads) p.bitmap[(Bs.i0 >> 5) + k] = S.swords[k];
     return true;
 }
 
 // ------------------------------------------------------------------ list resolution
 // This CTA's equal share [s0, s1) of the layer's neuron list -> slist/sbias.
+// A predicted list comes from an exclusive prefix scan of the bitmap's
+// popcounts (each thread owns a contiguous run of at most 4 words), so one
+// round trip to L2 suffices.
 template <typename T>
 static __device__ bool resolve_list(const StepParams &p, const Shm &S, const LayerDev &L, int l)
 {
@@ -519,68 +512,95 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
         wait_cta(S.lst_free, (l - 1) & 1, p, fail_word(S), ok);
         if (!cons_sync_ok(fail_word(S))) return false;
     }
-    int m;
+    int m, s0, s1;
     if (p.mode & M_PREDICT) {
-        for (int k = tid; k < G; k += kConsumerThreads) S.spref[k + 1] = __ldcg(p.loc_cnt + k);
-        cons_sync();
-        if (warp == 0) {
-            int base = 0;
-            for (int k0 = 0; k0 < G; k0 += 32) {
-                const int k = k0 + lane;
-                const int v = k < G ? S.spref[k + 1] : 0;
-                int incl = v;
+        const int nw = (L.n + 31) >> 5;
+        const int wpt = (nw + kConsumerThreads - 1) / kConsumerThreads; // <= 4 for n <= 65536
+        const int wb = min(nw, tid * wpt), we = min(nw, wb + wpt);
+        unsigned wv[4];
+        int cnt = 0;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += u;
-                }
-                if (k < G) S.spref[k + 1] = base + incl;
-                base += __shfl_sync(0xffffffffu, incl, 31);
+        for (int q = 0; q < 4; ++q) {
+            wv[q] = (wb + q < we) ? __ldcg(p.bitmap + wb + q) : 0u;
+            cnt += __popc(wv[q]);
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        int *wtot = reinterpret_cast<int *>(S.tmp);
+        if (lane == 31) wtot[warp] = incl;
+        cons_sync();
+        if (tid == 0) {
+            int run = 0;
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const int v = wtot[w];
+                wtot[w] = run;
+                run += v;
             }
-            if (lane == 0) S.spref[0] = 0;
+            S.info[INFO_M] = run;
         }
         cons_sync();
-        m = S.spref[G];
-    } else if (p.mode & M_IDX_IN) {
-        if (tid == 0) {
-            int v = *(volatile const int32_t *)p.count_in;
-            if (v < 0 || v > L.n) {
-                raise_error(p, PI_DEV_FLAG);
-                v = 0;
-            }
-            S.info[INFO_M] = v;
-        }
-        cons_sync(); // one read, broadcast: the slice bounds must agree across warps
         m = S.info[INFO_M];
+        s0 = slice_lo(m, c, G);
+        s1 = slice_lo(m, c + 1, G);
+        int pos = wtot[warp] + incl - cnt; // global position of this thread's first set bit
+        if (pos < s1 && pos + cnt > s0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                unsigned b = wv[q];
+                const int pc = __popc(b);
+                if (pos + pc <= s0 || pos >= s1) {
+                    pos += pc;
+                    continue;
+                }
+                while (b) {
+                    const int bit = __ffs(b) - 1;
+                    b &= b - 1;
+                    if (pos >= s0 && pos < s1) S.slist[pos - s0] = 32 * (wb + q) + bit;
+                    ++pos;
+                }
+            }
+        }
+        cons_sync();
     } else {
-        m = L.n;
+        if (p.mode & M_IDX_IN) {
+            if (tid == 0) {
+                int v = *(volatile const int32_t *)p.count_in;
+                if (v < 0 || v > L.n) {
+                    raise_error(p, PI_DEV_FLAG);
+                    v = 0;
+                }
+                S.info[INFO_M] = v;
+            }
+            cons_sync(); // one read, broadcast: the slice bounds must agree across warps
+            m = S.info[INFO_M];
+        } else {
+            m = L.n;
+        }
+        s0 = slice_lo(m, c, G);
+        s1 = slice_lo(m, c + 1, G);
+        for (int k = tid; k < s1 - s0; k += kConsumerThreads) {
+            int id = s0 + k;
+            if (p.mode & M_IDX_IN) {
+                id = p.idx_in[s0 + k];
+                if (id < 0 || id >= L.n) {
+                    raise_error(p, PI_DEV_FLAG);
+                    id = -1;
+                }
+            }
+            S.slist[k] = id;
+        }
+        cons_sync();
     }
-    const int s0 = slice_lo(m, c, G), s1 = slice_lo(m, c + 1, G);
     const int ncnt = s1 - s0;
     for (int k = tid; k < ncnt; k += kConsumerThreads) {
-        const int pos = s0 + k;
-        int id;
-        if (p.mode & M_PREDICT) {
-            int lo = 0, hi = G - 1; // largest c' with spref[c'] <= pos
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (S.spref[mid] <= pos) lo = mid;
-                else hi = mid - 1;
-            }
-            id = __ldcg(p.loc_list + word_row_start(L.n, lo, G) + (pos - S.spref[lo]));
-        } else if (p.mode & M_IDX_IN) {
-            id = p.idx_in[pos];
-            if (id < 0 || id >= L.n) {
-                raise_error(p, PI_DEV_FLAG);
-                id = -1;
-            }
-        } else {
-            id = pos;
-        }
-        S.slist[k] = id;
+        const int id = S.slist[k];
         S.sbias[k] = id >= 0 ? F::one(L.b[id]) : 0.f;
-        if (p.idx_out) p.idx_out[pos] = id;
-        if (p.tr_idx) p.tr_idx[(size_t)l * p.tr_n + pos] = id;
+        if (p.idx_out) p.idx_out[s0 + k] = id;
+        if (p.tr_idx) p.tr_idx[(size_t)l * p.tr_n + s0 + k] = id;
     }
     if (tid == 0) {
         S.info[INFO_NCNT] = ncnt;
@@ -598,7 +618,8 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
 // ch = tid and tid + 512 (kYSlots = 16 columns); Q4_0 -> half-block hb = tid
 // (16 columns of block hb/2).
 template <typename T, bool Q4, int TGF>
-static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd, int &rbuf)
+static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd, int &rbuf,
+                               bool xs_valid)
 {
     using F = F16T<T>;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -614,7 +635,8 @@ static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev
     bool ok = true;
     for (int g = 0; g < ngf; ++g) {
         const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
-        stage_xhat<T>(p, S, l, t0, nt);
+        // phase A left the x_hat of a single token group in xs
+        if (!(xs_valid && ngf == 1)) stage_xhat<T>(p, S, l, t0, nt);
         float y[TGF][kYSlots];
 #pragma unroll
         for (int t = 0; t < TGF; ++t)
@@ -626,7 +648,7 @@ static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev
             const int slot = s % p.nsd;
             const bool have = wait_cta(S.full_d + slot, (s / p.nsd) & 1, p, fail_word(S), ok);
             if (k == 0 && g == 0) mark(p, 1 + l * kTimelineEvents + 8);
-            const uint8_t *stage = S.ring_d + (size_t)slot * p.dslotB;
+            const uint8_t *stage = S.ring + (size_t)slot * p.dslotB;
             const int nn = have ? min(npd, ncnt - k * npd) : 0;
             float *red = S.red + (size_t)rbuf * kConsumerWarps * kMaxNeuronsPerStage * TGF * 2;
             // ---- partial dot products of this thread's columns
@@ -824,18 +846,26 @@ static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev
 }
 
 // ------------------------------------------------------------------ phase D: merge
+// Units of 4 columns; a warp per unit, its lanes over the partials in a fixed
+// order, then a butterfly.  x and b_down are loaded alongside the partials.
 template <typename T>
 static __device__ void phase_d(const StepParams &p, const LayerDev &L)
 {
     using F = F16T<T>;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, d = L.d;
     const int U = p.B * d / 4;
     const int u0 = slice_lo(U, blockIdx.x, G), u1 = slice_lo(U, blockIdx.x + 1, G);
     const size_t stride4 = (size_t)p.B * d / 4;
     const float4 *part = reinterpret_cast<const float4 *>(p.partial);
-    (void)tid;
     for (int u = u0 + warp; u < u1; u += kConsumerWarps) {
+        const int j = (4 * u) % d;
+        float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
+        uint2 bd = make_uint2(0, 0);
+        if (lane == 0) {
+            bd = *reinterpret_cast<const uint2 *>(L.bdown + j);
+            if (p.mode & M_RESID) xv = __ldcg(reinterpret_cast<const float4 *>(p.x) + u);
+        }
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int cc = lane; cc < G; cc += 32) {
             const float4 v = __ldcg(part + (size_t)cc * stride4 + u);
@@ -852,19 +882,17 @@ static __device__ void phase_d(const StepParams &p, const LayerDev &L)
             acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
         }
         if (lane == 0) {
-            const int j = (4 * u) % d;
-            acc.x += F::one(L.bdown[j]);
-            acc.y += F::one(L.bdown[j + 1]);
-            acc.z += F::one(L.bdown[j + 2]);
-            acc.w += F::one(L.bdown[j + 3]);
+            const float2 b01 = F::pair(bd.x), b23 = F::pair(bd.y);
+            acc.x += b01.x;
+            acc.y += b01.y;
+            acc.z += b23.x;
+            acc.w += b23.y;
             if (p.mode & M_RESID) {
-                float4 *xp = reinterpret_cast<float4 *>(p.x) + u;
-                float4 xv = __ldcg(xp);
                 xv.x += acc.x;
                 xv.y += acc.y;
                 xv.z += acc.z;
                 xv.w += acc.w;
-                __stcg(xp, xv);
+                __stcg(reinterpret_cast<float4 *>(p.x) + u, xv);
             } else {
                 const uint32_t lo = (uint32_t)F::round(acc.x) | ((uint32_t)F::round(acc.y) << 16);
                 const uint32_t hi = (uint32_t)F::round(acc.z) | ((uint32_t)F::round(acc.w) << 16);
@@ -876,7 +904,7 @@ static __device__ void phase_d(const StepParams &p, const LayerDev &L)
 
 // ------------------------------------------------------------------ the kernel
 template <typename T, bool Q4, int TGF>
-__global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
+__global__ void __maxnreg__(112) step_kernel(const StepParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const Shm S = carve(smem, p, TGF);
@@ -894,6 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
         mbar_init(S.lst_free, 1);
         fence_barrier_init();
         S.info[INFO_FAIL] = 0;
+        S.info[INFO_REGION] = 0;
         // An earlier launch failed and nobody has cleared the state yet.  Read
         // once and broadcast: every warp of the CTA must take the same path,
         // or the consumer warps that stay would block on a named barrier.
@@ -911,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
     }
     // ---- consumers
     uint32_t ss = 0, sd = 0;
-    int rbuf = 0;
+    int rbuf = 0, nbar = 0;
     const bool pred = (p.mode & (M_PREDICT | M_COUNTS)) != 0;
     mark(p, 0);
     for (int l = 0; l < p.L; ++l) {
@@ -920,12 +949,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
         if (pred) {
             if (!phase_a<T>(p, S, L, l, ss)) return;
             mark(p, ev + 0);
-            if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
+            if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG, nbar)) return;
             mark(p, ev + 1);
             if (!phase_b<T>(p, S, L, ss)) return;
             mark(p, ev + 2);
             if (!(p.mode & (M_FFN | M_COMPACT))) continue;
-            if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
+            if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG, nbar)) return;
             mark(p, ev + 3);
         }
         if (p.mode & (M_FFN | M_COMPACT)) {
@@ -933,13 +962,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
             mark(p, ev + 4);
             if (p.mode & M_FFN) {
                 if (threadIdx.x == 0) mbar_arrive(S.lst_full);
-                if (!phase_c<T, Q4, TGF>(p, S, L, l, sd, rbuf)) return;
+                if (!phase_c<T, Q4, TGF>(p, S, L, l, sd, rbuf, pred)) return;
+                // the ring is free again: the static producer may fill it for layer l+1
+                if (threadIdx.x == 0) atomicAdd(S.info + INFO_REGION, 1);
                 mark(p, ev + 5);
-                if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
+                if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG, nbar)) return;
                 mark(p, ev + 6);
                 phase_d<T>(p, L);
                 mark(p, ev + 7);
-                if (l + 1 < p.L && !grid_sync(p, fail_word(S), S.info + INFO_FLAG)) return;
+                if (l + 1 < p.L && !grid_sync(p, fail_word(S), S.info + INFO_FLAG, nbar)) return;
             }
         }
     }
