@@ -904,7 +904,7 @@ static __device__ void phase_d(const StepParams &p, const LayerDev &L)
 
 // ------------------------------------------------------------------ the kernel
 template <typename T, bool Q4, int TGF>
-__global__ void __maxnreg__(112) step_kernel(const StepParams p)
+__global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const Shm S = carve(smem, p, TGF);
