@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -67,6 +68,7 @@ struct pi_ctx {
     int bar_extra = 0;
     unsigned long long *timeline = nullptr;
     int tl_stride = 0;
+    int prefetch = 2, prefetch_ns = 800, cb_max = 1; // tuning, see StepParams
     std::string err;
 };
 
@@ -213,6 +215,9 @@ pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
     p.bar_extra = c->bar_extra;
     p.timeline = c->timeline;
     p.tl_stride = c->tl_stride;
+    p.prefetch = c->prefetch;
+    p.prefetch_ns = c->prefetch_ns;
+    p.cb_max = c->cb_max;
     const pi_layer_desc &d0 = c->layers[l0].desc;
     cudaError_t e;
     if (d0.w_dtype == PI_Q4_0) e = pi::launch_step_q4(p, tgf, c->G, c->stream);
@@ -255,6 +260,10 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     c->max_layers = max_layers;
     c->max_batch = max_batch;
     c->layers.resize(max_layers);
+    // tuning knobs (defaults are the measured best on GB300)
+    if (const char *v = getenv("PI_PREFETCH")) c->prefetch = atoi(v);
+    if (const char *v = getenv("PI_PREFETCH_NS")) c->prefetch_ns = atoi(v);
+    if (const char *v = getenv("PI_CB")) c->cb_max = atoi(v) > 0 ? atoi(v) : 1;
     int coop = 0;
     cudaError_t e = cudaDeviceGetAttribute(&c->G, cudaDevAttrMultiProcessorCount, device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device);
@@ -614,6 +623,15 @@ pi_status pi_debug_set_timeline(pi_ctx *c, uint64_t *stamps, int32_t per_cta)
     if (!c || (stamps && per_cta < 1)) return PI_ERR_ARG;
     c->timeline = (unsigned long long *)stamps;
     c->tl_stride = stamps ? per_cta : 0;
+    return PI_OK;
+}
+
+pi_status pi_debug_set_tuning(pi_ctx *c, int32_t prefetch, int32_t prefetch_ns, int32_t consumer_batch)
+{
+    if (!c || prefetch < 0 || prefetch > 2 || prefetch_ns < 0 || consumer_batch < 1) return PI_ERR_ARG;
+    c->prefetch = prefetch;
+    c->prefetch_ns = prefetch_ns;
+    c->cb_max = consumer_batch;
     return PI_OK;
 }
 

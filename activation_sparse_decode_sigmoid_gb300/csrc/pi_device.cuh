@@ -155,7 +155,7 @@ static __device__ __noinline__ bool grid_sync(const StepParams &p, volatile int 
         int ok = 1;
         const unsigned long long target =
             p.bar_base + (unsigned long long)k * (gridDim.x + (unsigned)p.bar_extra);
-        __threadfence();
+        asm volatile("fence.acq_rel.gpu;" ::: "memory"); // this CTA's writes (bar.sync above) before the arrival
         red_release_gpu_add_u64(p.bar, 1ull);
         if (ld_acquire_gpu_u64(p.bar) < target) {
             const uint64_t t0 = globaltimer();

@@ -85,6 +85,11 @@ struct StepParams {
     unsigned long long wait_ns;
     unsigned long long *timeline; // [G][tl_stride] globaltimer stamps (debug)
     int tl_stride;
+    // tuning: L2 prefetch of the next layer's predictor slice (0 off, 1 all
+    // at once, 2 paced: one 16 KB chunk per prefetch_ns), consumer batch cap
+    int prefetch;
+    int prefetch_ns;
+    int cb_max;
     // shared-memory plan.  The ring region [0, ringB) is time-shared: during
     // the predictor phases it is nss static slots of slotB bytes, during the
     // FFN phase nsd dynamic stages of dslotB bytes.

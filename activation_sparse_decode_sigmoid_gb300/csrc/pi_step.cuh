@@ -148,18 +148,37 @@ static __device__ void drain(uint64_t *full, uint32_t issued, int nslots)
     }
 }
 
-// L2 prefetch of layer l's predictor slice of this CTA (W1 rows, then W2 rows).
-static __device__ void prefetch_predictor(const StepParams &p, int l, uint64_t pol)
+// L2 prefetch of layer l's predictor slice of this CTA (W1 rows, then W2
+// rows).  Mode 1 issues it all at once; mode 2 paces it (one 16 KB chunk per
+// prefetch_ns) so the backlog never queues in front of latency-critical
+// requests (grid-barrier atomics, bitmap reads, the first FFN rows), and stops
+// early once the ring is free for the next layer (the regular loads then
+// fetch the rest).
+static __device__ void prefetch_predictor(const StepParams &p, const Shm &S, int l, int ready_at, uint64_t pol)
 {
     const LayerDev &L = p.layers[l];
     const SliceA A = slice_a(L, p);
     const SliceB Bs = slice_b(L, p);
-    const uint8_t *w1 = (const uint8_t *)L.w1 + (size_t)A.j0 * L.d * 2;
-    const uint8_t *w2 = (const uint8_t *)L.w2 + (size_t)Bs.i0 * L.r * 2;
-    const size_t b1 = (size_t)(A.j1 - A.j0) * L.d * 2, b2 = (size_t)(Bs.i1 - Bs.i0) * L.r * 2;
-    constexpr size_t kChunk = 65536;
-    for (size_t o = 0; o < b1; o += kChunk) bulk_prefetch_l2(w1 + o, (uint32_t)min(kChunk, b1 - o), pol);
-    for (size_t o = 0; o < b2; o += kChunk) bulk_prefetch_l2(w2 + o, (uint32_t)min(kChunk, b2 - o), pol);
+    const uint8_t *seg[2] = {(const uint8_t *)L.w1 + (size_t)A.j0 * L.d * 2,
+                             (const uint8_t *)L.w2 + (size_t)Bs.i0 * L.r * 2};
+    const size_t len[2] = {(size_t)(A.j1 - A.j0) * L.d * 2, (size_t)(Bs.i1 - Bs.i0) * L.r * 2};
+    const size_t chunk = p.prefetch == 1 ? 65536 : 16384;
+    uint64_t t = globaltimer();
+    for (int sgi = 0; sgi < 2; ++sgi) {
+        for (size_t o = 0; o < len[sgi];) {
+            if (p.prefetch == 2) {
+                if (*(volatile int *)(S.info + INFO_REGION) >= ready_at || aborted(p)) return;
+                const uint64_t now = globaltimer();
+                if (now < t) {
+                    __nanosleep(200);
+                    continue;
+                }
+                t = now + (uint64_t)p.prefetch_ns;
+            }
+            bulk_prefetch_l2(seg[sgi] + o, (uint32_t)min(chunk, len[sgi] - o), pol);
+            o += chunk;
+        }
+    }
 }
 
 static __device__ void static_producer(const StepParams &p, const Shm &S)
@@ -200,7 +219,8 @@ static __device__ void static_producer(const StepParams &p, const Shm &S)
         }
         // keep HBM busy through the barriers, the merge and the next layer's
         // first phases: pull the next layer's predictor slice into L2 now
-        if (ok && (p.mode & M_RESID)) prefetch_predictor(p, l + 1 < p.L ? l + 1 : 0, keep);
+        if (ok && (p.mode & M_RESID) && p.prefetch)
+            prefetch_predictor(p, S, l + 1 < p.L ? l + 1 : 0, ffn ? l + 1 : 0x7fffffff, keep);
     }
     drain(S.full_s, s, p.nss);
 }
@@ -616,7 +636,17 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
 // ------------------------------------------------------------------ phase C: gather FFN
 // Thread `tid` owns output columns: 16-bit rows -> chunks of 8 columns
 // ch = tid and tid + 512 (kYSlots = 16 columns); Q4_0 -> half-block hb = tid
-// (16 columns of block hb/2).
+// (16 columns of block hb/2).  Consumers take the ring in batches of `cb`
+// stages: the partial dot products of every neuron of the batch, one named
+// barrier to combine them across warps, then the down-projection rows; the
+// batch's stages are released together.  With single-neuron stages this
+// spreads the fixed per-barrier cost over several neurons while the other
+// stages of the ring keep loading.
+static __device__ __forceinline__ int consumer_batch(int npd, int nsd, int cap)
+{
+    return max(1, min(min(kMaxNeuronsPerStage / npd, nsd / 2), cap));
+}
+
 template <typename T, bool Q4, int TGF>
 static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd, int &rbuf,
                                bool xs_valid)
@@ -628,6 +658,7 @@ static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev
     const int nb = neuron_bytes(L);
     const int npd = neurons_per_stage(L, p);
     const int nst = (ncnt + npd - 1) / npd;
+    const int cb = consumer_batch(npd, p.nsd, p.cb_max);
     const bool reglu = L.gate != nullptr;
     const int ngf = (p.B + p.tg - 1) / p.tg;
     const int nch = d >> 3;     // 16-bit: chunks of 8 columns
@@ -637,175 +668,213 @@ static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev
         const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
         // phase A left the x_hat of a single token group in xs
         if (!(xs_valid && ngf == 1)) stage_xhat<T>(p, S, l, t0, nt);
+        // single-token kernel: this thread's x_hat chunks live in registers
+        uint4 xr[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if constexpr (TGF == 1) {
+            if (!Q4) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int ch = tid + q * kConsumerThreads;
+                    if (ch < nch) xr[q] = *reinterpret_cast<const uint4 *>(S.xs + (size_t)ch * 16);
+                }
+            } else if (tid < nhb) {
+                const uint8_t *xb = S.xs + ((size_t)(tid >> 1) * 32 + (tid & 1) * 16) * 2;
+                xr[0] = *reinterpret_cast<const uint4 *>(xb);
+                xr[1] = *reinterpret_cast<const uint4 *>(xb + 16);
+            }
+        }
         float y[TGF][kYSlots];
 #pragma unroll
         for (int t = 0; t < TGF; ++t)
 #pragma unroll
             for (int e = 0; e < kYSlots; ++e) y[t][e] = 0.f;
 
-        for (int k = 0; k < nst; ++k) {
-            const uint32_t s = sd++;
-            const int slot = s % p.nsd;
-            const bool have = wait_cta(S.full_d + slot, (s / p.nsd) & 1, p, fail_word(S), ok);
-            if (k == 0 && g == 0) mark(p, 1 + l * kTimelineEvents + 8);
-            const uint8_t *stage = S.ring + (size_t)slot * p.dslotB;
-            const int nn = have ? min(npd, ncnt - k * npd) : 0;
+        for (int k0 = 0; k0 < nst; k0 += cb) {
+            const int kb = min(cb, nst - k0);
             float *red = S.red + (size_t)rbuf * kConsumerWarps * kMaxNeuronsPerStage * TGF * 2;
-            // ---- partial dot products of this thread's columns
-            for (int j = 0; j < nn; ++j) {
-                const uint8_t *up = stage + (size_t)j * nb;
-                const uint8_t *gt = up + L.rowB;
-                float au[TGF], ag[TGF];
+            int got = 0; // stages of this batch this thread has seen land
+            // ---- partial dot products of this thread's columns, every neuron of the batch
+            for (int kk = 0; kk < kb; ++kk) {
+                const uint32_t s = sd + kk;
+                const int slot = s % p.nsd;
+                if (!wait_cta(S.full_d + slot, (s / p.nsd) & 1, p, fail_word(S), ok)) break;
+                ++got;
+                if (k0 == 0 && kk == 0 && g == 0) mark(p, 1 + l * kTimelineEvents + 8);
+                const uint8_t *stage = S.ring + (size_t)slot * p.dslotB;
+                const int nn = min(npd, ncnt - (k0 + kk) * npd);
+                for (int j = 0; j < nn; ++j) {
+                    const int jb = kk * npd + j;
+                    const uint8_t *up = stage + (size_t)j * nb;
+                    const uint8_t *gt = up + L.rowB;
+                    float au[TGF], ag[TGF];
 #pragma unroll
-                for (int t = 0; t < TGF; ++t) au[t] = ag[t] = 0.f;
-                if (!Q4) {
+                    for (int t = 0; t < TGF; ++t) au[t] = ag[t] = 0.f;
+                    if (!Q4) {
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int ch = tid + q * kConsumerThreads;
-                        if (ch < nch) {
-                            const uint4 wu = *reinterpret_cast<const uint4 *>(up + (size_t)ch * 16);
-                            uint4 wg = make_uint4(0, 0, 0, 0);
-                            if (reglu) wg = *reinterpret_cast<const uint4 *>(gt + (size_t)ch * 16);
+                        for (int q = 0; q < 2; ++q) {
+                            const int ch = tid + q * kConsumerThreads;
+                            if (ch < nch) {
+                                const uint4 wu = *reinterpret_cast<const uint4 *>(up + (size_t)ch * 16);
+                                uint4 wg = make_uint4(0, 0, 0, 0);
+                                if (reglu) wg = *reinterpret_cast<const uint4 *>(gt + (size_t)ch * 16);
 #pragma unroll
-                            for (int t = 0; t < TGF; ++t) {
-                                if (t < nt) {
-                                    const uint4 xv = *reinterpret_cast<const uint4 *>(S.xs + ((size_t)t * d + ch * 8) * 2);
-                                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                                    const uint32_t uw[4] = {wu.x, wu.y, wu.z, wu.w};
-                                    const uint32_t gw[4] = {wg.x, wg.y, wg.z, wg.w};
+                                for (int t = 0; t < TGF; ++t) {
+                                    if (t < nt) {
+                                        uint4 xv;
+                                        if constexpr (TGF == 1) xv = xr[q];
+                                        else xv = *reinterpret_cast<const uint4 *>(S.xs + ((size_t)t * d + ch * 8) * 2);
+                                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                                        const uint32_t uw[4] = {wu.x, wu.y, wu.z, wu.w};
+                                        const uint32_t gw[4] = {wg.x, wg.y, wg.z, wg.w};
 #pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        const float2 xf = F::pair(xw[e]);
-                                        const float2 uf = F::pair(uw[e]);
-                                        au[t] = fmaf(uf.x, xf.x, au[t]);
-                                        au[t] = fmaf(uf.y, xf.y, au[t]);
-                                        if (reglu) {
-                                            const float2 gf = F::pair(gw[e]);
-                                            ag[t] = fmaf(gf.x, xf.x, ag[t]);
-                                            ag[t] = fmaf(gf.y, xf.y, ag[t]);
+                                        for (int e = 0; e < 4; ++e) {
+                                            const float2 xf = F::pair(xw[e]);
+                                            const float2 uf = F::pair(uw[e]);
+                                            au[t] = fmaf(uf.x, xf.x, au[t]);
+                                            au[t] = fmaf(uf.y, xf.y, au[t]);
+                                            if (reglu) {
+                                                const float2 gf = F::pair(gw[e]);
+                                                ag[t] = fmaf(gf.x, xf.x, ag[t]);
+                                                ag[t] = fmaf(gf.y, xf.y, ag[t]);
+                                            }
                                         }
                                     }
                                 }
                             }
                         }
-                    }
-                } else {
-                    const int hb = tid;
-                    if (hb < nhb) {
-                        const int blk = hb >> 1, half = hb & 1;
-                        const uint4 qv = *reinterpret_cast<const uint4 *>(up + L.scB + (size_t)blk * 16);
-                        const float su = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(up)[blk]));
-                        uint4 qg = make_uint4(0, 0, 0, 0);
-                        float sg = 0.f;
-                        if (reglu) {
-                            qg = *reinterpret_cast<const uint4 *>(gt + L.scB + (size_t)blk * 16);
-                            sg = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(gt)[blk]));
-                        }
-                        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-                        const uint32_t gw[4] = {qg.x, qg.y, qg.z, qg.w};
-                        const int sh = half * 4;
+                    } else {
+                        const int hb = tid;
+                        if (hb < nhb) {
+                            const int blk = hb >> 1, half = hb & 1;
+                            const uint4 qv = *reinterpret_cast<const uint4 *>(up + L.scB + (size_t)blk * 16);
+                            const float su = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(up)[blk]));
+                            uint4 qg = make_uint4(0, 0, 0, 0);
+                            float sg = 0.f;
+                            if (reglu) {
+                                qg = *reinterpret_cast<const uint4 *>(gt + L.scB + (size_t)blk * 16);
+                                sg = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(gt)[blk]));
+                            }
+                            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                            const uint32_t gw[4] = {qg.x, qg.y, qg.z, qg.w};
+                            const int sh = half * 4;
 #pragma unroll
-                        for (int t = 0; t < TGF; ++t) {
-                            if (t < nt) {
-                                const uint8_t *xb = S.xs + ((size_t)t * d + blk * 32 + half * 16) * 2;
-                                const uint4 x0 = *reinterpret_cast<const uint4 *>(xb);
-                                const uint4 x1 = *reinterpret_cast<const uint4 *>(xb + 16);
-                                const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                                float su_acc = 0.f, sg_acc = 0.f;
-#pragma unroll
-                                for (int e = 0; e < 16; e += 2) {
-                                    const float2 xf = F::pair(xw[e >> 1]);
-                                    const int q0 = (int)((qw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8;
-                                    const int q1 = (int)((qw[(e + 1) >> 2] >> (8 * ((e + 1) & 3) + sh)) & 15u) - 8;
-                                    su_acc = fmaf((float)q0, xf.x, su_acc);
-                                    su_acc = fmaf((float)q1, xf.y, su_acc);
-                                    if (reglu) {
-                                        const int g0 = (int)((gw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8;
-                                        const int g1 = (int)((gw[(e + 1) >> 2] >> (8 * ((e + 1) & 3) + sh)) & 15u) - 8;
-                                        sg_acc = fmaf((float)g0, xf.x, sg_acc);
-                                        sg_acc = fmaf((float)g1, xf.y, sg_acc);
+                            for (int t = 0; t < TGF; ++t) {
+                                if (t < nt) {
+                                    uint4 x0, x1;
+                                    if constexpr (TGF == 1) {
+                                        x0 = xr[0];
+                                        x1 = xr[1];
+                                    } else {
+                                        const uint8_t *xb = S.xs + ((size_t)t * d + blk * 32 + half * 16) * 2;
+                                        x0 = *reinterpret_cast<const uint4 *>(xb);
+                                        x1 = *reinterpret_cast<const uint4 *>(xb + 16);
                                     }
+                                    const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                                    float su_acc = 0.f, sg_acc = 0.f;
+#pragma unroll
+                                    for (int e = 0; e < 16; e += 2) {
+                                        const float2 xf = F::pair(xw[e >> 1]);
+                                        const int q0 = (int)((qw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8;
+                                        const int q1 = (int)((qw[(e + 1) >> 2] >> (8 * ((e + 1) & 3) + sh)) & 15u) - 8;
+                                        su_acc = fmaf((float)q0, xf.x, su_acc);
+                                        su_acc = fmaf((float)q1, xf.y, su_acc);
+                                        if (reglu) {
+                                            const int g0 = (int)((gw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8;
+                                            const int g1 = (int)((gw[(e + 1) >> 2] >> (8 * ((e + 1) & 3) + sh)) & 15u) - 8;
+                                            sg_acc = fmaf((float)g0, xf.x, sg_acc);
+                                            sg_acc = fmaf((float)g1, xf.y, sg_acc);
+                                        }
+                                    }
+                                    au[t] = su_acc * su;
+                                    ag[t] = sg_acc * sg;
                                 }
-                                au[t] = su_acc * su;
-                                ag[t] = sg_acc * sg;
                             }
                         }
                     }
-                }
-#pragma unroll
-                for (int t = 0; t < TGF; ++t) {
-#pragma unroll
-                    for (int o = 16; o >= 1; o >>= 1) {
-                        au[t] += __shfl_xor_sync(0xffffffffu, au[t], o);
-                        if (reglu) ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], o);
-                    }
-                }
-                if (lane == 0) {
 #pragma unroll
                     for (int t = 0; t < TGF; ++t) {
-                        red[((warp * kMaxNeuronsPerStage + j) * TGF + t) * 2 + 0] = au[t];
-                        red[((warp * kMaxNeuronsPerStage + j) * TGF + t) * 2 + 1] = ag[t];
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1) {
+                            au[t] += __shfl_xor_sync(0xffffffffu, au[t], o);
+                            if (reglu) ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], o);
+                        }
+                    }
+                    if (lane == 0) {
+#pragma unroll
+                        for (int t = 0; t < TGF; ++t) {
+                            red[((warp * kMaxNeuronsPerStage + jb) * TGF + t) * 2 + 0] = au[t];
+                            red[((warp * kMaxNeuronsPerStage + jb) * TGF + t) * 2 + 1] = ag[t];
+                        }
                     }
                 }
             }
             cons_sync();
             // ---- activations, then the down-projection rows into this thread's columns
-            for (int j = 0; j < nn; ++j) {
-                const int id = S.slist[k * npd + j];
-                if (id < 0) continue;
-                const float bias = S.sbias[k * npd + j];
-                float a[TGF];
+            for (int kk = 0; kk < got; ++kk) {
+                const int slot = (sd + kk) % p.nsd;
+                const uint8_t *stage = S.ring + (size_t)slot * p.dslotB;
+                const int nn = min(npd, ncnt - (k0 + kk) * npd);
+                for (int j = 0; j < nn; ++j) {
+                    const int jb = kk * npd + j;
+                    const int id = S.slist[(k0 + kk) * npd + j];
+                    if (id < 0) continue;
+                    const float bias = S.sbias[(k0 + kk) * npd + j];
+                    float a[TGF];
 #pragma unroll
-                for (int t = 0; t < TGF; ++t) {
-                    float u = 0.f, gsum = 0.f;
-                    for (int w = 0; w < kConsumerWarps; ++w) {
-                        u += red[((w * kMaxNeuronsPerStage + j) * TGF + t) * 2 + 0];
-                        gsum += red[((w * kMaxNeuronsPerStage + j) * TGF + t) * 2 + 1];
+                    for (int t = 0; t < TGF; ++t) {
+                        float u = 0.f, gsum = 0.f;
+#pragma unroll
+                        for (int w = 0; w < kConsumerWarps; ++w) {
+                            u += red[((w * kMaxNeuronsPerStage + jb) * TGF + t) * 2 + 0];
+                            if (reglu) gsum += red[((w * kMaxNeuronsPerStage + jb) * TGF + t) * 2 + 1];
+                        }
+                        if (reglu) a[t] = fmaxf(gsum + bias, 0.f) * u;
+                        else a[t] = fmaxf(u + bias, 0.f);
                     }
-                    if (reglu) a[t] = fmaxf(gsum + bias, 0.f) * u;
-                    else a[t] = fmaxf(u + bias, 0.f);
-                }
-                const uint8_t *dn = stage + (size_t)j * nb + (size_t)(reglu ? 2 : 1) * L.rowB;
-                if (!Q4) {
+                    const uint8_t *dn = stage + (size_t)j * nb + (size_t)(reglu ? 2 : 1) * L.rowB;
+                    if (!Q4) {
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int ch = tid + q * kConsumerThreads;
-                        if (ch < nch) {
-                            const uint4 wv = *reinterpret_cast<const uint4 *>(dn + (size_t)ch * 16);
-                            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+                        for (int q = 0; q < 2; ++q) {
+                            const int ch = tid + q * kConsumerThreads;
+                            if (ch < nch) {
+                                const uint4 wv = *reinterpret_cast<const uint4 *>(dn + (size_t)ch * 16);
+                                const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 wf = F::pair(ww[e]);
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 wf = F::pair(ww[e]);
 #pragma unroll
-                                for (int t = 0; t < TGF; ++t) {
-                                    y[t][q * 8 + 2 * e] = fmaf(a[t], wf.x, y[t][q * 8 + 2 * e]);
-                                    y[t][q * 8 + 2 * e + 1] = fmaf(a[t], wf.y, y[t][q * 8 + 2 * e + 1]);
+                                    for (int t = 0; t < TGF; ++t) {
+                                        y[t][q * 8 + 2 * e] = fmaf(a[t], wf.x, y[t][q * 8 + 2 * e]);
+                                        y[t][q * 8 + 2 * e + 1] = fmaf(a[t], wf.y, y[t][q * 8 + 2 * e + 1]);
+                                    }
                                 }
                             }
                         }
-                    }
-                } else {
-                    const int hb = tid;
-                    if (hb < nhb) {
-                        const int blk = hb >> 1, sh = (hb & 1) * 4;
-                        const uint4 qv = *reinterpret_cast<const uint4 *>(dn + L.scB + (size_t)blk * 16);
-                        const float s = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(dn)[blk]));
-                        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-                        float as[TGF];
+                    } else {
+                        const int hb = tid;
+                        if (hb < nhb) {
+                            const int blk = hb >> 1, sh = (hb & 1) * 4;
+                            const uint4 qv = *reinterpret_cast<const uint4 *>(dn + L.scB + (size_t)blk * 16);
+                            const float s = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(dn)[blk]));
+                            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                            float as[TGF];
 #pragma unroll
-                        for (int t = 0; t < TGF; ++t) as[t] = a[t] * s;
+                            for (int t = 0; t < TGF; ++t) as[t] = a[t] * s;
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float q = (float)((int)((qw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8);
+                            for (int e = 0; e < 16; ++e) {
+                                const float q = (float)((int)((qw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8);
 #pragma unroll
-                            for (int t = 0; t < TGF; ++t) y[t][e] = fmaf(as[t], q, y[t][e]);
+                                for (int t = 0; t < TGF; ++t) y[t][e] = fmaf(as[t], q, y[t][e]);
+                            }
                         }
                     }
                 }
             }
             rbuf ^= 1;
             __syncwarp();
-            if (have && lane == 0) mbar_arrive(S.empty_d + slot);
+            if (lane == 0)
+                for (int kk = 0; kk < got; ++kk) mbar_arrive(S.empty_d + (sd + kk) % p.nsd);
+            sd += kb;
         }
         // ---- this CTA's fp32 partial of the layer output
         for (int t = 0; t < nt; ++t) {

@@ -29,7 +29,8 @@ PI_F16, PI_BF16, PI_Q4_0 = 0, 1, 2
 EXPORTS = ("pi_create", "pi_destroy", "pi_set_stream", "pi_load_layer", "pi_layer_counts",
            "pi_perm_from_counts", "pi_predict", "pi_sparse_ffn", "pi_dense_ffn", "pi_decode_step",
            "pi_dense_step", "pi_set_trace", "pi_sync_status", "pi_last_error", "pi_grid_size",
-           "pi_debug_set_wait_limit", "pi_debug_barrier_extra", "pi_debug_set_timeline")
+           "pi_debug_set_wait_limit", "pi_debug_barrier_extra", "pi_debug_set_timeline",
+           "pi_debug_set_tuning")
 
 
 class PiError(RuntimeError):
@@ -81,6 +82,7 @@ def load_library(path: str = LIB_PATH):
         "pi_debug_set_wait_limit": (st, [P, ctypes.c_uint64]),
         "pi_debug_barrier_extra": (st, [P, I32]),
         "pi_debug_set_timeline": (st, [P, P, I32]),
+        "pi_debug_set_tuning": (st, [P, I32, I32, I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -192,6 +194,11 @@ def pi_debug_set_wait_limit(ctx: int, ns: int) -> None:
 
 def pi_debug_set_timeline(ctx: int, stamps=None, per_cta: int = 0) -> None:
     _check(ctx, load_library().pi_debug_set_timeline(ctx, _ptr(stamps), per_cta), "pi_debug_set_timeline")
+
+
+def pi_debug_set_tuning(ctx: int, prefetch: int, prefetch_ns: int, consumer_batch: int) -> None:
+    rc = load_library().pi_debug_set_tuning(ctx, prefetch, prefetch_ns, consumer_batch)
+    _check(ctx, rc, "pi_debug_set_tuning")
 
 
 def pi_debug_barrier_extra(ctx: int, extra: int) -> None:

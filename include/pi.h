@@ -207,6 +207,13 @@ pi_status pi_debug_barrier_extra(pi_ctx *ctx, int32_t extra);
  * rows landed.  Stamps past per_cta are dropped.  NULL disables. */
 pi_status pi_debug_set_timeline(pi_ctx *ctx, uint64_t *stamps, int32_t per_cta);
 
+/* Tuning knobs of the step kernel (also read from PI_PREFETCH, PI_PREFETCH_NS
+ * and PI_CB at pi_create): prefetch = 0 no L2 prefetch of the next layer's
+ * predictor slice, 1 all at once, 2 paced at one 16 KB chunk per prefetch_ns
+ * per SM; consumer_batch = most ring stages the FFN consumers take per named
+ * barrier.  Results do not depend on them. */
+pi_status pi_debug_set_tuning(pi_ctx *ctx, int32_t prefetch, int32_t prefetch_ns, int32_t consumer_batch);
+
 #ifdef __cplusplus
 }
 #endif
