@@ -30,7 +30,7 @@ EXPORTS = ("pi_create", "pi_destroy", "pi_set_stream", "pi_load_layer", "pi_laye
            "pi_perm_from_counts", "pi_predict", "pi_sparse_ffn", "pi_dense_ffn", "pi_decode_step",
            "pi_dense_step", "pi_set_trace", "pi_sync_status", "pi_last_error", "pi_grid_size",
            "pi_debug_set_wait_limit", "pi_debug_barrier_extra", "pi_debug_set_timeline",
-           "pi_debug_set_tuning")
+           "pi_debug_set_tuning", "pi_sparse_ffn_noalloc")
 
 
 class PiError(RuntimeError):
@@ -42,6 +42,12 @@ class PiError(RuntimeError):
 class pi_layer_desc(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int32), ("d_ffn", ctypes.c_int32), ("rank", ctypes.c_int32),
                 ("act", ctypes.c_int32), ("w_dtype", ctypes.c_int32), ("act_dtype", ctypes.c_int32)]
+
+
+class pi_ffn_rows(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int32), ("d_ffn", ctypes.c_int32), ("act", ctypes.c_int32),
+                ("act_dtype", ctypes.c_int32), ("up", ctypes.c_void_p), ("gate", ctypes.c_void_p),
+                ("down_rows", ctypes.c_void_p), ("b", ctypes.c_void_p), ("b_down", ctypes.c_void_p)]
 
 
 class pi_layer_weights(ctypes.Structure):
@@ -83,6 +89,7 @@ def load_library(path: str = LIB_PATH):
         "pi_debug_barrier_extra": (st, [P, I32]),
         "pi_debug_set_timeline": (st, [P, P, I32]),
         "pi_debug_set_tuning": (st, [P, I32, I32, I32]),
+        "pi_sparse_ffn_noalloc": (st, [ctypes.POINTER(pi_ffn_rows), P, I32, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -155,6 +162,19 @@ def pi_predict(ctx: int, layer: int, x_hat, B: int, idx, count) -> None:
 def pi_sparse_ffn(ctx: int, layer: int, x_hat, B: int, idx, count, y) -> None:
     rc = load_library().pi_sparse_ffn(ctx, layer, _ptr(x_hat), B, _ptr(idx), _ptr(count), _ptr(y))
     _check(ctx, rc, "pi_sparse_ffn")
+
+
+def pi_sparse_ffn_noalloc(rows: pi_ffn_rows, x_hat, B: int, idx, count, y, dev_status=None,
+                          stream: int | None = None) -> int:
+    """Context-free sparse FFN that allocates nothing (for callers that may
+    not call cudaMalloc); scratch lives in a fixed per-GPU array inside the
+    library.  Returns the status instead of raising.  `stream` defaults to
+    torch's current stream."""
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    return load_library().pi_sparse_ffn_noalloc(ctypes.byref(rows), _ptr(x_hat), B, _ptr(idx), _ptr(count),
+                                                 _ptr(y), _ptr(dev_status), stream)
 
 
 def pi_dense_ffn(ctx: int, layer: int, x_hat, B: int, y) -> None:

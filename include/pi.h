@@ -158,6 +158,51 @@ pi_status pi_predict(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t B, i
 pi_status pi_sparse_ffn(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t B, const int32_t *idx,
                         const int32_t *count, void *y);
 
+/* No counterpart on the PowerInfer pages: an addition for callers that may
+ * not allocate device memory.
+ *
+ * pi_sparse_ffn_noalloc computes what pi_sparse_ffn computes, for one layer,
+ * without a context and without allocating anything.  It is meant for code
+ * that only receives pre-allocated buffers, runs under a fixed device-memory
+ * budget, or sits inside a server whose memory pool must not see foreign
+ * allocations -- callers for which pi_create (which allocates its workspace)
+ * is not an option.  The caller passes the layer's rows, the inputs and the
+ * output; the kernel's scratch (fp32 split-K partials, the grid-barrier
+ * counter, status words, a one-layer descriptor, zeros for absent biases)
+ * lives in one 8 MiB array that the library keeps on every GPU that loads it,
+ * until the process exits.
+ *
+ * w: the layer in the library's row layout, all device pointers, original
+ *    neuron order (no permutation):
+ *      up        [n][d]  W_up rows (16-byte aligned)
+ *      gate      [n][d]  W_gate rows, ReGLU only (else NULL)
+ *      down_rows [n][d]  W_down TRANSPOSED: row i = neuron i's output vector
+ *      b [n], b_down [d] may be NULL (= 0)
+ *    act_dtype PI_F16 or PI_BF16 for every tensor (no Q4_0 here);
+ *    d_model in [8, 8192] and a multiple of 8, d_ffn in [1, 65536].
+ * x_hat dev [B][d], idx/count dev int32 as for pi_sparse_ffn, y dev [B][d];
+ * B in [1, 64] and SMs * B * d_model <= 2,063,360 (the partials of every SM
+ * must fit the array: on a 152-SM GB300, B * d_model <= 13,574), else
+ * PI_ERR_SHAPE.  Misaligned pointers give PI_ERR_ARG.
+ * dev_status: optional dev int32, set to 0, then to the first device-side
+ * error (PI_ERR_DEVICE_FLAG for an index or count out of range,
+ * PI_ERR_TIMEOUT); when NULL that word stays inside the array.
+ * stream: cudaStream_t; the call runs on the current device.
+ * The first call on a device resolves and clears the array (module load,
+ * synchronous cudaMemset): make it before any stream capture.  Every call
+ * shares the array and leaves its contents behind; calls whose kernels can
+ * overlap on the GPU (other streams, other host threads) race on it, so
+ * serialise them. */
+typedef struct {
+    int32_t d_model, d_ffn;
+    int32_t act;       /* pi_act */
+    int32_t act_dtype; /* PI_F16 or PI_BF16 */
+    const void *up, *gate, *down_rows, *b, *b_down;
+} pi_ffn_rows;
+
+pi_status pi_sparse_ffn_noalloc(const pi_ffn_rows *w, const void *x_hat, int32_t B, const int32_t *idx,
+                                const int32_t *count, void *y, int32_t *dev_status, void *stream);
+
 /* The same FFN over every neuron (the dense baseline, no predictor). */
 pi_status pi_dense_ffn(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t B, void *y);
 
