@@ -68,7 +68,7 @@ struct pi_ctx {
     int bar_extra = 0;
     unsigned long long *timeline = nullptr;
     int tl_stride = 0;
-    int prefetch = 2, prefetch_ns = 800, cb_max = 1; // tuning, see StepParams
+    int prefetch = 2, prefetch_ns = 800, cb_max = 3; // tuning, see StepParams
     std::string err;
 };
 

@@ -119,6 +119,20 @@ static __device__ __forceinline__ uint64_t policy_evict_first()
     return pol;
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
 // named barrier over the consumer warps only (the producer warps never join)
 static __device__ __forceinline__ void cons_sync()
 {
@@ -218,6 +232,7 @@ static __device__ __forceinline__ bool wait_cta(uint64_t *bar, uint32_t parity, 
                                          bool &ok)
 {
     if (!ok) return false;
+    if (mbar_try_wait(bar, parity)) return true; // fast path, no call
     if (*fail || !mbar_wait(bar, parity, p)) {
         *fail = 1;
         ok = false;

@@ -329,7 +329,15 @@ template <typename T, bool VF, typename Emit>
 static __device__ __forceinline__ void stage_rows(const uint8_t *base, size_t rstride, int nrows, const void *v, int K,
                                                   int lane, Emit emit)
 {
+    // 8 independent row chains at a time (then 4, then 1): the per-row order
+    // is the canonical one, the interleaving only hides latency
     int r = 0;
+    for (; r + 8 <= nrows; r += 8) {
+        float acc[8];
+        cdot_rows<T, 8, VF>(base + (size_t)r * rstride, rstride, v, K, lane, acc);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) emit(r + u, acc[u]);
+    }
     for (; r + 4 <= nrows; r += 4) {
         float acc[4];
         cdot_rows<T, 4, VF>(base + (size_t)r * rstride, rstride, v, K, lane, acc);
@@ -637,21 +645,37 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
 // Thread `tid` owns output columns: 16-bit rows -> chunks of 8 columns
 // ch = tid and tid + 512 (kYSlots = 16 columns); Q4_0 -> half-block hb = tid
 // (16 columns of block hb/2).  Consumers take the ring in batches of `cb`
-// stages: the partial dot products of every neuron of the batch, one named
-// barrier to combine them across warps, then the down-projection rows; the
-// batch's stages are released together.  With single-neuron stages this
-// spreads the fixed per-barrier cost over several neurons while the other
-// stages of the ring keep loading.
+// stages: once the whole batch has landed, the partial dot products of all
+// its neurons are computed side by side (independent chains), one named
+// barrier combines them across warps, then the down-projection rows are
+// accumulated and the batch's stages are released together.
 static __device__ __forceinline__ int consumer_batch(int npd, int nsd, int cap)
 {
     return max(1, min(min(kMaxNeuronsPerStage / npd, nsd / 2), cap));
 }
 
-template <typename T, bool Q4, int TGF>
-static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd, int &rbuf,
-                               bool xs_valid)
+template <typename T>
+static __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8])
 {
     using F = F16T<T>;
+    const float2 a = F::pair(v.x), b = F::pair(v.y), c = F::pair(v.z), d = F::pair(v.w);
+    f[0] = a.x, f[1] = a.y, f[2] = b.x, f[3] = b.y, f[4] = c.x, f[5] = c.y, f[6] = d.x, f[7] = d.y;
+}
+
+// 16 nibbles of a Q4_0 half-block (low nibbles if sh == 0, high if sh == 4) as q - 8
+static __device__ __forceinline__ void unpack_q4(const uint4 v, int sh, float (&f)[16])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 16; ++e) f[e] = (float)((int)((w[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8);
+}
+
+template <typename T, bool Q4, int TGF, bool REGLU>
+static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd,
+                                    int &rbuf, bool xs_valid)
+{
+    using F = F16T<T>;
+    constexpr int NB = TGF == 1 ? 4 : 1; // neurons whose dot products run side by side
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = L.d;
     const int ncnt = S.info[INFO_NCNT];
@@ -659,28 +683,35 @@ static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev
     const int npd = neurons_per_stage(L, p);
     const int nst = (ncnt + npd - 1) / npd;
     const int cb = consumer_batch(npd, p.nsd, p.cb_max);
-    const bool reglu = L.gate != nullptr;
     const int ngf = (p.B + p.tg - 1) / p.tg;
     const int nch = d >> 3;     // 16-bit: chunks of 8 columns
     const int nhb = d >> 4;     // Q4_0: half-blocks of 16 columns
+    const uint32_t rowB = (uint32_t)L.rowB;
+    const uint32_t ring = smem_u32(S.ring);
+    float *act = S.tmp + 64; // [kMaxNeuronsPerStage][TGF] activations of the current batch
     bool ok = true;
+    uint32_t slot = sd % p.nsd, par = (sd / p.nsd) & 1; // ring position of the next stage
     for (int g = 0; g < ngf; ++g) {
         const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
         // phase A left the x_hat of a single token group in xs
         if (!(xs_valid && ngf == 1)) stage_xhat<T>(p, S, l, t0, nt);
-        // single-token kernel: this thread's x_hat chunks live in registers
-        uint4 xr[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        // single-token kernel: this thread's x_hat columns, as fp32, in registers
+        float xf[2][8];
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xf[q][e] = 0.f;
         if constexpr (TGF == 1) {
             if (!Q4) {
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int ch = tid + q * kConsumerThreads;
-                    if (ch < nch) xr[q] = *reinterpret_cast<const uint4 *>(S.xs + (size_t)ch * 16);
+                    if (ch < nch) unpack8<T>(*reinterpret_cast<const uint4 *>(S.xs + (size_t)ch * 16), xf[q]);
                 }
             } else if (tid < nhb) {
                 const uint8_t *xb = S.xs + ((size_t)(tid >> 1) * 32 + (tid & 1) * 16) * 2;
-                xr[0] = *reinterpret_cast<const uint4 *>(xb);
-                xr[1] = *reinterpret_cast<const uint4 *>(xb + 16);
+                unpack8<T>(*reinterpret_cast<const uint4 *>(xb), xf[0]);
+                unpack8<T>(*reinterpret_cast<const uint4 *>(xb + 16), xf[1]);
             }
         }
         float y[TGF][kYSlots];
@@ -692,188 +723,212 @@ static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev
         for (int k0 = 0; k0 < nst; k0 += cb) {
             const int kb = min(cb, nst - k0);
             float *red = S.red + (size_t)rbuf * kConsumerWarps * kMaxNeuronsPerStage * TGF * 2;
-            int got = 0; // stages of this batch this thread has seen land
-            // ---- partial dot products of this thread's columns, every neuron of the batch
-            for (int kk = 0; kk < kb; ++kk) {
-                const uint32_t s = sd + kk;
-                const int slot = s % p.nsd;
-                if (!wait_cta(S.full_d + slot, (s / p.nsd) & 1, p, fail_word(S), ok)) break;
-                ++got;
-                if (k0 == 0 && kk == 0 && g == 0) mark(p, 1 + l * kTimelineEvents + 8);
-                const uint8_t *stage = S.ring + (size_t)slot * p.dslotB;
-                const int nn = min(npd, ncnt - (k0 + kk) * npd);
-                for (int j = 0; j < nn; ++j) {
-                    const int jb = kk * npd + j;
-                    const uint8_t *up = stage + (size_t)j * nb;
-                    const uint8_t *gt = up + L.rowB;
-                    float au[TGF], ag[TGF];
+            // wait for the batch
+            int got = 0;
+            {
+                uint32_t sl = slot, pa = par;
+                for (int kk = 0; kk < kb; ++kk) {
+                    if (!wait_cta(S.full_d + sl, pa, p, fail_word(S), ok)) break;
+                    ++got;
+                    if (++sl == (uint32_t)p.nsd) sl = 0, pa ^= 1;
+                }
+            }
+            const int nnb = min(got * npd, ncnt - k0 * npd); // neurons of the batch in shared memory
+            // walks the batch's neurons in ring order (no division, no indexed array)
+            struct Cursor {
+                uint32_t a, sl;
+                int j;
+            };
+            const auto cur0 = [&]() { return Cursor{ring + slot * (uint32_t)p.dslotB, slot, 0}; };
+            const auto step = [&](Cursor &c) {
+                if (++c.j == npd) {
+                    c.j = 0;
+                    if (++c.sl == (uint32_t)p.nsd) c.sl = 0;
+                    c.a = ring + c.sl * (uint32_t)p.dslotB;
+                }
+            };
+            const auto addr = [&](const Cursor &c) { return c.a + (uint32_t)c.j * (uint32_t)nb; };
+            Cursor cj = cur0();
+            if (k0 == 0 && g == 0 && got) mark(p, 1 + l * kTimelineEvents + 8);
+            // ---- partial dot products of this thread's columns, NB neurons side by side
+            for (int j0 = 0; j0 < nnb; j0 += NB) {
+                uint32_t off[NB]; // compile-time indices only: stays in registers
 #pragma unroll
-                    for (int t = 0; t < TGF; ++t) au[t] = ag[t] = 0.f;
-                    if (!Q4) {
+                for (int u = 0; u < NB; ++u) {
+                    off[u] = addr(cj);
+                    step(cj);
+                }
+                float au[NB][TGF], ag[NB][TGF];
 #pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const int ch = tid + q * kConsumerThreads;
-                            if (ch < nch) {
-                                const uint4 wu = *reinterpret_cast<const uint4 *>(up + (size_t)ch * 16);
-                                uint4 wg = make_uint4(0, 0, 0, 0);
-                                if (reglu) wg = *reinterpret_cast<const uint4 *>(gt + (size_t)ch * 16);
+                for (int u = 0; u < NB; ++u)
 #pragma unroll
-                                for (int t = 0; t < TGF; ++t) {
-                                    if (t < nt) {
-                                        uint4 xv;
-                                        if constexpr (TGF == 1) xv = xr[q];
-                                        else xv = *reinterpret_cast<const uint4 *>(S.xs + ((size_t)t * d + ch * 8) * 2);
-                                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                                        const uint32_t uw[4] = {wu.x, wu.y, wu.z, wu.w};
-                                        const uint32_t gw[4] = {wg.x, wg.y, wg.z, wg.w};
+                    for (int t = 0; t < TGF; ++t) au[u][t] = ag[u][t] = 0.f;
+                if (!Q4) {
 #pragma unroll
-                                        for (int e = 0; e < 4; ++e) {
-                                            const float2 xf = F::pair(xw[e]);
-                                            const float2 uf = F::pair(uw[e]);
-                                            au[t] = fmaf(uf.x, xf.x, au[t]);
-                                            au[t] = fmaf(uf.y, xf.y, au[t]);
-                                            if (reglu) {
-                                                const float2 gf = F::pair(gw[e]);
-                                                ag[t] = fmaf(gf.x, xf.x, ag[t]);
-                                                ag[t] = fmaf(gf.y, xf.y, ag[t]);
+                    for (int q = 0; q < 2; ++q) {
+                        const int ch = tid + q * kConsumerThreads;
+                        if (ch < nch) {
+#pragma unroll
+                            for (int u = 0; u < NB; ++u) {
+                                if (j0 + u < nnb) {
+                                    const uint32_t a = off[u] + (uint32_t)ch * 16;
+                                    float wu[8], wg[8];
+                                    unpack8<T>(ld_shared_v4(a), wu);
+                                    if (REGLU) unpack8<T>(ld_shared_v4(a + rowB), wg);
+#pragma unroll
+                                    for (int t = 0; t < TGF; ++t) {
+                                        if (t < nt) {
+                                            float xv[8];
+                                            if constexpr (TGF == 1) {
+#pragma unroll
+                                                for (int e = 0; e < 8; ++e) xv[e] = xf[q][e];
+                                            } else {
+                                                unpack8<T>(*reinterpret_cast<const uint4 *>(S.xs + ((size_t)t * d + ch * 8) * 2), xv);
+                                            }
+#pragma unroll
+                                            for (int e = 0; e < 8; ++e) {
+                                                au[u][t] = fmaf(wu[e], xv[e], au[u][t]);
+                                                if (REGLU) ag[u][t] = fmaf(wg[e], xv[e], ag[u][t]);
                                             }
                                         }
                                     }
                                 }
                             }
                         }
-                    } else {
-                        const int hb = tid;
-                        if (hb < nhb) {
-                            const int blk = hb >> 1, half = hb & 1;
-                            const uint4 qv = *reinterpret_cast<const uint4 *>(up + L.scB + (size_t)blk * 16);
-                            const float su = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(up)[blk]));
-                            uint4 qg = make_uint4(0, 0, 0, 0);
-                            float sg = 0.f;
-                            if (reglu) {
-                                qg = *reinterpret_cast<const uint4 *>(gt + L.scB + (size_t)blk * 16);
-                                sg = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(gt)[blk]));
-                            }
-                            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-                            const uint32_t gw[4] = {qg.x, qg.y, qg.z, qg.w};
-                            const int sh = half * 4;
+                    }
+                } else {
+                    const int hb = tid;
+                    if (hb < nhb) {
+                        const int blk = hb >> 1, sh = (hb & 1) * 4;
 #pragma unroll
-                            for (int t = 0; t < TGF; ++t) {
-                                if (t < nt) {
-                                    uint4 x0, x1;
-                                    if constexpr (TGF == 1) {
-                                        x0 = xr[0];
-                                        x1 = xr[1];
-                                    } else {
-                                        const uint8_t *xb = S.xs + ((size_t)t * d + blk * 32 + half * 16) * 2;
-                                        x0 = *reinterpret_cast<const uint4 *>(xb);
-                                        x1 = *reinterpret_cast<const uint4 *>(xb + 16);
-                                    }
-                                    const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                                    float su_acc = 0.f, sg_acc = 0.f;
+                        for (int u = 0; u < NB; ++u) {
+                            if (j0 + u < nnb) {
+                                const uint32_t a = off[u];
+                                float qu[16], qg[16];
+                                unpack_q4(ld_shared_v4(a + L.scB + blk * 16), sh, qu);
+                                const float su = __half2float(__ushort_as_half(ld_shared_u16(a + blk * 2)));
+                                float sg = 0.f;
+                                if (REGLU) {
+                                    unpack_q4(ld_shared_v4(a + rowB + L.scB + blk * 16), sh, qg);
+                                    sg = __half2float(__ushort_as_half(ld_shared_u16(a + rowB + blk * 2)));
+                                }
 #pragma unroll
-                                    for (int e = 0; e < 16; e += 2) {
-                                        const float2 xf = F::pair(xw[e >> 1]);
-                                        const int q0 = (int)((qw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8;
-                                        const int q1 = (int)((qw[(e + 1) >> 2] >> (8 * ((e + 1) & 3) + sh)) & 15u) - 8;
-                                        su_acc = fmaf((float)q0, xf.x, su_acc);
-                                        su_acc = fmaf((float)q1, xf.y, su_acc);
-                                        if (reglu) {
-                                            const int g0 = (int)((gw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8;
-                                            const int g1 = (int)((gw[(e + 1) >> 2] >> (8 * ((e + 1) & 3) + sh)) & 15u) - 8;
-                                            sg_acc = fmaf((float)g0, xf.x, sg_acc);
-                                            sg_acc = fmaf((float)g1, xf.y, sg_acc);
+                                for (int t = 0; t < TGF; ++t) {
+                                    if (t < nt) {
+                                        float xv[16];
+                                        if constexpr (TGF == 1) {
+#pragma unroll
+                                            for (int e = 0; e < 8; ++e) xv[e] = xf[0][e], xv[8 + e] = xf[1][e];
+                                        } else {
+                                            const uint8_t *xb = S.xs + ((size_t)t * d + blk * 32 + (hb & 1) * 16) * 2;
+                                            float x0[8], x1[8];
+                                            unpack8<T>(*reinterpret_cast<const uint4 *>(xb), x0);
+                                            unpack8<T>(*reinterpret_cast<const uint4 *>(xb + 16), x1);
+#pragma unroll
+                                            for (int e = 0; e < 8; ++e) xv[e] = x0[e], xv[8 + e] = x1[e];
                                         }
+                                        float s0 = 0.f, s1 = 0.f, g0 = 0.f, g1 = 0.f;
+#pragma unroll
+                                        for (int e = 0; e < 16; e += 2) {
+                                            s0 = fmaf(qu[e], xv[e], s0);
+                                            s1 = fmaf(qu[e + 1], xv[e + 1], s1);
+                                            if (REGLU) {
+                                                g0 = fmaf(qg[e], xv[e], g0);
+                                                g1 = fmaf(qg[e + 1], xv[e + 1], g1);
+                                            }
+                                        }
+                                        au[u][t] = (s0 + s1) * su;
+                                        if (REGLU) ag[u][t] = (g0 + g1) * sg;
                                     }
-                                    au[t] = su_acc * su;
-                                    ag[t] = sg_acc * sg;
                                 }
                             }
                         }
                     }
+                }
 #pragma unroll
-                    for (int t = 0; t < TGF; ++t) {
-#pragma unroll
-                        for (int o = 16; o >= 1; o >>= 1) {
-                            au[t] += __shfl_xor_sync(0xffffffffu, au[t], o);
-                            if (reglu) ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], o);
-                        }
-                    }
-                    if (lane == 0) {
+                for (int u = 0; u < NB; ++u) {
+                    if (j0 + u < nnb) {
 #pragma unroll
                         for (int t = 0; t < TGF; ++t) {
-                            red[((warp * kMaxNeuronsPerStage + jb) * TGF + t) * 2 + 0] = au[t];
-                            red[((warp * kMaxNeuronsPerStage + jb) * TGF + t) * 2 + 1] = ag[t];
+#pragma unroll
+                            for (int o = 16; o >= 1; o >>= 1) {
+                                au[u][t] += __shfl_xor_sync(0xffffffffu, au[u][t], o);
+                                if (REGLU) ag[u][t] += __shfl_xor_sync(0xffffffffu, ag[u][t], o);
+                            }
+                            if (lane == 0) {
+                                red[((warp * kMaxNeuronsPerStage + j0 + u) * TGF + t) * 2 + 0] = au[u][t];
+                                if (REGLU) red[((warp * kMaxNeuronsPerStage + j0 + u) * TGF + t) * 2 + 1] = ag[u][t];
+                            }
                         }
                     }
                 }
             }
             cons_sync();
-            // ---- activations, then the down-projection rows into this thread's columns
-            for (int kk = 0; kk < got; ++kk) {
-                const int slot = (sd + kk) % p.nsd;
-                const uint8_t *stage = S.ring + (size_t)slot * p.dslotB;
-                const int nn = min(npd, ncnt - (k0 + kk) * npd);
-                for (int j = 0; j < nn; ++j) {
-                    const int jb = kk * npd + j;
-                    const int id = S.slist[(k0 + kk) * npd + j];
-                    if (id < 0) continue;
-                    const float bias = S.sbias[(k0 + kk) * npd + j];
-                    float a[TGF];
+            // ---- warp w (< nnb) combines neuron w's 16 partials and applies the activation
+            if (warp < nnb) {
+                const int id = S.slist[k0 * npd + warp];
+                const float bias = S.sbias[k0 * npd + warp];
 #pragma unroll
-                    for (int t = 0; t < TGF; ++t) {
-                        float u = 0.f, gsum = 0.f;
-#pragma unroll
-                        for (int w = 0; w < kConsumerWarps; ++w) {
-                            u += red[((w * kMaxNeuronsPerStage + jb) * TGF + t) * 2 + 0];
-                            if (reglu) gsum += red[((w * kMaxNeuronsPerStage + jb) * TGF + t) * 2 + 1];
-                        }
-                        if (reglu) a[t] = fmaxf(gsum + bias, 0.f) * u;
-                        else a[t] = fmaxf(u + bias, 0.f);
+                for (int t = 0; t < TGF; ++t) {
+                    float u = 0.f, gs = 0.f;
+                    if (lane < kConsumerWarps) {
+                        u = red[((lane * kMaxNeuronsPerStage + warp) * TGF + t) * 2 + 0];
+                        if (REGLU) gs = red[((lane * kMaxNeuronsPerStage + warp) * TGF + t) * 2 + 1];
                     }
-                    const uint8_t *dn = stage + (size_t)j * nb + (size_t)(reglu ? 2 : 1) * L.rowB;
-                    if (!Q4) {
 #pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const int ch = tid + q * kConsumerThreads;
-                            if (ch < nch) {
-                                const uint4 wv = *reinterpret_cast<const uint4 *>(dn + (size_t)ch * 16);
-                                const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+                    for (int o = kConsumerWarps / 2; o >= 1; o >>= 1) {
+                        u += __shfl_xor_sync(0xffffffffu, u, o);
+                        if (REGLU) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+                    }
+                    if (lane == 0) {
+                        const float av = REGLU ? fmaxf(gs + bias, 0.f) * u : fmaxf(u + bias, 0.f);
+                        act[warp * TGF + t] = id >= 0 ? av : 0.f;
+                    }
+                }
+            }
+            cons_sync();
+            // ---- the down-projection rows into this thread's columns
+            Cursor cd = cur0();
+            for (int jb = 0; jb < nnb; ++jb, step(cd)) {
+                float a[TGF];
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 wf = F::pair(ww[e]);
+                for (int t = 0; t < TGF; ++t) a[t] = act[jb * TGF + t];
+                const uint32_t dn = addr(cd) + (REGLU ? 2u : 1u) * rowB;
+                if (!Q4) {
 #pragma unroll
-                                    for (int t = 0; t < TGF; ++t) {
-                                        y[t][q * 8 + 2 * e] = fmaf(a[t], wf.x, y[t][q * 8 + 2 * e]);
-                                        y[t][q * 8 + 2 * e + 1] = fmaf(a[t], wf.y, y[t][q * 8 + 2 * e + 1]);
-                                    }
-                                }
-                            }
+                    for (int q = 0; q < 2; ++q) {
+                        const int ch = tid + q * kConsumerThreads;
+                        if (ch < nch) {
+                            float wf[8];
+                            unpack8<T>(ld_shared_v4(dn + (uint32_t)ch * 16), wf);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+#pragma unroll
+                                for (int t = 0; t < TGF; ++t) y[t][q * 8 + e] = fmaf(a[t], wf[e], y[t][q * 8 + e]);
                         }
-                    } else {
-                        const int hb = tid;
-                        if (hb < nhb) {
-                            const int blk = hb >> 1, sh = (hb & 1) * 4;
-                            const uint4 qv = *reinterpret_cast<const uint4 *>(dn + L.scB + (size_t)blk * 16);
-                            const float s = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(dn)[blk]));
-                            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-                            float as[TGF];
+                    }
+                } else {
+                    const int hb = tid;
+                    if (hb < nhb) {
+                        const int blk = hb >> 1, sh = (hb & 1) * 4;
+                        float qf[16];
+                        unpack_q4(ld_shared_v4(dn + L.scB + blk * 16), sh, qf);
+                        const float s = __half2float(__ushort_as_half(ld_shared_u16(dn + blk * 2)));
 #pragma unroll
-                            for (int t = 0; t < TGF; ++t) as[t] = a[t] * s;
+                        for (int t = 0; t < TGF; ++t) {
+                            const float as = a[t] * s;
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const float q = (float)((int)((qw[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8);
-#pragma unroll
-                                for (int t = 0; t < TGF; ++t) y[t][e] = fmaf(as[t], q, y[t][e]);
-                            }
+                            for (int e = 0; e < 16; ++e) y[t][e] = fmaf(as, qf[e], y[t][e]);
                         }
                     }
                 }
             }
             rbuf ^= 1;
             __syncwarp();
-            if (lane == 0)
-                for (int kk = 0; kk < got; ++kk) mbar_arrive(S.empty_d + (sd + kk) % p.nsd);
+            for (int kk = 0; kk < kb; ++kk) { // release the batch; advance the ring position
+                if (lane == 0 && kk < got) mbar_arrive(S.empty_d + slot);
+                if (++slot == (uint32_t)p.nsd) slot = 0, par ^= 1;
+            }
             sd += kb;
         }
         // ---- this CTA's fp32 partial of the layer output
@@ -912,6 +967,14 @@ static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev
         if (!cons_sync_ok(fail_word(S))) return false; // xs is rewritten by the next group
     }
     return true;
+}
+
+template <typename T, bool Q4, int TGF>
+static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd, int &rbuf,
+                               bool xs_valid)
+{
+    if (L.gate) return phase_c_impl<T, Q4, TGF, true>(p, S, L, l, sd, rbuf, xs_valid);
+    return phase_c_impl<T, Q4, TGF, false>(p, S, L, l, sd, rbuf, xs_valid);
 }
 
 // ------------------------------------------------------------------ phase D: merge
