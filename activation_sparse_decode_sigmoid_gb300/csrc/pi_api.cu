@@ -161,7 +161,7 @@ pi_status plan(pi_ctx *c, StepParams &p, int l0, int L, int B, int mode, int *tg
         const LayerSlot &s = c->layers[l];
         rmax = std::max(rmax, s.desc.rank);
         nmax = std::max(nmax, s.desc.d_ffn);
-        nbmax = std::max(nbmax, (s.desc.act == PI_REGLU ? 3 : 2) * s.dev.rowB);
+        nbmax = std::max(nbmax, s.dev.upB + (s.desc.act == PI_REGLU ? 2 : 1) * s.dev.rowB);
     }
     const bool pred = (mode & (pi::M_PREDICT | pi::M_COUNTS)) != 0;
     const bool ffn = (mode & pi::M_FFN) != 0;
@@ -355,6 +355,8 @@ pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, con
     L.q4 = q4;
     L.rowB = rowB;
     L.scB = scB;
+    L.upB = rowB + 16; // W_up rows carry the neuron's bias in a 16-byte tail
+    L.bias_tail = 1;
     void *pw1 = nullptr, *pb1 = nullptr, *pw2 = nullptr, *pb2 = nullptr, *pup = nullptr, *pgate = nullptr,
          *pdn = nullptr, *pb = nullptr, *pbd = nullptr;
 #define ALLOC(ptr, bytes)                                 \
@@ -369,7 +371,7 @@ pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, con
     ALLOC(pb1, (size_t)r * 2);
     ALLOC(pw2, (size_t)n * r * 2);
     ALLOC(pb2, (size_t)n * 2);
-    ALLOC(pup, (size_t)n * rowB);
+    ALLOC(pup, (size_t)n * (rowB + 16));
     if (reglu) ALLOC(pgate, (size_t)n * rowB);
     ALLOC(pdn, (size_t)n * rowB);
     ALLOC(pb, (size_t)n * 2);
@@ -425,16 +427,17 @@ pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, con
     };
     if (!rc) {
         if (q4) {
-            chk(pi::launch_q4_split((const uint8_t *)s_up, (uint8_t *)pup, dperm, n, d, scB, st0));
+            chk(pi::launch_q4_split((const uint8_t *)s_up, (uint8_t *)pup, dperm, n, d, scB, st0, (size_t)rowB + 16));
             if (reglu) chk(pi::launch_q4_split((const uint8_t *)s_gate, (uint8_t *)pgate, dperm, n, d, scB, st0));
             chk(pi::launch_q4_split((const uint8_t *)s_dn, (uint8_t *)pdn, dperm, n, d, scB, st0));
         } else {
-            chk(pi::launch_permute_rows(s_up, pup, dperm, n, (size_t)rowB, st0));
+            chk(pi::launch_permute_rows(s_up, pup, dperm, n, (size_t)rowB, st0, (size_t)rowB + 16));
             if (reglu) chk(pi::launch_permute_rows(s_gate, pgate, dperm, n, (size_t)rowB, st0));
             chk(pi::launch_transpose_permute16((const uint16_t *)s_dn, (uint16_t *)pdn, dperm, d, n, st0));
         }
         if (s_b) chk(pi::launch_permute16((const uint16_t *)s_b, (uint16_t *)pb, dperm, n, st0));
         else chk(cudaMemsetAsync(pb, 0, (size_t)n * 2, st0));
+        chk(pi::launch_bias_tail((const uint16_t *)pb, (uint8_t *)pup, n, (size_t)rowB, (size_t)rowB + 16, st0));
         chk(cudaMemcpyAsync(pw1, s_w1, (size_t)r * d * 2, cudaMemcpyDeviceToDevice, st0));
         if (s_b1) chk(cudaMemcpyAsync(pb1, s_b1, (size_t)r * 2, cudaMemcpyDeviceToDevice, st0));
         else chk(cudaMemsetAsync(pb1, 0, (size_t)r * 2, st0));

@@ -44,7 +44,9 @@ struct LayerDev {
     int d, n, r, act, q4;
     int rowB;               // bytes of one FFN row (16-bit: 2d; Q4_0: scB + d/2)
     int scB;                // Q4_0: bytes of the scale part of a row (16-byte padded)
-    int pad;
+    int upB;                // bytes of one W_up row in `up`: rowB, or rowB + 16 with the bias tail
+    int bias_tail;          // 1: neuron i's bias (16-bit) sits at up row i + rowB, so it arrives
+                            //    with the row; 0: read from b[]
     const uint16_t *w1;     // [r][d]
     const uint16_t *b1;     // [r]
     const uint16_t *w2;     // [n][r]   rows in physical order
@@ -162,11 +164,12 @@ cudaError_t occupancy_step_bf16(int tgf, int smem_bytes, int *blocks);
 cudaError_t occupancy_step_q4(int tgf, int smem_bytes, int *blocks);
 
 cudaError_t launch_permute_rows(const void *src, void *dst, const int32_t *perm, int rows, size_t rowBytes,
-                                cudaStream_t s);
+                                cudaStream_t s, size_t dstStride = 0);
+cudaError_t launch_bias_tail(const uint16_t *b, uint8_t *up, int n, size_t rowB, size_t upB, cudaStream_t s);
 cudaError_t launch_transpose_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int d, int n,
                                        cudaStream_t s);
 cudaError_t launch_q4_split(const uint8_t *src, uint8_t *dst, const int32_t *perm, int n, int d, int scB,
-                            cudaStream_t s);
+                            cudaStream_t s, size_t dstStride = 0);
 cudaError_t launch_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int n, cudaStream_t s);
 
 } // namespace pi

@@ -16,12 +16,12 @@ namespace pi {
 
 // dst row i = src row perm[i]; rowBytes is a multiple of 16.
 __global__ void permute_rows_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
-                                    const int32_t *__restrict__ perm, int rows, size_t row16)
+                                    const int32_t *__restrict__ perm, int rows, size_t row16, size_t dst16)
 {
     for (int i = blockIdx.x; i < rows; i += gridDim.x) {
         const int o = perm ? perm[i] : i;
         const uint4 *s = src + (size_t)o * row16;
-        uint4 *d = dst + (size_t)i * row16;
+        uint4 *d = dst + (size_t)i * dst16;
         for (size_t k = threadIdx.x; k < row16; k += blockDim.x) d[k] = s[k];
     }
 }
@@ -51,10 +51,9 @@ __global__ void transpose_permute16_kernel(const uint16_t *__restrict__ src, uin
 // Q4_0 rows of 18-byte blocks -> [scales (d/32 fp16, padded to scB bytes)]
 // [nibbles (d/32 x 16 bytes)], rows permuted.  One thread per block.
 __global__ void q4_split_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst,
-                                const int32_t *__restrict__ perm, int n, int nb, int scB)
+                                const int32_t *__restrict__ perm, int n, int nb, int scB, size_t rowB)
 {
     const size_t total = (size_t)n * nb;
-    const size_t rowB = (size_t)scB + (size_t)nb * 16;
     for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < total; k += (size_t)gridDim.x * blockDim.x) {
         const int i = (int)(k / nb), b = (int)(k % nb);
         const int o = perm ? perm[i] : i;
@@ -78,11 +77,30 @@ __global__ void permute16_kernel(const uint16_t *__restrict__ src, uint16_t *__r
 }
 
 cudaError_t launch_permute_rows(const void *src, void *dst, const int32_t *perm, int rows, size_t rowBytes,
-                                cudaStream_t s)
+                                cudaStream_t s, size_t dstStride)
 {
     if (rows <= 0) return cudaSuccess;
     const int grid = rows < 65535 ? rows : 65535;
-    permute_rows_kernel<<<grid, 256, 0, s>>>((const uint4 *)src, (uint4 *)dst, perm, rows, rowBytes / 16);
+    permute_rows_kernel<<<grid, 256, 0, s>>>((const uint4 *)src, (uint4 *)dst, perm, rows, rowBytes / 16,
+                                             (dstStride ? dstStride : rowBytes) / 16);
+    return cudaGetLastError();
+}
+
+// Bias tails: up row i (stride upB) gets b[i] at byte rowB, zeros after it,
+// so a predicted neuron's bias travels with its W_up row.
+__global__ void bias_tail_kernel(const uint16_t *__restrict__ b, uint8_t *__restrict__ up, int n, size_t rowB,
+                                 size_t upB)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        uint4 *t = reinterpret_cast<uint4 *>(up + (size_t)i * upB + rowB);
+        *t = make_uint4((uint32_t)b[i], 0u, 0u, 0u);
+    }
+}
+
+cudaError_t launch_bias_tail(const uint16_t *b, uint8_t *up, int n, size_t rowB, size_t upB, cudaStream_t s)
+{
+    const int grid = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    bias_tail_kernel<<<grid, 256, 0, s>>>(b, up, n, rowB, upB);
     return cudaGetLastError();
 }
 
@@ -95,12 +113,13 @@ cudaError_t launch_transpose_permute16(const uint16_t *src, uint16_t *dst, const
 }
 
 cudaError_t launch_q4_split(const uint8_t *src, uint8_t *dst, const int32_t *perm, int n, int d, int scB,
-                            cudaStream_t s)
+                            cudaStream_t s, size_t dstStride)
 {
     const int nb = d / 32;
     const size_t total = (size_t)n * nb;
     const int grid = (int)((total + 255) / 256 < 65535 ? (total + 255) / 256 : 65535);
-    q4_split_kernel<<<grid, 256, 0, s>>>(src, dst, perm, n, nb, scB);
+    const size_t rowB = (size_t)scB + (size_t)nb * 16;
+    q4_split_kernel<<<grid, 256, 0, s>>>(src, dst, perm, n, nb, scB, dstStride ? dstStride : rowB);
     return cudaGetLastError();
 }
 

@@ -133,6 +133,8 @@ extern "C" pi_status pi_sparse_ffn_noalloc(const pi_ffn_rows *w, const void *x_h
     L.r = 8;
     L.act = w->act;
     L.rowB = rowB;
+    L.upB = rowB;      // the caller's rows have no bias tail: biases are read from b[]
+    L.bias_tail = 0;
     L.up = static_cast<const uint8_t *>(w->up);
     L.gate = w->act == PI_REGLU ? static_cast<const uint8_t *>(w->gate) : nullptr;
     L.dn = static_cast<const uint8_t *>(w->down_rows);

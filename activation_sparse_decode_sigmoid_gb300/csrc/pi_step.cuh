@@ -124,9 +124,10 @@ static __device__ __forceinline__ SliceB slice_b(const LayerDev &L, const StepPa
     return b;
 }
 
+// One neuron in a ring stage: [W_up row (+ bias tail)][W_gate row][W_down^T row].
 static __device__ __forceinline__ int neuron_bytes(const LayerDev &L)
 {
-    return (L.gate ? 3 : 2) * L.rowB;
+    return L.upB + (L.gate ? 2 : 1) * L.rowB;
 }
 
 static __device__ __forceinline__ int neurons_per_stage(const LayerDev &L, const StepParams &p)
@@ -237,7 +238,7 @@ static __device__ void dynamic_producer(const StepParams &p, const Shm &S)
         const int nb = neuron_bytes(L);
         const int npd = neurons_per_stage(L, p);
         const int ngf = (p.B + p.tg - 1) / p.tg;
-        const size_t rowB = (size_t)L.rowB;
+        const size_t rowB = (size_t)L.rowB, upB = (size_t)L.upB;
         bool ok = true;
         for (int g = 0; g < ngf && ok; ++g) {
             for (int k = 0; k < ncnt; k += npd, ++sd) {
@@ -256,8 +257,8 @@ static __device__ void dynamic_producer(const StepParams &p, const Shm &S)
                     const int id = S.slist[k + j];
                     if (id < 0) continue;
                     uint8_t *o = dst + (size_t)j * nb;
-                    bulk_g2s(o, L.up + (size_t)id * rowB, (uint32_t)rowB, S.full_d + slot, pol);
-                    o += rowB;
+                    bulk_g2s(o, L.up + (size_t)id * upB, (uint32_t)upB, S.full_d + slot, pol);
+                    o += upB;
                     if (L.gate) {
                         bulk_g2s(o, L.gate + (size_t)id * rowB, (uint32_t)rowB, S.full_d + slot, pol);
                         o += rowB;
@@ -626,7 +627,8 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
     const int ncnt = s1 - s0;
     for (int k = tid; k < ncnt; k += kConsumerThreads) {
         const int id = S.slist[k];
-        S.sbias[k] = id >= 0 ? F::one(L.b[id]) : 0.f;
+        // with bias tails the bias arrives in the ring stage with the up row
+        if (!L.bias_tail) S.sbias[k] = id >= 0 ? F::one(L.b[id]) : 0.f;
         if (p.idx_out) p.idx_out[s0 + k] = id;
         if (p.tr_idx) p.tr_idx[(size_t)l * p.tr_n + s0 + k] = id;
     }
@@ -687,6 +689,7 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
     const int nch = d >> 3;     // 16-bit: chunks of 8 columns
     const int nhb = d >> 4;     // Q4_0: half-blocks of 16 columns
     const uint32_t rowB = (uint32_t)L.rowB;
+    const uint32_t upB = (uint32_t)L.upB; // offset of the gate row in a neuron
     const uint32_t ring = smem_u32(S.ring);
     float *act = S.tmp + 64; // [kMaxNeuronsPerStage][TGF] activations of the current batch
     bool ok = true;
@@ -720,8 +723,10 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
 #pragma unroll
             for (int e = 0; e < kYSlots; ++e) y[t][e] = 0.f;
 
-        for (int k0 = 0; k0 < nst; k0 += cb) {
-            const int kb = min(cb, nst - k0);
+        // the first batch of a token group takes one stage, so the consumers
+        // start as soon as the first neuron has landed
+        for (int k0 = 0, kb = 0; k0 < nst; k0 += kb) {
+            kb = min(k0 == 0 ? 1 : cb, nst - k0);
             float *red = S.red + (size_t)rbuf * kConsumerWarps * kMaxNeuronsPerStage * TGF * 2;
             // wait for the batch
             int got = 0;
@@ -774,7 +779,7 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
                                     const uint32_t a = off[u] + (uint32_t)ch * 16;
                                     float wu[8], wg[8];
                                     unpack8<T>(ld_shared_v4(a), wu);
-                                    if (REGLU) unpack8<T>(ld_shared_v4(a + rowB), wg);
+                                    if (REGLU) unpack8<T>(ld_shared_v4(a + upB), wg);
 #pragma unroll
                                     for (int t = 0; t < TGF; ++t) {
                                         if (t < nt) {
@@ -809,8 +814,8 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
                                 const float su = __half2float(__ushort_as_half(ld_shared_u16(a + blk * 2)));
                                 float sg = 0.f;
                                 if (REGLU) {
-                                    unpack_q4(ld_shared_v4(a + rowB + L.scB + blk * 16), sh, qg);
-                                    sg = __half2float(__ushort_as_half(ld_shared_u16(a + rowB + blk * 2)));
+                                    unpack_q4(ld_shared_v4(a + upB + L.scB + blk * 16), sh, qg);
+                                    sg = __half2float(__ushort_as_half(ld_shared_u16(a + upB + blk * 2)));
                                 }
 #pragma unroll
                                 for (int t = 0; t < TGF; ++t) {
@@ -867,7 +872,14 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
             // ---- warp w (< nnb) combines neuron w's 16 partials and applies the activation
             if (warp < nnb) {
                 const int id = S.slist[k0 * npd + warp];
-                const float bias = S.sbias[k0 * npd + warp];
+                float bias;
+                if (L.bias_tail) {
+                    Cursor cw = cur0();
+                    for (int j = 0; j < warp; ++j) step(cw);
+                    bias = id >= 0 ? F::one(ld_shared_u16(addr(cw) + rowB)) : 0.f;
+                } else {
+                    bias = S.sbias[k0 * npd + warp];
+                }
 #pragma unroll
                 for (int t = 0; t < TGF; ++t) {
                     float u = 0.f, gs = 0.f;
@@ -893,7 +905,7 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
                 float a[TGF];
 #pragma unroll
                 for (int t = 0; t < TGF; ++t) a[t] = act[jb * TGF + t];
-                const uint32_t dn = addr(cd) + (REGLU ? 2u : 1u) * rowB;
+                const uint32_t dn = addr(cd) + upB + (REGLU ? rowB : 0u);
                 if (!Q4) {
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
@@ -998,13 +1010,30 @@ static __device__ void phase_d(const StepParams &p, const LayerDev &L)
             bd = *reinterpret_cast<const uint2 *>(L.bdown + j);
             if (p.mode & M_RESID) xv = __ldcg(reinterpret_cast<const float4 *>(p.x) + u);
         }
+        // Request the first 32 * kPre partials of the unit before the first
+        // add, so that they cost one L2 round trip instead of one per 32 CTAs;
+        // the sum keeps the order cc = lane, lane + 32, ...
+        constexpr int kPre = 5;
+        float4 v[kPre];
+#pragma unroll
+        for (int i = 0; i < kPre; ++i) {
+            const int cc = lane + 32 * i;
+            v[i] = cc < G ? __ldcg(part + (size_t)cc * stride4 + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int cc = lane; cc < G; cc += 32) {
-            const float4 v = __ldcg(part + (size_t)cc * stride4 + u);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+#pragma unroll
+        for (int i = 0; i < kPre; ++i) {
+            acc.x += v[i].x;
+            acc.y += v[i].y;
+            acc.z += v[i].z;
+            acc.w += v[i].w;
+        }
+        for (int cc = lane + 32 * kPre; cc < G; cc += 32) {
+            const float4 w = __ldcg(part + (size_t)cc * stride4 + u);
+            acc.x += w.x;
+            acc.y += w.y;
+            acc.z += w.z;
+            acc.w += w.w;
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
