@@ -57,6 +57,7 @@ struct pi_ctx {
     float *h = nullptr;
     uint32_t *bitmap = nullptr;
     float *partial = nullptr;
+    float *xstage = nullptr; // [max_batch][kMaxD] residual staging of pi_decode_step_host
     int *ctl = nullptr; // [0..1] grid-barrier counter (u64), [2] status, [3] abort
     unsigned long long bar_base = 0; // counter value the next launch starts from
     // trace
@@ -275,7 +276,7 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     size_t need[] = {sizeof(LayerDev) * (size_t)max_layers,
                      sizeof(float) * (size_t)max_batch * pi::kMaxRank,
                      sizeof(uint32_t) * (size_t)(pi::kMaxN / 32),
-                     sizeof(int) * 64,
+                     sizeof(float) * (size_t)max_batch * pi::kMaxD,
                      sizeof(float) * (size_t)c->G * max_batch * pi::kMaxD,
                      sizeof(int) * 64};
     void *ptrs[6] = {};
@@ -290,7 +291,7 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     c->d_layers = (LayerDev *)ptrs[0];
     c->h = (float *)ptrs[1];
     c->bitmap = (uint32_t *)ptrs[2];
-    cudaFree(ptrs[3]); // (unused slot kept so the allocation list stays aligned with `need`)
+    c->xstage = (float *)ptrs[3];
     c->partial = (float *)ptrs[4];
     c->ctl = (int *)ptrs[5];
     *out = c;
@@ -308,6 +309,7 @@ pi_status pi_destroy(pi_ctx *c)
         cudaFree(c->h);
         cudaFree(c->bitmap);
         cudaFree(c->partial);
+        cudaFree(c->xstage);
         cudaFree(c->ctl);
     }
     delete c;
@@ -571,6 +573,26 @@ static pi_status step_common(pi_ctx *c, float *x, int32_t B, int mode)
 pi_status pi_decode_step(pi_ctx *c, float *x, int32_t B)
 {
     return step_common(c, x, B, pi::M_RMSNORM | pi::M_PREDICT | pi::M_FFN | pi::M_RESID);
+}
+
+pi_status pi_decode_step_host(pi_ctx *c, const float *x_in, float *x_out, int32_t B)
+{
+    if (!c) return PI_ERR_ARG;
+    if (!x_in || !x_out) return fail(c, PI_ERR_ARG, "host buffer NULL");
+    pi_status st = check_batch(c, B);
+    if (st) return st;
+    int L = 0;
+    st = stack_layers(c, &L);
+    if (st) return st;
+    DeviceGuard g(c->device);
+    const size_t bytes = (size_t)B * c->layers[0].desc.d_model * sizeof(float);
+    cudaError_t e = cudaMemcpyAsync(c->xstage, x_in, bytes, cudaMemcpyHostToDevice, c->stream);
+    if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "x to device: %s", cudaGetErrorString(e));
+    st = pi_decode_step(c, c->xstage, B);
+    if (st) return st;
+    e = cudaMemcpyAsync(x_out, c->xstage, bytes, cudaMemcpyDeviceToHost, c->stream);
+    if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "x to host: %s", cudaGetErrorString(e));
+    return pi_sync_status(c);
 }
 
 pi_status pi_dense_step(pi_ctx *c, float *x, int32_t B)

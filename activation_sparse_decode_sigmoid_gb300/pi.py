@@ -28,6 +28,7 @@ PI_F16, PI_BF16, PI_Q4_0 = 0, 1, 2
 # every symbol include/pi.h declares
 EXPORTS = ("pi_create", "pi_destroy", "pi_set_stream", "pi_load_layer", "pi_layer_counts",
            "pi_perm_from_counts", "pi_predict", "pi_sparse_ffn", "pi_dense_ffn", "pi_decode_step",
+           "pi_decode_step_host",
            "pi_dense_step", "pi_set_trace", "pi_sync_status", "pi_last_error", "pi_grid_size",
            "pi_debug_set_wait_limit", "pi_debug_barrier_extra", "pi_debug_set_timeline",
            "pi_debug_set_tuning", "pi_sparse_ffn_noalloc")
@@ -80,6 +81,7 @@ def load_library(path: str = LIB_PATH):
         "pi_sparse_ffn": (st, [P, I32, P, I32, P, P, P]),
         "pi_dense_ffn": (st, [P, I32, P, I32, P]),
         "pi_decode_step": (st, [P, P, I32]),
+        "pi_decode_step_host": (st, [P, P, P, I32]),
         "pi_dense_step": (st, [P, P, I32]),
         "pi_set_trace": (st, [P, P, P, P, P]),
         "pi_sync_status": (st, [P]),
@@ -183,6 +185,11 @@ def pi_dense_ffn(ctx: int, layer: int, x_hat, B: int, y) -> None:
 
 def pi_decode_step(ctx: int, x, B: int) -> None:
     _check(ctx, load_library().pi_decode_step(ctx, _ptr(x), B), "pi_decode_step")
+
+
+def pi_decode_step_host(ctx: int, x_in, x_out, B: int) -> None:
+    """x_in / x_out: host fp32 [B][d] (numpy arrays or CPU tensors, ideally pinned)."""
+    _check(ctx, load_library().pi_decode_step_host(ctx, _ptr(x_in), _ptr(x_out), B), "pi_decode_step_host")
 
 
 def pi_dense_step(ctx: int, x, B: int) -> None:
@@ -327,6 +334,10 @@ class Context:
     def decode_step(self, x) -> None:
         self._s()
         pi_decode_step(self.handle, x, x.shape[0])
+
+    def decode_step_host(self, x_in, x_out) -> None:
+        self._s()
+        pi_decode_step_host(self.handle, x_in, x_out, x_in.shape[0])
 
     def dense_step(self, x) -> None:
         self._s()

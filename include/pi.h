@@ -215,6 +215,15 @@ pi_status pi_dense_ffn(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t B,
  * One persistent kernel runs the whole stack. */
 pi_status pi_decode_step(pi_ctx *ctx, float *x, int32_t B);
 
+/* pi_decode_step on host buffers, for callers whose residual stream lives in
+ * host memory: x_in host fp32 [B][d] is copied to a device staging buffer of
+ * the context, the step runs, the result is copied to x_out (host fp32
+ * [B][d]; may equal x_in) and the stream is synchronised.  Page-locked host
+ * buffers give asynchronous copies; pageable ones work but are staged by the
+ * driver.  Returns the step's status as pi_sync_status would (device-side
+ * errors included), so x_out is valid only on PI_OK. */
+pi_status pi_decode_step_host(pi_ctx *ctx, const float *x_in, float *x_out, int32_t B);
+
 /* The same step with every neuron computed (dense baseline). */
 pi_status pi_dense_step(pi_ctx *ctx, float *x, int32_t B);
 

@@ -195,6 +195,28 @@ def test_decode_stack_teacher_forced(name, B, dense):
     c.close()
 
 
+def test_decode_step_host_buffers_match_device_step():
+    """The host-buffer step (copy in, step, copy out, synchronise) gives the
+    device step's result bit for bit, from pinned and from pageable memory."""
+    t = G.torch()
+    cfg, layer = _layer("relu_f16")
+    c = G.ctx(max_layers=1, max_batch=4)
+    c.load_layer(0, layer)
+    x0 = W.decode_inputs(cfg, 3, 5)
+    xd = t.from_numpy(x0.copy()).cuda()
+    c.decode_step(xd)
+    c.check()
+    want = xd.cpu().numpy()
+    pinned_in = t.from_numpy(x0.copy()).pin_memory()
+    pinned_out = t.empty_like(pinned_in).pin_memory()
+    c.decode_step_host(pinned_in, pinned_out)
+    assert np.array_equal(pinned_out.numpy(), want)
+    pageable = x0.copy()
+    c.decode_step_host(pageable, pageable)  # in place
+    assert np.array_equal(pageable, want)
+    c.close()
+
+
 def test_timeout_is_reported_and_context_recovers():
     """A grid barrier that can never complete (one phantom arrival expected)
     must time out, report PI_ERR_TIMEOUT and leave the context usable."""
