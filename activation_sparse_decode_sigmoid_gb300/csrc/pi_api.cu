@@ -54,8 +54,9 @@ struct pi_ctx {
     std::vector<LayerSlot> layers;
     LayerDev *d_layers = nullptr;
     // workspace
-    float *h = nullptr;
-    uint32_t *bitmap = nullptr;
+    uint64_t *hx = nullptr;  // tagged predictor hidden layer [max_batch][kMaxRank]
+    uint64_t *bmx = nullptr; // tagged mask words [kMaxN / 32]
+    unsigned epoch = 1;      // epoch of the next launch's first layer (0 = never written)
     float *partial = nullptr;
     float *xstage = nullptr; // [max_batch][kMaxD] residual staging of pi_decode_step_host
     int *ctl = nullptr; // [0..1] grid-barrier counter (u64), [2] status, [3] abort
@@ -69,7 +70,7 @@ struct pi_ctx {
     int bar_extra = 0;
     unsigned long long *timeline = nullptr;
     int tl_stride = 0;
-    int prefetch = 2, prefetch_ns = 800, cb_max = 3; // tuning, see StepParams
+    int prefetch = 2, prefetch_ns = 800, cb_max = 3, rows_ahead = 0; // tuning, see StepParams
     std::string err;
 };
 
@@ -205,8 +206,16 @@ pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
     p.layers = c->d_layers + l0;
     p.L = L;
     p.mode = mode;
-    p.h = c->h;
-    p.bitmap = c->bitmap;
+    if (c->epoch > 0xF0000000u - (unsigned)L) {
+        // epochs would wrap: clear every tag so that no stale word can match
+        cudaError_t e = cudaMemsetAsync(c->hx, 0, sizeof(uint64_t) * (size_t)c->max_batch * pi::kMaxRank, c->stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(c->bmx, 0, sizeof(uint64_t) * (size_t)(pi::kMaxN / 32), c->stream);
+        if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "tag reset: %s", cudaGetErrorString(e));
+        c->epoch = 1;
+    }
+    p.hx = c->hx;
+    p.bmx = c->bmx;
+    p.epoch = c->epoch;
     p.partial = c->partial;
     p.bar = reinterpret_cast<unsigned long long *>(c->ctl);
     p.bar_base = c->bar_base;
@@ -219,6 +228,7 @@ pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
     p.prefetch = c->prefetch;
     p.prefetch_ns = c->prefetch_ns;
     p.cb_max = c->cb_max;
+    p.rows_ahead = c->rows_ahead;
     const pi_layer_desc &d0 = c->layers[l0].desc;
     cudaError_t e;
     if (d0.w_dtype == PI_Q4_0) e = pi::launch_step_q4(p, tgf, c->G, c->stream);
@@ -227,6 +237,7 @@ pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
     if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "step kernel launch: %s", cudaGetErrorString(e));
     // every CTA arrives once per grid barrier of the launch
     c->bar_base += (unsigned long long)c->G * (unsigned long long)pi::launch_barriers(mode, L);
+    c->epoch += (unsigned)L;
     return PI_OK;
 }
 
@@ -265,6 +276,7 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     if (const char *v = getenv("PI_PREFETCH")) c->prefetch = atoi(v);
     if (const char *v = getenv("PI_PREFETCH_NS")) c->prefetch_ns = atoi(v);
     if (const char *v = getenv("PI_CB")) c->cb_max = atoi(v) > 0 ? atoi(v) : 1;
+    if (const char *v = getenv("PI_ROWS_AHEAD")) c->rows_ahead = atoi(v) > 0 ? atoi(v) : 0;
     int coop = 0;
     cudaError_t e = cudaDeviceGetAttribute(&c->G, cudaDevAttrMultiProcessorCount, device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device);
@@ -274,14 +286,16 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
         return PI_ERR_CUDA;
     }
     size_t need[] = {sizeof(LayerDev) * (size_t)max_layers,
-                     sizeof(float) * (size_t)max_batch * pi::kMaxRank,
-                     sizeof(uint32_t) * (size_t)(pi::kMaxN / 32),
+                     sizeof(uint64_t) * (size_t)max_batch * pi::kMaxRank,
+                     sizeof(uint64_t) * (size_t)(pi::kMaxN / 32),
                      sizeof(float) * (size_t)max_batch * pi::kMaxD,
                      sizeof(float) * (size_t)c->G * max_batch * pi::kMaxD,
                      sizeof(int) * 64};
     void *ptrs[6] = {};
     for (int i = 0; i < 6 && e == cudaSuccess; ++i) e = cudaMalloc(&ptrs[i], need[i]);
     if (e == cudaSuccess) e = cudaMemset(ptrs[0], 0, need[0]);
+    if (e == cudaSuccess) e = cudaMemset(ptrs[1], 0, need[1]); // epoch 0: never a valid tag
+    if (e == cudaSuccess) e = cudaMemset(ptrs[2], 0, need[2]);
     if (e == cudaSuccess) e = cudaMemset(ptrs[5], 0, need[5]);
     if (e != cudaSuccess) {
         for (void *p : ptrs) cudaFree(p);
@@ -289,8 +303,8 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
         return e == cudaErrorMemoryAllocation ? PI_ERR_OOM : PI_ERR_CUDA;
     }
     c->d_layers = (LayerDev *)ptrs[0];
-    c->h = (float *)ptrs[1];
-    c->bitmap = (uint32_t *)ptrs[2];
+    c->hx = (uint64_t *)ptrs[1];
+    c->bmx = (uint64_t *)ptrs[2];
     c->xstage = (float *)ptrs[3];
     c->partial = (float *)ptrs[4];
     c->ctl = (int *)ptrs[5];
@@ -306,8 +320,8 @@ pi_status pi_destroy(pi_ctx *c)
         cudaStreamSynchronize(c->stream);
         for (LayerSlot &s : c->layers) free_layer(s);
         cudaFree(c->d_layers);
-        cudaFree(c->h);
-        cudaFree(c->bitmap);
+        cudaFree(c->hx);
+        cudaFree(c->bmx);
         cudaFree(c->partial);
         cudaFree(c->xstage);
         cudaFree(c->ctl);
@@ -370,9 +384,9 @@ pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, con
         }                                                 \
     } while (0)
     ALLOC(pw1, (size_t)r * d * 2);
-    ALLOC(pb1, (size_t)r * 2);
+    ALLOC(pb1, (size_t)r * 2 + 32); // + 32: the kernel copies 16-byte-rounded slices
     ALLOC(pw2, (size_t)n * r * 2);
-    ALLOC(pb2, (size_t)n * 2);
+    ALLOC(pb2, (size_t)n * 2 + 32);
     ALLOC(pup, (size_t)n * (rowB + 16));
     if (reglu) ALLOC(pgate, (size_t)n * rowB);
     ALLOC(pdn, (size_t)n * rowB);
@@ -651,13 +665,26 @@ pi_status pi_debug_set_timeline(pi_ctx *c, uint64_t *stamps, int32_t per_cta)
     return PI_OK;
 }
 
-pi_status pi_debug_set_tuning(pi_ctx *c, int32_t prefetch, int32_t prefetch_ns, int32_t consumer_batch)
+pi_status pi_debug_set_tuning(pi_ctx *c, int32_t prefetch, int32_t prefetch_ns, int32_t consumer_batch,
+                              int32_t rows_ahead)
 {
-    if (!c || prefetch < 0 || prefetch > 2 || prefetch_ns < 0 || consumer_batch < 1) return PI_ERR_ARG;
+    if (!c || prefetch < 0 || prefetch > 3 || prefetch_ns < 0 || consumer_batch < 1 || rows_ahead < 0)
+        return PI_ERR_ARG;
     c->prefetch = prefetch;
     c->prefetch_ns = prefetch_ns;
     c->cb_max = consumer_batch;
+    c->rows_ahead = rows_ahead;
     return PI_OK;
+}
+
+pi_status pi_debug_copy_hidden(pi_ctx *c, float *dst, int32_t count)
+{
+    if (!c || !dst || count < 0 || (size_t)count > (size_t)c->max_batch * pi::kMaxRank) return PI_ERR_ARG;
+    DeviceGuard g(c->device);
+    // the values are the low halves of the tagged words
+    const cudaError_t e = cudaMemcpy2DAsync(dst, sizeof(float), c->hx, sizeof(uint64_t), sizeof(float), (size_t)count,
+                                            cudaMemcpyDefault, c->stream);
+    return e == cudaSuccess ? PI_OK : fail(c, PI_ERR_CUDA, "copy of h: %s", cudaGetErrorString(e));
 }
 
 pi_status pi_debug_barrier_extra(pi_ctx *c, int32_t extra)

@@ -90,12 +90,16 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, co
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    for (;;) {
+    // try_wait suspends the warp for a while by itself; the abort flag (an
+    // L2 read) and the clock are looked at every 16th round only
+    for (unsigned it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (aborted(p)) return false;
-        if (globaltimer() - t0 > p.wait_ns) {
-            raise_error(p, PI_DEV_TIMEOUT);
-            return false;
+        if ((it & 15) == 0) {
+            if (aborted(p)) return false;
+            if (globaltimer() - t0 > p.wait_ns) {
+                raise_error(p, PI_DEV_TIMEOUT);
+                return false;
+            }
         }
     }
 }
@@ -117,6 +121,43 @@ static __device__ __forceinline__ uint64_t policy_evict_first()
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
+}
+
+// c + a.lo * b.lo, then + a.hi * b.hi, for two 16-bit values (f16 or bf16)
+// packed in each 32-bit word, with an fp32 accumulator.  The mixed-precision
+// fma of sm_100+ multiplies the exactly widened operands and rounds once, so
+// each step equals fmaf(float(a), float(b), c) and no conversion is issued.
+template <typename T>
+__device__ __forceinline__ float fma_pair(uint32_t a, uint32_t b, float c);
+
+template <>
+__device__ __forceinline__ float fma_pair<__half>(uint32_t a, uint32_t b, float c)
+{
+    asm("{ .reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;"
+        " fma.rn.f32.f16 %0, al, bl, %0; fma.rn.f32.f16 %0, ah, bh, %0; }"
+        : "+f"(c)
+        : "r"(a), "r"(b));
+    return c;
+}
+
+template <>
+__device__ __forceinline__ float fma_pair<__nv_bfloat16>(uint32_t a, uint32_t b, float c)
+{
+    asm("{ .reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;"
+        " fma.rn.f32.bf16 %0, al, bl, %0; fma.rn.f32.bf16 %0, ah, bh, %0; }"
+        : "+f"(c)
+        : "r"(a), "r"(b));
+    return c;
+}
+
+// Eight 16-bit products of a chunk, in element order, onto c.
+template <typename T>
+__device__ __forceinline__ float fma_chunk(const uint4 &w, const uint4 &x, float c)
+{
+    c = fma_pair<T>(w.x, x.x, c);
+    c = fma_pair<T>(w.y, x.y, c);
+    c = fma_pair<T>(w.z, x.z, c);
+    return fma_pair<T>(w.w, x.w, c);
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
@@ -192,12 +233,68 @@ static __device__ __noinline__ bool grid_sync(const StepParams &p, volatile int 
     return *flag != 0;
 }
 
+// ------------------------------------------------------------------ epoch-tagged words
+// A tagged word is one naturally aligned 64-bit store (single-copy atomic):
+// epoch in the high half, the 32-bit value in the low half.  Strong relaxed
+// accesses at gpu scope: the writer needs no fence, the reader sees either
+// the old word or the new one, never a mix.
+__device__ __forceinline__ void st_tagged(uint64_t *a, unsigned epoch, uint32_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(((uint64_t)epoch << 32) | v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t *a)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+    return v;
+}
+
+// Poll (bounded) until the word at `a` carries `epoch`; returns its value.
+// On a timeout or an abort it sets the CTA's failure word and returns 0.
+static __device__ __noinline__ uint32_t wait_tagged(const uint64_t *a, unsigned epoch, const StepParams &p,
+                                                    volatile int *fail)
+{
+    const uint64_t t0 = globaltimer();
+    for (unsigned it = 1;; ++it) {
+        const uint64_t v = ld_tagged(a);
+        if ((unsigned)(v >> 32) == epoch) return (uint32_t)v;
+        if (*fail) return 0;
+        if ((it & 7) == 0) {
+            if (aborted(p)) {
+                *fail = 1;
+                return 0;
+            }
+            if (globaltimer() - t0 > p.wait_ns) {
+                raise_error(p, PI_DEV_TIMEOUT);
+                *fail = 1;
+                return 0;
+            }
+        }
+        __nanosleep(100);
+    }
+}
+
+// Value of a tagged word read earlier, or wait for the expected epoch.
+static __device__ __forceinline__ uint32_t tagged_value(uint64_t v, const uint64_t *a, unsigned epoch,
+                                                        const StepParams &p, volatile int *fail)
+{
+    return (unsigned)(v >> 32) == epoch ? (uint32_t)v : wait_tagged(a, epoch, p, fail);
+}
+
 // Bulk prefetch of [src, src+bytes) into L2 (no shared memory, no completion).
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes, uint64_t policy)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes),
                  "l"(policy)
                  : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
 __device__ __forceinline__ uint64_t policy_evict_last()
@@ -212,12 +309,14 @@ static __device__ __noinline__ bool wait_counter(volatile int *ctr, int target, 
 {
     if (*ctr >= target) return true;
     const uint64_t t0 = globaltimer();
-    for (;;) {
+    for (unsigned it = 1;; ++it) {
         if (*ctr >= target) return true;
-        if (aborted(p)) return false;
-        if (globaltimer() - t0 > p.wait_ns) {
-            raise_error(p, PI_DEV_TIMEOUT);
-            return false;
+        if ((it & 15) == 0) {
+            if (aborted(p)) return false;
+            if (globaltimer() - t0 > p.wait_ns) {
+                raise_error(p, PI_DEV_TIMEOUT);
+                return false;
+            }
         }
         __nanosleep(64);
     }

@@ -70,8 +70,13 @@ struct StepParams {
     uint16_t *y_out;        // [B][d]
     int32_t *counts_out;    // [n]
     // workspace
-    float *h;               // [B][r_max] predictor hidden activations
-    uint32_t *bitmap;       // [ceil(n_max/32)] predicted-mask words (union over tokens)
+    // Cross-SM exchanges that need no grid barrier: every 64-bit word holds
+    // a value (low half) and the epoch of the layer that wrote it (high
+    // half); a reader polls the words themselves until they carry the
+    // epoch it expects, so the data read is also the synchronisation.
+    uint64_t *hx;           // [B][r_max] predictor hidden activations (fp32 bits)
+    uint64_t *bmx;          // [ceil(n_max/32)] predicted-mask words (union over tokens)
+    unsigned epoch;         // epoch of layer 0 of this launch; layer l writes epoch + l
     float *partial;         // [G][B][d] split-K partials of the FFN output
     unsigned long long *bar;// grid barrier: monotonic arrival counter
     unsigned long long bar_base; // counter value when this launch starts
@@ -87,11 +92,16 @@ struct StepParams {
     unsigned long long wait_ns;
     unsigned long long *timeline; // [G][tl_stride] globaltimer stamps (debug)
     int tl_stride;
-    // tuning: L2 prefetch of the next layer's predictor slice (0 off, 1 all
-    // at once, 2 paced: one 16 KB chunk per prefetch_ns), consumer batch cap
+    // tuning: L2 prefetch of the predictor slices (0 off; the next layer's
+    // during phase C: 1 all at once, 2 paced at one 16 KB chunk per
+    // prefetch_ns; 3 this layer's W2 slice as one burst once phase C of the
+    // previous layer is over), consumer batch cap, and how many neurons of the
+    // CTA's list the dynamic producer prefetches into L2 ahead of its ring
+    // loads (0 off)
     int prefetch;
     int prefetch_ns;
     int cb_max;
+    int rows_ahead;
     // shared-memory plan.  The ring region [0, ringB) is time-shared: during
     // the predictor phases it is nss static slots of slotB bytes, during the
     // FFN phase nsd dynamic stages of dslotB bytes.
@@ -115,17 +125,16 @@ __host__ __device__ inline int launch_barriers(int mode, int L)
 {
     const bool pred = (mode & (M_PREDICT | M_COUNTS)) != 0;
     int n = 0;
-    for (int l = 0; l < L; ++l) {
-        if (pred) n += (mode & (M_FFN | M_COMPACT)) ? 2 : 1;
+    (void)pred; // the predictor's exchanges (h, mask words) are epoch-tagged
+    for (int l = 0; l < L; ++l)
         if (mode & M_FFN) n += (l + 1 < L) ? 2 : 1;
-    }
     return n;
 }
 
 // Byte offsets of the small shared-memory objects of the step kernel (the
 // "misc" region).  Computed identically by the host planner and the kernel.
 struct MiscLayout {
-    int bars, info, tmp, slist, sbias, swords, srb, red, total;
+    int bars, info, tmp, slist, sbias, swords, pbias, red, total;
 };
 
 __host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, int wcap, int rcap, int tgf)
@@ -133,7 +142,7 @@ __host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, in
     MiscLayout m;
     int o = 0;
     m.bars = o;
-    o += (2 * nss + 2 * nsd + 2) * 8;
+    o += (2 * nss + 2 * nsd + 3) * 8;
     o = (o + 15) & ~15;
     m.info = o;
     o += 16 * 4;
@@ -145,8 +154,9 @@ __host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, in
     o += lcap * 4;
     m.swords = o;
     o += wcap * 4;
-    m.srb = o;
-    o += rcap * 4;
+    o = (o + 15) & ~15;
+    m.pbias = o; // two 16-bit bias slices (b1, b2), each a 16-byte-rounded copy
+    o += 2 * ((rcap * 2 + 32 + 15) & ~15);
     o = (o + 15) & ~15;
     m.red = o;
     o += 2 * kConsumerWarps * kMaxNeuronsPerStage * tgf * 2 * 4;

@@ -51,7 +51,8 @@ struct Shm {
     int *slist;     // [lcap] this CTA's neuron ids (phase C)
     float *sbias;   // [lcap] their biases
     unsigned *swords; // [wcap] predicted-mask words of this CTA's rows
-    float *srb;     // [rcap] predictor-bias cache of this CTA's rows
+    uint16_t *pb1s, *pb2s; // this CTA's b1 / b2 slices, as copied (16-byte-rounded ranges)
+    uint64_t *bias_full;   // completes when a layer's bias slices have landed
     float *red;     // [2][warps][kMaxNeuronsPerStage][TGF][2] cross-warp dot sums
 };
 
@@ -65,6 +66,8 @@ static __device__ __forceinline__ void mark(const StepParams &p, int ev)
     if (p.timeline && threadIdx.x == 0 && ev < p.tl_stride)
         p.timeline[(size_t)blockIdx.x * p.tl_stride + ev] = globaltimer();
 }
+
+static __device__ __forceinline__ int rcap_bytes(int rcap) { return (rcap * 2 + 32 + 15) & ~15; }
 
 static __device__ __forceinline__ Shm carve(uint8_t *smem, const StepParams &p, int tgf)
 {
@@ -80,12 +83,14 @@ static __device__ __forceinline__ Shm carve(uint8_t *smem, const StepParams &p, 
     s.empty_d = s.full_d + p.nsd;
     s.lst_full = s.empty_d + p.nsd;
     s.lst_free = s.lst_full + 1;
+    s.bias_full = s.lst_free + 1;
     s.info = (int *)(base + m.info);
     s.tmp = (float *)(base + m.tmp);
     s.slist = (int *)(base + m.slist);
     s.sbias = (float *)(base + m.sbias);
     s.swords = (unsigned *)(base + m.swords);
-    s.srb = (float *)(base + m.srb);
+    s.pb1s = (uint16_t *)(base + m.pbias);
+    s.pb2s = s.pb1s + ((rcap_bytes(p.rcap)) >> 1);
     s.red = (float *)(base + m.red);
     return s;
 }
@@ -138,6 +143,22 @@ static __device__ __forceinline__ int neurons_per_stage(const LayerDev &L, const
 // ------------------------------------------------------------------ producers
 // Wait (bounded, ignoring the abort flag) until the copies of the last issued
 // stages have landed, so that no bulk copy is in flight when the CTA exits.
+static __device__ __forceinline__ const uint8_t *down16(const void *a)
+{
+    return reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(a) & ~(uintptr_t)15);
+}
+
+static __device__ __forceinline__ const uint8_t *up16(const void *a)
+{
+    return reinterpret_cast<const uint8_t *>((reinterpret_cast<uintptr_t>(a) + 15) & ~(uintptr_t)15);
+}
+
+// Element offset of a 16-bit array element within its 16-byte-rounded copy.
+static __device__ __forceinline__ int off16(const uint16_t *a)
+{
+    return (int)((reinterpret_cast<uintptr_t>(a) & 15) >> 1);
+}
+
 static __device__ void drain(uint64_t *full, uint32_t issued, int nslots)
 {
     const uint32_t first = issued > (uint32_t)nslots ? issued - nslots : 0;
@@ -187,15 +208,27 @@ static __device__ void static_producer(const StepParams &p, const Shm &S)
     if (!(p.mode & (M_PREDICT | M_COUNTS)) || p.nss == 0) return;
     const uint64_t pol = policy_evict_first();
     const uint64_t keep = policy_evict_last();
+    const uint64_t norm = policy_evict_normal();
     const bool ffn = (p.mode & M_FFN) != 0;
-    uint32_t s = 0;
+    uint32_t s = 0, nbias = 0;
     bool ok = true;
     for (int l = 0; l < p.L && ok; ++l) {
         // the ring holds dynamic stages during phase C of the previous layer
-        if (ffn && l > 0 && !wait_counter(S.info + INFO_REGION, l, p)) break;
+        // (without an FFN phase: the consumers are done with its phase B)
+        if (l > 0 && !wait_counter(S.info + INFO_REGION, l, p)) break;
         const LayerDev &L = p.layers[l];
         const SliceA A = slice_a(L, p);
         const SliceB Bs = slice_b(L, p);
+        {
+            // this CTA's b1 and b2 slices (16-byte-rounded ranges: the
+            // library pads both arrays), off the consumers' critical path
+            const uint8_t *s1 = down16(L.b1 + A.j0), *e1 = up16(L.b1 + A.j1);
+            const uint8_t *s2 = down16(L.b2 + Bs.i0), *e2 = up16(L.b2 + Bs.i1);
+            mbar_arrive_expect_tx(S.bias_full, (uint32_t)((e1 - s1) + (e2 - s2)));
+            if (e1 > s1) bulk_g2s(S.pb1s, s1, (uint32_t)(e1 - s1), S.bias_full, pol);
+            if (e2 > s2) bulk_g2s(S.pb2s, s2, (uint32_t)(e2 - s2), S.bias_full, pol);
+            ++nbias;
+        }
         const int nga = (p.B + p.tg - 1) / p.tg;
         const int ngb = (p.B + p.tgB - 1) / p.tgB;
         for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -205,6 +238,15 @@ static __device__ void static_producer(const StepParams &p, const Shm &S)
             const int rps = pass == 0 ? A.rps : Bs.rps;
             const size_t rowB = pass == 0 ? (size_t)L.d * 2 : (size_t)L.r * 2;
             const uint8_t *src = (const uint8_t *)(pass == 0 ? L.w1 : L.w2);
+            if (pass == 1 && p.prefetch == 3) {
+                // W1's slots are issued; W2's slice (most of it beyond the
+                // ring) streams into L2 while the merge, the barriers and
+                // phase A run, so phase B reads it from L2
+                const uint8_t *w = src + (size_t)lo * rowB;
+                const size_t len = (size_t)(hi - lo) * rowB;
+                for (size_t o = 0; o < len; o += 32768)
+                    bulk_prefetch_l2(w + o, (uint32_t)min((size_t)32768, len - o), norm);
+            }
             for (int g = 0; g < ng && ok; ++g) {
                 for (int row = lo; row < hi; row += rps, ++s) {
                     const int slot = s % p.nss;
@@ -220,16 +262,18 @@ static __device__ void static_producer(const StepParams &p, const Shm &S)
         }
         // keep HBM busy through the barriers, the merge and the next layer's
         // first phases: pull the next layer's predictor slice into L2 now
-        if (ok && (p.mode & M_RESID) && p.prefetch)
+        if (ok && (p.mode & M_RESID) && (p.prefetch == 1 || p.prefetch == 2))
             prefetch_predictor(p, S, l + 1 < p.L ? l + 1 : 0, ffn ? l + 1 : 0x7fffffff, keep);
     }
     drain(S.full_s, s, p.nss);
+    drain(S.bias_full, nbias, 1);
 }
 
 static __device__ void dynamic_producer(const StepParams &p, const Shm &S)
 {
     if (!(p.mode & M_FFN)) return;
     const uint64_t pol = policy_evict_first();
+    const uint64_t norm = policy_evict_normal();
     uint32_t sd = 0;
     for (int l = 0; l < p.L; ++l) {
         if (!mbar_wait(S.lst_full, l & 1, p)) break;
@@ -240,8 +284,21 @@ static __device__ void dynamic_producer(const StepParams &p, const Shm &S)
         const int ngf = (p.B + p.tg - 1) / p.tg;
         const size_t rowB = (size_t)L.rowB, upB = (size_t)L.upB;
         bool ok = true;
+        int pf = 0; // next list position to prefetch into L2
         for (int g = 0; g < ngf && ok; ++g) {
             for (int k = 0; k < ncnt; k += npd, ++sd) {
+                if (g == 0 && p.rows_ahead > 0) {
+                    // keep rows_ahead neurons beyond this stage on their way
+                    // into L2, so HBM streams at full rate however few bytes
+                    // the ring can hold
+                    for (const int lim = min(ncnt, k + npd + p.rows_ahead); pf < lim; ++pf) {
+                        const int id = S.slist[pf];
+                        if (id < 0) continue;
+                        bulk_prefetch_l2(L.up + (size_t)id * upB, (uint32_t)upB, norm);
+                        if (L.gate) bulk_prefetch_l2(L.gate + (size_t)id * rowB, (uint32_t)rowB, norm);
+                        bulk_prefetch_l2(L.dn + (size_t)id * rowB, (uint32_t)rowB, norm);
+                    }
+                }
                 const int slot = sd % p.nsd;
                 if (sd >= (uint32_t)p.nsd && !mbar_wait(S.empty_d + slot, ((sd / p.nsd) - 1) & 1, p)) {
                     ok = false;
@@ -293,35 +350,62 @@ static __device__ __forceinline__ void cdot_rows(const uint8_t *w, size_t rstrid
 #pragma unroll
     for (int r = 0; r < NR; ++r) acc[r] = 0.f;
     const int nch = K >> 3;
-    for (int ch = lane; ch < nch; ch += 32) {
-        float vv[8];
-        if (VF) {
+    if constexpr (!VF) {
+        // 16-bit vector: mixed-precision fma on the raw halves
+        if constexpr (NR == 1) {
+            // one chain: the next chunk's loads are in flight during this one's fmas
+            int ch = lane;
+            if (ch < nch) {
+                uint4 wv = *reinterpret_cast<const uint4 *>(w + (size_t)ch * 16);
+                uint4 xv = *reinterpret_cast<const uint4 *>((const uint8_t *)v + (size_t)ch * 16);
+                for (; ch < nch; ch += 32) {
+                    uint4 wn = wv, xn = xv;
+                    if (ch + 32 < nch) {
+                        wn = *reinterpret_cast<const uint4 *>(w + (size_t)(ch + 32) * 16);
+                        xn = *reinterpret_cast<const uint4 *>((const uint8_t *)v + (size_t)(ch + 32) * 16);
+                    }
+                    acc[0] = fma_chunk<T>(wv, xv, acc[0]);
+                    wv = wn;
+                    xv = xn;
+                }
+            }
+        } else {
+            for (int ch = lane; ch < nch; ch += 32) {
+                const uint4 xv = *reinterpret_cast<const uint4 *>((const uint8_t *)v + (size_t)ch * 16);
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    acc[r] = fma_chunk<T>(*reinterpret_cast<const uint4 *>(w + r * rstride + (size_t)ch * 16), xv,
+                                          acc[r]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) acc[r] = butterfly_sum(acc[r]);
+        return;
+    } else {
+        // fp32 vector (h): the rows are widened, the products and sums are fp32
+        for (int ch = lane; ch < nch; ch += 32) {
             const float4 a = *reinterpret_cast<const float4 *>((const float *)v + (size_t)ch * 8);
             const float4 b = *reinterpret_cast<const float4 *>((const float *)v + (size_t)ch * 8 + 4);
-            vv[0] = a.x, vv[1] = a.y, vv[2] = a.z, vv[3] = a.w, vv[4] = b.x, vv[5] = b.y, vv[6] = b.z, vv[7] = b.w;
-        } else {
-            const uint4 xv = *reinterpret_cast<const uint4 *>((const uint8_t *)v + (size_t)ch * 16);
-            const float2 x0 = F::pair(xv.x), x1 = F::pair(xv.y), x2 = F::pair(xv.z), x3 = F::pair(xv.w);
-            vv[0] = x0.x, vv[1] = x0.y, vv[2] = x1.x, vv[3] = x1.y, vv[4] = x2.x, vv[5] = x2.y, vv[6] = x3.x, vv[7] = x3.y;
+            const float vv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const uint4 wv = *reinterpret_cast<const uint4 *>(w + r * rstride + (size_t)ch * 16);
+                const float2 w0 = F::pair(wv.x), w1 = F::pair(wv.y), w2 = F::pair(wv.z), w3 = F::pair(wv.w);
+                float s = acc[r];
+                s = __fmaf_rn(w0.x, vv[0], s);
+                s = __fmaf_rn(w0.y, vv[1], s);
+                s = __fmaf_rn(w1.x, vv[2], s);
+                s = __fmaf_rn(w1.y, vv[3], s);
+                s = __fmaf_rn(w2.x, vv[4], s);
+                s = __fmaf_rn(w2.y, vv[5], s);
+                s = __fmaf_rn(w3.x, vv[6], s);
+                s = __fmaf_rn(w3.y, vv[7], s);
+                acc[r] = s;
+            }
         }
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-            const uint4 wv = *reinterpret_cast<const uint4 *>(w + r * rstride + (size_t)ch * 16);
-            const float2 w0 = F::pair(wv.x), w1 = F::pair(wv.y), w2 = F::pair(wv.z), w3 = F::pair(wv.w);
-            float a = acc[r];
-            a = __fmaf_rn(w0.x, vv[0], a);
-            a = __fmaf_rn(w0.y, vv[1], a);
-            a = __fmaf_rn(w1.x, vv[2], a);
-            a = __fmaf_rn(w1.y, vv[3], a);
-            a = __fmaf_rn(w2.x, vv[4], a);
-            a = __fmaf_rn(w2.y, vv[5], a);
-            a = __fmaf_rn(w3.x, vv[6], a);
-            a = __fmaf_rn(w3.y, vv[7], a);
-            acc[r] = a;
-        }
+        for (int r = 0; r < NR; ++r) acc[r] = butterfly_sum(acc[r]);
     }
-#pragma unroll
-    for (int r = 0; r < NR; ++r) acc[r] = butterfly_sum(acc[r]);
 }
 
 // Rows [0, nrows) of a static stage (row stride rstride), 4 independent rows
@@ -433,11 +517,12 @@ static __device__ bool phase_a(const StepParams &p, const Shm &S, const LayerDev
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const SliceA A = slice_a(L, p);
     bool ok = true;
-    for (int k = tid; k < A.j1 - A.j0; k += kConsumerThreads) S.srb[k] = F::one(L.b1[A.j0 + k]);
+    const uint16_t *b1s = S.pb1s + off16(L.b1 + A.j0); // b1[A.j0 + k] = b1s[k]
     const int nga = (p.B + p.tg - 1) / p.tg;
     for (int g = 0; g < nga; ++g) {
         const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
-        stage_xhat<T>(p, S, l, t0, nt); // ends with cons_sync (covers srb too)
+        stage_xhat<T>(p, S, l, t0, nt); // ends with cons_sync
+        wait_cta(S.bias_full, l & 1, p, fail_word(S), ok); // landed long ago: the copy is issued a layer ahead
         for (int k = 0; k < A.nst; ++k) {
             const uint32_t s = ss + k;
             const int slot = s % p.nss;
@@ -450,8 +535,9 @@ static __device__ bool phase_a(const StepParams &p, const Shm &S, const LayerDev
                                      [&](int r, float acc) {
                                          if (lane == 0) {
                                              const int j = jr0 + r;
-                                             const float s1 = __fadd_rn(acc, S.srb[j - A.j0]);
-                                             p.h[(size_t)(t0 + t) * L.r + j] = s1 > 0.f ? s1 : 0.f;
+                                             const float s1 = __fadd_rn(acc, F::one(b1s[j - A.j0]));
+                                             st_tagged(p.hx + (size_t)(t0 + t) * L.r + j, p.epoch + l,
+                                                       __float_as_uint(s1 > 0.f ? s1 : 0.f));
                                          }
                                      });
             }
@@ -466,7 +552,7 @@ static __device__ bool phase_a(const StepParams &p, const Shm &S, const LayerDev
 
 // ------------------------------------------------------------------ phase B: z = W2 h + b2 > 0
 template <typename T>
-static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev &L, uint32_t &ss)
+static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &ss)
 {
     using F = F16T<T>;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -474,18 +560,34 @@ static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev
     const int nrows = Bs.i1 - Bs.i0;
     const int nwords = (nrows + 31) >> 5;
     for (int k = tid; k < nwords; k += kConsumerThreads) S.swords[k] = 0u;
-    for (int k = tid; k < nrows; k += kConsumerThreads) S.srb[k] = F::one(L.b2[Bs.i0 + k]);
+    const uint16_t *b2s = S.pb2s + off16(L.b2 + Bs.i0); // b2[Bs.i0 + k] = b2s[k] (landed before phase A)
     float *hs = reinterpret_cast<float *>(S.hs);
     const int ngb = (p.B + p.tgB - 1) / p.tgB;
     bool ok = true;
     for (int g = 0; g < ngb; ++g) {
         const int t0 = g * p.tgB, nt = min(p.tgB, p.B - t0);
-        for (int k = tid; k < nt * L.r / 4; k += kConsumerThreads) {
-            const int t = (4 * k) / L.r, j = (4 * k) % L.r;
-            reinterpret_cast<float4 *>(hs)[k] =
-                __ldcg(reinterpret_cast<const float4 *>(p.h + (size_t)(t0 + t) * L.r + j));
+        // h of the group, straight from the writers' tagged words: the first
+        // read usually finds them all; stale ones are polled until phase A of
+        // every SM has written them
+        {
+            const uint64_t *src = p.hx + (size_t)t0 * L.r;
+            const unsigned ew = p.epoch + l + (unsigned)p.bar_extra;
+            const int nh = nt * L.r;
+            for (int k0 = tid; k0 < nh; k0 += 4 * kConsumerThreads) {
+                uint64_t v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = k0 + u * kConsumerThreads;
+                    v[u] = k < nh ? ld_tagged(src + k) : 0ull;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = k0 + u * kConsumerThreads;
+                    if (k < nh) hs[k] = __uint_as_float(tagged_value(v[u], src + k, ew, p, fail_word(S)));
+                }
+            }
         }
-        cons_sync();
+        if (!cons_sync_ok(fail_word(S))) return false;
         for (int k = 0; k < Bs.nst; ++k) {
             const uint32_t s = ss + k;
             const int slot = s % p.nss;
@@ -499,7 +601,7 @@ static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev
                 for (int t = 0; t < nt; ++t) {
                     stage_rows<T, true>(base + (size_t)r0 * L.r * 2, (size_t)L.r * 2, nrr, hs + (size_t)t * L.r, L.r,
                                         lane, [&](int r, float acc) {
-                                            if (__fadd_rn(acc, S.srb[ir0 + r0 + r - Bs.i0]) > 0.f) {
+                                            if (__fadd_rn(acc, F::one(b2s[ir0 + r0 + r - Bs.i0])) > 0.f) {
                                                 bits |= 1u << r;
                                                 if (lane == 0 && (p.mode & M_COUNTS))
                                                     atomicAdd(p.counts_out + ir0 + r0 + r, 1);
@@ -520,7 +622,7 @@ static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev
         if (!cons_sync_ok(fail_word(S))) return false; // hs is rewritten by the next group
     }
     if (p.mode & M_PREDICT)
-        for (int k = tid; k < nwords; k += kConsumerThreads) p.bitmap[(Bs.i0 >> 5) + k] = S.swords[k];
+        for (int k = tid; k < nwords; k += kConsumerThreads) st_tagged(p.bmx + (Bs.i0 >> 5) + k, p.epoch + l, S.swords[k]);
     return true;
 }
 
@@ -546,13 +648,22 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
         const int nw = (L.n + 31) >> 5;
         const int wpt = (nw + kConsumerThreads - 1) / kConsumerThreads; // <= 4 for n <= 65536
         const int wb = min(nw, tid * wpt), we = min(nw, wb + wpt);
+        // the mask words, straight from the writers' tagged words (phase B
+        // of every SM), polled until all carry this layer's epoch
         unsigned wv[4];
+        {
+            const unsigned ew = p.epoch + l + (unsigned)p.bar_extra;
+            uint64_t raw[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) raw[q] = (wb + q < we) ? ld_tagged(p.bmx + wb + q) : 0ull;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                wv[q] = (wb + q < we) ? tagged_value(raw[q], p.bmx + wb + q, ew, p, fail_word(S)) : 0u;
+        }
+        if (!cons_sync_ok(fail_word(S))) return false;
         int cnt = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            wv[q] = (wb + q < we) ? __ldcg(p.bitmap + wb + q) : 0u;
-            cnt += __popc(wv[q]);
-        }
+        for (int q = 0; q < 4; ++q) cnt += __popc(wv[q]);
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -575,23 +686,27 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
         m = S.info[INFO_M];
         s0 = slice_lo(m, c, G);
         s1 = slice_lo(m, c + 1, G);
-        int pos = wtot[warp] + incl - cnt; // global position of this thread's first set bit
-        if (pos < s1 && pos + cnt > s0) {
+        // Lane-parallel extraction: every word that overlaps [s0, s1) is
+        // broadcast to its warp, lane j ranks bit j by a popcount of the
+        // lower bits and writes it if the rank falls in the slice.
+        int pos = wtot[warp] + incl - cnt; // global rank of this thread's first set bit
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                unsigned b = wv[q];
-                const int pc = __popc(b);
-                if (pos + pc <= s0 || pos >= s1) {
-                    pos += pc;
-                    continue;
-                }
-                while (b) {
-                    const int bit = __ffs(b) - 1;
-                    b &= b - 1;
-                    if (pos >= s0 && pos < s1) S.slist[pos - s0] = 32 * (wb + q) + bit;
-                    ++pos;
+        for (int q = 0; q < 4; ++q) {
+            const int pc = __popc(wv[q]);
+            const bool mine = pc && pos < s1 && pos + pc > s0;
+            unsigned lanes = __ballot_sync(0xffffffffu, mine);
+            while (lanes) {
+                const int src = __ffs(lanes) - 1;
+                lanes &= lanes - 1;
+                const unsigned w = __shfl_sync(0xffffffffu, wv[q], src);
+                const int base = __shfl_sync(0xffffffffu, pos, src);
+                const int widx = __shfl_sync(0xffffffffu, wb + q, src);
+                if ((w >> lane) & 1u) {
+                    const int rank = base + __popc(w & ((1u << lane) - 1u));
+                    if (rank >= s0 && rank < s1) S.slist[rank - s0] = 32 * widx + lane;
                 }
             }
+            pos += pc;
         }
         cons_sync();
     } else {
@@ -1081,6 +1196,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
         }
         mbar_init(S.lst_full, 1);
         mbar_init(S.lst_free, 1);
+        mbar_init(S.bias_full, 1);
         fence_barrier_init();
         S.info[INFO_FAIL] = 0;
         S.info[INFO_REGION] = 0;
@@ -1110,13 +1226,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
         if (pred) {
             if (!phase_a<T>(p, S, L, l, ss)) return;
             mark(p, ev + 0);
-            if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG, nbar)) return;
-            mark(p, ev + 1);
-            if (!phase_b<T>(p, S, L, ss)) return;
+            mark(p, ev + 1); // (no barrier: phase B polls the tagged h)
+            if (!phase_b<T>(p, S, L, l, ss)) return;
             mark(p, ev + 2);
+            // without an FFN phase the static producer may now refill the
+            // bias slices for the next layer
+            if (!(p.mode & M_FFN) && threadIdx.x == 0) atomicAdd(S.info + INFO_REGION, 1);
             if (!(p.mode & (M_FFN | M_COMPACT))) continue;
-            if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG, nbar)) return;
-            mark(p, ev + 3);
+            mark(p, ev + 3); // (no barrier: the list resolution polls the tagged mask words)
         }
         if (p.mode & (M_FFN | M_COMPACT)) {
             if (!resolve_list<T>(p, S, L, l)) return;

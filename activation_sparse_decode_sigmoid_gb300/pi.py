@@ -31,7 +31,7 @@ EXPORTS = ("pi_create", "pi_destroy", "pi_set_stream", "pi_load_layer", "pi_laye
            "pi_decode_step_host",
            "pi_dense_step", "pi_set_trace", "pi_sync_status", "pi_last_error", "pi_grid_size",
            "pi_debug_set_wait_limit", "pi_debug_barrier_extra", "pi_debug_set_timeline",
-           "pi_debug_set_tuning", "pi_sparse_ffn_noalloc")
+           "pi_debug_set_tuning", "pi_debug_copy_hidden", "pi_sparse_ffn_noalloc")
 
 
 class PiError(RuntimeError):
@@ -90,7 +90,8 @@ def load_library(path: str = LIB_PATH):
         "pi_debug_set_wait_limit": (st, [P, ctypes.c_uint64]),
         "pi_debug_barrier_extra": (st, [P, I32]),
         "pi_debug_set_timeline": (st, [P, P, I32]),
-        "pi_debug_set_tuning": (st, [P, I32, I32, I32]),
+        "pi_debug_set_tuning": (st, [P, I32, I32, I32, I32]),
+        "pi_debug_copy_hidden": (st, [P, P, I32]),
         "pi_sparse_ffn_noalloc": (st, [ctypes.POINTER(pi_ffn_rows), P, I32, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -223,9 +224,13 @@ def pi_debug_set_timeline(ctx: int, stamps=None, per_cta: int = 0) -> None:
     _check(ctx, load_library().pi_debug_set_timeline(ctx, _ptr(stamps), per_cta), "pi_debug_set_timeline")
 
 
-def pi_debug_set_tuning(ctx: int, prefetch: int, prefetch_ns: int, consumer_batch: int) -> None:
-    rc = load_library().pi_debug_set_tuning(ctx, prefetch, prefetch_ns, consumer_batch)
+def pi_debug_set_tuning(ctx: int, prefetch: int, prefetch_ns: int, consumer_batch: int, rows_ahead: int = 0) -> None:
+    rc = load_library().pi_debug_set_tuning(ctx, prefetch, prefetch_ns, consumer_batch, rows_ahead)
     _check(ctx, rc, "pi_debug_set_tuning")
+
+
+def pi_debug_copy_hidden(ctx: int, dst, count: int) -> None:
+    _check(ctx, load_library().pi_debug_copy_hidden(ctx, _ptr(dst), count), "pi_debug_copy_hidden")
 
 
 def pi_debug_barrier_extra(ctx: int, extra: int) -> None:

@@ -217,6 +217,46 @@ def test_decode_step_host_buffers_match_device_step():
     c.close()
 
 
+@pytest.mark.parametrize("name", list(CFGS))
+def test_predictor_hidden_layer_bit_exact(c64, name):
+    """h = max(CDOT(W1, x_hat) + b1, 0) of every token equals the oracle's
+    canonical fp32 h bit for bit (the mixed-precision fma of the kernel
+    widens both 16-bit operands exactly and rounds once per step)."""
+    t = G.torch()
+    cfg, layer = _layer(name)
+    c64.load_layer(0, layer)
+    B = 4
+    x = W.xhat_inputs(cfg, B, 17)
+    idx, cnt = c64.predict(0, G.dev16(x))
+    h = t.zeros(B * cfg.r, dtype=t.float32, device="cuda")
+    pi.pi_debug_copy_hidden(c64.handle, h, B * cfg.r)
+    c64.check()
+    want = O.layer_predict(layer, x)["h"].astype(np.float32)
+    got = h.cpu().numpy().reshape(B, cfg.r)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("knobs", [(0, 0, 1, 0), (1, 0, 2, 4), (2, 400, 4, 0), (3, 800, 3, 8), (3, 0, 8, 64)])
+def test_tuning_knobs_do_not_change_results(knobs):
+    """Prefetch modes, consumer batching and row prefetch only move data
+    earlier: a 3-layer decode step is bit-identical under every setting."""
+    t = G.torch()
+    cfg = CFGS["relu_f16"]
+    c = G.ctx(max_layers=3, max_batch=4)
+    for l in range(3):
+        c.load_layer(l, W.make_layer(cfg, l, 0, random_b1=True, random_bdown=True))
+    x0 = t.from_numpy(W.decode_inputs(cfg, 2, 6)).cuda()
+    ref = x0.clone()
+    c.decode_step(ref)
+    c.check()
+    pi.pi_debug_set_tuning(c.handle, *knobs)
+    got = x0.clone()
+    c.decode_step(got)
+    c.check()
+    assert t.equal(got, ref)
+    c.close()
+
+
 def test_timeout_is_reported_and_context_recovers():
     """A grid barrier that can never complete (one phantom arrival expected)
     must time out, report PI_ERR_TIMEOUT and leave the context usable."""
