@@ -57,10 +57,10 @@ struct pi_ctx {
     uint64_t *hx = nullptr;  // tagged predictor hidden layer [max_batch][kMaxRank]
     uint64_t *bmx = nullptr; // tagged mask words [kMaxN / 32]
     unsigned epoch = 1;      // epoch of the next launch's first layer (0 = never written)
-    float *partial = nullptr;
+    uint64_t *partx = nullptr; // tagged split-K partials [G][max_batch][kMaxD]
+    uint64_t *xx = nullptr;    // tagged residual between layers [max_batch][kMaxD]
     float *xstage = nullptr; // [max_batch][kMaxD] residual staging of pi_decode_step_host
     int *ctl = nullptr; // [0..1] grid-barrier counter (u64), [2] status, [3] abort
-    unsigned long long bar_base = 0; // counter value the next launch starts from
     // trace
     float *tr_x = nullptr;
     void *tr_xhat = nullptr;
@@ -208,17 +208,19 @@ pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
     p.mode = mode;
     if (c->epoch > 0xF0000000u - (unsigned)L) {
         // epochs would wrap: clear every tag so that no stale word can match
+        const size_t bd = (size_t)c->max_batch * pi::kMaxD;
         cudaError_t e = cudaMemsetAsync(c->hx, 0, sizeof(uint64_t) * (size_t)c->max_batch * pi::kMaxRank, c->stream);
         if (e == cudaSuccess) e = cudaMemsetAsync(c->bmx, 0, sizeof(uint64_t) * (size_t)(pi::kMaxN / 32), c->stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(c->partx, 0, sizeof(uint64_t) * (size_t)c->G * bd, c->stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(c->xx, 0, sizeof(uint64_t) * bd, c->stream);
         if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "tag reset: %s", cudaGetErrorString(e));
         c->epoch = 1;
     }
     p.hx = c->hx;
     p.bmx = c->bmx;
     p.epoch = c->epoch;
-    p.partial = c->partial;
-    p.bar = reinterpret_cast<unsigned long long *>(c->ctl);
-    p.bar_base = c->bar_base;
+    p.partx = c->partx;
+    p.xx = c->xx;
     p.status = c->ctl + 2;
     p.abort_flag = c->ctl + 3;
     p.wait_ns = c->wait_ns;
@@ -235,9 +237,7 @@ pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
     else if (d0.act_dtype == PI_BF16) e = pi::launch_step_bf16(p, tgf, c->G, c->stream);
     else e = pi::launch_step_f16(p, tgf, c->G, c->stream);
     if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "step kernel launch: %s", cudaGetErrorString(e));
-    // every CTA arrives once per grid barrier of the launch
-    c->bar_base += (unsigned long long)c->G * (unsigned long long)pi::launch_barriers(mode, L);
-    c->epoch += (unsigned)L;
+    c->epoch += (unsigned)L; // the next launch's words can never match this one's
     return PI_OK;
 }
 
@@ -289,14 +289,15 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
                      sizeof(uint64_t) * (size_t)max_batch * pi::kMaxRank,
                      sizeof(uint64_t) * (size_t)(pi::kMaxN / 32),
                      sizeof(float) * (size_t)max_batch * pi::kMaxD,
-                     sizeof(float) * (size_t)c->G * max_batch * pi::kMaxD,
+                     sizeof(uint64_t) * (size_t)c->G * max_batch * pi::kMaxD,
+                     sizeof(uint64_t) * (size_t)max_batch * pi::kMaxD,
                      sizeof(int) * 64};
-    void *ptrs[6] = {};
-    for (int i = 0; i < 6 && e == cudaSuccess; ++i) e = cudaMalloc(&ptrs[i], need[i]);
-    if (e == cudaSuccess) e = cudaMemset(ptrs[0], 0, need[0]);
-    if (e == cudaSuccess) e = cudaMemset(ptrs[1], 0, need[1]); // epoch 0: never a valid tag
-    if (e == cudaSuccess) e = cudaMemset(ptrs[2], 0, need[2]);
-    if (e == cudaSuccess) e = cudaMemset(ptrs[5], 0, need[5]);
+    constexpr int kBufs = (int)(sizeof need / sizeof need[0]);
+    void *ptrs[kBufs] = {};
+    for (int i = 0; i < kBufs && e == cudaSuccess; ++i) e = cudaMalloc(&ptrs[i], need[i]);
+    // zero everything: epoch 0 is never a valid tag
+    for (int i = 0; i < kBufs && e == cudaSuccess; ++i)
+        if (i != 3) e = cudaMemset(ptrs[i], 0, need[i]);
     if (e != cudaSuccess) {
         for (void *p : ptrs) cudaFree(p);
         delete c;
@@ -306,8 +307,9 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     c->hx = (uint64_t *)ptrs[1];
     c->bmx = (uint64_t *)ptrs[2];
     c->xstage = (float *)ptrs[3];
-    c->partial = (float *)ptrs[4];
-    c->ctl = (int *)ptrs[5];
+    c->partx = (uint64_t *)ptrs[4];
+    c->xx = (uint64_t *)ptrs[5];
+    c->ctl = (int *)ptrs[6];
     *out = c;
     return PI_OK;
 }
@@ -322,7 +324,8 @@ pi_status pi_destroy(pi_ctx *c)
         cudaFree(c->d_layers);
         cudaFree(c->hx);
         cudaFree(c->bmx);
-        cudaFree(c->partial);
+        cudaFree(c->partx);
+        cudaFree(c->xx);
         cudaFree(c->xstage);
         cudaFree(c->ctl);
     }
@@ -635,7 +638,6 @@ pi_status pi_sync_status(pi_ctx *c)
     if (ctl[2] != 0 || ctl[3] != 0) {
         // a failed launch leaves the barrier counter wherever its CTAs stopped
         CU(cudaMemset(c->ctl, 0, sizeof(int) * 4));
-        c->bar_base = 0;
         const int code = ctl[2] ? ctl[2] : PI_ERR_TIMEOUT;
         return fail(c, code, code == PI_ERR_TIMEOUT ? "a device-side wait timed out" : "a kernel flagged invalid device data");
     }

@@ -180,59 +180,6 @@ static __device__ __forceinline__ void cons_sync()
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
-// ------------------------------------------------------------------ grid barrier
-__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long *ptr)
-{
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void red_release_gpu_add_u64(unsigned long long *ptr, unsigned long long v)
-{
-    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
-}
-
-// All CTAs of the (co-resident, cooperative) grid meet here.  Called by every
-// consumer thread with the launch-local barrier number k (1, 2, ...); the
-// first consumer thread posts one arrival on a monotonic 64-bit counter and
-// polls it until all G arrivals of barrier k are in (counter >= base + k*G).
-// No reset, no generation word: one release-add and the polls.  `fail` is the
-// CTA's shared failure word (see wait_cta): a CTA that already failed does
-// not arrive.  Returns false when the kernel must unwind.
-static __device__ __noinline__ bool grid_sync(const StepParams &p, volatile int *fail, volatile int *flag,
-                                              int &k)
-{
-    cons_sync();
-    if (*fail) return false;
-    ++k;
-    if (threadIdx.x == 0) {
-        int ok = 1;
-        const unsigned long long target =
-            p.bar_base + (unsigned long long)k * (gridDim.x + (unsigned)p.bar_extra);
-        asm volatile("fence.acq_rel.gpu;" ::: "memory"); // this CTA's writes (bar.sync above) before the arrival
-        red_release_gpu_add_u64(p.bar, 1ull);
-        if (ld_acquire_gpu_u64(p.bar) < target) {
-            const uint64_t t0 = globaltimer();
-            for (unsigned it = 1;; ++it) {
-                if (ld_acquire_gpu_u64(p.bar) >= target) break;
-                if ((it & 63) == 0) {
-                    if (aborted(p)) { ok = 0; break; }
-                    if (globaltimer() - t0 > p.wait_ns) {
-                        raise_error(p, PI_DEV_TIMEOUT);
-                        ok = 0;
-                        break;
-                    }
-                }
-            }
-        }
-        *flag = ok;
-        if (!ok) *fail = 1;
-    }
-    cons_sync();
-    return *flag != 0;
-}
-
 // ------------------------------------------------------------------ epoch-tagged words
 // A tagged word is one naturally aligned 64-bit store (single-copy atomic):
 // epoch in the high half, the 32-bit value in the low half.  Strong relaxed
@@ -250,36 +197,45 @@ __device__ __forceinline__ uint64_t ld_tagged(const uint64_t *a)
     return v;
 }
 
-// Poll (bounded) until the word at `a` carries `epoch`; returns its value.
-// On a timeout or an abort it sets the CTA's failure word and returns 0.
-static __device__ __noinline__ uint32_t wait_tagged(const uint64_t *a, unsigned epoch, const StepParams &p,
-                                                    volatile int *fail)
+// Two adjacent tagged words (a 16-byte aligned), one vector access; each
+// word is still atomic on its own.
+__device__ __forceinline__ void st_tagged2(uint64_t *a, unsigned epoch, uint32_t v0, uint32_t v1)
+{
+    const uint64_t hi = (uint64_t)epoch << 32;
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(a), "l"(hi | v0), "l"(hi | v1) : "memory");
+}
+
+__device__ __forceinline__ void ld_tagged2(const uint64_t *a, uint64_t &v0, uint64_t &v1)
+{
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v0), "=l"(v1) : "l"(a) : "memory");
+}
+
+__device__ __forceinline__ bool tag_is(uint64_t v, unsigned epoch) { return (unsigned)(v >> 32) == epoch; }
+
+// Retry `reload_ok` (re-read a set of tagged words, report whether all carry
+// the expected epoch) until it succeeds, with a short sleep between rounds,
+// for at most the wait limit.  Inline on purpose: the caller's words stay in
+// registers.  On a timeout or an abort it sets the CTA's failure word.
+template <typename F>
+__device__ __forceinline__ bool poll_tags(const StepParams &p, volatile int *fail, F reload_ok)
 {
     const uint64_t t0 = globaltimer();
     for (unsigned it = 1;; ++it) {
-        const uint64_t v = ld_tagged(a);
-        if ((unsigned)(v >> 32) == epoch) return (uint32_t)v;
-        if (*fail) return 0;
+        __nanosleep(100);
+        if (reload_ok()) return true;
+        if (*fail) return false;
         if ((it & 7) == 0) {
             if (aborted(p)) {
                 *fail = 1;
-                return 0;
+                return false;
             }
             if (globaltimer() - t0 > p.wait_ns) {
                 raise_error(p, PI_DEV_TIMEOUT);
                 *fail = 1;
-                return 0;
+                return false;
             }
         }
-        __nanosleep(100);
     }
-}
-
-// Value of a tagged word read earlier, or wait for the expected epoch.
-static __device__ __forceinline__ uint32_t tagged_value(uint64_t v, const uint64_t *a, unsigned epoch,
-                                                        const StepParams &p, volatile int *fail)
-{
-    return (unsigned)(v >> 32) == epoch ? (uint32_t)v : wait_tagged(a, epoch, p, fail);
 }
 
 // Bulk prefetch of [src, src+bytes) into L2 (no shared memory, no completion).

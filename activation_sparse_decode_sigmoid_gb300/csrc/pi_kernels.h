@@ -77,9 +77,8 @@ struct StepParams {
     uint64_t *hx;           // [B][r_max] predictor hidden activations (fp32 bits)
     uint64_t *bmx;          // [ceil(n_max/32)] predicted-mask words (union over tokens)
     unsigned epoch;         // epoch of layer 0 of this launch; layer l writes epoch + l
-    float *partial;         // [G][B][d] split-K partials of the FFN output
-    unsigned long long *bar;// grid barrier: monotonic arrival counter
-    unsigned long long bar_base; // counter value when this launch starts
+    uint64_t *partx;        // [G][B][d] split-K partials of the FFN output (fp32 bits)
+    uint64_t *xx;           // [B][d] the residual after each layer (fp32 bits), read by the next
     int *status;            // first device error
     int *abort_flag;
     // trace
@@ -88,7 +87,7 @@ struct StepParams {
     int32_t *tr_idx;        // [L][tr_n]
     int32_t *tr_cnt;        // [L]
     int tr_n;
-    int bar_extra;
+    int bar_extra;          // test hook: readers expect epoch + bar_extra, which never comes
     unsigned long long wait_ns;
     unsigned long long *timeline; // [G][tl_stride] globaltimer stamps (debug)
     int tl_stride;
@@ -119,17 +118,6 @@ struct StepParams {
     int smem_bytes;
 };
 
-// Number of grid barriers one launch performs (host and kernel agree on it:
-// the host advances the barrier base by G times this after each launch).
-__host__ __device__ inline int launch_barriers(int mode, int L)
-{
-    const bool pred = (mode & (M_PREDICT | M_COUNTS)) != 0;
-    int n = 0;
-    (void)pred; // the predictor's exchanges (h, mask words) are epoch-tagged
-    for (int l = 0; l < L; ++l)
-        if (mode & M_FFN) n += (l + 1 < L) ? 2 : 1;
-    return n;
-}
 
 // Byte offsets of the small shared-memory objects of the step kernel (the
 // "misc" region).  Computed identically by the host planner and the kernel.

@@ -24,13 +24,13 @@
 namespace {
 
 // Byte layout of the static scratch array.
-constexpr size_t kCtlOff = 0;              // u64 barrier counter, int status, int abort
+constexpr size_t kCtlOff = 0;              // (unused u64), int status, int abort
 constexpr size_t kLayerOff = 256;          // one pi::LayerDev
 constexpr size_t kZeroOff = 4096;          // zeros for absent biases (65536 x 16-bit)
 constexpr size_t kZeroBytes = 65536 * 2;
 constexpr size_t kPartialOff = kZeroOff + kZeroBytes;
-constexpr size_t kScratchBytes = 8u << 20; // 8 MiB in total
-constexpr size_t kPartialFloats = (kScratchBytes - kPartialOff) / 4;
+constexpr size_t kScratchBytes = 16u << 20; // 16 MiB in total
+constexpr size_t kPartialWords = (kScratchBytes - kPartialOff) / 8; // epoch-tagged fp32 partials
 
 static_assert(sizeof(pi::LayerDev) <= kZeroOff - kLayerOff, "layer table does not fit its slot");
 
@@ -46,11 +46,12 @@ namespace {
 
 std::mutex g_mu;
 unsigned char *g_ptr[kMaxDevices] = {};
+unsigned g_epoch[kMaxDevices] = {}; // epoch of the last call on each device (the array starts zeroed)
 
 // Device address of the scratch array on the current device.  The first call
 // on a device resolves it (cudaGetSymbolAddress may load the module) and
 // clears the array once; later calls only read the cache.
-cudaError_t noalloc_scratch(int dev, unsigned char **out)
+cudaError_t noalloc_scratch(int dev, unsigned char **out, unsigned *epoch)
 {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_mu);
@@ -63,6 +64,14 @@ cudaError_t noalloc_scratch(int dev, unsigned char **out)
         g_ptr[dev] = static_cast<unsigned char *>(ptr);
     }
     *out = g_ptr[dev];
+    // every call writes its partials under a new epoch, so what earlier
+    // calls left in the array can never be taken for this call's
+    if (++g_epoch[dev] == 0xF0000000u) {
+        const cudaError_t e = cudaMemset(g_ptr[dev], 0, kScratchBytes);
+        if (e != cudaSuccess) return e;
+        g_epoch[dev] = 1;
+    }
+    *epoch = g_epoch[dev];
     return cudaSuccess;
 }
 
@@ -93,9 +102,10 @@ extern "C" pi_status pi_sparse_ffn_noalloc(const pi_ffn_rows *w, const void *x_h
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return PI_ERR_CUDA;
     // the fp32 split-K partials of every SM must fit the fixed scratch
-    if ((size_t)G * B * d > kPartialFloats) return PI_ERR_SHAPE;
+    if ((size_t)G * B * d > kPartialWords) return PI_ERR_SHAPE;
     unsigned char *scratch = nullptr;
-    if (noalloc_scratch(dev, &scratch) != cudaSuccess) return PI_ERR_CUDA;
+    unsigned epoch = 0;
+    if (noalloc_scratch(dev, &scratch, &epoch) != cudaSuccess) return PI_ERR_CUDA;
 
     // shared-memory plan of the FFN-only launch (no predictor phases)
     pi::StepParams p{};
@@ -143,8 +153,8 @@ extern "C" pi_status pi_sparse_ffn_noalloc(const pi_ffn_rows *w, const void *x_h
                         : reinterpret_cast<const uint16_t *>(scratch + kZeroOff);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the array keeps the previous call's contents: clear the barrier counter
-    // and the status words, then publish this call's layer descriptor
+    // the array keeps the previous call's contents: clear the status words,
+    // then publish this call's layer descriptor
     if (cudaMemsetAsync(scratch + kCtlOff, 0, 16, s) != cudaSuccess) return PI_ERR_CUDA;
     if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess) return PI_ERR_CUDA;
     if (cudaMemcpyAsync(scratch + kLayerOff, &L, sizeof L, cudaMemcpyHostToDevice, s) != cudaSuccess)
@@ -155,9 +165,8 @@ extern "C" pi_status pi_sparse_ffn_noalloc(const pi_ffn_rows *w, const void *x_h
     p.idx_in = idx;
     p.count_in = count;
     p.y_out = static_cast<uint16_t *>(y);
-    p.partial = reinterpret_cast<float *>(scratch + kPartialOff);
-    p.bar = reinterpret_cast<unsigned long long *>(scratch + kCtlOff);
-    p.bar_base = 0;
+    p.partx = reinterpret_cast<uint64_t *>(scratch + kPartialOff);
+    p.epoch = epoch;
     p.status = dev_status ? dev_status : reinterpret_cast<int *>(scratch + kCtlOff + 8);
     p.abort_flag = reinterpret_cast<int *>(scratch + kCtlOff + 12);
     p.wait_ns = 2000000000ull;

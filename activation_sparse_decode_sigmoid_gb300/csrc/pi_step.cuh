@@ -24,18 +24,22 @@
 // consumers have finished phase C).
 // Per layer (consumers):
 //   A  x_hat = RMSNorm(x) (or given); h = max(CDOT(W1, x_hat) + b1, 0)  -> global
-//   -- grid barrier --
 //   B  z = CDOT(W2, h) + b2 for this CTA's rows; z > 0 sets a bit of the
 //      CTA's mask words -> global bitmap
-//   -- grid barrier --
 //   C  a prefix scan of the bitmap gives the ascending global list; this CTA
 //      takes an equal share of it, streams those neurons' rows, computes
 //      a = act(W_up x_hat + b ...) and accumulates a * W_down^T rows -> fp32
 //      partial [B][d] of this CTA -> global
-//   -- grid barrier --
 //   D  every CTA reduces a slice of the columns over all partials in a fixed
 //      order and adds the result (+ b_down) into x (or writes y)
-//   -- grid barrier (before the next layer reads x) --
+// Each step reads what every SM wrote in the step before (h, the mask words,
+// the partials, the new x), so each hand-over is all-to-all.  There is no grid
+// barrier: those four hand-overs are 64-bit words carrying the value and the
+// epoch of the layer that wrote it, and the reader polls the words themselves
+// until they carry its epoch (one L2 round trip when the writers are done,
+// instead of a barrier's arrive, poll and then the read).  The all-to-all
+// pattern also orders reuse: no SM can write layer l+1's h, mask, partials or
+// x before every SM has read layer l's.
 #pragma once
 
 #include "pi_device.cuh"
@@ -442,7 +446,7 @@ static __device__ __forceinline__ void stage_rows(const uint8_t *base, size_t rs
 // of the caller's x_hat.  One round trip to L2 per token.  CTA 0 writes the
 // trace.
 template <typename T>
-static __device__ void stage_xhat(const StepParams &p, const Shm &S, int l, int t0, int nt)
+static __device__ bool stage_xhat(const StepParams &p, const Shm &S, int l, int t0, int nt)
 {
     using F = F16T<T>;
     const int d = p.d, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -450,12 +454,46 @@ static __device__ void stage_xhat(const StepParams &p, const Shm &S, int l, int 
     const int n4 = d / 4; // float4 chunks of a row; thread owns k = tid + 512 q, q < 4
     if (p.mode & M_RMSNORM) {
         for (int t = 0; t < nt; ++t) {
-            const float4 *xr = reinterpret_cast<const float4 *>(p.x + (size_t)(t0 + t) * d);
             float4 v[4];
+            if (l == 0) {
+                // the caller's residual, written before the launch
+                const float4 *xr = reinterpret_cast<const float4 *>(p.x + (size_t)(t0 + t) * d);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int k = tid + q * kConsumerThreads;
-                v[q] = k < n4 ? __ldcg(xr + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q = 0; q < 4; ++q) {
+                    const int k = tid + q * kConsumerThreads;
+                    v[q] = k < n4 ? __ldcg(xr + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            } else {
+                // the previous layer's merge output, from its tagged words
+                const uint64_t *xr = p.xx + (size_t)(t0 + t) * d;
+                const unsigned ew = p.epoch + l - 1 + (unsigned)p.bar_extra;
+#pragma unroll
+                for (int h2 = 0; h2 < 4; h2 += 2) { // two float4 per round: fewer live registers
+                    uint64_t w[2][4];
+                    const auto reload_ok = [&]() {
+                        bool good = true;
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const int k = tid + (h2 + q) * kConsumerThreads;
+                            if (k < n4) {
+                                ld_tagged2(xr + 4 * k, w[q][0], w[q][1]);
+                                ld_tagged2(xr + 4 * k + 2, w[q][2], w[q][3]);
+                            } else {
+                                w[q][0] = w[q][1] = w[q][2] = w[q][3] = (uint64_t)ew << 32; // zero-padded
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 2; ++q)
+                            good &= tag_is(w[q][0], ew) & tag_is(w[q][1], ew) & tag_is(w[q][2], ew) &
+                                    tag_is(w[q][3], ew);
+                        return good;
+                    };
+                    if (!reload_ok()) poll_tags(p, fail_word(S), reload_ok);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        v[h2 + q] = make_float4(__uint_as_float((uint32_t)w[q][0]), __uint_as_float((uint32_t)w[q][1]),
+                                                __uint_as_float((uint32_t)w[q][2]), __uint_as_float((uint32_t)w[q][3]));
+                }
             }
             float ss = 0.f;
 #pragma unroll
@@ -467,7 +505,7 @@ static __device__ void stage_xhat(const StepParams &p, const Shm &S, int l, int 
             }
             ss = butterfly_sum(ss);
             if (lane == 0) S.tmp[warp] = ss;
-            cons_sync();
+            if (!cons_sync_ok(fail_word(S))) return false;
             if (tid == 0) {
                 float tot = 0.f;
                 for (int w = 0; w < kConsumerWarps; ++w) tot = __fadd_rn(tot, S.tmp[w]);
@@ -504,6 +542,7 @@ static __device__ void stage_xhat(const StepParams &p, const Shm &S, int l, int 
             for (int k = tid; k < d / 8; k += kConsumerThreads) dst[k] = src[k];
         }
     }
+    return true;
 }
 
 // ------------------------------------------------------------------ phase A: h = relu(W1 x_hat + b1)
@@ -521,7 +560,7 @@ static __device__ bool phase_a(const StepParams &p, const Shm &S, const LayerDev
     const int nga = (p.B + p.tg - 1) / p.tg;
     for (int g = 0; g < nga; ++g) {
         const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
-        stage_xhat<T>(p, S, l, t0, nt); // ends with cons_sync
+        if (!stage_xhat<T>(p, S, l, t0, nt)) return false; // ends with cons_sync
         wait_cta(S.bias_full, l & 1, p, fail_word(S), ok); // landed long ago: the copy is issued a layer ahead
         for (int k = 0; k < A.nst; ++k) {
             const uint32_t s = ss + k;
@@ -575,15 +614,22 @@ static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev
             const int nh = nt * L.r;
             for (int k0 = tid; k0 < nh; k0 += 4 * kConsumerThreads) {
                 uint64_t v[4];
+                const auto reload_ok = [&]() {
+                    bool good = true;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int k = k0 + u * kConsumerThreads;
+                        v[u] = k < nh ? ld_tagged(src + k) : ((uint64_t)ew << 32);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) good &= tag_is(v[u], ew);
+                    return good;
+                };
+                if (!reload_ok() && !poll_tags(p, fail_word(S), reload_ok)) break;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int k = k0 + u * kConsumerThreads;
-                    v[u] = k < nh ? ld_tagged(src + k) : 0ull;
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int k = k0 + u * kConsumerThreads;
-                    if (k < nh) hs[k] = __uint_as_float(tagged_value(v[u], src + k, ew, p, fail_word(S)));
+                    if (k < nh) hs[k] = __uint_as_float((uint32_t)v[u]);
                 }
             }
         }
@@ -654,11 +700,17 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
         {
             const unsigned ew = p.epoch + l + (unsigned)p.bar_extra;
             uint64_t raw[4];
+            const auto reload_ok = [&]() {
+                bool good = true;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) raw[q] = (wb + q < we) ? ld_tagged(p.bmx + wb + q) : 0ull;
+                for (int q = 0; q < 4; ++q) raw[q] = (wb + q < we) ? ld_tagged(p.bmx + wb + q) : ((uint64_t)ew << 32);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                wv[q] = (wb + q < we) ? tagged_value(raw[q], p.bmx + wb + q, ew, p, fail_word(S)) : 0u;
+                for (int q = 0; q < 4; ++q) good &= tag_is(raw[q], ew);
+                return good;
+            };
+            if (!reload_ok()) poll_tags(p, fail_word(S), reload_ok);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) wv[q] = (uint32_t)raw[q];
         }
         if (!cons_sync_ok(fail_word(S))) return false;
         int cnt = 0;
@@ -812,7 +864,7 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
     for (int g = 0; g < ngf; ++g) {
         const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
         // phase A left the x_hat of a single token group in xs
-        if (!(xs_valid && ngf == 1)) stage_xhat<T>(p, S, l, t0, nt);
+        if (!(xs_valid && ngf == 1) && !stage_xhat<T>(p, S, l, t0, nt)) return false;
         // single-token kernel: this thread's x_hat columns, as fp32, in registers
         float xf[2][8];
 #pragma unroll
@@ -1059,34 +1111,36 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
             sd += kb;
         }
         // ---- this CTA's fp32 partial of the layer output
+        // (tagged with this layer's epoch: the merge polls these words)
+        const unsigned ep = p.epoch + l;
         for (int t = 0; t < nt; ++t) {
-            float *dst = p.partial + ((size_t)blockIdx.x * p.B + t0 + t) * d;
+            uint64_t *dst = p.partx + ((size_t)blockIdx.x * p.B + t0 + t) * d;
             if (!Q4) {
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int ch = tid + q * kConsumerThreads;
                     if (ch < nch) {
-                        float4 *o = reinterpret_cast<float4 *>(dst + ch * 8);
 #pragma unroll
-                        for (int tt = 0; tt < TGF; ++tt) {
-                            if (tt == t) {
-                                o[0] = make_float4(y[tt][q * 8 + 0], y[tt][q * 8 + 1], y[tt][q * 8 + 2], y[tt][q * 8 + 3]);
-                                o[1] = make_float4(y[tt][q * 8 + 4], y[tt][q * 8 + 5], y[tt][q * 8 + 6], y[tt][q * 8 + 7]);
-                            }
+                        for (int e = 0; e < 8; e += 2) {
+                            float a0 = 0.f, a1 = 0.f; // token t's pair (t is not a compile-time index)
+#pragma unroll
+                            for (int tt = 0; tt < TGF; ++tt)
+                                if (tt == t) a0 = y[tt][q * 8 + e], a1 = y[tt][q * 8 + e + 1];
+                            st_tagged2(dst + ch * 8 + e, ep, __float_as_uint(a0), __float_as_uint(a1));
                         }
                     }
                 }
             } else {
                 const int hb = tid;
                 if (hb < nhb) {
-                    float4 *o = reinterpret_cast<float4 *>(dst + (hb >> 1) * 32 + (hb & 1) * 16);
+                    uint64_t *o = dst + (hb >> 1) * 32 + (hb & 1) * 16;
 #pragma unroll
-                    for (int tt = 0; tt < TGF; ++tt) {
-                        if (tt == t) {
+                    for (int e = 0; e < 16; e += 2) {
+                        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                            for (int v = 0; v < 4; ++v)
-                                o[v] = make_float4(y[tt][4 * v], y[tt][4 * v + 1], y[tt][4 * v + 2], y[tt][4 * v + 3]);
-                        }
+                        for (int tt = 0; tt < TGF; ++tt)
+                            if (tt == t) a0 = y[tt][e], a1 = y[tt][e + 1];
+                        st_tagged2(o + e, ep, __float_as_uint(a0), __float_as_uint(a1));
                     }
                 }
             }
@@ -1107,16 +1161,21 @@ static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev
 // ------------------------------------------------------------------ phase D: merge
 // Units of 4 columns; a warp per unit, its lanes over the partials in a fixed
 // order, then a butterfly.  x and b_down are loaded alongside the partials.
+// The partials are read straight from the writers' tagged words: the first
+// read usually finds them all, stale words are polled until phase C of every
+// SM has written them, so no grid barrier stands between C and D.  The new
+// residual goes to x and, tagged, to xx, which the next layer polls.
 template <typename T>
-static __device__ void phase_d(const StepParams &p, const LayerDev &L)
+static __device__ void phase_d(const StepParams &p, const Shm &S, const LayerDev &L, int l)
 {
     using F = F16T<T>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, d = L.d;
     const int U = p.B * d / 4;
     const int u0 = slice_lo(U, blockIdx.x, G), u1 = slice_lo(U, blockIdx.x + 1, G);
-    const size_t stride4 = (size_t)p.B * d / 4;
-    const float4 *part = reinterpret_cast<const float4 *>(p.partial);
+    const size_t stride = (size_t)p.B * d; // words between two SMs' partials
+    const unsigned ep = p.epoch + l, ew = ep + (unsigned)p.bar_extra;
+    volatile int *fail = fail_word(S);
     for (int u = u0 + warp; u < u1; u += kConsumerWarps) {
         const int j = (4 * u) % d;
         float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1126,29 +1185,51 @@ static __device__ void phase_d(const StepParams &p, const LayerDev &L)
             if (p.mode & M_RESID) xv = __ldcg(reinterpret_cast<const float4 *>(p.x) + u);
         }
         // Request the first 32 * kPre partials of the unit before the first
-        // add, so that they cost one L2 round trip instead of one per 32 CTAs;
+        // add, so that they cost one L2 round trip instead of one per 32 SMs;
         // the sum keeps the order cc = lane, lane + 32, ...
         constexpr int kPre = 5;
-        float4 v[kPre];
+        uint64_t w[kPre][4];
+        const auto reload_ok = [&]() {
+            bool good = true;
 #pragma unroll
-        for (int i = 0; i < kPre; ++i) {
-            const int cc = lane + 32 * i;
-            v[i] = cc < G ? __ldcg(part + (size_t)cc * stride4 + u) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+            for (int i = 0; i < kPre; ++i) {
+                const int cc = lane + 32 * i;
+                if (cc < G) {
+                    const uint64_t *a = p.partx + (size_t)cc * stride + 4 * (size_t)u;
+                    ld_tagged2(a, w[i][0], w[i][1]);
+                    ld_tagged2(a + 2, w[i][2], w[i][3]);
+                } else {
+                    w[i][0] = w[i][1] = w[i][2] = w[i][3] = (uint64_t)ew << 32; // +0.0
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kPre; ++i)
+                good &= tag_is(w[i][0], ew) & tag_is(w[i][1], ew) & tag_is(w[i][2], ew) & tag_is(w[i][3], ew);
+            return good;
+        };
+        if (!reload_ok()) poll_tags(p, fail, reload_ok);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < kPre; ++i) {
-            acc.x += v[i].x;
-            acc.y += v[i].y;
-            acc.z += v[i].z;
-            acc.w += v[i].w;
+            acc.x += __uint_as_float((uint32_t)w[i][0]);
+            acc.y += __uint_as_float((uint32_t)w[i][1]);
+            acc.z += __uint_as_float((uint32_t)w[i][2]);
+            acc.w += __uint_as_float((uint32_t)w[i][3]);
         }
         for (int cc = lane + 32 * kPre; cc < G; cc += 32) {
-            const float4 w = __ldcg(part + (size_t)cc * stride4 + u);
-            acc.x += w.x;
-            acc.y += w.y;
-            acc.z += w.z;
-            acc.w += w.w;
+            // (more than 160 SMs only)
+            const uint64_t *a = p.partx + (size_t)cc * stride + 4 * (size_t)u;
+            uint64_t v[4];
+            const auto reload1 = [&]() {
+                ld_tagged2(a, v[0], v[1]);
+                ld_tagged2(a + 2, v[2], v[3]);
+                return tag_is(v[0], ew) & tag_is(v[1], ew) & tag_is(v[2], ew) & tag_is(v[3], ew);
+            };
+            if (!reload1()) poll_tags(p, fail, reload1);
+            acc.x += __uint_as_float((uint32_t)v[0]);
+            acc.y += __uint_as_float((uint32_t)v[1]);
+            acc.z += __uint_as_float((uint32_t)v[2]);
+            acc.w += __uint_as_float((uint32_t)v[3]);
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
@@ -1169,6 +1250,10 @@ static __device__ void phase_d(const StepParams &p, const LayerDev &L)
                 xv.z += acc.z;
                 xv.w += acc.w;
                 __stcg(reinterpret_cast<float4 *>(p.x) + u, xv);
+                if (l + 1 < p.L) {
+                    st_tagged2(p.xx + 4 * (size_t)u, ep, __float_as_uint(xv.x), __float_as_uint(xv.y));
+                    st_tagged2(p.xx + 4 * (size_t)u + 2, ep, __float_as_uint(xv.z), __float_as_uint(xv.w));
+                }
             } else {
                 const uint32_t lo = (uint32_t)F::round(acc.x) | ((uint32_t)F::round(acc.y) << 16);
                 const uint32_t hi = (uint32_t)F::round(acc.z) | ((uint32_t)F::round(acc.w) << 16);
@@ -1217,7 +1302,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
     }
     // ---- consumers
     uint32_t ss = 0, sd = 0;
-    int rbuf = 0, nbar = 0;
+    int rbuf = 0;
     const bool pred = (p.mode & (M_PREDICT | M_COUNTS)) != 0;
     mark(p, 0);
     for (int l = 0; l < p.L; ++l) {
@@ -1244,11 +1329,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
                 // the ring is free again: the static producer may fill it for layer l+1
                 if (threadIdx.x == 0) atomicAdd(S.info + INFO_REGION, 1);
                 mark(p, ev + 5);
-                if (!grid_sync(p, fail_word(S), S.info + INFO_FLAG, nbar)) return;
-                mark(p, ev + 6);
-                phase_d<T>(p, L);
+                mark(p, ev + 6); // (no barrier: the merge polls the tagged partials)
+                phase_d<T>(p, S, L, l);
+                if (!cons_sync_ok(fail_word(S))) return; // (CTA-uniform: every consumer warp leaves or none)
                 mark(p, ev + 7);
-                if (l + 1 < p.L && !grid_sync(p, fail_word(S), S.info + INFO_FLAG, nbar)) return;
             }
         }
     }

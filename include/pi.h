@@ -167,10 +167,10 @@ pi_status pi_sparse_ffn(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t B
  * budget, or sits inside a server whose memory pool must not see foreign
  * allocations -- callers for which pi_create (which allocates its workspace)
  * is not an option.  The caller passes the layer's rows, the inputs and the
- * output; the kernel's scratch (fp32 split-K partials, the grid-barrier
- * counter, status words, a one-layer descriptor, zeros for absent biases)
- * lives in one 8 MiB array that the library keeps on every GPU that loads it,
- * until the process exits.
+ * output; the kernel's scratch (epoch-tagged fp32 split-K partials, status
+ * words, a one-layer descriptor, zeros for absent biases) lives in one
+ * 16 MiB array that the library keeps on every GPU that loads it, until the
+ * process exits.
  *
  * w: the layer in the library's row layout, all device pointers, original
  *    neuron order (no permutation):
@@ -247,17 +247,20 @@ int32_t pi_grid_size(pi_ctx *ctx);
 
 /* Test and profiling hooks.  pi_debug_set_wait_limit: nanoseconds a device-side wait may
  * spin before it gives up with PI_ERR_TIMEOUT (default 2e9).
- * pi_debug_barrier_extra: add `extra` phantom arrivals to the grid barrier's
- * target count, so the next step's barrier can never complete and must time
- * out (0 restores normal operation). */
+ * pi_debug_barrier_extra: make every cross-SM exchange of the following
+ * launches wait for an epoch `extra` steps ahead of the one its writers tag
+ * (SMs pass h, mask words, partials and the residual to one another as
+ * epoch-tagged words instead of meeting at grid barriers), so the first
+ * exchange can never complete and must time out (0 restores normal
+ * operation). */
 pi_status pi_debug_set_wait_limit(pi_ctx *ctx, uint64_t ns);
 pi_status pi_debug_barrier_extra(pi_ctx *ctx, int32_t extra);
 
 /* Debug timeline: when `stamps` (dev uint64 [grid][per_cta]) is set, thread 0
  * of every CTA of the step kernel writes %globaltimer (ns) at phase ends:
  * index 0 = start, then per layer l at 1 + 9*l + k, k = 0 predictor hidden
- * layer done, 1 its grid barrier, 2 predictor output done, 3 its barrier,
- * 4 list resolved, 5 FFN done, 6 its barrier, 7 merge done, 8 first FFN
+ * layer done, 1 (same moment: no barrier follows), 2 predictor output done,
+ * 3 (same), 4 list resolved, 5 FFN done, 6 (same), 7 merge done, 8 first FFN
  * rows landed.  Stamps past per_cta are dropped.  NULL disables. */
 pi_status pi_debug_set_timeline(pi_ctx *ctx, uint64_t *stamps, int32_t per_cta);
 
