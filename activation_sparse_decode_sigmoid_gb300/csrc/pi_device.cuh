@@ -212,30 +212,38 @@ __device__ __forceinline__ void ld_tagged2(const uint64_t *a, uint64_t &v0, uint
 
 __device__ __forceinline__ bool tag_is(uint64_t v, unsigned epoch) { return (unsigned)(v >> 32) == epoch; }
 
-// Retry `reload_ok` (re-read a set of tagged words, report whether all carry
-// the expected epoch) until it succeeds, with a short sleep between rounds,
-// for at most the wait limit.  Inline on purpose: the caller's words stay in
-// registers.  On a timeout or an abort it sets the CTA's failure word.
+// Wait for a set of tagged words.  `reload` re-reads the caller's words
+// (they stay in its registers: this is inline on purpose) and returns the
+// address of one that does not carry `epoch` yet, or nullptr when all do.
+// While a word is stale only that word is polled (8 bytes per round, with a
+// short sleep), then the whole set is read again; re-reading the whole set
+// every round floods L2 while the last writers are still at work.  Bounded by
+// the wait limit; on a timeout or an abort it sets the CTA's failure word.
 template <typename F>
-__device__ __forceinline__ bool poll_tags(const StepParams &p, volatile int *fail, F reload_ok)
+__device__ __forceinline__ bool poll_tags(const StepParams &p, volatile int *fail, unsigned epoch,
+                                          const uint64_t *stale, F reload)
 {
     const uint64_t t0 = globaltimer();
-    for (unsigned it = 1;; ++it) {
-        __nanosleep(100);
-        if (reload_ok()) return true;
-        if (*fail) return false;
-        if ((it & 7) == 0) {
-            if (aborted(p)) {
-                *fail = 1;
-                return false;
-            }
-            if (globaltimer() - t0 > p.wait_ns) {
-                raise_error(p, PI_DEV_TIMEOUT);
-                *fail = 1;
-                return false;
+    unsigned it = 0;
+    while (stale) {
+        while (!tag_is(ld_tagged(stale), epoch)) {
+            __nanosleep(64);
+            if (*fail) return false;
+            if ((++it & 15) == 0) {
+                if (aborted(p)) {
+                    *fail = 1;
+                    return false;
+                }
+                if (globaltimer() - t0 > p.wait_ns) {
+                    raise_error(p, PI_DEV_TIMEOUT);
+                    *fail = 1;
+                    return false;
+                }
             }
         }
+        stale = reload();
     }
+    return true;
 }
 
 // Bulk prefetch of [src, src+bytes) into L2 (no shared memory, no completion).

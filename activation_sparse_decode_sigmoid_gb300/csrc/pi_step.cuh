@@ -470,8 +470,8 @@ static __device__ bool stage_xhat(const StepParams &p, const Shm &S, int l, int 
 #pragma unroll
                 for (int h2 = 0; h2 < 4; h2 += 2) { // two float4 per round: fewer live registers
                     uint64_t w[2][4];
-                    const auto reload_ok = [&]() {
-                        bool good = true;
+                    const auto reload = [&]() {
+                        const uint64_t *stale = nullptr;
 #pragma unroll
                         for (int q = 0; q < 2; ++q) {
                             const int k = tid + (h2 + q) * kConsumerThreads;
@@ -483,12 +483,15 @@ static __device__ bool stage_xhat(const StepParams &p, const Shm &S, int l, int 
                             }
                         }
 #pragma unroll
-                        for (int q = 0; q < 2; ++q)
-                            good &= tag_is(w[q][0], ew) & tag_is(w[q][1], ew) & tag_is(w[q][2], ew) &
-                                    tag_is(w[q][3], ew);
-                        return good;
+                        for (int q = 0; q < 2; ++q) {
+                            const int k = tid + (h2 + q) * kConsumerThreads;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (!tag_is(w[q][e], ew)) stale = xr + 4 * k + e;
+                        }
+                        return stale;
                     };
-                    if (!reload_ok()) poll_tags(p, fail_word(S), reload_ok);
+                    poll_tags(p, fail_word(S), ew, reload(), reload);
 #pragma unroll
                     for (int q = 0; q < 2; ++q)
                         v[h2 + q] = make_float4(__uint_as_float((uint32_t)w[q][0]), __uint_as_float((uint32_t)w[q][1]),
@@ -614,18 +617,19 @@ static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev
             const int nh = nt * L.r;
             for (int k0 = tid; k0 < nh; k0 += 4 * kConsumerThreads) {
                 uint64_t v[4];
-                const auto reload_ok = [&]() {
-                    bool good = true;
+                const auto reload = [&]() {
+                    const uint64_t *stale = nullptr;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int k = k0 + u * kConsumerThreads;
                         v[u] = k < nh ? ld_tagged(src + k) : ((uint64_t)ew << 32);
                     }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) good &= tag_is(v[u], ew);
-                    return good;
+                    for (int u = 0; u < 4; ++u)
+                        if (!tag_is(v[u], ew)) stale = src + k0 + u * kConsumerThreads;
+                    return stale;
                 };
-                if (!reload_ok() && !poll_tags(p, fail_word(S), reload_ok)) break;
+                if (!poll_tags(p, fail_word(S), ew, reload(), reload)) break;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int k = k0 + u * kConsumerThreads;
@@ -700,15 +704,16 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
         {
             const unsigned ew = p.epoch + l + (unsigned)p.bar_extra;
             uint64_t raw[4];
-            const auto reload_ok = [&]() {
-                bool good = true;
+            const auto reload = [&]() {
+                const uint64_t *stale = nullptr;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) raw[q] = (wb + q < we) ? ld_tagged(p.bmx + wb + q) : ((uint64_t)ew << 32);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) good &= tag_is(raw[q], ew);
-                return good;
+                for (int q = 0; q < 4; ++q)
+                    if (!tag_is(raw[q], ew)) stale = p.bmx + wb + q;
+                return stale;
             };
-            if (!reload_ok()) poll_tags(p, fail_word(S), reload_ok);
+            poll_tags(p, fail_word(S), ew, reload(), reload);
 #pragma unroll
             for (int q = 0; q < 4; ++q) wv[q] = (uint32_t)raw[q];
         }
@@ -1189,8 +1194,8 @@ static __device__ void phase_d(const StepParams &p, const Shm &S, const LayerDev
         // the sum keeps the order cc = lane, lane + 32, ...
         constexpr int kPre = 5;
         uint64_t w[kPre][4];
-        const auto reload_ok = [&]() {
-            bool good = true;
+        const auto reload = [&]() {
+            const uint64_t *stale = nullptr;
 #pragma unroll
             for (int i = 0; i < kPre; ++i) {
                 const int cc = lane + 32 * i;
@@ -1203,11 +1208,15 @@ static __device__ void phase_d(const StepParams &p, const Shm &S, const LayerDev
                 }
             }
 #pragma unroll
-            for (int i = 0; i < kPre; ++i)
-                good &= tag_is(w[i][0], ew) & tag_is(w[i][1], ew) & tag_is(w[i][2], ew) & tag_is(w[i][3], ew);
-            return good;
+            for (int i = 0; i < kPre; ++i) {
+                const int cc = lane + 32 * i;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (!tag_is(w[i][e], ew)) stale = p.partx + (size_t)cc * stride + 4 * (size_t)u + e;
+            }
+            return stale;
         };
-        if (!reload_ok()) poll_tags(p, fail, reload_ok);
+        poll_tags(p, fail, ew, reload(), reload);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < kPre; ++i) {
@@ -1221,11 +1230,15 @@ static __device__ void phase_d(const StepParams &p, const Shm &S, const LayerDev
             const uint64_t *a = p.partx + (size_t)cc * stride + 4 * (size_t)u;
             uint64_t v[4];
             const auto reload1 = [&]() {
+                const uint64_t *stale = nullptr;
                 ld_tagged2(a, v[0], v[1]);
                 ld_tagged2(a + 2, v[2], v[3]);
-                return tag_is(v[0], ew) & tag_is(v[1], ew) & tag_is(v[2], ew) & tag_is(v[3], ew);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (!tag_is(v[e], ew)) stale = a + e;
+                return stale;
             };
-            if (!reload1()) poll_tags(p, fail, reload1);
+            poll_tags(p, fail, ew, reload1(), reload1);
             acc.x += __uint_as_float((uint32_t)v[0]);
             acc.y += __uint_as_float((uint32_t)v[1]);
             acc.z += __uint_as_float((uint32_t)v[2]);
