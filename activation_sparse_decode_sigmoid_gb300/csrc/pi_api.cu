@@ -70,7 +70,7 @@ struct pi_ctx {
     int bar_extra = 0;
     unsigned long long *timeline = nullptr;
     int tl_stride = 0;
-    int prefetch = 2, prefetch_ns = 800, cb_max = 3, rows_ahead = 0; // tuning, see StepParams
+    int prefetch = 0, prefetch_ns = 800, lookahead = 16, rows_ahead = 0; // tuning, see StepParams
     std::string err;
 };
 
@@ -229,7 +229,7 @@ pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
     p.tl_stride = c->tl_stride;
     p.prefetch = c->prefetch;
     p.prefetch_ns = c->prefetch_ns;
-    p.cb_max = c->cb_max;
+    p.lookahead = c->lookahead;
     p.rows_ahead = c->rows_ahead;
     const pi_layer_desc &d0 = c->layers[l0].desc;
     cudaError_t e;
@@ -275,7 +275,7 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     // tuning knobs (defaults are the measured best on GB300)
     if (const char *v = getenv("PI_PREFETCH")) c->prefetch = atoi(v);
     if (const char *v = getenv("PI_PREFETCH_NS")) c->prefetch_ns = atoi(v);
-    if (const char *v = getenv("PI_CB")) c->cb_max = atoi(v) > 0 ? atoi(v) : 1;
+    if (const char *v = getenv("PI_LOOKAHEAD")) c->lookahead = atoi(v) >= 0 ? atoi(v) : 0;
     if (const char *v = getenv("PI_ROWS_AHEAD")) c->rows_ahead = atoi(v) > 0 ? atoi(v) : 0;
     int coop = 0;
     cudaError_t e = cudaDeviceGetAttribute(&c->G, cudaDevAttrMultiProcessorCount, device);
@@ -667,14 +667,14 @@ pi_status pi_debug_set_timeline(pi_ctx *c, uint64_t *stamps, int32_t per_cta)
     return PI_OK;
 }
 
-pi_status pi_debug_set_tuning(pi_ctx *c, int32_t prefetch, int32_t prefetch_ns, int32_t consumer_batch,
+pi_status pi_debug_set_tuning(pi_ctx *c, int32_t prefetch, int32_t prefetch_ns, int32_t lookahead,
                               int32_t rows_ahead)
 {
-    if (!c || prefetch < 0 || prefetch > 3 || prefetch_ns < 0 || consumer_batch < 1 || rows_ahead < 0)
+    if (!c || prefetch < 0 || prefetch > 3 || prefetch_ns < 0 || lookahead < 0 || rows_ahead < 0)
         return PI_ERR_ARG;
     c->prefetch = prefetch;
     c->prefetch_ns = prefetch_ns;
-    c->cb_max = consumer_batch;
+    c->lookahead = lookahead;
     c->rows_ahead = rows_ahead;
     return PI_OK;
 }

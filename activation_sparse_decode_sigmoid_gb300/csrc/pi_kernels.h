@@ -94,12 +94,13 @@ struct StepParams {
     // tuning: L2 prefetch of the predictor slices (0 off; the next layer's
     // during phase C: 1 all at once, 2 paced at one 16 KB chunk per
     // prefetch_ns; 3 this layer's W2 slice as one burst once phase C of the
-    // previous layer is over), consumer batch cap, and how many neurons of the
+    // previous layer is over), how many stages past the one being merged an
+    // owner warp may compute activations for (phase C), and how many neurons of the
     // CTA's list the dynamic producer prefetches into L2 ahead of its ring
     // loads (0 off)
     int prefetch;
     int prefetch_ns;
-    int cb_max;
+    int lookahead;
     int rows_ahead;
     // shared-memory plan.  The ring region [0, ringB) is time-shared: during
     // the predictor phases it is nss static slots of slotB bytes, during the
@@ -130,7 +131,7 @@ __host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, in
     MiscLayout m;
     int o = 0;
     m.bars = o;
-    o += (2 * nss + 2 * nsd + 3) * 8;
+    o += (2 * nss + 3 * nsd + 3) * 8;
     o = (o + 15) & ~15;
     m.info = o;
     o += 16 * 4;

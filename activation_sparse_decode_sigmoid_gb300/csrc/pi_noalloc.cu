@@ -171,7 +171,7 @@ extern "C" pi_status pi_sparse_ffn_noalloc(const pi_ffn_rows *w, const void *x_h
     p.abort_flag = reinterpret_cast<int *>(scratch + kCtlOff + 12);
     p.wait_ns = 2000000000ull;
     p.prefetch = 0;
-    p.cb_max = 1;
+    p.lookahead = 16;
     const cudaError_t e = w->act_dtype == PI_BF16 ? pi::launch_step_bf16(p, tgf, G, s) : pi::launch_step_f16(p, tgf, G, s);
     return e == cudaSuccess ? PI_OK : PI_ERR_CUDA;
 }

@@ -57,6 +57,7 @@ struct Shm {
     unsigned *swords; // [wcap] predicted-mask words of this CTA's rows
     uint16_t *pb1s, *pb2s; // this CTA's b1 / b2 slices, as copied (16-byte-rounded ranges)
     uint64_t *bias_full;   // completes when a layer's bias slices have landed
+    uint64_t *act_full;    // [nsd] completes when a stage's owner warp has written its activations
     float *red;     // [2][warps][kMaxNeuronsPerStage][TGF][2] cross-warp dot sums
 };
 
@@ -88,6 +89,7 @@ static __device__ __forceinline__ Shm carve(uint8_t *smem, const StepParams &p, 
     s.lst_full = s.empty_d + p.nsd;
     s.lst_free = s.lst_full + 1;
     s.bias_full = s.lst_free + 1;
+    s.act_full = s.bias_full + 1;
     s.info = (int *)(base + m.info);
     s.tmp = (float *)(base + m.tmp);
     s.slist = (int *)(base + m.slist);
@@ -816,18 +818,18 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
 }
 
 // ------------------------------------------------------------------ phase C: gather FFN
-// Thread `tid` owns output columns: 16-bit rows -> chunks of 8 columns
-// ch = tid and tid + 512 (kYSlots = 16 columns); Q4_0 -> half-block hb = tid
-// (16 columns of block hb/2).  Consumers take the ring in batches of `cb`
-// stages: once the whole batch has landed, the partial dot products of all
-// its neurons are computed side by side (independent chains), one named
-// barrier combines them across warps, then the down-projection rows are
-// accumulated and the batch's stages are released together.
-static __device__ __forceinline__ int consumer_batch(int npd, int nsd, int cap)
-{
-    return max(1, min(min(kMaxNeuronsPerStage / npd, nsd / 2), cap));
-}
-
+// The ring delivers stages (npd whole neurons each) in list order.  Stage k
+// has an owner warp, k mod 16, which computes the dot products of its
+// neurons over the whole row (W_up, W_gate) and the activations, writes them
+// to shared memory and arrives on the stage's act_full barrier; no other warp
+// takes part, so there is no cross-warp reduction and no CTA barrier per
+// stage.  Every warp then adds the stage's down-projection rows into the
+// output columns its threads own and releases the stage (empty_d counts the
+// 16 warps).  Owners compute ahead, up to `ahead` stages past the stage
+// being merged, on stages that have already landed.
+// Output columns of thread `tid`: 16-bit rows -> chunks of 8 columns ch = tid
+// and tid + 512 (kYSlots = 16 columns); Q4_0 -> half-block hb = tid (16
+// columns of block hb/2).
 template <typename T>
 static __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8])
 {
@@ -844,277 +846,197 @@ static __device__ __forceinline__ void unpack_q4(const uint4 v, int sh, float (&
     for (int e = 0; e < 16; ++e) f[e] = (float)((int)((w[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8);
 }
 
+// One warp: the dot products of one neuron's W_up row (at a) and, for ReGLU,
+// its W_gate row (at a + upB) with the nt tokens' x_hat in xs (16-bit [t][d]),
+// over the whole row; full sums in every lane.
+template <typename T, bool Q4, int TGF, bool REGLU>
+static __device__ __forceinline__ void row_dots(const LayerDev &L, uint32_t a, uint32_t upB, uint32_t xs, int d,
+                                                int nt, int lane, float (&au)[TGF], float (&ag)[TGF])
+{
+#pragma unroll
+    for (int t = 0; t < TGF; ++t) au[t] = ag[t] = 0.f;
+    if constexpr (!Q4) {
+        const int nch = d >> 3;
+        // two chains per token (alternate chunks) halve the dependent fma run
+        float bu[TGF], bg[TGF];
+#pragma unroll
+        for (int t = 0; t < TGF; ++t) bu[t] = bg[t] = 0.f;
+        for (int ch = lane; ch < nch; ch += 64) {
+            const bool two = ch + 32 < nch;
+            const uint4 w0 = ld_shared_v4(a + (uint32_t)ch * 16);
+            const uint4 w1 = two ? ld_shared_v4(a + (uint32_t)(ch + 32) * 16) : make_uint4(0, 0, 0, 0);
+            uint4 g0 = make_uint4(0, 0, 0, 0), g1 = make_uint4(0, 0, 0, 0);
+            if (REGLU) {
+                g0 = ld_shared_v4(a + upB + (uint32_t)ch * 16);
+                if (two) g1 = ld_shared_v4(a + upB + (uint32_t)(ch + 32) * 16);
+            }
+#pragma unroll
+            for (int t = 0; t < TGF; ++t) {
+                if (t < nt) {
+                    const uint32_t xr = xs + (uint32_t)(t * d) * 2;
+                    const uint4 x0 = ld_shared_v4(xr + (uint32_t)ch * 16);
+                    const uint4 x1 = two ? ld_shared_v4(xr + (uint32_t)(ch + 32) * 16) : make_uint4(0, 0, 0, 0);
+                    au[t] = fma_chunk<T>(w0, x0, au[t]);
+                    bu[t] = fma_chunk<T>(w1, x1, bu[t]);
+                    if (REGLU) {
+                        ag[t] = fma_chunk<T>(g0, x0, ag[t]);
+                        bg[t] = fma_chunk<T>(g1, x1, bg[t]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TGF; ++t) au[t] += bu[t], ag[t] += bg[t];
+    } else {
+        const int nhb = d >> 4;
+        for (int hb = lane; hb < nhb; hb += 32) {
+            const int blk = hb >> 1, sh = (hb & 1) * 4;
+            float qu[16], qg[16];
+            unpack_q4(ld_shared_v4(a + L.scB + blk * 16), sh, qu);
+            const float su = __half2float(__ushort_as_half(ld_shared_u16(a + blk * 2)));
+            float sg = 0.f;
+            if (REGLU) {
+                unpack_q4(ld_shared_v4(a + upB + L.scB + blk * 16), sh, qg);
+                sg = __half2float(__ushort_as_half(ld_shared_u16(a + upB + blk * 2)));
+            }
+#pragma unroll
+            for (int t = 0; t < TGF; ++t) {
+                if (t < nt) {
+                    const uint32_t xb = xs + (uint32_t)(t * d + blk * 32 + (hb & 1) * 16) * 2;
+                    float x0[8], x1[8];
+                    unpack8<T>(ld_shared_v4(xb), x0);
+                    unpack8<T>(ld_shared_v4(xb + 16), x1);
+                    float pu = 0.f, pg = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        pu = fmaf(qu[e], x0[e], pu);
+                        pu = fmaf(qu[8 + e], x1[e], pu);
+                        if (REGLU) {
+                            pg = fmaf(qg[e], x0[e], pg);
+                            pg = fmaf(qg[8 + e], x1[e], pg);
+                        }
+                    }
+                    au[t] = fmaf(su, pu, au[t]);
+                    if (REGLU) ag[t] = fmaf(sg, pg, ag[t]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TGF; ++t) {
+        au[t] = butterfly_sum(au[t]);
+        if (REGLU) ag[t] = butterfly_sum(ag[t]);
+    }
+}
+
 template <typename T, bool Q4, int TGF, bool REGLU>
 static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd,
-                                    int &rbuf, bool xs_valid)
+                                    bool xs_valid)
 {
     using F = F16T<T>;
-    constexpr int NB = TGF == 1 ? 4 : 1; // neurons whose dot products run side by side
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = L.d;
     const int ncnt = S.info[INFO_NCNT];
     const int nb = neuron_bytes(L);
     const int npd = neurons_per_stage(L, p);
     const int nst = (ncnt + npd - 1) / npd;
-    const int cb = consumer_batch(npd, p.nsd, p.cb_max);
     const int ngf = (p.B + p.tg - 1) / p.tg;
     const int nch = d >> 3;     // 16-bit: chunks of 8 columns
     const int nhb = d >> 4;     // Q4_0: half-blocks of 16 columns
+    const int ahead = max(0, min(p.nsd - 1, p.lookahead)); // lookahead < nsd keeps the ring deadlock-free
     const uint32_t rowB = (uint32_t)L.rowB;
     const uint32_t upB = (uint32_t)L.upB; // offset of the gate row in a neuron
+    const uint32_t dnoff = upB + (REGLU ? rowB : 0u); // offset of the W_down^T row
     const uint32_t ring = smem_u32(S.ring);
-    float *act = S.tmp + 64; // [kMaxNeuronsPerStage][TGF] activations of the current batch
+    const uint32_t xs = smem_u32(S.xs);
+    float *act = S.red; // [nsd][kMaxNeuronsPerStage][TGF] activations of the stages in the ring
     bool ok = true;
-    uint32_t slot = sd % p.nsd, par = (sd / p.nsd) & 1; // ring position of the next stage
     for (int g = 0; g < ngf; ++g) {
         const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
         // phase A left the x_hat of a single token group in xs
         if (!(xs_valid && ngf == 1) && !stage_xhat<T>(p, S, l, t0, nt)) return false;
-        // single-token kernel: this thread's x_hat columns, as fp32, in registers
-        float xf[2][8];
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xf[q][e] = 0.f;
-        if constexpr (TGF == 1) {
-            if (!Q4) {
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int ch = tid + q * kConsumerThreads;
-                    if (ch < nch) unpack8<T>(*reinterpret_cast<const uint4 *>(S.xs + (size_t)ch * 16), xf[q]);
-                }
-            } else if (tid < nhb) {
-                const uint8_t *xb = S.xs + ((size_t)(tid >> 1) * 32 + (tid & 1) * 16) * 2;
-                unpack8<T>(*reinterpret_cast<const uint4 *>(xb), xf[0]);
-                unpack8<T>(*reinterpret_cast<const uint4 *>(xb + 16), xf[1]);
-            }
-        }
         float y[TGF][kYSlots];
 #pragma unroll
         for (int t = 0; t < TGF; ++t)
 #pragma unroll
             for (int e = 0; e < kYSlots; ++e) y[t][e] = 0.f;
 
-        // the first batch of a token group takes one stage, so the consumers
-        // start as soon as the first neuron has landed
-        for (int k0 = 0, kb = 0; k0 < nst; k0 += kb) {
-            kb = min(k0 == 0 ? 1 : cb, nst - k0);
-            float *red = S.red + (size_t)rbuf * kConsumerWarps * kMaxNeuronsPerStage * TGF * 2;
-            // wait for the batch
-            int got = 0;
-            {
-                uint32_t sl = slot, pa = par;
-                for (int kk = 0; kk < kb; ++kk) {
-                    if (!wait_cta(S.full_d + sl, pa, p, fail_word(S), ok)) break;
-                    ++got;
-                    if (++sl == (uint32_t)p.nsd) sl = 0, pa ^= 1;
+        uint32_t slot = sd % p.nsd, par = (sd / p.nsd) & 1; // ring position of stage k
+        int own = warp;                                      // next stage this warp owns
+        for (int k = 0; k < nst; ++k) {
+            // ---- owned stages up to k + ahead: their activations
+            while (own < nst && own <= k + ahead) {
+                const uint32_t sa = sd + (uint32_t)own;
+                const uint32_t os = sa % p.nsd, op = (sa / p.nsd) & 1;
+                if (own > k && !mbar_test(S.full_d + os, op)) break; // not landed yet: later
+                if (wait_cta(S.full_d + os, op, p, fail_word(S), ok)) {
+                    if (own == 0 && g == 0) mark(p, 1 + l * kTimelineEvents + 8);
+                    const uint32_t base = ring + os * (uint32_t)p.dslotB;
+                    const int nn = min(npd, ncnt - own * npd);
+                    for (int j = 0; j < nn; ++j) {
+                        const int pos = own * npd + j;
+                        const int id = S.slist[pos];
+                        float au[TGF], ag[TGF];
+                        row_dots<T, Q4, TGF, REGLU>(L, base + (uint32_t)(j * nb), upB, xs, d, nt, lane, au, ag);
+                        if (lane == 0) {
+                            const float bias = L.bias_tail ? F::one(ld_shared_u16(base + (uint32_t)(j * nb) + rowB))
+                                                           : S.sbias[pos];
+#pragma unroll
+                            for (int t = 0; t < TGF; ++t) {
+                                const float av = REGLU ? fmaxf(ag[t] + bias, 0.f) * au[t] : fmaxf(au[t] + bias, 0.f);
+                                act[(os * kMaxNeuronsPerStage + j) * TGF + t] = id >= 0 && t < nt ? av : 0.f;
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(S.act_full + os);
                 }
+                own += kConsumerWarps;
             }
-            const int nnb = min(got * npd, ncnt - k0 * npd); // neurons of the batch in shared memory
-            // walks the batch's neurons in ring order (no division, no indexed array)
-            struct Cursor {
-                uint32_t a, sl;
-                int j;
-            };
-            const auto cur0 = [&]() { return Cursor{ring + slot * (uint32_t)p.dslotB, slot, 0}; };
-            const auto step = [&](Cursor &c) {
-                if (++c.j == npd) {
-                    c.j = 0;
-                    if (++c.sl == (uint32_t)p.nsd) c.sl = 0;
-                    c.a = ring + c.sl * (uint32_t)p.dslotB;
-                }
-            };
-            const auto addr = [&](const Cursor &c) { return c.a + (uint32_t)c.j * (uint32_t)nb; };
-            Cursor cj = cur0();
-            if (k0 == 0 && g == 0 && got) mark(p, 1 + l * kTimelineEvents + 8);
-            // ---- partial dot products of this thread's columns, NB neurons side by side
-            for (int j0 = 0; j0 < nnb; j0 += NB) {
-                uint32_t off[NB]; // compile-time indices only: stays in registers
+            // ---- stage k: its down-projection rows into this thread's columns
+            if (wait_cta(S.full_d + slot, par, p, fail_word(S), ok) && wait_cta(S.act_full + slot, par, p, fail_word(S), ok)) {
+                const uint32_t base = ring + slot * (uint32_t)p.dslotB;
+                const int nn = min(npd, ncnt - k * npd);
+                for (int j = 0; j < nn; ++j) {
+                    float a[TGF];
 #pragma unroll
-                for (int u = 0; u < NB; ++u) {
-                    off[u] = addr(cj);
-                    step(cj);
-                }
-                float au[NB][TGF], ag[NB][TGF];
+                    for (int t = 0; t < TGF; ++t) a[t] = act[(slot * kMaxNeuronsPerStage + j) * TGF + t];
+                    const uint32_t dn = base + (uint32_t)(j * nb) + dnoff;
+                    if (!Q4) {
 #pragma unroll
-                for (int u = 0; u < NB; ++u)
+                        for (int q = 0; q < 2; ++q) {
+                            const int ch = tid + q * kConsumerThreads;
+                            if (ch < nch) {
+                                float wf[8];
+                                unpack8<T>(ld_shared_v4(dn + (uint32_t)ch * 16), wf);
 #pragma unroll
-                    for (int t = 0; t < TGF; ++t) au[u][t] = ag[u][t] = 0.f;
-                if (!Q4) {
+                                for (int e = 0; e < 8; ++e)
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int ch = tid + q * kConsumerThreads;
-                        if (ch < nch) {
-#pragma unroll
-                            for (int u = 0; u < NB; ++u) {
-                                if (j0 + u < nnb) {
-                                    const uint32_t a = off[u] + (uint32_t)ch * 16;
-                                    float wu[8], wg[8];
-                                    unpack8<T>(ld_shared_v4(a), wu);
-                                    if (REGLU) unpack8<T>(ld_shared_v4(a + upB), wg);
-#pragma unroll
-                                    for (int t = 0; t < TGF; ++t) {
-                                        if (t < nt) {
-                                            float xv[8];
-                                            if constexpr (TGF == 1) {
-#pragma unroll
-                                                for (int e = 0; e < 8; ++e) xv[e] = xf[q][e];
-                                            } else {
-                                                unpack8<T>(*reinterpret_cast<const uint4 *>(S.xs + ((size_t)t * d + ch * 8) * 2), xv);
-                                            }
-#pragma unroll
-                                            for (int e = 0; e < 8; ++e) {
-                                                au[u][t] = fmaf(wu[e], xv[e], au[u][t]);
-                                                if (REGLU) ag[u][t] = fmaf(wg[e], xv[e], ag[u][t]);
-                                            }
-                                        }
-                                    }
-                                }
+                                    for (int t = 0; t < TGF; ++t) y[t][q * 8 + e] = fmaf(a[t], wf[e], y[t][q * 8 + e]);
                             }
                         }
-                    }
-                } else {
-                    const int hb = tid;
-                    if (hb < nhb) {
-                        const int blk = hb >> 1, sh = (hb & 1) * 4;
+                    } else {
+                        const int hb = tid;
+                        if (hb < nhb) {
+                            const int blk = hb >> 1, sh = (hb & 1) * 4;
+                            float qf[16];
+                            unpack_q4(ld_shared_v4(dn + L.scB + blk * 16), sh, qf);
+                            const float s = __half2float(__ushort_as_half(ld_shared_u16(dn + blk * 2)));
 #pragma unroll
-                        for (int u = 0; u < NB; ++u) {
-                            if (j0 + u < nnb) {
-                                const uint32_t a = off[u];
-                                float qu[16], qg[16];
-                                unpack_q4(ld_shared_v4(a + L.scB + blk * 16), sh, qu);
-                                const float su = __half2float(__ushort_as_half(ld_shared_u16(a + blk * 2)));
-                                float sg = 0.f;
-                                if (REGLU) {
-                                    unpack_q4(ld_shared_v4(a + upB + L.scB + blk * 16), sh, qg);
-                                    sg = __half2float(__ushort_as_half(ld_shared_u16(a + upB + blk * 2)));
-                                }
+                            for (int t = 0; t < TGF; ++t) {
+                                const float as = a[t] * s;
 #pragma unroll
-                                for (int t = 0; t < TGF; ++t) {
-                                    if (t < nt) {
-                                        float xv[16];
-                                        if constexpr (TGF == 1) {
-#pragma unroll
-                                            for (int e = 0; e < 8; ++e) xv[e] = xf[0][e], xv[8 + e] = xf[1][e];
-                                        } else {
-                                            const uint8_t *xb = S.xs + ((size_t)t * d + blk * 32 + (hb & 1) * 16) * 2;
-                                            float x0[8], x1[8];
-                                            unpack8<T>(*reinterpret_cast<const uint4 *>(xb), x0);
-                                            unpack8<T>(*reinterpret_cast<const uint4 *>(xb + 16), x1);
-#pragma unroll
-                                            for (int e = 0; e < 8; ++e) xv[e] = x0[e], xv[8 + e] = x1[e];
-                                        }
-                                        float s0 = 0.f, s1 = 0.f, g0 = 0.f, g1 = 0.f;
-#pragma unroll
-                                        for (int e = 0; e < 16; e += 2) {
-                                            s0 = fmaf(qu[e], xv[e], s0);
-                                            s1 = fmaf(qu[e + 1], xv[e + 1], s1);
-                                            if (REGLU) {
-                                                g0 = fmaf(qg[e], xv[e], g0);
-                                                g1 = fmaf(qg[e + 1], xv[e + 1], g1);
-                                            }
-                                        }
-                                        au[u][t] = (s0 + s1) * su;
-                                        if (REGLU) ag[u][t] = (g0 + g1) * sg;
-                                    }
-                                }
-                            }
-                        }
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < NB; ++u) {
-                    if (j0 + u < nnb) {
-#pragma unroll
-                        for (int t = 0; t < TGF; ++t) {
-#pragma unroll
-                            for (int o = 16; o >= 1; o >>= 1) {
-                                au[u][t] += __shfl_xor_sync(0xffffffffu, au[u][t], o);
-                                if (REGLU) ag[u][t] += __shfl_xor_sync(0xffffffffu, ag[u][t], o);
-                            }
-                            if (lane == 0) {
-                                red[((warp * kMaxNeuronsPerStage + j0 + u) * TGF + t) * 2 + 0] = au[u][t];
-                                if (REGLU) red[((warp * kMaxNeuronsPerStage + j0 + u) * TGF + t) * 2 + 1] = ag[u][t];
+                                for (int e = 0; e < 16; ++e) y[t][e] = fmaf(as, qf[e], y[t][e]);
                             }
                         }
                     }
                 }
             }
-            cons_sync();
-            // ---- warp w (< nnb) combines neuron w's 16 partials and applies the activation
-            if (warp < nnb) {
-                const int id = S.slist[k0 * npd + warp];
-                float bias;
-                if (L.bias_tail) {
-                    Cursor cw = cur0();
-                    for (int j = 0; j < warp; ++j) step(cw);
-                    bias = id >= 0 ? F::one(ld_shared_u16(addr(cw) + rowB)) : 0.f;
-                } else {
-                    bias = S.sbias[k0 * npd + warp];
-                }
-#pragma unroll
-                for (int t = 0; t < TGF; ++t) {
-                    float u = 0.f, gs = 0.f;
-                    if (lane < kConsumerWarps) {
-                        u = red[((lane * kMaxNeuronsPerStage + warp) * TGF + t) * 2 + 0];
-                        if (REGLU) gs = red[((lane * kMaxNeuronsPerStage + warp) * TGF + t) * 2 + 1];
-                    }
-#pragma unroll
-                    for (int o = kConsumerWarps / 2; o >= 1; o >>= 1) {
-                        u += __shfl_xor_sync(0xffffffffu, u, o);
-                        if (REGLU) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-                    }
-                    if (lane == 0) {
-                        const float av = REGLU ? fmaxf(gs + bias, 0.f) * u : fmaxf(u + bias, 0.f);
-                        act[warp * TGF + t] = id >= 0 ? av : 0.f;
-                    }
-                }
-            }
-            cons_sync();
-            // ---- the down-projection rows into this thread's columns
-            Cursor cd = cur0();
-            for (int jb = 0; jb < nnb; ++jb, step(cd)) {
-                float a[TGF];
-#pragma unroll
-                for (int t = 0; t < TGF; ++t) a[t] = act[jb * TGF + t];
-                const uint32_t dn = addr(cd) + upB + (REGLU ? rowB : 0u);
-                if (!Q4) {
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int ch = tid + q * kConsumerThreads;
-                        if (ch < nch) {
-                            float wf[8];
-                            unpack8<T>(ld_shared_v4(dn + (uint32_t)ch * 16), wf);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-#pragma unroll
-                                for (int t = 0; t < TGF; ++t) y[t][q * 8 + e] = fmaf(a[t], wf[e], y[t][q * 8 + e]);
-                        }
-                    }
-                } else {
-                    const int hb = tid;
-                    if (hb < nhb) {
-                        const int blk = hb >> 1, sh = (hb & 1) * 4;
-                        float qf[16];
-                        unpack_q4(ld_shared_v4(dn + L.scB + blk * 16), sh, qf);
-                        const float s = __half2float(__ushort_as_half(ld_shared_u16(dn + blk * 2)));
-#pragma unroll
-                        for (int t = 0; t < TGF; ++t) {
-                            const float as = a[t] * s;
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) y[t][e] = fmaf(as, qf[e], y[t][e]);
-                        }
-                    }
-                }
-            }
-            rbuf ^= 1;
             __syncwarp();
-            for (int kk = 0; kk < kb; ++kk) { // release the batch; advance the ring position
-                if (lane == 0 && kk < got) mbar_arrive(S.empty_d + slot);
-                if (++slot == (uint32_t)p.nsd) slot = 0, par ^= 1;
-            }
-            sd += kb;
+            if (lane == 0) mbar_arrive(S.empty_d + slot); // this warp is done with stage k
+            if (++slot == (uint32_t)p.nsd) slot = 0, par ^= 1;
         }
+        sd += (uint32_t)nst;
         // ---- this CTA's fp32 partial of the layer output
         // (tagged with this layer's epoch: the merge polls these words)
         const unsigned ep = p.epoch + l;
@@ -1156,11 +1078,11 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
 }
 
 template <typename T, bool Q4, int TGF>
-static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd, int &rbuf,
+static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd,
                                bool xs_valid)
 {
-    if (L.gate) return phase_c_impl<T, Q4, TGF, true>(p, S, L, l, sd, rbuf, xs_valid);
-    return phase_c_impl<T, Q4, TGF, false>(p, S, L, l, sd, rbuf, xs_valid);
+    if (L.gate) return phase_c_impl<T, Q4, TGF, true>(p, S, L, l, sd, xs_valid);
+    return phase_c_impl<T, Q4, TGF, false>(p, S, L, l, sd, xs_valid);
 }
 
 // ------------------------------------------------------------------ phase D: merge
@@ -1295,6 +1217,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
         mbar_init(S.lst_full, 1);
         mbar_init(S.lst_free, 1);
         mbar_init(S.bias_full, 1);
+        for (int i = 0; i < p.nsd; ++i) mbar_init(S.act_full + i, 1);
         fence_barrier_init();
         S.info[INFO_FAIL] = 0;
         S.info[INFO_REGION] = 0;
@@ -1315,7 +1238,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
     }
     // ---- consumers
     uint32_t ss = 0, sd = 0;
-    int rbuf = 0;
     const bool pred = (p.mode & (M_PREDICT | M_COUNTS)) != 0;
     mark(p, 0);
     for (int l = 0; l < p.L; ++l) {
@@ -1338,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
             mark(p, ev + 4);
             if (p.mode & M_FFN) {
                 if (threadIdx.x == 0) mbar_arrive(S.lst_full);
-                if (!phase_c<T, Q4, TGF>(p, S, L, l, sd, rbuf, pred)) return;
+                if (!phase_c<T, Q4, TGF>(p, S, L, l, sd, pred)) return;
                 // the ring is free again: the static producer may fill it for layer l+1
                 if (threadIdx.x == 0) atomicAdd(S.info + INFO_REGION, 1);
                 mark(p, ev + 5);

@@ -224,8 +224,8 @@ def pi_debug_set_timeline(ctx: int, stamps=None, per_cta: int = 0) -> None:
     _check(ctx, load_library().pi_debug_set_timeline(ctx, _ptr(stamps), per_cta), "pi_debug_set_timeline")
 
 
-def pi_debug_set_tuning(ctx: int, prefetch: int, prefetch_ns: int, consumer_batch: int, rows_ahead: int = 0) -> None:
-    rc = load_library().pi_debug_set_tuning(ctx, prefetch, prefetch_ns, consumer_batch, rows_ahead)
+def pi_debug_set_tuning(ctx: int, prefetch: int, prefetch_ns: int, lookahead: int, rows_ahead: int = 0) -> None:
+    rc = load_library().pi_debug_set_tuning(ctx, prefetch, prefetch_ns, lookahead, rows_ahead)
     _check(ctx, rc, "pi_debug_set_tuning")
 
 

@@ -265,15 +265,16 @@ pi_status pi_debug_barrier_extra(pi_ctx *ctx, int32_t extra);
 pi_status pi_debug_set_timeline(pi_ctx *ctx, uint64_t *stamps, int32_t per_cta);
 
 /* Tuning knobs of the step kernel (also read from PI_PREFETCH, PI_PREFETCH_NS,
- * PI_CB and PI_ROWS_AHEAD at pi_create): prefetch = L2 prefetch of the
- * predictor weights: 0 none; the next layer's slice during the FFN phase,
- * 1 all at once or 2 paced at one 16 KB chunk per prefetch_ns per SM; 3 each
- * layer's W2 slice in one burst as soon as the previous layer's FFN phase is
- * over.  consumer_batch = most ring stages the FFN consumers take per named
- * barrier.  rows_ahead = neurons of an SM's list whose rows are prefetched
- * into L2 ahead of the shared-memory ring (0 none).  Results do not depend on
- * them. */
-pi_status pi_debug_set_tuning(pi_ctx *ctx, int32_t prefetch, int32_t prefetch_ns, int32_t consumer_batch,
+ * PI_LOOKAHEAD and PI_ROWS_AHEAD at pi_create): prefetch = L2 prefetch of the
+ * predictor weights: 0 none (default); the next layer's slice during the FFN
+ * phase, 1 all at once or 2 paced at one 16 KB chunk per prefetch_ns per SM;
+ * 3 each layer's W2 slice in one burst as soon as the previous layer's FFN
+ * phase is over.  lookahead = how many ring stages past the one being merged
+ * an owner warp may compute activations for in the FFN phase (capped at the
+ * ring size minus one; default 16).  rows_ahead = neurons of an SM's list
+ * whose rows are prefetched into L2 ahead of the shared-memory ring (0 none).
+ * Results do not depend on them. */
+pi_status pi_debug_set_tuning(pi_ctx *ctx, int32_t prefetch, int32_t prefetch_ns, int32_t lookahead,
                               int32_t rows_ahead);
 
 /* Copy the first `count` floats of the predictor's hidden layer as the last

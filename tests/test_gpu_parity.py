@@ -236,9 +236,9 @@ def test_predictor_hidden_layer_bit_exact(c64, name):
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
 
 
-@pytest.mark.parametrize("knobs", [(0, 0, 1, 0), (1, 0, 2, 4), (2, 400, 4, 0), (3, 800, 3, 8), (3, 0, 8, 64)])
+@pytest.mark.parametrize("knobs", [(0, 0, 0, 0), (1, 0, 2, 4), (2, 400, 4, 0), (3, 800, 3, 8), (3, 0, 16, 64)])
 def test_tuning_knobs_do_not_change_results(knobs):
-    """Prefetch modes, consumer batching and row prefetch only move data
+    """Prefetch modes, the FFN lookahead and row prefetch only move data
     earlier: a 3-layer decode step is bit-identical under every setting."""
     t = G.torch()
     cfg = CFGS["relu_f16"]
