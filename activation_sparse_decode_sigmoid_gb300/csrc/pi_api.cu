@@ -60,6 +60,11 @@ struct pi_ctx {
     uint64_t *partx = nullptr; // tagged split-K partials [G][max_batch][kMaxD]
     uint64_t *xx = nullptr;    // tagged residual between layers [max_batch][kMaxD]
     float *xstage = nullptr; // [max_batch][kMaxD] residual staging of pi_decode_step_host
+    // tensor-core FFN of large batches: activations, x_hat and the list of one layer
+    uint16_t *actT = nullptr;    // [max_batch][kMaxN]
+    uint16_t *xhat_ws = nullptr; // [max_batch][kMaxD]
+    int32_t *lidx = nullptr;     // [kMaxN] list, then [1] its count
+    int mma_min_b = 8;           // batches of at least this many tokens use the tensor cores (0: never)
     int *ctl = nullptr; // [0..1] grid-barrier counter (u64), [2] status, [3] abort
     // trace
     float *tr_x = nullptr;
@@ -291,7 +296,10 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
                      sizeof(float) * (size_t)max_batch * pi::kMaxD,
                      sizeof(uint64_t) * (size_t)c->G * max_batch * pi::kMaxD,
                      sizeof(uint64_t) * (size_t)max_batch * pi::kMaxD,
-                     sizeof(int) * 64};
+                     sizeof(int) * 64,
+                     sizeof(uint16_t) * (size_t)max_batch * pi::kMaxN,
+                     sizeof(uint16_t) * (size_t)max_batch * pi::kMaxD,
+                     sizeof(int32_t) * ((size_t)pi::kMaxN + 64)};
     constexpr int kBufs = (int)(sizeof need / sizeof need[0]);
     void *ptrs[kBufs] = {};
     for (int i = 0; i < kBufs && e == cudaSuccess; ++i) e = cudaMalloc(&ptrs[i], need[i]);
@@ -310,6 +318,9 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     c->partx = (uint64_t *)ptrs[4];
     c->xx = (uint64_t *)ptrs[5];
     c->ctl = (int *)ptrs[6];
+    c->actT = (uint16_t *)ptrs[7];
+    c->xhat_ws = (uint16_t *)ptrs[8];
+    c->lidx = (int32_t *)ptrs[9];
     *out = c;
     return PI_OK;
 }
@@ -328,6 +339,9 @@ pi_status pi_destroy(pi_ctx *c)
         cudaFree(c->xx);
         cudaFree(c->xstage);
         cudaFree(c->ctl);
+        cudaFree(c->actT);
+        cudaFree(c->xhat_ws);
+        cudaFree(c->lidx);
     }
     delete c;
     return PI_OK;
@@ -519,6 +533,39 @@ pi_status pi_layer_counts(pi_ctx *c, int32_t layer, const void *x_hat, int32_t T
     return PI_OK;
 }
 
+// Batches of at least mma_min_b tokens with 16-bit FFN weights take the
+// tensor-core gather-GEMM (pi_mma.cu); smaller ones, and Q4_0, the step kernel.
+static bool use_mma(const pi_ctx *c, int layer, int B)
+{
+    return c->mma_min_b > 0 && B >= c->mma_min_b && c->layers[layer].desc.w_dtype != PI_Q4_0;
+}
+
+// The FFN of one layer on the tensor cores: into y (16-bit), or added into
+// the fp32 residual x.  idx/count NULL = every neuron.
+static pi_status mma_ffn(pi_ctx *c, int layer, const uint16_t *xhat, int B, const int32_t *idx, const int32_t *count,
+                         uint16_t *y, float *x)
+{
+    const pi_layer_desc &dsc = c->layers[layer].desc;
+    pi::MmaParams q{};
+    q.layer = c->d_layers + layer;
+    q.xhat = xhat;
+    q.B = B;
+    q.Npad = (B + 15) / 16 * 16;
+    q.d = dsc.d_model;
+    q.idx = idx;
+    q.count = count;
+    q.actT = c->actT;
+    q.mstride = pi::kMaxN;
+    q.y = y;
+    q.x = x;
+    q.status = c->ctl + 2;
+    q.abort_flag = c->ctl + 3;
+    q.wait_ns = c->wait_ns;
+    const cudaError_t e = pi::launch_ffn_mma(q, dsc.act_dtype == PI_BF16, dsc.act == PI_REGLU, c->G, c->stream);
+    if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "tensor-core FFN launch: %s", cudaGetErrorString(e));
+    return PI_OK;
+}
+
 pi_status pi_predict(pi_ctx *c, int32_t layer, const void *x_hat, int32_t B, int32_t *idx, int32_t *count)
 {
     if (!c) return PI_ERR_ARG;
@@ -543,6 +590,7 @@ pi_status pi_sparse_ffn(pi_ctx *c, int32_t layer, const void *x_hat, int32_t B, 
     if (st) return st;
     if (!x_hat || !idx || !count || !y) return fail(c, PI_ERR_ARG, "x_hat/idx/count/y NULL");
     DeviceGuard g(c->device);
+    if (use_mma(c, layer, B)) return mma_ffn(c, layer, (const uint16_t *)x_hat, B, idx, count, (uint16_t *)y, nullptr);
     StepParams p{};
     p.xhat_in = (const uint16_t *)x_hat;
     p.idx_in = idx;
@@ -559,6 +607,7 @@ pi_status pi_dense_ffn(pi_ctx *c, int32_t layer, const void *x_hat, int32_t B, v
     if (st) return st;
     if (!x_hat || !y) return fail(c, PI_ERR_ARG, "x_hat/y NULL");
     DeviceGuard g(c->device);
+    if (use_mma(c, layer, B)) return mma_ffn(c, layer, (const uint16_t *)x_hat, B, nullptr, nullptr, (uint16_t *)y, nullptr);
     StepParams p{};
     p.xhat_in = (const uint16_t *)x_hat;
     p.y_out = (uint16_t *)y;
@@ -584,7 +633,36 @@ static pi_status step_common(pi_ctx *c, float *x, int32_t B, int mode)
     int nmax = 0;
     for (int l = 0; l < L; ++l) nmax = std::max(nmax, c->layers[l].desc.d_ffn);
     p.tr_n = nmax;
-    return launch(c, 0, L, B, mode, p);
+    if (!use_mma(c, 0, B)) return launch(c, 0, L, B, mode, p);
+    // Large batch: per layer, the step kernel computes x_hat (CTA 0 writes it
+    // to the workspace through the x_hat trace) and the predicted list (or the
+    // whole list), then the tensor-core FFN adds the layer's output into x.
+    const int d = c->layers[0].desc.d_model;
+    const bool dense = (mode & pi::M_DENSE) != 0;
+    for (int l = 0; l < L; ++l) {
+        StepParams q{};
+        q.x = x;
+        q.tr_x = c->tr_x ? c->tr_x + (size_t)l * B * d : nullptr;
+        q.tr_xhat = c->xhat_ws;
+        q.tr_idx = c->tr_idx ? c->tr_idx + (size_t)l * nmax : nullptr;
+        q.tr_cnt = c->tr_cnt ? c->tr_cnt + l : nullptr;
+        q.tr_n = nmax;
+        q.idx_out = c->lidx;
+        q.count_out = c->lidx + pi::kMaxN;
+        const int m = dense ? (pi::M_RMSNORM | pi::M_DENSE | pi::M_COMPACT)
+                            : (pi::M_RMSNORM | pi::M_PREDICT | pi::M_COMPACT);
+        st = launch(c, l, 1, B, m, q);
+        if (st) return st;
+        if (c->tr_xhat) {
+            const cudaError_t e = cudaMemcpyAsync((uint16_t *)c->tr_xhat + (size_t)l * B * d, c->xhat_ws,
+                                                  (size_t)B * d * 2, cudaMemcpyDeviceToDevice, c->stream);
+            if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "x_hat trace: %s", cudaGetErrorString(e));
+        }
+        st = mma_ffn(c, l, c->xhat_ws, B, dense ? nullptr : c->lidx, dense ? nullptr : c->lidx + pi::kMaxN, nullptr,
+                     x);
+        if (st) return st;
+    }
+    return PI_OK;
 }
 
 pi_status pi_decode_step(pi_ctx *c, float *x, int32_t B)
@@ -687,6 +765,13 @@ pi_status pi_debug_copy_hidden(pi_ctx *c, float *dst, int32_t count)
     const cudaError_t e = cudaMemcpy2DAsync(dst, sizeof(float), c->hx, sizeof(uint64_t), sizeof(float), (size_t)count,
                                             cudaMemcpyDefault, c->stream);
     return e == cudaSuccess ? PI_OK : fail(c, PI_ERR_CUDA, "copy of h: %s", cudaGetErrorString(e));
+}
+
+pi_status pi_debug_set_mma_min_batch(pi_ctx *c, int32_t min_batch)
+{
+    if (!c || min_batch < 0) return PI_ERR_ARG;
+    c->mma_min_b = min_batch;
+    return PI_OK;
 }
 
 pi_status pi_debug_barrier_extra(pi_ctx *c, int32_t extra)

@@ -153,6 +153,22 @@ __host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, in
     return m;
 }
 
+// Parameters of the tensor-core FFN kernels (pi_mma.cu), batches of 8..64.
+struct MmaParams {
+    const LayerDev *layer;   // device pointer to the layer's descriptor
+    const uint16_t *xhat;    // [B][d] 16-bit
+    int B, Npad, d;          // tokens, tokens rounded up to 16, d_model
+    const int32_t *idx;      // [m] physical neuron ids, ascending; NULL = all n neurons (dense)
+    const int32_t *count;    // device m; NULL = n
+    uint16_t *actT;          // [B][mstride] activations, rounded to the weights' type
+    size_t mstride;          // row stride of actT (multiple of 64, >= m rounded up to 64)
+    uint16_t *y;             // [B][d] 16-bit output, or NULL when x is set
+    float *x;                // [B][d] fp32 residual to add into, or NULL
+    int *status;
+    int *abort_flag;
+    unsigned long long wait_ns;
+};
+
 // Launchers (host side of the kernels), in the step/load translation units.
 // tgf: 1 (single-token kernel) or 4 (up to four tokens per FFN pass)
 cudaError_t launch_step_f16(const StepParams &p, int tgf, int grid, cudaStream_t s);
@@ -161,6 +177,8 @@ cudaError_t launch_step_q4(const StepParams &p, int tgf, int grid, cudaStream_t 
 cudaError_t occupancy_step_f16(int tgf, int smem_bytes, int *blocks);
 cudaError_t occupancy_step_bf16(int tgf, int smem_bytes, int *blocks);
 cudaError_t occupancy_step_q4(int tgf, int smem_bytes, int *blocks);
+// the union-mask FFN on tcgen05: up/gate kernel on `grid` SMs, then the down kernel
+cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, cudaStream_t s);
 
 cudaError_t launch_permute_rows(const void *src, void *dst, const int32_t *perm, int rows, size_t rowBytes,
                                 cudaStream_t s, size_t dstStride = 0);

@@ -1243,6 +1243,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
     for (int l = 0; l < p.L; ++l) {
         const LayerDev L = p.layers[l];
         const int ev = 1 + l * kTimelineEvents;
+        if ((p.mode & M_RMSNORM) && !pred && !(p.mode & M_FFN)) {
+            // x_hat only (for the tensor-core FFN of large batches): CTA 0
+            // writes it through the x_hat trace; with M_DENSE | M_COMPACT
+            // the whole list follows
+            if (blockIdx.x == 0)
+                for (int t0 = 0; t0 < p.B; t0 += p.tg)
+                    if (!stage_xhat<T>(p, S, l, t0, min(p.tg, p.B - t0))) return;
+            if (!(p.mode & M_COMPACT)) continue;
+        }
         if (pred) {
             if (!phase_a<T>(p, S, L, l, ss)) return;
             mark(p, ev + 0);

@@ -31,7 +31,8 @@ EXPORTS = ("pi_create", "pi_destroy", "pi_set_stream", "pi_load_layer", "pi_laye
            "pi_decode_step_host",
            "pi_dense_step", "pi_set_trace", "pi_sync_status", "pi_last_error", "pi_grid_size",
            "pi_debug_set_wait_limit", "pi_debug_barrier_extra", "pi_debug_set_timeline",
-           "pi_debug_set_tuning", "pi_debug_copy_hidden", "pi_sparse_ffn_noalloc")
+           "pi_debug_set_tuning", "pi_debug_copy_hidden", "pi_debug_set_mma_min_batch",
+           "pi_sparse_ffn_noalloc")
 
 
 class PiError(RuntimeError):
@@ -92,6 +93,7 @@ def load_library(path: str = LIB_PATH):
         "pi_debug_set_timeline": (st, [P, P, I32]),
         "pi_debug_set_tuning": (st, [P, I32, I32, I32, I32]),
         "pi_debug_copy_hidden": (st, [P, P, I32]),
+        "pi_debug_set_mma_min_batch": (st, [P, I32]),
         "pi_sparse_ffn_noalloc": (st, [ctypes.POINTER(pi_ffn_rows), P, I32, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -231,6 +233,10 @@ def pi_debug_set_tuning(ctx: int, prefetch: int, prefetch_ns: int, lookahead: in
 
 def pi_debug_copy_hidden(ctx: int, dst, count: int) -> None:
     _check(ctx, load_library().pi_debug_copy_hidden(ctx, _ptr(dst), count), "pi_debug_copy_hidden")
+
+
+def pi_debug_set_mma_min_batch(ctx: int, min_batch: int) -> None:
+    _check(ctx, load_library().pi_debug_set_mma_min_batch(ctx, min_batch), "pi_debug_set_mma_min_batch")
 
 
 def pi_debug_barrier_extra(ctx: int, extra: int) -> None:

@@ -284,6 +284,11 @@ pi_status pi_debug_set_tuning(pi_ctx *ctx, int32_t prefetch, int32_t prefetch_ns
  * most max_batch * 2048. */
 pi_status pi_debug_copy_hidden(pi_ctx *ctx, float *dst, int32_t count);
 
+/* Smallest batch (tokens) whose FFN runs on the tensor cores (tcgen05
+ * gather-GEMM, 16-bit weights; default 8); 0 keeps every batch on the step
+ * kernel's CUDA-core path.  For comparing the two paths. */
+pi_status pi_debug_set_mma_min_batch(pi_ctx *ctx, int32_t min_batch);
+
 #ifdef __cplusplus
 }
 #endif

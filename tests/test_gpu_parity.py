@@ -147,14 +147,14 @@ def test_layer_counts_and_calibrated_permutation(c64):
 
 
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4"])
-@pytest.mark.parametrize("B", [1, 3])
+@pytest.mark.parametrize("B", [1, 3, 8, 16])
 @pytest.mark.parametrize("dense", [False, True])
 def test_decode_stack_teacher_forced(name, B, dense):
     """Three-layer stack, one persistent launch: per layer the oracle consumes
     the GPU's x_hat (trace) and must give the same list and the same update."""
     t = G.torch()
     cfg = CFGS[name]
-    c = G.ctx(max_layers=3, max_batch=8)
+    c = G.ctx(max_layers=3, max_batch=max(8, B))
     layers, perms = [], []
     for l in range(3):
         lw = W.make_layer(cfg, l, 0, random_b1=True, random_bdown=True)
@@ -234,6 +234,37 @@ def test_predictor_hidden_layer_bit_exact(c64, name):
     want = O.layer_predict(layer, x)["h"].astype(np.float32)
     got = h.cpu().numpy().reshape(B, cfg.r)
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16"])
+@pytest.mark.parametrize("B", [8, 16, 40, 64])
+def test_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
+    """Batches of 8+ tokens run the FFN as a gather-GEMM on tcgen05 (A^T
+    rounded to the weights' 16-bit type between the two GEMMs); it must match
+    the oracle within the usual tolerance, and the CUDA-core path of the step
+    kernel on the same list within twice it."""
+    t = G.torch()
+    cfg, layer = _layer(name)
+    c64.load_layer(0, layer)
+    x = W.xhat_inputs(cfg, B, 23 + B)
+    xd = G.dev16(x)
+    idx, cnt = c64.predict(0, xd)
+    y_tc = c64.sparse_ffn(0, xd, idx, cnt)
+    c64.check()
+    pi.pi_debug_set_mma_min_batch(c64.handle, 0)
+    y_cc = c64.sparse_ffn(0, xd, idx, cnt)
+    c64.check()
+    pi.pi_debug_set_mma_min_batch(c64.handle, 8)
+    m = int(cnt.item())
+    oidx = np.sort(idx[:m].cpu().numpy())
+    got = G.y_to_f64(y_tc, cfg.act_dtype)
+    want = O.masked_ffn(layer, x, oidx)
+    assert max_rel_err(got, want) <= G.tol(layer)
+    assert max_rel_err(got, G.y_to_f64(y_cc, cfg.act_dtype)) <= 2 * G.tol(layer)
+    # the dense variant (every neuron) on the same path
+    yd = c64.dense_ffn(0, xd)
+    c64.check()
+    assert max_rel_err(G.y_to_f64(yd, cfg.act_dtype), O.masked_ffn(layer, x, np.arange(cfg.n))) <= G.tol(layer)
 
 
 @pytest.mark.parametrize("knobs", [(0, 0, 0, 0), (1, 0, 2, 4), (2, 400, 4, 0), (3, 800, 3, 8), (3, 0, 16, 64)])
