@@ -25,6 +25,9 @@ struct LayerSlot {
     pi_layer_desc desc{};
     LayerDev dev{};
     std::vector<void *> bufs;
+    // TMA maps of the 16-bit FFN rows for the tensor-core path (one-row boxes for gather4)
+    bool maps = false;
+    CUtensorMap tm_up{}, tm_gate{}, tm_dn{};
 };
 
 int round_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -64,6 +67,7 @@ struct pi_ctx {
     uint16_t *actT = nullptr;    // [max_batch][kMaxN]
     uint16_t *xhat_ws = nullptr; // [max_batch][kMaxD]
     int32_t *lidx = nullptr;     // [kMaxN] list, then [1] its count
+    float *mpart = nullptr;      // [8][max_batch][kMaxD] partials of the tensor-core down-projection
     int mma_min_b = 8;           // batches of at least this many tokens use the tensor cores (0: never)
     int *ctl = nullptr; // [0..1] grid-barrier counter (u64), [2] status, [3] abort
     // trace
@@ -299,7 +303,8 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
                      sizeof(int) * 64,
                      sizeof(uint16_t) * (size_t)max_batch * pi::kMaxN,
                      sizeof(uint16_t) * (size_t)max_batch * pi::kMaxD,
-                     sizeof(int32_t) * ((size_t)pi::kMaxN + 64)};
+                     sizeof(int32_t) * ((size_t)pi::kMaxN + 64),
+                     sizeof(float) * 8 * (size_t)max_batch * pi::kMaxD};
     constexpr int kBufs = (int)(sizeof need / sizeof need[0]);
     void *ptrs[kBufs] = {};
     for (int i = 0; i < kBufs && e == cudaSuccess; ++i) e = cudaMalloc(&ptrs[i], need[i]);
@@ -321,6 +326,7 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     c->actT = (uint16_t *)ptrs[7];
     c->xhat_ws = (uint16_t *)ptrs[8];
     c->lidx = (int32_t *)ptrs[9];
+    c->mpart = (float *)ptrs[10];
     *out = c;
     return PI_OK;
 }
@@ -342,6 +348,7 @@ pi_status pi_destroy(pi_ctx *c)
         cudaFree(c->actT);
         cudaFree(c->xhat_ws);
         cudaFree(c->lidx);
+        cudaFree(c->mpart);
     }
     delete c;
     return PI_OK;
@@ -503,6 +510,13 @@ pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, con
     }
     s.desc = *desc;
     s.loaded = true;
+    s.maps = false;
+    if (!q4) {
+        cudaError_t me = pi::encode_map(&s.tm_up, pup, (uint64_t)d, (uint64_t)n, (uint64_t)rowB + 16, 1);
+        if (me == cudaSuccess && reglu) me = pi::encode_map(&s.tm_gate, pgate, (uint64_t)d, (uint64_t)n, (uint64_t)rowB, 1);
+        if (me == cudaSuccess) me = pi::encode_map(&s.tm_dn, pdn, (uint64_t)d, (uint64_t)n, (uint64_t)rowB, 1);
+        s.maps = me == cudaSuccess; // without maps the layer keeps the CUDA-core path
+    }
     return PI_OK;
 }
 
@@ -537,7 +551,8 @@ pi_status pi_layer_counts(pi_ctx *c, int32_t layer, const void *x_hat, int32_t T
 // tensor-core gather-GEMM (pi_mma.cu); smaller ones, and Q4_0, the step kernel.
 static bool use_mma(const pi_ctx *c, int layer, int B)
 {
-    return c->mma_min_b > 0 && B >= c->mma_min_b && c->layers[layer].desc.w_dtype != PI_Q4_0;
+    return c->mma_min_b > 0 && B >= c->mma_min_b && c->layers[layer].desc.w_dtype != PI_Q4_0 &&
+           c->layers[layer].maps;
 }
 
 // The FFN of one layer on the tensor cores: into y (16-bit), or added into
@@ -545,8 +560,18 @@ static bool use_mma(const pi_ctx *c, int layer, int B)
 static pi_status mma_ffn(pi_ctx *c, int layer, const uint16_t *xhat, int B, const int32_t *idx, const int32_t *count,
                          uint16_t *y, float *x)
 {
-    const pi_layer_desc &dsc = c->layers[layer].desc;
+    const LayerSlot &ls = c->layers[layer];
+    const pi_layer_desc &dsc = ls.desc;
     pi::MmaParams q{};
+    q.tm_up = ls.tm_up;
+    q.tm_gate = ls.tm_gate;
+    q.tm_dn = ls.tm_dn;
+    const int np = (B + 15) / 16 * 16;
+    if (reinterpret_cast<uintptr_t>(xhat) & 15u) return fail(c, PI_ERR_ARG, "x_hat must be 16-byte aligned");
+    cudaError_t me = pi::encode_map(&q.tm_x, xhat, (uint64_t)dsc.d_model, (uint64_t)B, (uint64_t)dsc.d_model * 2, np);
+    if (me == cudaSuccess)
+        me = pi::encode_map(&q.tm_act, c->actT, (uint64_t)pi::kMaxN, (uint64_t)B, (uint64_t)pi::kMaxN * 2, np);
+    if (me != cudaSuccess) return fail(c, PI_ERR_CUDA, "tensor map: %s", cudaGetErrorString(me));
     q.layer = c->d_layers + layer;
     q.xhat = xhat;
     q.B = B;
@@ -558,6 +583,7 @@ static pi_status mma_ffn(pi_ctx *c, int layer, const uint16_t *xhat, int B, cons
     q.mstride = pi::kMaxN;
     q.y = y;
     q.x = x;
+    q.part = c->mpart;
     q.status = c->ctl + 2;
     q.abort_flag = c->ctl + 3;
     q.wait_ns = c->wait_ns;

@@ -1,6 +1,7 @@
 // Structures shared by the host side of libpi and its kernels.
 #pragma once
 
+#include <cuda.h> // CUtensorMap (types only; the encoder is fetched from the driver at run time)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -155,6 +156,10 @@ __host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, in
 
 // Parameters of the tensor-core FFN kernels (pi_mma.cu), batches of 8..64.
 struct MmaParams {
+    // TMA maps (16-bit elements, 64-column boxes, 128-byte swizzle): the
+    // layer's W_up / W_gate / W_down^T rows (one-row boxes, for gather4),
+    // x_hat and A^T (tile boxes of Npad rows; rows past B read as zeros)
+    CUtensorMap tm_up, tm_gate, tm_dn, tm_x, tm_act;
     const LayerDev *layer;   // device pointer to the layer's descriptor
     const uint16_t *xhat;    // [B][d] 16-bit
     int B, Npad, d;          // tokens, tokens rounded up to 16, d_model
@@ -164,6 +169,7 @@ struct MmaParams {
     size_t mstride;          // row stride of actT (multiple of 64, >= m rounded up to 64)
     uint16_t *y;             // [B][d] 16-bit output, or NULL when x is set
     float *x;                // [B][d] fp32 residual to add into, or NULL
+    float *part;             // [8][B][d] fp32 partials of column blocks split over list shares
     int *status;
     int *abort_flag;
     unsigned long long wait_ns;
@@ -179,6 +185,9 @@ cudaError_t occupancy_step_bf16(int tgf, int smem_bytes, int *blocks);
 cudaError_t occupancy_step_q4(int tgf, int smem_bytes, int *blocks);
 // the union-mask FFN on tcgen05: up/gate kernel on `grid` SMs, then the down kernel
 cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, cudaStream_t s);
+// a 2D TMA map over a row-major 16-bit matrix: box = 64 columns x box_rows rows, 128-byte swizzle
+cudaError_t encode_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                       uint32_t box_rows);
 
 cudaError_t launch_permute_rows(const void *src, void *dst, const int32_t *perm, int rows, size_t rowBytes,
                                 cudaStream_t s, size_t dstStride = 0);

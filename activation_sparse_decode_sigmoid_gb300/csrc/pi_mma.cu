@@ -12,20 +12,21 @@
 //
 // Two kernels, both on tcgen05 with the accumulators in tensor memory:
 //   ffn_up_mma    neuron-parallel: SM c takes the equal slice [s0, s1) of the
-//                 list, gathers 128 rows at a time (cp.async, 128-byte
-//                 swizzle), D = W_rows (M = 128, K-major) x X_hat^T (N = B
-//                 rounded up to 16, K-major), K = d_model in steps of 64;
-//                 the epilogue applies the activation and writes A^T [B][m]
-//                 rounded to the weights' 16-bit type (the product of a
+//                 list, up to 256 gathered rows per pass (TMA tile::gather4,
+//                 128-byte swizzle), D = W_rows (two M = 128 tiles, K-major) x X_hat^T
+//                 (N = B rounded up to 16, K-major), K = d_model in steps of
+//                 64; the epilogue applies the activation and writes A^T
+//                 [B][m] rounded to the weights' 16-bit type (the product of a
 //                 16-bit GEMM takes both operands in one type).
-//   ffn_down_mma  column-parallel: SM c owns 64-column tiles of the output,
-//                 D = A^T (M = 128 token rows, zero past B, K-major) x
-//                 W_down^T rows (N = 64 columns, MN-major), K = the list in
-//                 steps of 64 neurons; the epilogue adds b_down and writes y
-//                 (16-bit) or adds into the fp32 residual x.  Every output
-//                 column has one owner: no split-K partials, no merge.
-// Between the two kernels A^T goes through global memory (m * B * 2 bytes,
-// small next to the rows); stream order separates them.
+//   ffn_down_mma  column blocks of 256 x shares of the list: D = W_down^T
+//                 (M = 128 columns per tile, MN-major: 512-byte segments of
+//                 the gathered rows, by gather4) x A^T (N = B rounded up to 16, K-major),
+//                 K = the share of the list in steps of 64 neurons; the
+//                 epilogue adds b_down and writes y (16-bit) or adds into the
+//                 fp32 residual x, or, when a block has several shares, fp32
+//                 partials that ffn_merge adds in share order.
+// Between the kernels A^T goes through global memory (m * B * 2 bytes, small
+// next to the rows); stream order separates them.
 //
 // Shared-memory operand layouts are the canonical 128-byte-swizzle layouts:
 // a "row" of 128 bytes (64 16-bit elements) at 128-byte pitch, 16-byte chunk
@@ -40,8 +41,8 @@
 namespace pi {
 namespace {
 
-constexpr int kMT = 128;      // threads per CTA (4 warps: TMEM lanes 0..127)
-constexpr int kStages = 4;    // pipeline depth
+constexpr int kIssuers = 5;                // TMA producer warps
+constexpr int kMT = 32 * (kIssuers + 1);  // + the MMA warp; warps 0..3 (TMEM lanes 0..127) run the epilogues
 constexpr int kBK = 64;       // K elements per stage (one 128-byte row)
 constexpr uint32_t kTileA = 16384; // 128 rows x 128 bytes
 constexpr uint32_t kTileX = 8192;  // up to 64 rows x 128 bytes
@@ -73,24 +74,18 @@ __device__ __forceinline__ void fail(const MmaParams &p, int code)
     atomicExch(p.abort_flag, 1);
 }
 
-// byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled tile
-__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk)
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count)
 {
-    return (row >> 3) * 1024u + (row & 7u) * 128u + ((chunk ^ (row & 7u)) << 4);
+    asm volatile("mbarrier.init.shared.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count));
 }
+__device__ __forceinline__ void mbar_init1(uint64_t *b) { mbar_init(b, 1); }
 
-// 16-byte global -> shared copy; n = 0 writes zeros and reads nothing
-__device__ __forceinline__ void cp16(uint32_t dst, const void *src, uint32_t n)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N> __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__device__ __forceinline__ void mbar_init1(uint64_t *b)
-{
-    asm volatile("mbarrier.init.shared.b64 [%0], 1;" ::"r"(smem_addr(b)));
-}
+// TMA issue is split over the producer warps (one lane each): warp 0 and
+// warps 2.. take every kIssuers-th load of a stage and each posts its own
+// expected bytes on the stage's full barrier (kIssuers arrivals); warp 1
+// issues the MMAs.  One lane issues TMA loads at a limited rate, so several
+// are needed to keep enough bytes in flight.
+__device__ __forceinline__ int issuer_index(int warp) { return warp == 0 ? 0 : (warp >= 2 ? warp - 1 : -1); }
 
 // bounded wait for the phase of the given parity; false after the wait limit or an abort
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *b, uint32_t parity, const MmaParams &p)
@@ -191,141 +186,161 @@ __device__ __forceinline__ int list_len(const MmaParams &p, int n)
     return m;
 }
 
+// ------------------------------------------------------------------ TMA
+__device__ __forceinline__ void mbar_expect(uint64_t *b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
+}
+
+// rows r0..r3 (tensor-map row indices; out-of-range rows read as zeros) x 64
+// columns from column `col` into 4 consecutive 128-byte rows at dst, swizzled
+__device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap *tm, int col, int r0, int r1, int r2, int r3,
+                                        uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+                 "l"(tm), "r"(smem_addr(bar)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
+// a box of 64 columns x box-rows rows at (col, row)
+__device__ __forceinline__ void tile_load(uint32_t dst, const CUtensorMap *tm, int col, int row, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+                     dst),
+                 "l"(tm), "r"(smem_addr(bar)), "r"(col), "r"(row)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------ up / gate kernel
-template <typename T, bool REGLU>
-__global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const MmaParams p)
+// Rows of the SM's slice are taken up to 256 at a time (two 128-row MMA
+// tiles share each K step, so a short slice does not cost a second pass).
+// Warp 0 (one lane) produces: per stage, gather4 loads of the rows' next 64
+// columns (W_up, W_gate) and a tile load of x_hat; warp 1 (one lane) issues
+// the MMAs and commits each stage back to the producer; all four warps run
+// the epilogue.  Rows past the slice are gathered from row n (out of range:
+// zeros) or left stale; their accumulator rows are never read.
+template <typename T, bool REGLU, int STAGES>
+__global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ MmaParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     using H = H16<T>;
     const LayerDev &L = *p.layer;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = L.d, n = L.n, B = p.B, Np = p.Npad;
-    constexpr uint32_t kStage = kTileA * (REGLU ? 2 : 1) + kTileX;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kStages * kStage); // [kStages] MMA done per stage
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + kStages);
-    int *sid = reinterpret_cast<int *>(tslot + 4); // [128] row ids of the current tile
+    constexpr uint32_t kW = 2 * kTileA; // 256 rows x 128 bytes of one weight matrix
+    constexpr uint32_t kStage = kW * (REGLU ? 2 : 1) + kTileX;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * kStage);
+    uint64_t *empty = full + STAGES;
+    uint64_t *done = empty + STAGES;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
+    int *sid = reinterpret_cast<int *>(tslot + 4); // [256] row ids of the current pass
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init1(bar + s);
+        for (int s = 0; s < STAGES; ++s) mbar_init(full + s, kIssuers), mbar_init1(empty + s);
+        mbar_init1(done);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    const uint32_t tmem = tmem_alloc(tslot, 128); // U at columns [0, Np), gate at [Np, 2 Np)
+    // TMEM: tile j (0, 1) of U at columns [j Np, (j+1) Np), of the gate at [(2+j) Np, ...)
+    const uint32_t tmem = tmem_alloc(tslot, 256);
     const int m = list_len(p, n);
     const int s0 = slice_at(m, blockIdx.x, gridDim.x), s1 = slice_at(m, blockIdx.x + 1, gridDim.x);
     const int KT = (d + kBK - 1) / kBK;
     const uint32_t base = smem_addr(smem);
     const uint32_t id_up = idesc(H::fmt, 0, 0, 128, (uint32_t)Np);
-    uint32_t g = 0; // stages consumed so far by this CTA (ring position and mbarrier phase)
+    uint32_t gp = 0, gc = 0, pass = 0; // stages produced / consumed, passes
     bool ok = true;
 
-    // rows padded beyond d read nothing (zeros)
-    auto load = [&](uint32_t st, int kt) {
-        const uint32_t sbase = base + st * kStage;
-        const int col = kt * kBK;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) { // 128 rows x 8 chunks of W_up (and W_gate)
-            const int q = tid + i * kMT, r = q >> 3, ch = q & 7;
-            const int id = sid[r];
-            const int c = col + ch * 8;
-            const bool v = id >= 0 && c < d;
-            const uint8_t *src = v ? L.up + (size_t)id * L.upB + (size_t)c * 2 : L.up;
-            cp16(sbase + sw128(r, ch), src, v ? 16u : 0u);
-            if (REGLU) {
-                const uint8_t *sg = v ? L.gate + (size_t)id * L.rowB + (size_t)c * 2 : L.gate;
-                cp16(sbase + kTileA + sw128(r, ch), sg, v ? 16u : 0u);
-            }
-        }
-        for (int q = tid; q < Np * 8; q += kMT) { // x_hat rows (tokens) x 8 chunks
-            const int t = q >> 3, ch = q & 7, c = col + ch * 8;
-            const bool v = t < B && c < d;
-            const uint16_t *src = v ? p.xhat + (size_t)t * d + c : p.xhat;
-            cp16(sbase + kTileA * (REGLU ? 2 : 1) + sw128(t, ch), src, v ? 16u : 0u);
-        }
-    };
-
-    for (int r0 = s0; r0 < s1; r0 += 128) {
-        const int rows = min(128, s1 - r0);
-        {
-            int id = -1;
-            if (tid < rows) {
-                id = p.idx ? p.idx[r0 + tid] : r0 + tid;
+    for (int r0 = s0; r0 < s1; r0 += 256, ++pass) {
+        const int rows = min(256, s1 - r0);
+        const int ntile = (rows + 127) / 128;
+        for (int r = tid; r < 256; r += kMT) {
+            int id = n; // out of range: zeros
+            if (r < rows) {
+                id = p.idx ? p.idx[r0 + r] : r0 + r;
                 if (id < 0 || id >= n) {
                     fail(p, PI_DEV_FLAG);
-                    id = -1;
+                    id = n;
                 }
             }
-            sid[tid] = id;
+            sid[r] = id;
         }
         __syncthreads();
-        // prologue: stages 0 .. kStages-2
-        for (int s = 0; s < kStages - 1; ++s) {
-            if (s < KT) load((g + s) % kStages, s);
-            cp_commit();
-        }
-        for (int kt = 0; kt < KT; ++kt) {
-            const uint32_t st = (g + kt) % kStages;
-            cp_wait<kStages - 2>(); // this thread's copies of stage kt have landed
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncthreads();        // ... and everyone's
-            if (tid == 0) {
+        const int iss = issuer_index(warp);
+        if (iss >= 0 && lane == 0) {
+            const int nq = (rows + 3) / 4;
+            const int mine = (nq - iss + kIssuers - 1) / kIssuers; // gathers q = iss, iss + 3, ...
+            const uint32_t bytes = (uint32_t)mine * 512u * (REGLU ? 2u : 1u) + (iss == 0 ? (uint32_t)Np * 128u : 0u);
+            for (int kt = 0; kt < KT && ok; ++kt, ++gp) {
+                const uint32_t st = gp % STAGES;
+                if (gp >= STAGES && !mbar_wait_bounded(empty + st, ((gp / STAGES) - 1) & 1, p)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sb = base + st * kStage;
+                mbar_expect(full + st, bytes);
+                for (int q = iss; q < nq; q += kIssuers) {
+                    const int r = 4 * q;
+                    const uint32_t dst = sb + (uint32_t)(r >> 7) * kTileA + (uint32_t)(r & 127) * 128u;
+                    gather4(dst, &p.tm_up, kt * kBK, sid[r], sid[r + 1], sid[r + 2], sid[r + 3], full + st);
+                    if (REGLU) gather4(dst + kW, &p.tm_gate, kt * kBK, sid[r], sid[r + 1], sid[r + 2], sid[r + 3], full + st);
+                }
+                if (iss == 0) tile_load(sb + kW * (REGLU ? 2 : 1), &p.tm_x, kt * kBK, 0, full + st);
+            }
+        } else if (warp == 1 && lane == 0) {
+            for (int kt = 0; kt < KT && ok; ++kt, ++gc) {
+                const uint32_t st = gc % STAGES;
+                if (!mbar_wait_bounded(full + st, (gc / STAGES) & 1, p)) {
+                    ok = false;
+                    break;
+                }
                 tc_after();
                 const uint32_t sb = base + st * kStage;
-                const uint32_t xb = sb + kTileA * (REGLU ? 2 : 1);
+                const uint32_t xb = sb + kW * (REGLU ? 2 : 1);
 #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k) {
                     const uint64_t bx = sdesc(xb + k * 32, 16, 1024);
-                    mma(tmem, sdesc(sb + k * 32, 16, 1024), bx, id_up, (kt | k) != 0);
-                    if (REGLU) mma(tmem + (uint32_t)Np, sdesc(sb + kTileA + k * 32, 16, 1024), bx, id_up, (kt | k) != 0);
+                    for (int j = 0; j < ntile; ++j) {
+                        mma(tmem + (uint32_t)(j * Np), sdesc(sb + j * kTileA + k * 32, 16, 1024), bx, id_up,
+                            (kt | k) != 0);
+                        if (REGLU)
+                            mma(tmem + (uint32_t)((2 + j) * Np), sdesc(sb + kW + j * kTileA + k * 32, 16, 1024), bx,
+                                id_up, (kt | k) != 0);
+                    }
                 }
-                mma_commit(bar + st);
+                mma_commit(empty + st);
             }
-            // refill the stage that K-step kt-1 used, once its MMAs are done
-            const int nk = kt + kStages - 1;
-            if (nk < KT) {
-                if (kt >= 1) {
-                    const uint32_t gp = g + kt - 1;
-                    if (ok && !mbar_wait_bounded(bar + gp % kStages, (gp / kStages) & 1, p)) ok = false;
-                }
-                load((g + nk) % kStages, nk);
-            }
-            cp_commit();
+            mma_commit(done);
         }
-        // the last commit covers every MMA of the tile
-        {
-            const uint32_t gl = g + KT - 1;
-            if (ok && !mbar_wait_bounded(bar + gl % kStages, (gl / kStages) & 1, p)) ok = false;
-        }
-        // every stage's last use must be waited for once, so the phases stay in step
-        for (int s = 0; s < kStages - 1 && s < KT - 1; ++s) {
-            const uint32_t gp = g + KT - 2 - s;
-            if (ok && !mbar_wait_bounded(bar + gp % kStages, (gp / kStages) & 1, p)) ok = false;
-        }
-        g += (uint32_t)KT;
+        __syncwarp(); // (gp lives in the producer lane, gc in the MMA lane)
+        if (!mbar_wait_bounded(done, pass & 1, p)) ok = false;
         tc_after();
-        // epilogue: thread = neuron row r of the tile (TMEM lane), 16 token columns at a time
-        const int r = warp * 32 + lane;
-        const int id = sid[r];
-        float bias = 0.f;
-        if (id >= 0)
-            bias = L.bias_tail ? H::one(*reinterpret_cast<const uint16_t *>(L.up + (size_t)id * L.upB + L.rowB))
-                               : H::one(L.b[id]);
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-        for (int c0 = 0; c0 < Np; c0 += 16) {
-            float u[16], gt[16];
-            tmem_ld16(lane_addr + (uint32_t)c0, u);
-            if (REGLU) tmem_ld16(lane_addr + (uint32_t)(Np + c0), gt);
-            if (r < rows && ok) {
+        // epilogue (warps 0..3): thread = row r of tile j (TMEM lane), 16 token columns at a time
+        for (int j = 0; j < ntile && warp < 4; ++j) {
+            const int r = j * 128 + warp * 32 + lane;
+            const int id = sid[r];
+            float bias = 0.f;
+            if (id < n)
+                bias = L.bias_tail ? H::one(*reinterpret_cast<const uint16_t *>(L.up + (size_t)id * L.upB + L.rowB))
+                                   : H::one(L.b[id]);
+            const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+            for (int c0 = 0; c0 < Np; c0 += 16) {
+                float u[16], gt[16];
+                tmem_ld16(lane_addr + (uint32_t)(j * Np + c0), u);
+                if (REGLU) tmem_ld16(lane_addr + (uint32_t)((2 + j) * Np + c0), gt);
+                if (r < rows && ok) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = c0 + j;
-                    if (t < B) {
-                        const float a = REGLU ? fmaxf(gt[j] + bias, 0.f) * u[j] : fmaxf(u[j] + bias, 0.f);
-                        p.actT[(size_t)t * p.mstride + r0 + r] = H::round(id >= 0 ? a : 0.f);
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int t = c0 + jj;
+                        if (t < B) {
+                            const float a = REGLU ? fmaxf(gt[jj] + bias, 0.f) * u[jj] : fmaxf(u[jj] + bias, 0.f);
+                            p.actT[(size_t)t * p.mstride + r0 + r] = H::round(id < n ? a : 0.f);
+                        }
                     }
                 }
             }
         }
         tc_before();
-        __syncthreads(); // TMEM and sid are reused by the next tile
+        __syncthreads(); // TMEM and sid are reused by the next pass
         tc_after();
     }
     // the list's tail up to a whole 64-neuron step reads as zeros in the down kernel
@@ -336,118 +351,131 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const MmaParams p)
             p.actT[(size_t)t * p.mstride + i] = 0;
         }
     }
-    cp_wait<0>();
-    tmem_free(tmem, 128);
+    tmem_free(tmem, 256);
 }
 
 // ------------------------------------------------------------------ down kernel
-template <typename T>
-__global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const MmaParams p)
+// Work unit u = (256-column block cb, share ks of the list).  For each of the
+// block's two 128-column tiles, D[128 columns x Np tokens] = W_down^T (MN-
+// major A: per stage 64 neurons x 256 columns, four 64-column atoms filled by
+// gather4) x A^T (K-major B: a tile load of tokens x 64 neurons).  When the
+// list is split over several shares, the units write fp32 partials that
+// ffn_merge adds in share order; with one share the unit writes y or x.
+template <typename T, int STAGES>
+__global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ MmaParams p, int nks)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     using H = H16<T>;
     const LayerDev &L = *p.layer;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int d = L.d, n = L.n, B = p.B;
-    constexpr uint32_t kStage = kTileA + kTileX; // A^T rows (128 x 64 neurons) + W_down^T (64 neurons x 64 columns)
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kStages * kStage);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + kStages);
+    const int d = L.d, n = L.n, B = p.B, Np = p.Npad;
+    constexpr uint32_t kAtom = 8192;   // 64 neurons x 64 columns (128 bytes)
+    constexpr uint32_t kW = 4 * kAtom; // 64 neurons x 256 columns
+    constexpr uint32_t kStage = kW + kTileX;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * kStage);
+    uint64_t *empty = full + STAGES;
+    uint64_t *done = empty + STAGES;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
+    int *sidd = reinterpret_cast<int *>(tslot + 4); // [kIssuers][64] ids of the stage each producer is on
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init1(bar + s);
+        for (int s = 0; s < STAGES; ++s) mbar_init(full + s, kIssuers), mbar_init1(empty + s);
+        mbar_init1(done);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // token rows B..127 of every A^T stage stay zero
-    for (int q = tid; q < kStages * (int)kTileA / 16; q += kMT) {
-        const int s = q / ((int)kTileA / 16), o = q % ((int)kTileA / 16);
-        const int row = (o * 16) / 128;
-        if (row >= B) *reinterpret_cast<uint4 *>(smem + s * kStage + o * 16) = make_uint4(0, 0, 0, 0);
-    }
-    const uint32_t tmem = tmem_alloc(tslot, 64);
+    const uint32_t tmem = tmem_alloc(tslot, 128); // tile j at columns [j Np, (j+1) Np)
     const int m = list_len(p, n);
-    const int KT = (m + kBK - 1) / kBK;
-    const int ntile = (d + 63) / 64;
+    const int KTall = (m + kBK - 1) / kBK;
+    const int ncb = (d + 255) / 256;
     const uint32_t base = smem_addr(smem);
-    const uint32_t id_dn = idesc(H::fmt, 0, 1, 128, 64);
-    uint32_t g = 0;
+    const uint32_t id_dn = idesc(H::fmt, 1, 0, 128, (uint32_t)Np);
+    const int iss = issuer_index(warp);
+    // 64 gathers per stage (4 column atoms x 16 groups of 4 neurons): g = iss, iss + 3, ...
+    const uint32_t bytes = (uint32_t)((64 - iss + kIssuers - 1) / kIssuers) * 512u + (iss == 0 ? (uint32_t)Np * 128u : 0u);
+    int *myids = sidd + (iss < 0 ? 0 : iss) * 64;
+    uint32_t gp = 0, gc = 0, pass = 0;
     bool ok = true;
 
-    for (int tile = blockIdx.x; tile < ntile; tile += gridDim.x) {
-        const int c0 = tile * 64;
-        auto load = [&](uint32_t st, int kt) {
-            const uint32_t sbase = base + st * kStage;
-            const int k0 = kt * kBK;
-            for (int q = tid; q < B * 8; q += kMT) { // A^T: token rows x 8 chunks of 8 neurons
-                const int t = q >> 3, ch = q & 7;
-                cp16(sbase + sw128(t, ch), p.actT + (size_t)t * p.mstride + k0 + ch * 8, 16u);
-            }
+    for (int u = blockIdx.x; u < ncb * nks; u += gridDim.x, ++pass) {
+        const int cb = u / nks, ks = u % nks;
+        const int c0 = cb * 256;
+        const int k_lo = slice_at(KTall, ks, nks), KT = slice_at(KTall, ks + 1, nks) - k_lo;
+        if (iss >= 0) {
+            for (int kt = 0; kt < KT; ++kt, ++gp) {
+                const uint32_t st = gp % STAGES;
+                const int k0 = (k_lo + kt) * kBK;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) { // W_down^T: 64 neuron rows x 8 chunks of 8 columns
-                const int q = tid + i * kMT, j = q >> 3, ch = q & 7;
-                const int pos = k0 + j, c = c0 + ch * 8;
-                int id = -1;
-                if (pos < m) {
-                    id = p.idx ? p.idx[pos] : pos;
-                    if (id < 0 || id >= n) id = -1; // flagged by the up kernel
+                for (int h = 0; h < 2; ++h) {
+                    const int pos = k0 + lane + 32 * h;
+                    int id = n; // past the list: zeros (their A^T entries are 0, but 0 x garbage could be NaN)
+                    if (pos < m) {
+                        id = p.idx ? p.idx[pos] : pos;
+                        if (id < 0 || id >= n) id = n; // flagged by the up kernel
+                    }
+                    myids[lane + 32 * h] = id;
                 }
-                const bool v = id >= 0 && c < d;
-                const uint8_t *src = v ? L.dn + (size_t)id * L.rowB + (size_t)c * 2 : L.dn;
-                cp16(sbase + kTileA + sw128(j, ch), src, v ? 16u : 0u);
+                __syncwarp();
+                if (lane == 0 && ok) {
+                    if (gp >= STAGES && !mbar_wait_bounded(empty + st, ((gp / STAGES) - 1) & 1, p)) ok = false;
+                    if (ok) {
+                        const uint32_t sb = base + st * kStage;
+                        mbar_expect(full + st, bytes);
+                        for (int gi = iss; gi < 64; gi += kIssuers) {
+                            const int a = gi >> 4, q = gi & 15;
+                            gather4(sb + (uint32_t)a * kAtom + (uint32_t)q * 512u, &p.tm_dn, c0 + 64 * a,
+                                    myids[4 * q], myids[4 * q + 1], myids[4 * q + 2], myids[4 * q + 3], full + st);
+                        }
+                        if (iss == 0) tile_load(sb + kW, &p.tm_act, k0, 0, full + st);
+                    }
+                }
+                __syncwarp(); // myids is rewritten for the next stage
             }
-        };
-        for (int s = 0; s < kStages - 1; ++s) {
-            if (s < KT) load((g + s) % kStages, s);
-            cp_commit();
+        } else {
+            gp += (uint32_t)KT;
         }
-        for (int kt = 0; kt < KT; ++kt) {
-            const uint32_t st = (g + kt) % kStages;
-            cp_wait<kStages - 2>();
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncthreads();
-            if (tid == 0) {
+        if (warp == 1 && lane == 0) {
+            for (int kt = 0; kt < KT && ok; ++kt, ++gc) {
+                const uint32_t st = gc % STAGES;
+                if (!mbar_wait_bounded(full + st, (gc / STAGES) & 1, p)) {
+                    ok = false;
+                    break;
+                }
                 tc_after();
                 const uint32_t sb = base + st * kStage;
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k)
-                    mma(tmem, sdesc(sb + k * 32, 16, 1024), sdesc(sb + kTileA + k * 16 * 128, 8192, 1024), id_dn,
-                        (kt | k) != 0);
-                mma_commit(bar + st);
-            }
-            const int nk = kt + kStages - 1;
-            if (nk < KT) {
-                if (kt >= 1) {
-                    const uint32_t gp = g + kt - 1;
-                    if (ok && !mbar_wait_bounded(bar + gp % kStages, (gp / kStages) & 1, p)) ok = false;
-                }
-                load((g + nk) % kStages, nk);
-            }
-            cp_commit();
-        }
-        if (KT > 0) {
-            const uint32_t gl = g + KT - 1;
-            if (ok && !mbar_wait_bounded(bar + gl % kStages, (gl / kStages) & 1, p)) ok = false;
-            for (int s = 0; s < kStages - 1 && s < KT - 1; ++s) {
-                const uint32_t gp = g + KT - 2 - s;
-                if (ok && !mbar_wait_bounded(bar + gp % kStages, (gp / kStages) & 1, p)) ok = false;
-            }
-        }
-        g += (uint32_t)KT;
-        tc_after();
-        // epilogue: thread = token row t (TMEM lane), 64 output columns
-        const int t = warp * 32 + lane;
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-        for (int j0 = 0; j0 < 64; j0 += 16) {
-            float v[16];
-            if (KT > 0) tmem_ld16(lane_addr + (uint32_t)j0, v);
-            else
-                for (int j = 0; j < 16; ++j) v[j] = 0.f;
-            if (t < B && ok) {
+                for (int k = 0; k < kBK / 16; ++k) {
+                    const uint64_t bx = sdesc(sb + kW + k * 32, 16, 1024);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c = c0 + j0 + j;
-                    if (c < d) {
-                        const float y = v[j] + H::one(L.bdown[c]);
-                        if (p.x) p.x[(size_t)t * d + c] += y;
-                        else p.y[(size_t)t * d + c] = H::round(y);
+                    for (int j = 0; j < 2; ++j) // atoms 2j, 2j+1: LBO steps from one 64-column atom to the next
+                        mma(tmem + (uint32_t)(j * Np), sdesc(sb + (uint32_t)(2 * j) * kAtom + k * 16 * 128, kAtom, 1024),
+                            bx, id_dn, (kt | k) != 0);
+                }
+                mma_commit(empty + st);
+            }
+            mma_commit(done);
+        } else {
+            gc += (uint32_t)KT;
+        }
+        if (!mbar_wait_bounded(done, pass & 1, p)) ok = false;
+        tc_after();
+        // epilogue: thread = output column (TMEM lane) of tile j, 16 tokens at a time
+        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        for (int j = 0; j < 2 && warp < 4; ++j) { // epilogue: warps 0..3
+            const int c = c0 + j * 128 + warp * 32 + lane;
+            const float bd = c < d ? H::one(L.bdown[c]) : 0.f;
+            for (int t0 = 0; t0 < Np; t0 += 16) {
+                float v[16];
+                if (KT > 0) tmem_ld16(lane_addr + (uint32_t)(j * Np + t0), v);
+                else
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                if (c < d && ok) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int t = t0 + i;
+                        if (t < B) {
+                            if (nks > 1) p.part[((size_t)ks * B + t) * d + c] = v[i];
+                            else if (p.x) p.x[(size_t)t * d + c] += v[i] + bd;
+                            else p.y[(size_t)t * d + c] = H::round(v[i] + bd);
+                        }
                     }
                 }
             }
@@ -456,21 +484,34 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const MmaParams p)
         __syncthreads();
         tc_after();
     }
-    cp_wait<0>();
-    tmem_free(tmem, 64);
+    tmem_free(tmem, 128);
+}
+
+// y (or x +=) = the shares' partials added in share order, + b_down
+template <typename T>
+__global__ void ffn_merge(const __grid_constant__ MmaParams p, int nks)
+{
+    using H = H16<T>;
+    const LayerDev &L = *p.layer;
+    const int d = L.d;
+    const size_t total = (size_t)p.B * d;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        float s = 0.f;
+        for (int k = 0; k < nks; ++k) s += p.part[(size_t)k * total + i];
+        s += H::one(L.bdown[i % d]);
+        if (p.x) p.x[i] += s;
+        else p.y[i] = H::round(s);
+    }
 }
 
 template <typename T, bool REGLU>
 cudaError_t launch_up(const MmaParams &p, int grid, cudaStream_t s)
 {
-    const int smem = kStages * (int)(kTileA * (REGLU ? 2 : 1) + kTileX) + 256 + 128 * 4;
-    auto kern = ffn_up_mma<T, REGLU>;
-    static bool configured = false;
-    if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    constexpr int st = REGLU ? 3 : 5;
+    const int smem = st * (int)(2 * kTileA * (REGLU ? 2 : 1) + kTileX) + 128 + 256 * 4;
+    auto kern = ffn_up_mma<T, REGLU, st>;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
     kern<<<grid, kMT, smem, s>>>(p);
     return cudaGetLastError();
 }
@@ -478,19 +519,48 @@ cudaError_t launch_up(const MmaParams &p, int grid, cudaStream_t s)
 template <typename T>
 cudaError_t launch_down(const MmaParams &p, int grid, cudaStream_t s)
 {
-    const int smem = kStages * (int)(kTileA + kTileX) + 256;
-    auto kern = ffn_down_mma<T>;
-    static bool configured = false;
-    if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    kern<<<grid, kMT, smem, s>>>(p);
+    constexpr int st = 5;
+    const int smem = st * (int)(4 * 8192 + kTileX) + 128 + kIssuers * 64 * 4;
+    auto kern = ffn_down_mma<T, st>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    // as many shares of the list per 256-column block as keep every SM busy with one unit
+    const int ncb = (p.d + 255) / 256;
+    const int nks = grid / ncb > 8 ? 8 : (grid / ncb < 1 ? 1 : grid / ncb);
+    const int units = ncb * nks;
+    kern<<<units < grid ? units : grid, kMT, smem, s>>>(p, nks);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || nks == 1) return e;
+    ffn_merge<T><<<grid * 4, 256, 0, s>>>(p, nks);
     return cudaGetLastError();
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
 } // namespace
+
+cudaError_t encode_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                       uint32_t box_rows)
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f) return e != cudaSuccess ? e : cudaErrorNotSupported;
+        fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, cudaStream_t s)
 {
@@ -498,9 +568,7 @@ cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, 
     if (bf16) e = reglu ? launch_up<__nv_bfloat16, true>(p, grid, s) : launch_up<__nv_bfloat16, false>(p, grid, s);
     else e = reglu ? launch_up<__half, true>(p, grid, s) : launch_up<__half, false>(p, grid, s);
     if (e != cudaSuccess) return e;
-    const int ntile = (p.d + 63) / 64;
-    const int gd = ntile < grid ? ntile : grid;
-    return bf16 ? launch_down<__nv_bfloat16>(p, gd, s) : launch_down<__half>(p, gd, s);
+    return bf16 ? launch_down<__nv_bfloat16>(p, grid, s) : launch_down<__half>(p, grid, s);
 }
 
 } // namespace pi
