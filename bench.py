@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-extras", action="store_true", help="skip dense, e2e and CPU legs")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
+    ap.add_argument("--mode", choices=["step", "ffn"], default="step",
+                    help="step: the decode step over the stack (the headline); ffn: the sparse FFN of one "
+                         "full-size layer alone, for per-kernel numbers")
     return ap.parse_args()
 
 
@@ -391,11 +394,70 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_ffn(args, world, rank, local):
+    """pi_sparse_ffn on one calibrated full-size layer with the tokens' predicted
+    union list: batches of 8+ run the tensor-core kernels, smaller ones the
+    step kernel's FFN phase.  Bytes = the rows of the listed neurons."""
+    import numpy as np
+    import torch
+    from activation_sparse_decode_sigmoid_gb300 import build as libbuild
+    from activation_sparse_decode_sigmoid_gb300 import pi
+    from activation_sparse_decode_sigmoid_gb300 import workload as W
+    from activation_sparse_decode_sigmoid_gb300.calibrate import calibrate_and_load
+
+    libbuild.build()
+    torch.cuda.set_device(local)
+    cfg = W.CONFIGS[args.config]
+    B, K, Wm = args.batch, args.steps, args.warmup
+    ctx = pi.Context(local, max_layers=1, max_batch=max(B, 1))
+    dev = torch.device("cuda", local)
+    lw = W.make_layer_device(cfg, 0, args.seed, dev)
+    cal = torch.from_numpy(W.calibration_inputs(cfg, 0, args.seed).view(np.int16)).to(dev)
+    calibrate_and_load(ctx, 0, lw, cal)
+    del lw
+    x = torch.from_numpy(W.xhat_inputs(cfg, B, args.seed + 5).view(np.int16)).to(dev)
+    idx, cnt = ctx.predict(0, x)
+    y = ctx.sparse_ffn(0, x, idx, cnt)
+    for _ in range(Wm):
+        ctx.sparse_ffn(0, x, idx, cnt, y)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(K):
+        ctx.sparse_ffn(0, x, idx, cnt, y)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ctx.check()
+    ms = allreduce_max(world, e0.elapsed_time(e1) / K, dev)
+    m = int(cnt.item())
+    rows = 3 if cfg.act == W.REGLU else 2
+    row = cfg.d * 18 / 32 if cfg.w_dtype == W.Q4_0 else cfg.d * 2
+    byts = m * (rows * row + 2) + B * cfg.d * 4
+    gbs = byts / (ms / 1e3) / 1e9
+    peak, kind = measured_hbm()
+    ctx.close()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "sparse FFN of one layer, effective HBM GB/s", "value": gbs * world, "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": W.DTYPE_NAMES[cfg.w_dtype], "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: one layer, d_model {cfg.d}, d_ffn {cfg.n}, batch {B}, "
+                                   f"{m} listed neurons ({m / cfg.n:.3f} of d_ffn)",
+                       "path": "tensor cores (tcgen05)" if B >= 8 and cfg.w_dtype != W.Q4_0 else "step kernel"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "peak_source": f"{kind} copy bandwidth (hbm_gbs)", "traffic": None},
+            "gpu_launches": K * (3 if B >= 8 else 1)}), flush=True)
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.mode == "ffn":
+        run_ffn(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:
