@@ -68,6 +68,8 @@ struct pi_ctx {
     uint16_t *xhat_ws = nullptr; // [max_batch][kMaxD]
     int32_t *lidx = nullptr;     // [kMaxN] list, then [1] its count
     float *mpart = nullptr;      // [8][max_batch][kMaxD] partials of the tensor-core down-projection
+    float *hbuf = nullptr;       // [max_batch][kMaxRank] predictor hidden layer of large batches
+    uint32_t *mbits = nullptr;   // [kMaxN / 32] union mask words of large batches
     int mma_min_b = 8;           // batches of at least this many tokens use the tensor cores (0: never)
     int *ctl = nullptr; // [0..1] grid-barrier counter (u64), [2] status, [3] abort
     // trace
@@ -304,7 +306,9 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
                      sizeof(uint16_t) * (size_t)max_batch * pi::kMaxN,
                      sizeof(uint16_t) * (size_t)max_batch * pi::kMaxD,
                      sizeof(int32_t) * ((size_t)pi::kMaxN + 64),
-                     sizeof(float) * 8 * (size_t)max_batch * pi::kMaxD};
+                     sizeof(float) * 8 * (size_t)max_batch * pi::kMaxD,
+                     sizeof(float) * (size_t)max_batch * pi::kMaxRank,
+                     sizeof(uint32_t) * (size_t)(pi::kMaxN / 32)};
     constexpr int kBufs = (int)(sizeof need / sizeof need[0]);
     void *ptrs[kBufs] = {};
     for (int i = 0; i < kBufs && e == cudaSuccess; ++i) e = cudaMalloc(&ptrs[i], need[i]);
@@ -327,6 +331,8 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     c->xhat_ws = (uint16_t *)ptrs[8];
     c->lidx = (int32_t *)ptrs[9];
     c->mpart = (float *)ptrs[10];
+    c->hbuf = (float *)ptrs[11];
+    c->mbits = (uint32_t *)ptrs[12];
     *out = c;
     return PI_OK;
 }
@@ -349,6 +355,8 @@ pi_status pi_destroy(pi_ctx *c)
         cudaFree(c->xhat_ws);
         cudaFree(c->lidx);
         cudaFree(c->mpart);
+        cudaFree(c->hbuf);
+        cudaFree(c->mbits);
     }
     delete c;
     return PI_OK;
@@ -592,6 +600,31 @@ static pi_status mma_ffn(pi_ctx *c, int layer, const uint16_t *xhat, int B, cons
     return PI_OK;
 }
 
+// Batches of at least mma_min_b tokens run the predictor as short launches
+// of register-tiled dot products (pi_pred.cu) instead of the step kernel.
+static bool use_pred_batch(const pi_ctx *c, int B) { return c->mma_min_b > 0 && B >= c->mma_min_b; }
+
+static pi::PredParams pred_params(pi_ctx *c, int layer, int B)
+{
+    pi::PredParams q{};
+    q.L = c->layers[layer].dev;
+    q.B = B;
+    q.h = c->hbuf;
+    q.mask = c->mbits;
+    q.status = c->ctl + 2;
+    q.abort_flag = c->ctl + 3;
+    q.wait_ns = c->wait_ns;
+    return q;
+}
+
+static pi_status pred_batch(pi_ctx *c, const pi::PredParams &q, int layer)
+{
+    const cudaError_t e =
+        pi::launch_predict_batch(q, c->layers[layer].desc.act_dtype == PI_BF16, c->G, c->stream);
+    if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "predictor launch: %s", cudaGetErrorString(e));
+    return PI_OK;
+}
+
 pi_status pi_predict(pi_ctx *c, int32_t layer, const void *x_hat, int32_t B, int32_t *idx, int32_t *count)
 {
     if (!c) return PI_ERR_ARG;
@@ -600,6 +633,14 @@ pi_status pi_predict(pi_ctx *c, int32_t layer, const void *x_hat, int32_t B, int
     if (st) return st;
     if (!x_hat || !idx || !count) return fail(c, PI_ERR_ARG, "x_hat/idx/count NULL");
     DeviceGuard g(c->device);
+    if (use_pred_batch(c, B)) {
+        if (reinterpret_cast<uintptr_t>(x_hat) & 15u) return fail(c, PI_ERR_ARG, "x_hat must be 16-byte aligned");
+        pi::PredParams q = pred_params(c, layer, B);
+        q.xhat = (uint16_t *)x_hat;
+        q.idx = idx;
+        q.count = count;
+        return pred_batch(c, q, layer);
+    }
     StepParams p{};
     p.xhat_in = (const uint16_t *)x_hat;
     p.idx_out = idx;
@@ -660,25 +701,32 @@ static pi_status step_common(pi_ctx *c, float *x, int32_t B, int mode)
     for (int l = 0; l < L; ++l) nmax = std::max(nmax, c->layers[l].desc.d_ffn);
     p.tr_n = nmax;
     if (!use_mma(c, 0, B)) return launch(c, 0, L, B, mode, p);
-    // Large batch: per layer, the step kernel computes x_hat (CTA 0 writes it
-    // to the workspace through the x_hat trace) and the predicted list (or the
-    // whole list), then the tensor-core FFN adds the layer's output into x.
+    // Large batch, per layer: x_hat = RMSNorm(x) into the workspace, the
+    // predicted list (or the whole list), then the tensor-core FFN adds the
+    // layer's output into x.
     const int d = c->layers[0].desc.d_model;
     const bool dense = (mode & pi::M_DENSE) != 0;
+    const bool bf16 = c->layers[0].desc.act_dtype == PI_BF16;
     for (int l = 0; l < L; ++l) {
-        StepParams q{};
+        pi::PredParams q = pred_params(c, l, B);
         q.x = x;
         q.tr_x = c->tr_x ? c->tr_x + (size_t)l * B * d : nullptr;
-        q.tr_xhat = c->xhat_ws;
+        q.xhat = c->xhat_ws;
+        q.idx = c->lidx;
+        q.count = c->lidx + pi::kMaxN;
         q.tr_idx = c->tr_idx ? c->tr_idx + (size_t)l * nmax : nullptr;
         q.tr_cnt = c->tr_cnt ? c->tr_cnt + l : nullptr;
-        q.tr_n = nmax;
-        q.idx_out = c->lidx;
-        q.count_out = c->lidx + pi::kMaxN;
-        const int m = dense ? (pi::M_RMSNORM | pi::M_DENSE | pi::M_COMPACT)
-                            : (pi::M_RMSNORM | pi::M_PREDICT | pi::M_COMPACT);
-        st = launch(c, l, 1, B, m, q);
-        if (st) return st;
+        cudaError_t e = pi::launch_rmsnorm_rows(q, bf16, c->stream);
+        if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "RMSNorm launch: %s", cudaGetErrorString(e));
+        if (dense) {
+            if (q.tr_idx || q.tr_cnt) {
+                e = pi::launch_list_all(q, c->stream);
+                if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "list launch: %s", cudaGetErrorString(e));
+            }
+        } else {
+            st = pred_batch(c, q, l);
+            if (st) return st;
+        }
         if (c->tr_xhat) {
             const cudaError_t e = cudaMemcpyAsync((uint16_t *)c->tr_xhat + (size_t)l * B * d, c->xhat_ws,
                                                   (size_t)B * d * 2, cudaMemcpyDeviceToDevice, c->stream);

@@ -185,6 +185,29 @@ cudaError_t occupancy_step_bf16(int tgf, int smem_bytes, int *blocks);
 cudaError_t occupancy_step_q4(int tgf, int smem_bytes, int *blocks);
 // the union-mask FFN on tcgen05: up/gate kernel on `grid` SMs, then the down kernel
 cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, cudaStream_t s);
+
+// The predictor of one layer for a batch of 8 or more tokens (pi_pred.cu).
+struct PredParams {
+    LayerDev L;               // the layer (device pointers)
+    int B;                    // tokens
+    const float *x;           // [B][d] fp32 residual: input of the RMSNorm launch
+    float *tr_x;              // [B][d] copy of x (trace), or NULL
+    uint16_t *xhat;           // [B][d] x_hat: written by the RMSNorm launch, read by the predictor
+    float *h;                 // [B][r] fp32 hidden activations
+    uint32_t *mask;           // [ceil(n/32)] union mask words
+    int32_t *idx, *count;     // the ascending list of predicted neurons and its length
+    int32_t *tr_idx, *tr_cnt; // copies of the list and its length (trace), or NULL
+    int dense;                // list launch only: the list of every neuron
+    int *status;
+    int *abort_flag;
+    unsigned long long wait_ns;
+};
+// x_hat = RMSNorm(x) of B tokens, in the step kernel's reduction order
+cudaError_t launch_rmsnorm_rows(const PredParams &p, bool bf16, cudaStream_t s);
+// h, the union mask, then the list (three launches on `sms` SMs)
+cudaError_t launch_predict_batch(const PredParams &p, bool bf16, int sms, cudaStream_t s);
+// the list of every neuron 0..n-1 (dense steps), with its trace copies
+cudaError_t launch_list_all(const PredParams &p, cudaStream_t s);
 // a 2D TMA map over a row-major 16-bit matrix: box = 64 columns x box_rows rows, 128-byte swizzle
 cudaError_t encode_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
                        uint32_t box_rows);
