@@ -400,18 +400,26 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
         const int c0 = cb * 256;
         const int k_lo = slice_at(KTall, ks, nks), KT = slice_at(KTall, ks + 1, nks) - k_lo;
         if (iss >= 0) {
+            // the list entries of stage kt (two per lane), fetched three stages
+            // ahead so that the gathers never wait for the list itself
+            const auto fetch = [&](int kt, int h) {
+                const int pos = (k_lo + kt) * kBK + lane + 32 * h;
+                return kt < KT && pos < m ? (p.idx ? __ldg(p.idx + pos) : pos) : n;
+            };
+            int f0[2], f1[2], f2[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) f0[h] = fetch(0, h), f1[h] = fetch(1, h), f2[h] = fetch(2, h);
             for (int kt = 0; kt < KT; ++kt, ++gp) {
                 const uint32_t st = gp % STAGES;
                 const int k0 = (k_lo + kt) * kBK;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int pos = k0 + lane + 32 * h;
-                    int id = n; // past the list: zeros (their A^T entries are 0, but 0 x garbage could be NaN)
-                    if (pos < m) {
-                        id = p.idx ? p.idx[pos] : pos;
-                        if (id < 0 || id >= n) id = n; // flagged by the up kernel
-                    }
+                    int id = f0[h]; // past the list: n, i.e. zeros (their A^T entries are 0, but 0 x garbage could be NaN)
+                    if (id < 0 || id >= n) id = n; // flagged by the up kernel
                     myids[lane + 32 * h] = id;
+                    f0[h] = f1[h];
+                    f1[h] = f2[h];
+                    f2[h] = fetch(kt + 3, h);
                 }
                 __syncwarp();
                 if (lane == 0 && ok) {

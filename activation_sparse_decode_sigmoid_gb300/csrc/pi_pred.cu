@@ -219,6 +219,13 @@ __global__ void __launch_bounds__(kPT, 1) pred_hidden(const PredParams p)
     const int tb = blockIdx.x % ntb, cta = blockIdx.x / ntb;
     const int ncta = ((int)gridDim.x - tb + ntb - 1) / ntb;
     const int t0 = tb * kTok, nch = d >> 3;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nrg = (r + 8 * R - 1) / (8 * R);
+    if (lane == 0) // this warp's rows of every unit start for L2 now: the loads below then wait on L2, not HBM
+        for (int rg = cta; rg < nrg; rg += ncta) {
+            const int i0 = rg * 8 * R + warp * R, nr = min(R, r - i0);
+            if (nr > 0) bulk_prefetch_l2(L.w1 + (size_t)i0 * d, (uint32_t)nr * d * 2, policy_evict_normal());
+        }
     for (int k = blockIdx.x * kPT + threadIdx.x; k < (L.n + 31) >> 5; k += (int)gridDim.x * kPT) p.mask[k] = 0u;
     for (int q = threadIdx.x; q < kTok * nch; q += kPT) {
         const int t = q / nch, ch = q - t * nch;
@@ -230,12 +237,12 @@ __global__ void __launch_bounds__(kPT, 1) pred_hidden(const PredParams p)
     cp_commit();
     cp_wait<0>();
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int NV = R * kTok;
-    const int nrg = (r + 8 * R - 1) / (8 * R);
     for (int rg = cta; rg < nrg; rg += ncta) {
         const int i0 = rg * 8 * R + warp * R;
         if (i0 >= r) continue; // warp-uniform; no CTA barrier below
+        // the rows' biases, loaded now so that the epilogue does not wait for them
+        const float b1r = lane < R && i0 + lane < r ? F::one(L.b1[i0 + lane]) : 0.f;
         float acc[R][kTok];
 #pragma unroll
         for (int rr = 0; rr < R; ++rr)
@@ -249,15 +256,14 @@ __global__ void __launch_bounds__(kPT, 1) pred_hidden(const PredParams p)
             for (int t = 0; t < kTok; ++t) v[rr * kTok + t] = acc[rr][t];
         int base = 0;
         halve<NV, 16, NV>(v, lane, base);
-        if ((lane & dup_mask(NV)) == 0) {
 #pragma unroll
-            for (int j = 0; j < held(NV); ++j) {
-                const int k = base + j, rr = k / kTok, t = k % kTok;
-                const int row = i0 + rr, tok = t0 + t;
-                if (row < r && tok < B) {
-                    const float s1 = __fadd_rn(v[j], F::one(L.b1[row]));
-                    p.h[(size_t)tok * r + row] = s1 > 0.f ? s1 : 0.f;
-                }
+        for (int j = 0; j < held(NV); ++j) {
+            const int k = base + j, rr = k / kTok, t = k % kTok;
+            const int row = i0 + rr, tok = t0 + t;
+            const float b1v = __shfl_sync(0xffffffffu, b1r, rr, 32); // (every lane: a full-warp shuffle)
+            if ((lane & dup_mask(NV)) == 0 && row < r && tok < B) {
+                const float s1 = __fadd_rn(v[j], b1v);
+                p.h[(size_t)tok * r + row] = s1 > 0.f ? s1 : 0.f;
             }
         }
     }
@@ -271,30 +277,34 @@ __global__ void __launch_bounds__(kPT, 1) pred_hidden(const PredParams p)
 __device__ __forceinline__ int hpos(int ch, int hf) { return (ch >> 5) * 256 + hf * 128 + (ch & 31) * 4; }
 
 // z = CDOT(W2[i], h_t) + b2[i] > 0, OR over the batch.  Unit u = rows
-// [8R u, 8R (u+1)): warp w's R rows arrive by one bulk copy into its own
-// part of the tile; the h blocks of 8 tokens pass through two buffers.
-template <typename T, int R>
+// [8R u, 8R (u+1)): warp w's R rows arrive by one bulk copy into its own part
+// of the tile and stay while the batch's h passes through in blocks of 8
+// tokens (two buffers).  With WS = 2 tile slots, a warp issues the copy of
+// its rows of the next unit before it computes this one (small batches,
+// where the rows' transfer, not the arithmetic, is the longer part).
+template <typename T, int R, int WS>
 __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
 {
     using F = F16T<T>;
+    constexpr int RT = 8 * R; // rows per unit
     extern __shared__ __align__(128) uint8_t smem[];
     const LayerDev &L = p.L;
     const int r = L.r, n = L.n, B = p.B;
     const int Kp = (r + 255) & ~255, nch = r >> 3;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t wB = (uint32_t)R * r * 2; // bytes of one warp's rows
-    uint8_t *wtile = smem + (size_t)warp * wB;
-    float *hbuf = reinterpret_cast<float *>(smem + 8 * (size_t)wB);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 8 * (size_t)wB + 2 * (size_t)kTok * Kp * 4);
-    uint32_t *smask = reinterpret_cast<uint32_t *>(bar + 8);
-    if (threadIdx.x < 8) mbar_init(bar + threadIdx.x, 1);
-    if (threadIdx.x < 2) smask[threadIdx.x] = 0u;
+    uint8_t *wtile = smem + (size_t)warp * WS * wB;
+    float *hbuf = reinterpret_cast<float *>(smem + 8 * (size_t)WS * wB);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 8 * (size_t)WS * wB + 2 * (size_t)kTok * Kp * 4);
+    uint32_t *smask = reinterpret_cast<uint32_t *>(bar + 8 * WS);
+    if (threadIdx.x < 8 * WS) mbar_init(bar + threadIdx.x, 1);
+    if (threadIdx.x < (RT + 31) / 32) smask[threadIdx.x] = 0u;
     fence_barrier_init();
     if (cta_aborted(p)) return; // (its barrier also publishes the initialised mbarriers)
     const int ntb = (B + kTok - 1) / kTok;
-    const int nrt = (n + 8 * R - 1) / (8 * R);
+    const int nrt = (n + RT - 1) / RT;
     const int nwords = (n + 31) >> 5;
-    // h block tb into buffer b (zeros past B)
+    // h block tb into buffer b (zeros past B), in the conflict-free layout
     const auto stage_h = [&](int tb, int b) {
         const int t0 = tb * kTok;
         float *dst = hbuf + (size_t)b * kTok * Kp;
@@ -306,17 +316,34 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
         }
         cp_commit();
     };
-    if (ntb == 1) stage_h(0, 0); // one block serves every unit
-    bool ok = true;
-    uint32_t it = 0;
-    for (int u = blockIdx.x; u < nrt; u += gridDim.x, ++it) {
-        const int i0 = u * 8 * R + warp * R;
+    // warp-level: bring this warp's rows of unit u into tile slot sl
+    const auto load_rows = [&](int u, int sl) {
+        const int i0 = u * RT + warp * R;
         const int nr = max(0, min(R, n - i0));
         if (lane == 0 && nr > 0) {
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar + warp, (uint32_t)nr * r * 2);
-            bulk_g2s(wtile, L.w2 + (size_t)i0 * r, (uint32_t)nr * r * 2, bar + warp, policy_evict_first());
+            mbar_arrive_expect_tx(bar + warp * WS + sl, (uint32_t)nr * r * 2);
+            bulk_g2s(wtile + (size_t)sl * wB, L.w2 + (size_t)i0 * r, (uint32_t)nr * r * 2, bar + warp * WS + sl,
+                     policy_evict_first());
         }
+    };
+    if (ntb == 1) stage_h(0, 0); // one block serves every unit
+    bool ok = true;
+    uint32_t it = 0;
+    if (WS == 2 && blockIdx.x < nrt) load_rows(blockIdx.x, 0);
+    for (int u = blockIdx.x; u < nrt; u += gridDim.x, ++it) {
+        const int sl = WS == 2 ? (int)(it & 1) : 0;
+        const uint32_t par = WS == 2 ? (it >> 1) & 1 : it & 1;
+        if (WS == 2) {
+            if (u + (int)gridDim.x < nrt) load_rows(u + gridDim.x, sl ^ 1); // slot sl ^ 1 was read by the last unit
+        } else {
+            load_rows(u, 0);
+        }
+        const int i0 = u * RT + warp * R;
+        const int nr = max(0, min(R, n - i0));
+        const uint8_t *wt = wtile + (size_t)sl * wB;
+        // the rows' biases, loaded now so that the epilogues do not wait for them
+        const float b2r = lane < nr ? F::one(L.b2[i0 + lane]) : 0.f;
         if (ntb > 1) stage_h(0, 0);
         uint32_t bits = 0; // bit rr: row i0 + rr active for some token
         bool landed = nr == 0;
@@ -329,7 +356,9 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
             }
             __syncthreads();
             if (!landed) {
-                if (ok && !wait_bounded(bar + warp, it & 1, p)) ok = false;
+                // every lane waits; the warp goes on only if all saw the rows (shuffles follow)
+                const bool got = ok && wait_bounded(bar + warp * WS + sl, par, p);
+                ok = __all_sync(0xffffffffu, got);
                 landed = true;
             }
             if (nr > 0 && ok) {
@@ -343,7 +372,7 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
                     uint4 w[R];
 #pragma unroll
                     for (int rr = 0; rr < R; ++rr)
-                        w[rr] = *reinterpret_cast<const uint4 *>(wtile + (size_t)rr * r * 2 + (size_t)ch * 16);
+                        w[rr] = *reinterpret_cast<const uint4 *>(wt + (size_t)rr * r * 2 + (size_t)ch * 16);
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         float4 hv[kTok];
@@ -351,7 +380,7 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
                         for (int t = 0; t < kTok; ++t)
                             hv[t] = *reinterpret_cast<const float4 *>(hs + (size_t)t * Kp + hpos(ch, hf));
 #pragma unroll
-                        for (int e2 = 0; e2 < 2; ++e2) { // element pairs (4 hf + 2 e2, +1)
+                        for (int e2 = 0; e2 < 2; ++e2) { // elements 4 hf + 2 e2 and 4 hf + 2 e2 + 1
 #pragma unroll
                             for (int rr = 0; rr < R; ++rr) {
                                 const uint32_t word = hf == 0 ? (e2 == 0 ? w[rr].x : w[rr].y) : (e2 == 0 ? w[rr].z : w[rr].w);
@@ -377,8 +406,8 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
 #pragma unroll
                 for (int j = 0; j < held(NV); ++j) {
                     const int k = base + j, rr = k / kTok, t = k % kTok;
-                    if (rr < nr && tb * kTok + t < B && __fadd_rn(v[j], F::one(L.b2[i0 + rr])) > 0.f)
-                        mine |= 1u << rr;
+                    const float b2v = __shfl_sync(0xffffffffu, b2r, rr, 32);
+                    if (rr < nr && tb * kTok + t < B && __fadd_rn(v[j], b2v) > 0.f) mine |= 1u << rr;
                 }
                 bits |= __reduce_or_sync(0xffffffffu, mine);
             }
@@ -386,42 +415,53 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
         }
         if (lane == 0 && bits) atomicOr(smask + ((warp * R) >> 5), bits << ((warp * R) & 31));
         __syncthreads();
-        if (threadIdx.x < (8 * R + 31) / 32) {
-            const int wi = u * (8 * R) / 32 + threadIdx.x;
-            if constexpr (8 * R % 32 == 0) { // whole words: this CTA's alone
+        if (threadIdx.x < (RT + 31) / 32) {
+            const int wi = u * RT / 32 + threadIdx.x;
+            if constexpr (RT % 32 == 0) { // whole words: this CTA's alone
                 if (wi < nwords) p.mask[wi] = smask[threadIdx.x];
             } else if (smask[threadIdx.x]) { // part of a word (cleared by the hidden-layer launch)
-                atomicOr(p.mask + wi, smask[threadIdx.x] << ((u * 8 * R) & 31));
+                atomicOr(p.mask + wi, smask[threadIdx.x] << ((u * RT) & 31));
             }
             smask[threadIdx.x] = 0u;
         }
-        // (the next unit's atomics come after the CTA barrier of its first block)
+        // (the next unit's shared-mask atomics come after the barrier of its first block)
     }
     cp_wait<0>();
 }
 
 // ------------------------------------------------------------------ compaction
-// One CTA of 1024 threads; thread k owns mask words 2k, 2k + 1 (n <= 65536).
-__global__ void __launch_bounds__(1024) pred_compact(const PredParams p)
+// CTA c of 256 threads owns mask words [256 c, 256 c + 256), one per thread.
+// Its list offset is the popcount of all words before them (every CTA adds
+// those up itself: n <= 65536 is at most 2048 words); a block scan places
+// each word, then each warp writes its 32 words' ids lane-parallel, one
+// word per round.
+__global__ void __launch_bounds__(256) pred_compact(const PredParams p)
 {
-    __shared__ int wsum[32];
+    __shared__ int red[8];
+    __shared__ int wsum[8];
     if (cta_aborted(p)) return;
     const int n = p.L.n, nwords = (n + 31) >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (p.dense) { // every neuron
-        for (int k = threadIdx.x; k < n; k += 1024) {
+        for (int k = blockIdx.x * 256 + tid; k < n; k += (int)gridDim.x * 256) {
             p.idx[k] = k;
             if (p.tr_idx) p.tr_idx[k] = k;
         }
-        if (threadIdx.x == 0) {
+        if (blockIdx.x == 0 && tid == 0) {
             *p.count = n;
             if (p.tr_cnt) *p.tr_cnt = n;
         }
         return;
     }
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int w0 = 2 * tid;
-    const uint32_t m0 = w0 < nwords ? p.mask[w0] : 0u, m1 = w0 + 1 < nwords ? p.mask[w0 + 1] : 0u;
-    const int c = __popc(m0) + __popc(m1);
+    const int w0 = blockIdx.x * 256;
+    int before = 0;
+    for (int k = tid; k < w0; k += 256) before += __popc(p.mask[k]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+    if (lane == 0) red[warp] = before;
+    const int wi = w0 + tid;
+    const uint32_t m = wi < nwords ? p.mask[wi] : 0u;
+    const int c = __popc(m);
     int incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -430,78 +470,78 @@ __global__ void __launch_bounds__(1024) pred_compact(const PredParams p)
     }
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-        int s = wsum[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += y;
-        }
-        wsum[lane] = s; // inclusive
+    int off = 0, tot = 0;
+    for (int w = 0; w < 8; ++w) {
+        off += w < warp ? wsum[w] : 0;
+        tot += wsum[w];
     }
-    __syncthreads();
-    int pos = incl - c + (warp > 0 ? wsum[warp - 1] : 0);
-    const int total = wsum[31];
-    for (int q = 0; q < 2; ++q) {
-        uint32_t m = q == 0 ? m0 : m1;
-        const int wb = (w0 + q) * 32;
-        while (m) {
-            const int b = __ffs(m) - 1;
-            m &= m - 1;
-            p.idx[pos] = wb + b;
-            if (p.tr_idx) p.tr_idx[pos] = wb + b;
-            ++pos;
+    int base = 0;
+    for (int w = 0; w < 8; ++w) base += red[w];
+    const int pos = base + off + incl - c; // list position of this word's first id
+    for (int k = 0; k < 32; ++k) {
+        const uint32_t mk = __shfl_sync(0xffffffffu, m, k);
+        const int pk = __shfl_sync(0xffffffffu, pos, k);
+        if ((mk >> lane) & 1u) {
+            const int at = pk + __popc(mk & ((1u << lane) - 1u));
+            const int id = (w0 + warp * 32 + k) * 32 + lane;
+            p.idx[at] = id;
+            if (p.tr_idx) p.tr_idx[at] = id;
         }
     }
-    if (tid == 0) {
-        *p.count = total;
-        if (p.tr_cnt) *p.tr_cnt = total;
+    if (blockIdx.x == gridDim.x - 1 && tid == 0) {
+        *p.count = base + tot;
+        if (p.tr_cnt) *p.tr_cnt = base + tot;
     }
 }
 
-// shared memory of pred_out: W tile, two h blocks, 8 mbarriers, 2 mask words
-int out_smem(int R, int r) { return 8 * R * r * 2 + 2 * kTok * ((r + 255) & ~255) * 4 + 8 * 8 + 16; }
+// shared memory of pred_out: WS tile slots, two h blocks, the mbarriers, the mask words
+int out_smem(int R, int WS, int r) { return 8 * WS * R * r * 2 + 2 * kTok * ((r + 255) & ~255) * 4 + 8 * WS * 8 + 16; }
+
+int compact_grid(int n) { return std::max(1, ((n + 31) / 32 + 255) / 256); }
+
+template <typename T, int R, int PD>
+cudaError_t launch_hidden(const PredParams &p, int sms, cudaStream_t s)
+{
+    const int smem = kTok * p.L.d * 2, ntb = (p.B + kTok - 1) / kTok;
+    auto kern = pred_hidden<T, R, PD>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 1;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPT, smem);
+    if (e != cudaSuccess) return e;
+    const int nrg = (p.L.r + 8 * R - 1) / (8 * R);
+    int grid = std::min(ntb * nrg, std::max(1, per_sm) * sms);
+    grid = std::max(ntb, grid / ntb * ntb); // every token block gets the same number of CTAs
+    kern<<<grid, kPT, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T, int R, int WS>
+cudaError_t launch_out(const PredParams &p, int sms, cudaStream_t s)
+{
+    const int smem = out_smem(R, WS, p.L.r);
+    auto kern = pred_out<T, R, WS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int nrt = (p.L.n + 8 * R - 1) / (8 * R);
+    kern<<<std::min(nrt, sms), kPT, smem, s>>>(p);
+    return cudaGetLastError();
+}
 
 template <typename T>
 cudaError_t launch_all(const PredParams &p, int sms, cudaStream_t s)
 {
-    const int B = p.B, d = p.L.d, r = p.L.r, n = p.L.n;
-    const int ntb = (B + kTok - 1) / kTok;
-    cudaError_t e;
-    {
-        // hidden layer: R = 1 row per warp for one token block (more CTAs), else 2
-        const int smem = kTok * d * 2;
-        const bool r1 = ntb == 1;
-        const void *kern = r1 ? (const void *)pred_hidden<T, 1, 4> : (const void *)pred_hidden<T, 2, 4>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        int per_sm = 1;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPT, smem);
-        if (e != cudaSuccess) return e;
-        const int nrg = (r + 8 * (r1 ? 1 : 2) - 1) / (8 * (r1 ? 1 : 2));
-        int grid = std::min(ntb * nrg, std::max(1, per_sm) * sms);
-        grid = std::max(ntb, grid / ntb * ntb);
-        if (r1) pred_hidden<T, 1, 4><<<grid, kPT, smem, s>>>(p);
-        else pred_hidden<T, 2, 4><<<grid, kPT, smem, s>>>(p);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    {
-        // output layer: 8 rows per warp up to r = 1024, else 2 (the tile stays within shared memory)
-        const bool r8 = r <= 1024;
-        const int R = r8 ? 8 : 2;
-        const int smem = out_smem(R, r);
-        const void *kern = r8 ? (const void *)pred_out<T, 8> : (const void *)pred_out<T, 2>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        const int nrt = (n + 8 * R - 1) / (8 * R);
-        const int grid = std::min(nrt, sms);
-        if (r8) pred_out<T, 8><<<grid, kPT, smem, s>>>(p);
-        else pred_out<T, 2><<<grid, kPT, smem, s>>>(p);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    pred_compact<<<1, 1024, 0, s>>>(p);
+    // hidden layer: one row per warp for a single token block (more CTAs), else two
+    cudaError_t e = p.B <= kTok ? launch_hidden<T, 1, 8>(p, sms, s) : launch_hidden<T, 2, 4>(p, sms, s);
+    if (e != cudaSuccess) return e;
+    // output layer (the tile stays within shared memory): up to r = 1024, 8 rows
+    // per warp, or for one or two token blocks 4 rows with the next unit's in
+    // flight; beyond, 2 rows
+    if (p.L.r > 1024) e = launch_out<T, 2, 1>(p, sms, s);
+    else if (p.B <= 2 * kTok) e = launch_out<T, 4, 2>(p, sms, s);
+    else e = launch_out<T, 8, 1>(p, sms, s);
+    if (e != cudaSuccess) return e;
+    pred_compact<<<compact_grid(p.L.n), 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -518,7 +558,7 @@ cudaError_t launch_list_all(const PredParams &p, cudaStream_t s)
 {
     PredParams q = p;
     q.dense = 1;
-    pred_compact<<<1, 1024, 0, s>>>(q);
+    pred_compact<<<compact_grid(p.L.n), 256, 0, s>>>(q);
     return cudaGetLastError();
 }
 
