@@ -41,7 +41,7 @@
 namespace pi {
 namespace {
 
-constexpr int kIssuers = 5;                // TMA producer warps
+constexpr int kIssuers = 11;                // TMA producer warps
 constexpr int kMT = 32 * (kIssuers + 1);  // + the MMA warp; warps 0..3 (TMEM lanes 0..127) run the epilogues
 constexpr int kBK = 64;       // K elements per stage (one 128-byte row)
 constexpr uint32_t kTileA = 16384; // 128 rows x 128 bytes
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
         const int iss = issuer_index(warp);
         if (iss >= 0 && lane == 0) {
             const int nq = (rows + 3) / 4;
-            const int mine = (nq - iss + kIssuers - 1) / kIssuers; // gathers q = iss, iss + 3, ...
+            const int mine = (nq - iss + kIssuers - 1) / kIssuers; // gathers q = iss, iss + kIssuers, ...
             const uint32_t bytes = (uint32_t)mine * 512u * (REGLU ? 2u : 1u) + (iss == 0 ? (uint32_t)Np * 128u : 0u);
             for (int kt = 0; kt < KT && ok; ++kt, ++gp) {
                 const uint32_t st = gp % STAGES;
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
     const uint32_t base = smem_addr(smem);
     const uint32_t id_dn = idesc(H::fmt, 1, 0, 128, (uint32_t)Np);
     const int iss = issuer_index(warp);
-    // 64 gathers per stage (4 column atoms x 16 groups of 4 neurons): g = iss, iss + 3, ...
+    // 64 gathers per stage (4 column atoms x 16 groups of 4 neurons): g = iss, iss + kIssuers, ...
     const uint32_t bytes = (uint32_t)((64 - iss + kIssuers - 1) / kIssuers) * 512u + (iss == 0 ? (uint32_t)Np * 128u : 0u);
     int *myids = sidd + (iss < 0 ? 0 : iss) * 64;
     uint32_t gp = 0, gc = 0, pass = 0;
