@@ -267,6 +267,62 @@ def test_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
     assert max_rel_err(G.y_to_f64(yd, cfg.act_dtype), O.masked_ffn(layer, x, np.arange(cfg.n))) <= G.tol(layer)
 
 
+@pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "ring_wrap", "opt_1layer"])
+@pytest.mark.parametrize("B", [8, 9, 16, 17, 40, 64])
+def test_batched_predictor_matches_oracle_and_step_kernel(c64, name, B):
+    """From 8 tokens the predictor runs as register-tiled launches (8-token
+    blocks, a halving butterfly over R x 8 dot products per warp); its lists
+    equal the oracle's and, entry for entry, the step kernel's on the same
+    x_hat (one, two and several token blocks; r = 2048 takes the narrow
+    output tile that shares mask words between CTAs)."""
+    cfg, layer = _layer(name)
+    c64.load_layer(0, layer)
+    x = W.xhat_inputs(cfg, B, 31 + B)
+    idx, cnt, _ = G.predict_checked(c64, 0, layer, x)
+    pi.pi_debug_set_mma_min_batch(c64.handle, 0)
+    try:
+        idx2, cnt2 = c64.predict(0, G.dev16(x))
+        c64.check()
+    finally:
+        pi.pi_debug_set_mma_min_batch(c64.handle, 8)
+    m = int(cnt.item())
+    assert m == int(cnt2.item())
+    assert np.array_equal(idx[:m].cpu().numpy(), idx2[:m].cpu().numpy())
+
+
+def test_large_batch_decode_x_hat_and_list_match_fused_kernel():
+    """A batch of 8 decodes layer by layer (RMSNorm launch, batched
+    predictor, tensor-core FFN); with the tensor cores off the same batch
+    runs in the persistent step kernel.  Both compute x_hat in one reduction
+    order and the lists by the same dot products: layer 0's x_hat and list
+    are bit-identical (later layers see slightly different FFN sums)."""
+    t = G.torch()
+    cfg = CFGS["relu_f16"]
+    B, L = 8, 2
+    c = G.ctx(max_layers=L, max_batch=B)
+    for l in range(L):
+        c.load_layer(l, W.make_layer(cfg, l, 0, random_b1=True, random_bdown=True))
+    x0 = W.decode_inputs(cfg, B, 8)
+    out = []
+    for mma in (8, 0):
+        pi.pi_debug_set_mma_min_batch(c.handle, mma)
+        x = t.from_numpy(x0.copy()).cuda()
+        tx = t.zeros((L, B, cfg.d), dtype=t.float32, device="cuda")
+        txh = t.zeros((L, B, cfg.d), dtype=t.int16, device="cuda")
+        tidx = t.full((L, cfg.n), -1, dtype=t.int32, device="cuda")
+        tcnt = t.zeros(L, dtype=t.int32, device="cuda")
+        c.set_trace(tx, txh, tidx, tcnt)
+        c.decode_step(x)
+        c.check()
+        c.set_trace(None, None, None, None)
+        m = int(tcnt[0].item())
+        out.append((txh[0].cpu().numpy(), tidx[0, :m].cpu().numpy(), tx[0].cpu().numpy()))
+    assert np.array_equal(out[0][2], out[1][2]) and np.array_equal(out[0][2], x0)
+    assert np.array_equal(out[0][0], out[1][0])
+    assert np.array_equal(out[0][1], out[1][1])
+    c.close()
+
+
 @pytest.mark.parametrize("knobs", [(0, 0, 0, 0), (1, 0, 2, 4), (2, 400, 4, 0), (3, 800, 3, 8), (3, 0, 16, 64)])
 def test_tuning_knobs_do_not_change_results(knobs):
     """Prefetch modes, the FFN lookahead and row prefetch only move data
