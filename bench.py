@@ -147,9 +147,17 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
 
 
+# The sources the persistent step kernel is built from, with the host plan
+# that sizes its rings (pi_api.cu): a profile's DRAM counters stand for the
+# kernel only while these files are unchanged.
+STEP_SOURCES = ("pi_api.cu", "pi_device.cuh", "pi_kernels.h", "pi_step.cuh", "pi_step_bf16.cu", "pi_step_f16.cu",
+                "pi_step_q4.cu")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "activation_sparse_decode_sigmoid_gb300", "csrc", "*")))
+    csrc = os.path.join(ROOT, "activation_sparse_decode_sigmoid_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in STEP_SOURCES)
     for p in files:
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode() + f.read())
