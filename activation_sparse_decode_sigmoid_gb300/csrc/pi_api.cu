@@ -70,7 +70,11 @@ struct pi_ctx {
     float *mpart = nullptr;      // [8][max_batch][kMaxD] partials of the tensor-core down-projection
     float *hbuf = nullptr;       // [max_batch][kMaxRank] predictor hidden layer of large batches
     uint32_t *mbits = nullptr;   // [kMaxN / 32] union mask words of large batches
-    int mma_min_b = 8;           // batches of at least this many tokens use the tensor cores (0: never)
+    bool h_batched = false;      // the last predictor pass was the batched one (h in hbuf)
+    // Batches of at least this many tokens run layer by layer: batched predictor launches and the
+    // tensor-core FFN (0: never).  Measured on GB300: from 2 tokens on LLaMA-70B-shaped (ReGLU)
+    // layers, from 3 on OPT-30B-shaped ones (equal at 2), the step kernel's per-group passes lose.
+    int mma_min_b = 2;
     int *ctl = nullptr; // [0..1] grid-barrier counter (u64), [2] status, [3] abort
     // trace
     float *tr_x = nullptr;
@@ -217,6 +221,7 @@ pi_status launch(pi_ctx *c, int l0, int L, int B, int mode, StepParams &p)
     p.layers = c->d_layers + l0;
     p.L = L;
     p.mode = mode;
+    if (mode & (pi::M_PREDICT | pi::M_COUNTS)) c->h_batched = false;
     if (c->epoch > 0xF0000000u - (unsigned)L) {
         // epochs would wrap: clear every tag so that no stale word can match
         const size_t bd = (size_t)c->max_batch * pi::kMaxD;
@@ -622,6 +627,7 @@ static pi_status pred_batch(pi_ctx *c, const pi::PredParams &q, int layer)
     const cudaError_t e =
         pi::launch_predict_batch(q, c->layers[layer].desc.act_dtype == PI_BF16, c->G, c->stream);
     if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "predictor launch: %s", cudaGetErrorString(e));
+    c->h_batched = true;
     return PI_OK;
 }
 
@@ -835,9 +841,11 @@ pi_status pi_debug_copy_hidden(pi_ctx *c, float *dst, int32_t count)
 {
     if (!c || !dst || count < 0 || (size_t)count > (size_t)c->max_batch * pi::kMaxRank) return PI_ERR_ARG;
     DeviceGuard g(c->device);
-    // the values are the low halves of the tagged words
-    const cudaError_t e = cudaMemcpy2DAsync(dst, sizeof(float), c->hx, sizeof(uint64_t), sizeof(float), (size_t)count,
-                                            cudaMemcpyDefault, c->stream);
+    // batched pass: plain fp32 [B][rank]; step kernel: the low halves of the tagged words
+    const cudaError_t e =
+        c->h_batched ? cudaMemcpyAsync(dst, c->hbuf, sizeof(float) * (size_t)count, cudaMemcpyDefault, c->stream)
+                     : cudaMemcpy2DAsync(dst, sizeof(float), c->hx, sizeof(uint64_t), sizeof(float), (size_t)count,
+                                         cudaMemcpyDefault, c->stream);
     return e == cudaSuccess ? PI_OK : fail(c, PI_ERR_CUDA, "copy of h: %s", cudaGetErrorString(e));
 }
 

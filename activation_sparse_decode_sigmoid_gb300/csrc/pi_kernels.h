@@ -154,7 +154,7 @@ __host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, in
     return m;
 }
 
-// Parameters of the tensor-core FFN kernels (pi_mma.cu), batches of 8..64.
+// Parameters of the tensor-core FFN kernels (pi_mma.cu), batches of 2..64.
 struct MmaParams {
     // TMA maps (16-bit elements, 64-column boxes, 128-byte swizzle): the
     // layer's W_up / W_gate / W_down^T rows (one-row boxes, for gather4),
@@ -186,7 +186,7 @@ cudaError_t occupancy_step_q4(int tgf, int smem_bytes, int *blocks);
 // the union-mask FFN on tcgen05: up/gate kernel on `grid` SMs, then the down kernel
 cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, cudaStream_t s);
 
-// The predictor of one layer for a batch of 8 or more tokens (pi_pred.cu).
+// The predictor of one layer for a batch of several tokens (pi_pred.cu).
 struct PredParams {
     LayerDev L;               // the layer (device pointers)
     int B;                    // tokens

@@ -1,10 +1,10 @@
-// Tensor-core (tcgen05) path of the sparse FFN for batches of 8 to 64 tokens.
+// Tensor-core (tcgen05) path of the sparse FFN for batches of 2 to 64 tokens.
 //
 // PowerInfer (blog.csdn.net QbitAI/IPADS article, section "CPU/GPU混合推理设计";
 // arXiv 2312.12456, section 5, neuron-aware operators): a batch computes the
 // union of its tokens' predicted neurons, reading only those rows of W_up
 // (W_gate) and W_down.  With B tokens every row read feeds B dot products, so
-// from 8 tokens up the work is a gather-GEMM:
+// from a few tokens up the work is a gather-GEMM:
 //
 //   U[i, t] = W_up[idx_i] . x_hat_t           (m x B, K = d_model)
 //   A[i, t] = act(U[i, t] + b_i)  (ReGLU: relu(W_gate[idx_i] . x_hat_t + b_i) * U[i, t])

@@ -1,4 +1,4 @@
-// Predictor of a batch of 8 to 64 tokens, as short launches per layer.
+// Predictor of a batch of 2 to 64 tokens, as short launches per layer.
 //
 // PowerInfer (arXiv 2312.12456, section 5 "online predictors"; blog.csdn.net
 // QbitAI/IPADS article, section "充分利用模型和硬件特点"): each layer's small

@@ -147,6 +147,11 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
 
 
+# The library's default: batches of this many tokens or more run layer by
+# layer (batched predictor launches, tensor-core FFN) instead of in the
+# persistent step kernel.
+LAYERWISE_MIN_BATCH = 2
+
 # The sources the persistent step kernel is built from, with the host plan
 # that sizes its rings (pi_api.cu): a profile's DRAM counters stand for the
 # kernel only while these files are unchanged.
@@ -341,6 +346,12 @@ def run_ours(args, world, rank, local):
     achieved = statistics.mean(bytes_per_step) / mean_launch_s / 1e9
     peak, peak_kind = measured_hbm()
     value = world * K * B / (ms / 1e3)
+    # batches of LAYERWISE_MIN_BATCH+ tokens with 16-bit weights run layer by layer: per layer
+    # RMSNorm, the predictor's hidden layer, output layer and compaction, the FFN's up and down
+    # kernels and the share merge; everything else is one persistent launch per step
+    layerwise = B >= LAYERWISE_MIN_BATCH and cfg.w_dtype != W.Q4_0
+    kernel = ("per-layer launches: RMSNorm, batched predictor (3), tensor-core FFN (3)" if layerwise
+              else "step_kernel (one persistent launch per step)")
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
@@ -350,9 +361,9 @@ def run_ours(args, world, rank, local):
         "mean_active_neurons_per_layer": float(counts.mean()), "mean_active_fraction": float(counts.mean() / cfg.n),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
-                     "traffic": profiled_traffic(cfg.name + f"/L{L}/B{B}"),
-                     "kernel": "step_kernel (one persistent launch per step)"},
-        "gpu_launches": K,
+                     "traffic": None if layerwise else profiled_traffic(cfg.name + f"/L{L}/B{B}"),
+                     "kernel": kernel},
+        "gpu_launches": K * 7 * L if layerwise else K,
     }
 
     if do_extras:
@@ -373,7 +384,8 @@ def run_ours(args, world, rank, local):
         dense_bytes = L * cfg.n * ((3 if cfg.act == W.REGLU else 2) * row + 2)
         line["dense_baseline"] = {"tokens_per_s": B / (dense_ms / 1e3), "ms_per_step": dense_ms,
                                   "effective_hbm_gbs": dense_bytes / (dense_ms / 1e3) / 1e9,
-                                  "what": "same persistent kernel over every neuron, no predictor (cuBLAS-free dense GEMV)"}
+                                  "what": ("every neuron, no predictor, layer by layer on the tensor-core FFN" if layerwise
+                                           else "same persistent kernel over every neuron, no predictor (cuBLAS-free dense GEMV)")}
         # end to end through the public API: one pi_decode_step_host call per
         # step (pinned host x in, H2D, the step, D2H, stream synchronised),
         # timed by the host clock
@@ -453,10 +465,11 @@ def run_ffn(args, world, rank, local):
             "scaling": "weak", "vs_baseline": None, "dtype": W.DTYPE_NAMES[cfg.w_dtype], "data": "synthetic",
             "config": {"workload": f"{cfg.name}: one layer, d_model {cfg.d}, d_ffn {cfg.n}, batch {B}, "
                                    f"{m} listed neurons ({m / cfg.n:.3f} of d_ffn)",
-                       "path": "tensor cores (tcgen05)" if B >= 8 and cfg.w_dtype != W.Q4_0 else "step kernel"},
+                       "path": "tensor cores (tcgen05)" if B >= LAYERWISE_MIN_BATCH and cfg.w_dtype != W.Q4_0
+                       else "step kernel"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "peak_source": f"{kind} copy bandwidth (hbm_gbs)", "traffic": None},
-            "gpu_launches": K * (3 if B >= 8 else 1)}), flush=True)
+            "gpu_launches": K * (3 if B >= LAYERWISE_MIN_BATCH and cfg.w_dtype != W.Q4_0 else 1)}), flush=True)
 
 
 def main():

@@ -278,15 +278,17 @@ pi_status pi_debug_set_tuning(pi_ctx *ctx, int32_t prefetch, int32_t prefetch_ns
                               int32_t rows_ahead);
 
 /* Copy the first `count` floats of the predictor's hidden layer as the last
- * predictor pass left it (fp32 [B][rank], h = max(W1 x_hat + b1, 0)) to dst
+ * predictor pass left it, batched or in the step kernel (fp32 [B][rank],
+ * h = max(W1 x_hat + b1, 0)) to dst
  * (device or host memory), asynchronously on the context's stream, so a test
  * can compare h itself, not only the index list it leads to.  count is at
  * most max_batch * 2048. */
 pi_status pi_debug_copy_hidden(pi_ctx *ctx, float *dst, int32_t count);
 
-/* Smallest batch (tokens) whose FFN runs on the tensor cores (tcgen05
- * gather-GEMM, 16-bit weights; default 8); 0 keeps every batch on the step
- * kernel's CUDA-core path.  For comparing the two paths. */
+/* Smallest batch (tokens) that runs layer by layer (default 2): the
+ * predictor as batched launches and, with 16-bit weights, the FFN on the
+ * tensor cores (tcgen05 gather-GEMM).  0 keeps every batch on the persistent
+ * step kernel (CUDA cores).  For comparing the two paths. */
 pi_status pi_debug_set_mma_min_batch(pi_ctx *ctx, int32_t min_batch);
 
 #ifdef __cplusplus

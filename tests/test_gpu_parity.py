@@ -14,6 +14,9 @@ from tests._helpers import max_rel_err, worked_example_layer
 
 pytestmark = pytest.mark.gpu
 
+# the library's default: batches of this many tokens or more run layer by layer
+LAYERWISE_MIN_BATCH = 2
+
 # small layers spanning several tiles with ragged tails (n not a multiple of
 # 32, d not a multiple of 256), every activation / weight kind
 CFGS = {
@@ -52,7 +55,10 @@ def test_predict_and_sparse_ffn(c64, name, B):
 
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4"])
 @pytest.mark.parametrize("B", [1, 2, 7, 9, 64])
-def test_batch_sizes(c64, name, B):
+@pytest.mark.parametrize("path", ["default", "step kernel"], indirect=True)
+def test_batch_sizes(c64, name, B, path):
+    """Every batch size on the default path (layer by layer from 2 tokens)
+    and on the persistent step kernel (its multi-token groups)."""
     cfg, layer = _layer(name)
     c64.load_layer(0, layer)
     x = W.xhat_inputs(cfg, B, 11)
@@ -60,8 +66,18 @@ def test_batch_sizes(c64, name, B):
     G.ffn_checked(c64, 0, layer, x, idx, cnt, oidx)
 
 
+@pytest.fixture
+def path(c64, request):
+    """Run a test on the default path, or with every batch on the step kernel."""
+    if request.param == "step kernel":
+        pi.pi_debug_set_mma_min_batch(c64.handle, 0)
+    yield request.param
+    pi.pi_debug_set_mma_min_batch(c64.handle, LAYERWISE_MIN_BATCH)
+
+
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4"])
-def test_dense_ffn(c64, name):
+@pytest.mark.parametrize("path", ["default", "step kernel"], indirect=True)
+def test_dense_ffn(c64, name, path):
     cfg, layer = _layer(name)
     c64.load_layer(0, layer)
     x = W.xhat_inputs(cfg, 4, 3)
@@ -72,7 +88,8 @@ def test_dense_ffn(c64, name):
 
 
 @pytest.mark.parametrize("name", ["relu_f16", "relu_q4"])
-def test_edge_lists(c64, name):
+@pytest.mark.parametrize("path", ["default", "step kernel"], indirect=True)
+def test_edge_lists(c64, name, path):
     """Empty list -> b_down; full list -> dense; an unordered subset."""
     t = G.torch()
     cfg, layer = _layer(name)
@@ -149,12 +166,16 @@ def test_layer_counts_and_calibrated_permutation(c64):
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4"])
 @pytest.mark.parametrize("B", [1, 3, 8, 16])
 @pytest.mark.parametrize("dense", [False, True])
-def test_decode_stack_teacher_forced(name, B, dense):
-    """Three-layer stack, one persistent launch: per layer the oracle consumes
-    the GPU's x_hat (trace) and must give the same list and the same update."""
+@pytest.mark.parametrize("layerwise", [True, False])
+def test_decode_stack_teacher_forced(name, B, dense, layerwise):
+    """Three-layer stack, on the default path (batches layer by layer) or all
+    in one persistent launch: per layer the oracle consumes the GPU's x_hat
+    (trace) and must give the same list and the same update."""
     t = G.torch()
     cfg = CFGS[name]
     c = G.ctx(max_layers=3, max_batch=max(8, B))
+    if not layerwise:
+        pi.pi_debug_set_mma_min_batch(c.handle, 0)
     layers, perms = [], []
     for l in range(3):
         lw = W.make_layer(cfg, l, 0, random_b1=True, random_bdown=True)
@@ -218,7 +239,8 @@ def test_decode_step_host_buffers_match_device_step():
 
 
 @pytest.mark.parametrize("name", list(CFGS))
-def test_predictor_hidden_layer_bit_exact(c64, name):
+@pytest.mark.parametrize("path", ["default", "step kernel"], indirect=True)
+def test_predictor_hidden_layer_bit_exact(c64, name, path):
     """h = max(CDOT(W1, x_hat) + b1, 0) of every token equals the oracle's
     canonical fp32 h bit for bit (the mixed-precision fma of the kernel
     widens both 16-bit operands exactly and rounds once per step)."""
@@ -239,7 +261,7 @@ def test_predictor_hidden_layer_bit_exact(c64, name):
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16"])
 @pytest.mark.parametrize("B", [8, 16, 40, 64])
 def test_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
-    """Batches of 8+ tokens run the FFN as a gather-GEMM on tcgen05 (A^T
+    """Batches of several tokens run the FFN as a gather-GEMM on tcgen05 (A^T
     rounded to the weights' 16-bit type between the two GEMMs); it must match
     the oracle within the usual tolerance, and the CUDA-core path of the step
     kernel on the same list within twice it."""
@@ -254,7 +276,7 @@ def test_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
     pi.pi_debug_set_mma_min_batch(c64.handle, 0)
     y_cc = c64.sparse_ffn(0, xd, idx, cnt)
     c64.check()
-    pi.pi_debug_set_mma_min_batch(c64.handle, 8)
+    pi.pi_debug_set_mma_min_batch(c64.handle, LAYERWISE_MIN_BATCH)
     m = int(cnt.item())
     oidx = np.sort(idx[:m].cpu().numpy())
     got = G.y_to_f64(y_tc, cfg.act_dtype)
@@ -268,9 +290,9 @@ def test_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
 
 
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "ring_wrap", "opt_1layer"])
-@pytest.mark.parametrize("B", [8, 9, 16, 17, 40, 64])
+@pytest.mark.parametrize("B", [2, 5, 8, 9, 16, 17, 40, 64])
 def test_batched_predictor_matches_oracle_and_step_kernel(c64, name, B):
-    """From 8 tokens the predictor runs as register-tiled launches (8-token
+    """From 2 tokens the predictor runs as register-tiled launches (8-token
     blocks, a halving butterfly over R x 8 dot products per warp); its lists
     equal the oracle's and, entry for entry, the step kernel's on the same
     x_hat (one, two and several token blocks; r = 2048 takes the narrow
@@ -284,7 +306,7 @@ def test_batched_predictor_matches_oracle_and_step_kernel(c64, name, B):
         idx2, cnt2 = c64.predict(0, G.dev16(x))
         c64.check()
     finally:
-        pi.pi_debug_set_mma_min_batch(c64.handle, 8)
+        pi.pi_debug_set_mma_min_batch(c64.handle, LAYERWISE_MIN_BATCH)
     m = int(cnt.item())
     assert m == int(cnt2.item())
     assert np.array_equal(idx[:m].cpu().numpy(), idx2[:m].cpu().numpy())
@@ -304,7 +326,7 @@ def test_large_batch_decode_x_hat_and_list_match_fused_kernel():
         c.load_layer(l, W.make_layer(cfg, l, 0, random_b1=True, random_bdown=True))
     x0 = W.decode_inputs(cfg, B, 8)
     out = []
-    for mma in (8, 0):
+    for mma in (LAYERWISE_MIN_BATCH, 0):
         pi.pi_debug_set_mma_min_batch(c.handle, mma)
         x = t.from_numpy(x0.copy()).cuda()
         tx = t.zeros((L, B, cfg.d), dtype=t.float32, device="cuda")
@@ -330,6 +352,7 @@ def test_tuning_knobs_do_not_change_results(knobs):
     t = G.torch()
     cfg = CFGS["relu_f16"]
     c = G.ctx(max_layers=3, max_batch=4)
+    pi.pi_debug_set_mma_min_batch(c.handle, 0)  # the knobs tune the step kernel
     for l in range(3):
         c.load_layer(l, W.make_layer(cfg, l, 0, random_b1=True, random_bdown=True))
     x0 = t.from_numpy(W.decode_inputs(cfg, 2, 6)).cuda()
