@@ -213,14 +213,16 @@ __device__ __forceinline__ void tile_load(uint32_t dst, const CUtensorMap *tm, i
 }
 
 // ------------------------------------------------------------------ up / gate kernel
-// Rows of the SM's slice are taken up to 256 at a time (two 128-row MMA
-// tiles share each K step, so a short slice does not cost a second pass).
+// Rows of the SM's slice are taken up to RP at a time: 256 for ReLU (two
+// 128-row MMA tiles share each K step, so a short slice does not cost a
+// second pass), 128 for ReGLU, whose stages carry two matrices: five stages
+// of 128 rows keep more bytes in flight than three of 256.
 // Warp 0 (one lane) produces: per stage, gather4 loads of the rows' next 64
 // columns (W_up, W_gate) and a tile load of x_hat; warp 1 (one lane) issues
 // the MMAs and commits each stage back to the producer; all four warps run
 // the epilogue.  Rows past the slice are gathered from row n (out of range:
 // zeros) or left stale; their accumulator rows are never read.
-template <typename T, bool REGLU, int STAGES>
+template <typename T, bool REGLU, int STAGES, int RP>
 __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ MmaParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -228,13 +230,13 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
     const LayerDev &L = *p.layer;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = L.d, n = L.n, B = p.B, Np = p.Npad;
-    constexpr uint32_t kW = 2 * kTileA; // 256 rows x 128 bytes of one weight matrix
+    constexpr uint32_t kW = RP / 128 * kTileA; // RP rows x 128 bytes of one weight matrix
     constexpr uint32_t kStage = kW * (REGLU ? 2 : 1) + kTileX;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * kStage);
     uint64_t *empty = full + STAGES;
     uint64_t *done = empty + STAGES;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
-    int *sid = reinterpret_cast<int *>(tslot + 4); // [256] row ids of the current pass
+    int *sid = reinterpret_cast<int *>(tslot + 4); // [RP] row ids of the current pass
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(full + s, kIssuers), mbar_init1(empty + s);
         mbar_init1(done);
@@ -250,10 +252,10 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
     uint32_t gp = 0, gc = 0, pass = 0; // stages produced / consumed, passes
     bool ok = true;
 
-    for (int r0 = s0; r0 < s1; r0 += 256, ++pass) {
-        const int rows = min(256, s1 - r0);
+    for (int r0 = s0; r0 < s1; r0 += RP, ++pass) {
+        const int rows = min(RP, s1 - r0);
         const int ntile = (rows + 127) / 128;
-        for (int r = tid; r < 256; r += kMT) {
+        for (int r = tid; r < RP; r += kMT) {
             int id = n; // out of range: zeros
             if (r < rows) {
                 id = p.idx ? p.idx[r0 + r] : r0 + r;
@@ -515,9 +517,9 @@ __global__ void ffn_merge(const __grid_constant__ MmaParams p, int nks)
 template <typename T, bool REGLU>
 cudaError_t launch_up(const MmaParams &p, int grid, cudaStream_t s)
 {
-    constexpr int st = REGLU ? 3 : 5;
-    const int smem = st * (int)(2 * kTileA * (REGLU ? 2 : 1) + kTileX) + 128 + 256 * 4;
-    auto kern = ffn_up_mma<T, REGLU, st>;
+    constexpr int st = 5, rp = REGLU ? 128 : 256;
+    const int smem = st * (int)(rp / 128 * kTileA * (REGLU ? 2 : 1) + kTileX) + 128 + rp * 4;
+    auto kern = ffn_up_mma<T, REGLU, st, rp>;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kMT, smem, s>>>(p);
