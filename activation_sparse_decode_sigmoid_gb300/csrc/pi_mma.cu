@@ -213,10 +213,10 @@ __device__ __forceinline__ void tile_load(uint32_t dst, const CUtensorMap *tm, i
 }
 
 // ------------------------------------------------------------------ up / gate kernel
-// Rows of the SM's slice are taken up to RP at a time: 256 for ReLU (two
-// 128-row MMA tiles share each K step, so a short slice does not cost a
-// second pass), 128 for ReGLU, whose stages carry two matrices: five stages
-// of 128 rows keep more bytes in flight than three of 256.
+// Rows of the SM's slice are taken up to RP = 128 at a time (one MMA tile;
+// RP = 256 would let two tiles share each K step).  Small stages leave room
+// for more of them in shared memory: nine for ReLU, five for ReGLU, whose
+// stages carry two matrices; more stages keep more bytes in flight.
 // Warp 0 (one lane) produces: per stage, gather4 loads of the rows' next 64
 // columns (W_up, W_gate) and a tile load of x_hat; warp 1 (one lane) issues
 // the MMAs and commits each stage back to the producer; all four warps run
@@ -517,8 +517,9 @@ __global__ void ffn_merge(const __grid_constant__ MmaParams p, int nks)
 template <typename T, bool REGLU>
 cudaError_t launch_up(const MmaParams &p, int grid, cudaStream_t s)
 {
-    constexpr int st = 5, rp = REGLU ? 128 : 256;
-    const int smem = st * (int)(rp / 128 * kTileA * (REGLU ? 2 : 1) + kTileX) + 128 + rp * 4;
+    constexpr int st = REGLU ? 5 : 9, rp = 128;
+    // stages, then full[st], empty[st], done, the TMEM slot (16 bytes) and the row ids [rp]
+    const int smem = st * (int)(rp / 128 * kTileA * (REGLU ? 2 : 1) + kTileX) + (2 * st + 1) * 8 + 16 + rp * 4;
     auto kern = ffn_up_mma<T, REGLU, st, rp>;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
