@@ -7,24 +7,24 @@
 // batch takes the union of its tokens' sets.  With B tokens every weight row
 // feeds B dot products (at B = 64, 1.9 G multiply-adds per layer for the
 // 29 M-weight output layer), so the work is arithmetic, not streaming: these
-// kernels give each warp a register tile of R rows x 8 tokens and read every
-// weight row from HBM once.
+// kernels give each warp a register tile of R rows x TT tokens (TT = 2, 4 or
+// 8 by batch size) and read every weight row from HBM once.
 //
 //   rmsnorm_rows  x_hat = RMSNorm(x), one CTA per token, in the step
 //                 kernel's reduction order (the same bits)
 //   pred_hidden   h = relu(W1 x_hat + b1), fp32 [B][r]: a CTA keeps one block
-//                 of 8 tokens' x_hat in shared memory; its warps stream R rows
+//                 of TT tokens' x_hat in shared memory; its warps stream R rows
 //                 of W1 each from global memory, PD chunks ahead
 //   pred_out      union mask words: a CTA owns 8R rows of W2, brought into
 //                 shared memory by one bulk copy per warp, and streams the
-//                 batch's h through in blocks of 8 tokens; each CTA writes
+//                 batch's h through in blocks of TT tokens; each CTA writes
 //                 whole mask words (no atomics, nothing to clear first)
 //   pred_compact  mask words -> ascending list + count (one CTA)
 //
 // Every dot product is CDOT: lane l of 32 accumulates chunks l, l+32, ... of
 // 8 consecutive elements with correctly rounded fmas, then the 32 lane sums
 // meet in the xor butterfly (16, 8, 4, 2, 1).  A lane here holds its lane
-// sum of R x 8 dot products and the warp combines them by a halving
+// sum of R x TT dot products and the warp combines them by a halving
 // butterfly: each level exchanges half of the values and lane l keeps the
 // half its bit selects, so every value still meets its partner lanes in the
 // butterfly's order (fp32 addition is commutative): the same bits as one dot
@@ -42,7 +42,6 @@ namespace pi {
 namespace {
 
 constexpr int kPT = 256; // threads per CTA of the predictor kernels (8 warps)
-constexpr int kTok = 8;  // tokens per register tile
 
 __device__ __forceinline__ void cp16(uint32_t dst, const void *src, uint32_t src_bytes)
 {
@@ -168,11 +167,11 @@ __global__ void __launch_bounds__(512) rmsnorm_rows(const PredParams p)
 
 // ------------------------------------------------------------------ hidden layer
 // acc[rr][t] += the lane's chunks of CDOT(W1[i0 + rr], x_hat_t): rows from
-// global memory, PD chunks in flight per row; x_hat of the 8 tokens in
+// global memory, PD chunks in flight per row; x_hat of the TT tokens in
 // shared memory ([8][K] 16-bit); the mixed-precision fma needs no conversion.
-template <typename T, int R, int PD>
+template <typename T, int R, int PD, int TT>
 __device__ __forceinline__ void cdot_x16(const uint16_t *W, int K, int M, int i0, const uint8_t *xs, int lane,
-                                         float (&acc)[R][kTok])
+                                         float (&acc)[R][TT])
 {
     const int nch = K >> 3;
     const uint4 *wr[R];
@@ -190,7 +189,7 @@ __device__ __forceinline__ void cdot_x16(const uint16_t *W, int K, int M, int i0
             const int ch = c0 + 32 * s;
             if (ch < nch) {
 #pragma unroll
-                for (int t = 0; t < kTok; ++t) {
+                for (int t = 0; t < TT; ++t) {
                     const uint4 xv = *reinterpret_cast<const uint4 *>(xs + (size_t)t * K * 2 + (size_t)ch * 16);
 #pragma unroll
                     for (int rr = 0; rr < R; ++rr) acc[rr][t] = fma_chunk<T>(w[s][rr], xv, acc[rr][t]);
@@ -207,7 +206,7 @@ __device__ __forceinline__ void cdot_x16(const uint16_t *W, int K, int M, int i0
 // h[t][j] = max(CDOT(W1[j], x_hat_t) + b1[j], 0).  CTA c takes token block
 // c mod ntb and every ncta-th group of 8R rows.  It also clears the mask
 // words, for output tiles narrower than a word.
-template <typename T, int R, int PD>
+template <typename T, int R, int PD, int TT>
 __global__ void __launch_bounds__(kPT, 1) pred_hidden(const PredParams p)
 {
     using F = F16T<T>;
@@ -215,10 +214,10 @@ __global__ void __launch_bounds__(kPT, 1) pred_hidden(const PredParams p)
     if (cta_aborted(p)) return;
     const LayerDev &L = p.L;
     const int d = L.d, r = L.r, B = p.B;
-    const int ntb = (B + kTok - 1) / kTok;
+    const int ntb = (B + TT - 1) / TT;
     const int tb = blockIdx.x % ntb, cta = blockIdx.x / ntb;
     const int ncta = ((int)gridDim.x - tb + ntb - 1) / ntb;
-    const int t0 = tb * kTok, nch = d >> 3;
+    const int t0 = tb * TT, nch = d >> 3;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nrg = (r + 8 * R - 1) / (8 * R);
     if (lane == 0) // this warp's rows of every unit start for L2 now: the loads below then wait on L2, not HBM
@@ -227,7 +226,7 @@ __global__ void __launch_bounds__(kPT, 1) pred_hidden(const PredParams p)
             if (nr > 0) bulk_prefetch_l2(L.w1 + (size_t)i0 * d, (uint32_t)nr * d * 2, policy_evict_normal());
         }
     for (int k = blockIdx.x * kPT + threadIdx.x; k < (L.n + 31) >> 5; k += (int)gridDim.x * kPT) p.mask[k] = 0u;
-    for (int q = threadIdx.x; q < kTok * nch; q += kPT) {
+    for (int q = threadIdx.x; q < TT * nch; q += kPT) {
         const int t = q / nch, ch = q - t * nch;
         const bool v = t0 + t < B;
         cp16(smem_u32(smem) + (uint32_t)(t * d * 2 + ch * 16), v ? (const void *)(p.xhat + (size_t)(t0 + t) * d + ch * 8)
@@ -237,28 +236,28 @@ __global__ void __launch_bounds__(kPT, 1) pred_hidden(const PredParams p)
     cp_commit();
     cp_wait<0>();
     __syncthreads();
-    constexpr int NV = R * kTok;
+    constexpr int NV = R * TT;
     for (int rg = cta; rg < nrg; rg += ncta) {
         const int i0 = rg * 8 * R + warp * R;
         if (i0 >= r) continue; // warp-uniform; no CTA barrier below
         // the rows' biases, loaded now so that the epilogue does not wait for them
         const float b1r = lane < R && i0 + lane < r ? F::one(L.b1[i0 + lane]) : 0.f;
-        float acc[R][kTok];
+        float acc[R][TT];
 #pragma unroll
         for (int rr = 0; rr < R; ++rr)
 #pragma unroll
-            for (int t = 0; t < kTok; ++t) acc[rr][t] = 0.f;
-        cdot_x16<T, R, PD>(L.w1, d, r, i0, smem, lane, acc);
+            for (int t = 0; t < TT; ++t) acc[rr][t] = 0.f;
+        cdot_x16<T, R, PD, TT>(L.w1, d, r, i0, smem, lane, acc);
         float v[NV];
 #pragma unroll
         for (int rr = 0; rr < R; ++rr)
 #pragma unroll
-            for (int t = 0; t < kTok; ++t) v[rr * kTok + t] = acc[rr][t];
+            for (int t = 0; t < TT; ++t) v[rr * TT + t] = acc[rr][t];
         int base = 0;
         halve<NV, 16, NV>(v, lane, base);
 #pragma unroll
         for (int j = 0; j < held(NV); ++j) {
-            const int k = base + j, rr = k / kTok, t = k % kTok;
+            const int k = base + j, rr = k / TT, t = k % TT;
             const int row = i0 + rr, tok = t0 + t;
             const float b1v = __shfl_sync(0xffffffffu, b1r, rr, 32); // (every lane: a full-warp shuffle)
             if ((lane & dup_mask(NV)) == 0 && row < r && tok < B) {
@@ -282,7 +281,7 @@ __device__ __forceinline__ int hpos(int ch, int hf) { return (ch >> 5) * 256 + h
 // tokens (two buffers).  With WS = 2 tile slots, a warp issues the copy of
 // its rows of the next unit before it computes this one (small batches,
 // where the rows' transfer, not the arithmetic, is the longer part).
-template <typename T, int R, int WS>
+template <typename T, int R, int WS, int TT>
 __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
 {
     using F = F16T<T>;
@@ -295,20 +294,20 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
     const uint32_t wB = (uint32_t)R * r * 2; // bytes of one warp's rows
     uint8_t *wtile = smem + (size_t)warp * WS * wB;
     float *hbuf = reinterpret_cast<float *>(smem + 8 * (size_t)WS * wB);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 8 * (size_t)WS * wB + 2 * (size_t)kTok * Kp * 4);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 8 * (size_t)WS * wB + 2 * (size_t)TT * Kp * 4);
     uint32_t *smask = reinterpret_cast<uint32_t *>(bar + 8 * WS);
     if (threadIdx.x < 8 * WS) mbar_init(bar + threadIdx.x, 1);
     if (threadIdx.x < (RT + 31) / 32) smask[threadIdx.x] = 0u;
     fence_barrier_init();
     if (cta_aborted(p)) return; // (its barrier also publishes the initialised mbarriers)
-    const int ntb = (B + kTok - 1) / kTok;
+    const int ntb = (B + TT - 1) / TT;
     const int nrt = (n + RT - 1) / RT;
     const int nwords = (n + 31) >> 5;
     // h block tb into buffer b (zeros past B), in the conflict-free layout
     const auto stage_h = [&](int tb, int b) {
-        const int t0 = tb * kTok;
-        float *dst = hbuf + (size_t)b * kTok * Kp;
-        for (int q = threadIdx.x; q < kTok * nch * 2; q += kPT) {
+        const int t0 = tb * TT;
+        float *dst = hbuf + (size_t)b * TT * Kp;
+        for (int q = threadIdx.x; q < TT * nch * 2; q += kPT) {
             const int t = q / (nch * 2), c = q - t * nch * 2, ch = c >> 1, hf = c & 1;
             const bool v = t0 + t < B;
             cp16(smem_u32(dst + (size_t)t * Kp + hpos(ch, hf)),
@@ -362,12 +361,12 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
                 landed = true;
             }
             if (nr > 0 && ok) {
-                const float *hs = hbuf + (size_t)(ntb > 1 ? (tb & 1) : 0) * kTok * Kp;
-                float acc[R][kTok];
+                const float *hs = hbuf + (size_t)(ntb > 1 ? (tb & 1) : 0) * TT * Kp;
+                float acc[R][TT];
 #pragma unroll
                 for (int rr = 0; rr < R; ++rr)
 #pragma unroll
-                    for (int t = 0; t < kTok; ++t) acc[rr][t] = 0.f;
+                    for (int t = 0; t < TT; ++t) acc[rr][t] = 0.f;
                 for (int ch = lane; ch < nch; ch += 32) {
                     uint4 w[R];
 #pragma unroll
@@ -375,9 +374,9 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
                         w[rr] = *reinterpret_cast<const uint4 *>(wt + (size_t)rr * r * 2 + (size_t)ch * 16);
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
-                        float4 hv[kTok];
+                        float4 hv[TT];
 #pragma unroll
-                        for (int t = 0; t < kTok; ++t)
+                        for (int t = 0; t < TT; ++t)
                             hv[t] = *reinterpret_cast<const float4 *>(hs + (size_t)t * Kp + hpos(ch, hf));
 #pragma unroll
                         for (int e2 = 0; e2 < 2; ++e2) { // elements 4 hf + 2 e2 and 4 hf + 2 e2 + 1
@@ -386,7 +385,7 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
                                 const uint32_t word = hf == 0 ? (e2 == 0 ? w[rr].x : w[rr].y) : (e2 == 0 ? w[rr].z : w[rr].w);
                                 const float2 wf = F::pair(word);
 #pragma unroll
-                                for (int t = 0; t < kTok; ++t) {
+                                for (int t = 0; t < TT; ++t) {
                                     const float h0 = e2 == 0 ? hv[t].x : hv[t].z, h1 = e2 == 0 ? hv[t].y : hv[t].w;
                                     acc[rr][t] = __fmaf_rn(wf.y, h1, __fmaf_rn(wf.x, h0, acc[rr][t]));
                                 }
@@ -394,20 +393,20 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
                         }
                     }
                 }
-                constexpr int NV = R * kTok;
+                constexpr int NV = R * TT;
                 float v[NV];
 #pragma unroll
                 for (int rr = 0; rr < R; ++rr)
 #pragma unroll
-                    for (int t = 0; t < kTok; ++t) v[rr * kTok + t] = acc[rr][t];
+                    for (int t = 0; t < TT; ++t) v[rr * TT + t] = acc[rr][t];
                 int base = 0;
                 halve<NV, 16, NV>(v, lane, base);
                 uint32_t mine = 0;
 #pragma unroll
                 for (int j = 0; j < held(NV); ++j) {
-                    const int k = base + j, rr = k / kTok, t = k % kTok;
+                    const int k = base + j, rr = k / TT, t = k % TT;
                     const float b2v = __shfl_sync(0xffffffffu, b2r, rr, 32);
-                    if (rr < nr && tb * kTok + t < B && __fadd_rn(v[j], b2v) > 0.f) mine |= 1u << rr;
+                    if (rr < nr && tb * TT + t < B && __fadd_rn(v[j], b2v) > 0.f) mine |= 1u << rr;
                 }
                 bits |= __reduce_or_sync(0xffffffffu, mine);
             }
@@ -494,16 +493,16 @@ __global__ void __launch_bounds__(256) pred_compact(const PredParams p)
     }
 }
 
-// shared memory of pred_out: WS tile slots, two h blocks, the mbarriers, the mask words
-int out_smem(int R, int WS, int r) { return 8 * WS * R * r * 2 + 2 * kTok * ((r + 255) & ~255) * 4 + 8 * WS * 8 + 16; }
+// shared memory of pred_out: WS tile slots, two h blocks of TT tokens, the mbarriers, the mask words
+int out_smem(int R, int WS, int TT, int r) { return 8 * WS * R * r * 2 + 2 * TT * ((r + 255) & ~255) * 4 + 8 * WS * 8 + 16; }
 
 int compact_grid(int n) { return std::max(1, ((n + 31) / 32 + 255) / 256); }
 
-template <typename T, int R, int PD>
+template <typename T, int R, int PD, int TT>
 cudaError_t launch_hidden(const PredParams &p, int sms, cudaStream_t s)
 {
-    const int smem = kTok * p.L.d * 2, ntb = (p.B + kTok - 1) / kTok;
-    auto kern = pred_hidden<T, R, PD>;
+    const int smem = TT * p.L.d * 2, ntb = (p.B + TT - 1) / TT;
+    auto kern = pred_hidden<T, R, PD, TT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int per_sm = 1;
@@ -516,11 +515,11 @@ cudaError_t launch_hidden(const PredParams &p, int sms, cudaStream_t s)
     return cudaGetLastError();
 }
 
-template <typename T, int R, int WS>
+template <typename T, int R, int WS, int TT>
 cudaError_t launch_out(const PredParams &p, int sms, cudaStream_t s)
 {
-    const int smem = out_smem(R, WS, p.L.r);
-    auto kern = pred_out<T, R, WS>;
+    const int smem = out_smem(R, WS, TT, p.L.r);
+    auto kern = pred_out<T, R, WS, TT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nrt = (p.L.n + 8 * R - 1) / (8 * R);
@@ -531,15 +530,21 @@ cudaError_t launch_out(const PredParams &p, int sms, cudaStream_t s)
 template <typename T>
 cudaError_t launch_all(const PredParams &p, int sms, cudaStream_t s)
 {
-    // hidden layer: one row per warp for a single token block (more CTAs), else two
-    cudaError_t e = p.B <= kTok ? launch_hidden<T, 1, 8>(p, sms, s) : launch_hidden<T, 2, 4>(p, sms, s);
+    const int B = p.B;
+    // hidden layer: token tiles of 2, 4 (two blocks up to 8 tokens: twice the CTAs) or 8;
+    // one row per warp up to 8 tokens, else two
+    cudaError_t e = B <= 2   ? launch_hidden<T, 1, 8, 2>(p, sms, s)
+                    : B <= 8 ? launch_hidden<T, 1, 8, 4>(p, sms, s)
+                             : launch_hidden<T, 2, 4, 8>(p, sms, s);
     if (e != cudaSuccess) return e;
-    // output layer (the tile stays within shared memory): up to r = 1024, 8 rows
-    // per warp, or for one or two token blocks 4 rows with the next unit's in
-    // flight; beyond, 2 rows
-    if (p.L.r > 1024) e = launch_out<T, 2, 1>(p, sms, s);
-    else if (p.B <= 2 * kTok) e = launch_out<T, 4, 2>(p, sms, s);
-    else e = launch_out<T, 8, 1>(p, sms, s);
+    // output layer (the tile stays within shared memory): beyond r = 1024, 2 rows per
+    // warp; else for one or two token blocks 4 rows with the next unit's in flight,
+    // else 8 rows; token tiles of 2, 4 or 8
+    if (p.L.r > 1024) e = B <= 2 ? launch_out<T, 2, 1, 2>(p, sms, s) : launch_out<T, 2, 1, 8>(p, sms, s);
+    else if (B <= 2) e = launch_out<T, 4, 2, 2>(p, sms, s);
+    else if (B <= 4) e = launch_out<T, 4, 2, 4>(p, sms, s);
+    else if (B <= 16) e = launch_out<T, 4, 2, 8>(p, sms, s);
+    else e = launch_out<T, 8, 1, 8>(p, sms, s);
     if (e != cudaSuccess) return e;
     pred_compact<<<compact_grid(p.L.n), 256, 0, s>>>(p);
     return cudaGetLastError();
