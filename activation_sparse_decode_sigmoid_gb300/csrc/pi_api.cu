@@ -125,7 +125,7 @@ bool valid_dtype16(int dt) { return dt == PI_F16 || dt == PI_BF16; }
 pi_status check_desc(pi_ctx *c, const pi_layer_desc *d)
 {
     if (!d) return fail(c, PI_ERR_ARG, "desc is NULL");
-    if (d->act != PI_RELU && d->act != PI_REGLU) return fail(c, PI_ERR_ARG, "act %d invalid", d->act);
+    if (d->act != PI_RELU && d->act != PI_REGLU && d->act != PI_SQRELU) return fail(c, PI_ERR_ARG, "act %d invalid", d->act);
     if (!valid_dtype16(d->act_dtype)) return fail(c, PI_ERR_ARG, "act_dtype %d invalid", d->act_dtype);
     if (d->w_dtype != d->act_dtype && !(d->w_dtype == PI_Q4_0 && d->act_dtype == PI_F16))
         return fail(c, PI_ERR_ARG, "w_dtype %d with act_dtype %d unsupported", d->w_dtype, d->act_dtype);

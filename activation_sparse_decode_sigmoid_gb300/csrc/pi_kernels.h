@@ -25,6 +25,9 @@ constexpr int kMaxNeuronsPerStage = 8;
 constexpr int kPhaseBTokens = 4;     // tokens per inner pass of the W2 dot products
 constexpr int kTimelineEvents = 9;   // stamps per layer in the debug timeline
 
+// activation families (mirror pi.h's pi_act)
+constexpr int ACT_RELU = 0, ACT_REGLU = 1, ACT_SQRELU = 2;
+
 // device status codes (mirror pi.h)
 constexpr int PI_DEV_TIMEOUT = -6;
 constexpr int PI_DEV_FLAG = -7;

@@ -334,7 +334,8 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
                     for (int jj = 0; jj < 16; ++jj) {
                         const int t = c0 + jj;
                         if (t < B) {
-                            const float a = REGLU ? fmaxf(gt[jj] + bias, 0.f) * u[jj] : fmaxf(u[jj] + bias, 0.f);
+                            const float rl = fmaxf((REGLU ? gt[jj] : u[jj]) + bias, 0.f);
+                            const float a = REGLU ? rl * u[jj] : (L.act == ACT_SQRELU ? rl * rl : rl);
                             p.actT[(size_t)t * p.mstride + r0 + r] = H::round(id < n ? a : 0.f);
                         }
                     }

@@ -85,7 +85,7 @@ extern "C" pi_status pi_sparse_ffn_noalloc(const pi_ffn_rows *w, const void *x_h
                                            const int32_t *count, void *y, int32_t *dev_status, void *stream)
 {
     if (!w || !x_hat || !idx || !count || !y || !w->up || !w->down_rows) return PI_ERR_ARG;
-    if (w->act != PI_RELU && w->act != PI_REGLU) return PI_ERR_ARG;
+    if (w->act != PI_RELU && w->act != PI_REGLU && w->act != PI_SQRELU) return PI_ERR_ARG;
     if (w->act == PI_REGLU && !w->gate) return PI_ERR_ARG;
     if (w->act_dtype != PI_F16 && w->act_dtype != PI_BF16) return PI_ERR_ARG;
     const int d = w->d_model, n = w->d_ffn;

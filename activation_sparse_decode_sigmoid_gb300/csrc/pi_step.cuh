@@ -929,7 +929,7 @@ static __device__ __forceinline__ void row_dots(const LayerDev &L, uint32_t a, u
     }
 }
 
-template <typename T, bool Q4, int TGF, bool REGLU>
+template <typename T, bool Q4, int TGF, bool REGLU, bool SQ>
 static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd,
                                     bool xs_valid)
 {
@@ -983,7 +983,8 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
                                                            : S.sbias[pos];
 #pragma unroll
                             for (int t = 0; t < TGF; ++t) {
-                                const float av = REGLU ? fmaxf(ag[t] + bias, 0.f) * au[t] : fmaxf(au[t] + bias, 0.f);
+                                const float r = fmaxf((REGLU ? ag[t] : au[t]) + bias, 0.f);
+                                const float av = REGLU ? r * au[t] : (SQ ? r * r : r);
                                 act[(os * kMaxNeuronsPerStage + j) * TGF + t] = id >= 0 && t < nt ? av : 0.f;
                             }
                         }
@@ -1081,8 +1082,9 @@ template <typename T, bool Q4, int TGF>
 static __device__ bool phase_c(const StepParams &p, const Shm &S, const LayerDev &L, int l, uint32_t &sd,
                                bool xs_valid)
 {
-    if (L.gate) return phase_c_impl<T, Q4, TGF, true>(p, S, L, l, sd, xs_valid);
-    return phase_c_impl<T, Q4, TGF, false>(p, S, L, l, sd, xs_valid);
+    if (L.gate) return phase_c_impl<T, Q4, TGF, true, false>(p, S, L, l, sd, xs_valid);
+    if (L.act == ACT_SQRELU) return phase_c_impl<T, Q4, TGF, false, true>(p, S, L, l, sd, xs_valid);
+    return phase_c_impl<T, Q4, TGF, false, false>(p, S, L, l, sd, xs_valid);
 }
 
 // ------------------------------------------------------------------ phase D: merge

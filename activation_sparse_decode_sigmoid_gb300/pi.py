@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libpi.so")
 PI_OK = 0
 PI_ERR_ARG, PI_ERR_SHAPE, PI_ERR_CUDA, PI_ERR_OOM = -1, -2, -3, -4
 PI_ERR_NOT_LOADED, PI_ERR_TIMEOUT, PI_ERR_DEVICE_FLAG, PI_ERR_UNSUPPORTED = -5, -6, -7, -8
-PI_RELU, PI_REGLU = 0, 1
+PI_RELU, PI_REGLU, PI_SQRELU = 0, 1, 2
 PI_F16, PI_BF16, PI_Q4_0 = 0, 1, 2
 
 # every symbol include/pi.h declares

@@ -34,7 +34,7 @@ from dataclasses import dataclass, field, replace
 import numpy as np
 
 F16, BF16, Q4_0 = 0, 1, 2
-RELU, REGLU = 0, 1
+RELU, REGLU, SQRELU = 0, 1, 2
 DTYPE_NAMES = {F16: "f16", BF16: "bf16", Q4_0: "q4_0"}
 
 
@@ -45,7 +45,7 @@ class LayerConfig:
     n: int                 # d_ffn (neurons)
     r: int                 # predictor rank
     L: int                 # layers in the stack
-    act: int               # RELU / REGLU
+    act: int               # RELU / REGLU / SQRELU
     w_dtype: int           # F16 / BF16 / Q4_0 (FFN matrices)
     act_dtype: int         # F16 / BF16 (activations, predictor, biases)
     alpha: float           # Zipf exponent of the activation probabilities
@@ -76,6 +76,10 @@ CONFIGS = {
     # Falcon-40B-shaped stack with Q4_0 FFN weights, fp16 predictor
     "falcon40b_relu_q4": LayerConfig("falcon40b_relu_q4", 8192, 32768, 1024, 60, RELU, Q4_0, F16,
                                      alpha=0.9, batches=(64, 1), tokens=128, prompt=64, cfg_id=5),
+    # the third activation family on OPT-30B shapes: squared ReLU, fp16 (measurement of that
+    # family; the pages name no model for it)
+    "opt30b_sqrelu_f16": LayerConfig("opt30b_sqrelu_f16", 7168, 28672, 1024, 48, SQRELU, F16, F16,
+                                     alpha=1.0, batches=(1, 8), tokens=128, cfg_id=6),
 }
 
 # tensor ids for keyed random streams

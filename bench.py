@@ -147,6 +147,8 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
 
 
+ACT_NAMES = ("ReLU", "ReGLU", "squared ReLU")  # by the workload's activation ids 0, 1, 2
+
 # The library's default: batches of this many tokens or more run layer by
 # layer (batched predictor launches, tensor-core FFN) instead of in the
 # persistent step kernel.
@@ -283,7 +285,7 @@ def run_reference(args, world, rank):
 def config_block(cfg, L, B):
     from activation_sparse_decode_sigmoid_gb300 import workload as W
     return {"workload": f"{cfg.name}: {L} layers, d_model {cfg.d}, d_ffn {cfg.n}, predictor rank {cfg.r}, "
-                        f"{'ReGLU' if cfg.act == W.REGLU else 'ReLU'}, weights {W.DTYPE_NAMES[cfg.w_dtype]}, "
+                        f"{ACT_NAMES[cfg.act]}, weights {W.DTYPE_NAMES[cfg.w_dtype]}, "
                         f"Zipf alpha {cfg.alpha}, mean activation {cfg.rho}",
             "batch": B, "seq_len": 1, "parallelism": "replicas (one independent stack per GPU)",
             "l2": "no flush: each step streams the whole stack (GBs) through the 129 MB L2",

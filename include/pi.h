@@ -61,7 +61,13 @@ typedef int32_t pi_status;
 #define PI_ERR_DEVICE_FLAG (-7)  /* a kernel flagged invalid device data */
 #define PI_ERR_UNSUPPORTED (-8)  /* valid request this build does not serve */
 
-typedef enum { PI_RELU = 0, PI_REGLU = 1 } pi_act;
+/* Activation families (de.news.hada.io summary, "Einschränkungen und FAQ":
+ * ReLU, ReGLU and squared ReLU models):
+ *   PI_RELU    a_i = max(W_up[i].x_hat + b_i, 0)
+ *   PI_REGLU   a_i = max(W_gate[i].x_hat + b_i, 0) * (W_up[i].x_hat)
+ *   PI_SQRELU  a_i = max(W_up[i].x_hat + b_i, 0)^2
+ * A neuron is active (its activation nonzero) exactly when its ReLU is. */
+typedef enum { PI_RELU = 0, PI_REGLU = 1, PI_SQRELU = 2 } pi_act;
 typedef enum { PI_F16 = 0, PI_BF16 = 1, PI_Q4_0 = 2 } pi_dtype;
 
 /* Shape and types of one FFN layer and its predictor.

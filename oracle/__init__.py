@@ -13,7 +13,9 @@ GPU; blog.csdn.net QbitAI/IPADS article and de.news.hada.io summary):
   a small MLP decides which neurons fire; here d -> r -> n with ReLU, then
   sigmoid(z) > 0.5, i.e. z > 0, evaluated in the canonical fp32 order CDOT.
 * ``union``        -- the batch's active set: union of the per-token sets.
-* ``ffn_act``      -- ReLU / ReGLU activations of every neuron (fp64).
+* ``ffn_act``      -- ReLU / ReGLU / squared-ReLU activations of every neuron
+  (fp64; the three families the pages name, de.news.hada.io summary,
+  "Einschränkungen und FAQ").
 * ``ffn_down``     -- only the listed neurons' columns of W_down are summed
   (neuron-aware sparse operator); merging partial results over any partition
   of the list gives the whole ("CPU/GPU混合推理设计" worked example {3,4,5}).
@@ -37,7 +39,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "liboracle.so")
 
 F16, BF16, Q4_0 = 0, 1, 2
-RELU, REGLU = 0, 1
+RELU, REGLU, SQRELU = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -181,7 +183,7 @@ def union(mask) -> np.ndarray:
 
 # ---------------------------------------------------------------- FFN
 def ffn_act(Wup, Wgate, b, xhat, act: int, wdt: int, adt: int, nthreads: int | None = None):
-    """fp64 activations a[B,n] of every neuron (ReLU or ReGLU)."""
+    """fp64 activations a[B,n] of every neuron (ReLU, ReGLU or squared ReLU)."""
     lib = _load()
     xhat = _u16(xhat)
     if wdt == Q4_0:

@@ -38,7 +38,7 @@
 #include <string.h>
 
 enum { OR_F16 = 0, OR_BF16 = 1, OR_Q4_0 = 2 };
-enum { OR_RELU = 0, OR_REGLU = 1 };
+enum { OR_RELU = 0, OR_REGLU = 1, OR_SQRELU = 2 };
 enum { OR_OK = 0, OR_EARG = -1 };
 
 /* ------------------------------------------------------------------ */
@@ -306,8 +306,10 @@ typedef struct {
     double *a;       /* B*n */
 } act_ctx;
 
-/* ReLU:  a_i = max(W_up[i].x + b_i, 0)
- * ReGLU: a_i = max(W_gate[i].x + b_i, 0) * (W_up[i].x)      (bias on the gate) */
+/* ReLU:         a_i = max(W_up[i].x + b_i, 0)
+ * ReGLU:        a_i = max(W_gate[i].x + b_i, 0) * (W_up[i].x)      (bias on the gate)
+ * Squared ReLU: a_i = max(W_up[i].x + b_i, 0)^2  (the third family the engine
+ *               serves: de.news.hada.io summary, "Einschränkungen und FAQ") */
 static void act_row(void *p, long i)
 {
     act_ctx *c = (act_ctx *)p;
@@ -324,6 +326,7 @@ static void act_row(void *p, long i)
         } else {
             up += bi;
             a = up > 0.0 ? up : 0.0;
+            if (c->act == OR_SQRELU) a = a * a;
         }
         c->a[(long)t * c->n + i] = a;
     }

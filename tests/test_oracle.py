@@ -17,6 +17,7 @@ from tests._helpers import (dequant_q4_numpy, layer_dense_f64, permute_layer,
 SMALL = W.LayerConfig("small", 256, 384, 64, 1, W.RELU, W.F16, W.F16, alpha=0.8, cfg_id=101)
 SMALL_REGLU = W.LayerConfig("small_reglu", 256, 320, 32, 1, W.REGLU, W.BF16, W.BF16, alpha=0.7, cfg_id=102)
 SMALL_Q4 = W.LayerConfig("small_q4", 256, 256, 64, 1, W.RELU, W.Q4_0, W.F16, alpha=0.9, cfg_id=103)
+SMALL_SQ = W.LayerConfig("small_sqrelu", 256, 288, 64, 1, W.SQRELU, W.BF16, W.BF16, alpha=0.8, cfg_id=105)
 
 
 # ------------------------------------------------------------------ number formats
@@ -225,7 +226,7 @@ def test_union_matches_flatnonzero():
 
 
 # ------------------------------------------------------------------ FFN
-@pytest.mark.parametrize("cfg", [SMALL, SMALL_REGLU, SMALL_Q4])
+@pytest.mark.parametrize("cfg", [SMALL, SMALL_REGLU, SMALL_Q4, SMALL_SQ])
 def test_dense_ffn_matches_numpy(cfg):
     layer = W.make_layer(cfg, 0, 0, random_bdown=True)
     x = W.xhat_inputs(cfg, 3, 0)
@@ -234,6 +235,8 @@ def test_dense_ffn_matches_numpy(cfg):
     xf = W.from_bits(x, cfg.act_dtype).astype(np.float64)
     if cfg.act == W.REGLU:
         a_ref = np.maximum(xf @ wg.T + b, 0) * (xf @ wu.T)
+    elif cfg.act == W.SQRELU:
+        a_ref = np.square(np.maximum(xf @ wu.T + b, 0))
     else:
         a_ref = np.maximum(xf @ wu.T + b, 0)
     assert np.allclose(a, a_ref, rtol=1e-12, atol=1e-12)
@@ -242,7 +245,7 @@ def test_dense_ffn_matches_numpy(cfg):
     assert np.allclose(y, y_ref, rtol=1e-11, atol=1e-11)
 
 
-@pytest.mark.parametrize("cfg", [SMALL, SMALL_REGLU, SMALL_Q4])
+@pytest.mark.parametrize("cfg", [SMALL, SMALL_REGLU, SMALL_Q4, SMALL_SQ])
 def test_masked_ffn_invariants(cfg):
     layer = W.make_layer(cfg, 0, 0, random_bdown=True)
     x = W.xhat_inputs(cfg, 2, 0)
@@ -288,16 +291,28 @@ def test_golden_worked_example(dt):
     assert dense[0].tolist() == exp["y_dense"]
 
 
+def test_squared_relu_is_the_relu_activation_squared():
+    """Squared ReLU fires exactly where ReLU does, with the ReLU value squared
+    (the ReLU path is pinned on its own above); Q4_0 rows included."""
+    for cfg in (SMALL, SMALL_Q4):
+        layer = W.make_layer(cfg, 0, 0)
+        x = W.xhat_inputs(cfg, 3, 2)
+        relu = O.ffn_act(layer["w_up"], None, layer["b"], x, W.RELU, cfg.w_dtype, cfg.act_dtype)
+        sq = O.ffn_act(layer["w_up"], None, layer["b"], x, W.SQRELU, cfg.w_dtype, cfg.act_dtype)
+        assert np.array_equal(sq, relu * relu)
+        assert np.array_equal(sq != 0, relu != 0) and (relu != 0).any() and (relu == 0).any()
+
+
 def test_bruteforce_tiny_layer_exact_rationals():
     """Pure-Python exact arithmetic on a tiny layer: the fp64 oracle agrees to
-    rounding, for ReLU and ReGLU."""
-    for act in (W.RELU, W.REGLU):
+    rounding, for ReLU, ReGLU and squared ReLU."""
+    for act in (W.RELU, W.REGLU, W.SQRELU):
         cfg = W.LayerConfig("tiny", 16, 12, 8, 1, act, W.F16, W.F16, alpha=0.5, rho=0.3, cfg_id=104)
         layer = W.make_layer(cfg, 0, 3, random_bdown=True)
         x = W.xhat_inputs(cfg, 1, 3)
         xv = [Fraction(float(v)) for v in W.from_bits(x[0], W.F16)]
         wu = [[Fraction(float(v)) for v in row] for row in W.from_bits(layer["w_up"], W.F16)]
-        wg = None if act == W.RELU else [[Fraction(float(v)) for v in row] for row in W.from_bits(layer["w_gate"], W.F16)]
+        wg = None if act != W.REGLU else [[Fraction(float(v)) for v in row] for row in W.from_bits(layer["w_gate"], W.F16)]
         b = [Fraction(float(v)) for v in W.from_bits(layer["b"], W.F16)]
         wd = [[Fraction(float(v)) for v in row] for row in W.from_bits(layer["w_down"], W.F16)]
         bd = [Fraction(float(v)) for v in W.from_bits(layer["b_down"], W.F16)]
@@ -306,6 +321,8 @@ def test_bruteforce_tiny_layer_exact_rationals():
             up = sum(wu[i][k] * xv[k] for k in range(cfg.d))
             if act == W.RELU:
                 a_exact.append(max(up + b[i], Fraction(0)))
+            elif act == W.SQRELU:
+                a_exact.append(max(up + b[i], Fraction(0)) ** 2)
             else:
                 g = sum(wg[i][k] * xv[k] for k in range(cfg.d)) + b[i]
                 a_exact.append(max(g, Fraction(0)) * up)
