@@ -350,6 +350,42 @@ def test_large_batch_decode_x_hat_and_list_match_fused_kernel():
     c.close()
 
 
+def test_layerwise_decode_step_replays_from_a_cuda_graph():
+    """Batches that run layer by layer depend on no host state that changes
+    between calls, so a decode step captured once into a CUDA graph replays
+    on new inputs with the eager step's results, bit for bit."""
+    t = G.torch()
+    cfg = CFGS["reglu_bf16"]
+    B, L = 8, 2
+    c = G.ctx(max_layers=L, max_batch=B)
+    for l in range(L):
+        c.load_layer(l, W.make_layer(cfg, l, 0, random_b1=True, random_bdown=True))
+    xs = [t.from_numpy(W.decode_inputs(cfg, B, s)).cuda() for s in (11, 12, 13)]
+    want = []
+    for x in xs:
+        y = x.clone()
+        c.decode_step(y)
+        c.check()
+        want.append(y)
+    buf = xs[0].clone()
+    side = t.cuda.Stream()
+    side.wait_stream(t.cuda.current_stream())
+    with t.cuda.stream(side):  # warm-up on the capture's side stream
+        c.decode_step(buf)
+    t.cuda.current_stream().wait_stream(side)
+    t.cuda.synchronize()
+    g = t.cuda.CUDAGraph()
+    with t.cuda.graph(g):
+        c.decode_step(buf)
+    for x, w in zip(xs, want):
+        buf.copy_(x)
+        g.replay()
+        t.cuda.synchronize()
+        c.check()
+        assert t.equal(buf, w)
+    c.close()
+
+
 @pytest.mark.parametrize("knobs", [(0, 0, 0, 0), (1, 0, 2, 4), (2, 400, 4, 0), (3, 800, 3, 8), (3, 0, 16, 64)])
 def test_tuning_knobs_do_not_change_results(knobs):
     """Prefetch modes, the FFN lookahead and row prefetch only move data
