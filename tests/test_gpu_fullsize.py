@@ -87,3 +87,61 @@ def test_full_stack_decode_opt30b_sampled_layers():
         err = max_rel_err(xs[l + 1] - xs[l], O.masked_ffn(lw, xh[l], oidx))
         assert err <= 1e-2, f"layer {l}: {err:.3g}"
     c.close()
+
+
+# every dimension at the library's limit: d_model 8192, d_ffn 65536, rank 2048,
+# ReGLU (three 1 GiB matrices), 64 tokens
+MAX = W.LayerConfig("max_sizes", 8192, 65536, 2048, 1, W.REGLU, W.BF16, W.BF16, alpha=0.9, cfg_id=7)
+
+
+def test_maximum_sizes():
+    """Predictor lists bit-exact for 1 and 64 tokens; the FFN and a decode
+    step (one launch at 1 token, layer by layer at 64) match the oracle on
+    sampled tokens, with every dimension at its limit."""
+    t = G.torch()
+    cfg = MAX
+    c = G.ctx(max_layers=1, max_batch=64)
+    dev = t.device("cuda", 0)
+    lw = W.make_layer_device(cfg, 0, 0, dev)
+    cal = t.from_numpy(W.calibration_inputs(cfg, 0, 0).view(np.int16)).to(dev)
+    perm = calibrate_and_load(c, 0, lw, cal)
+    host = W.layer_to_host(lw)
+    del lw
+    for B in (1, 64):
+        x = W.xhat_inputs(cfg, B, 43)
+        idx, cnt, oidx = G.predict_checked(c, 0, host, x, perm)
+        y = c.sparse_ffn(0, G.dev16(x), idx, cnt)
+        c.check()
+        got = G.y_to_f64(y, cfg.act_dtype)
+        for tok in ([0] if B == 1 else [0, 37, 63]):
+            xt = x[tok: tok + 1]
+            want = O.masked_ffn(host, xt, oidx)
+            if B == 1:
+                assert max_rel_err(got[tok: tok + 1], want) <= G.tol(host)
+            else:  # the tensor-core path: within the bound of its arithmetic
+                assert np.all(np.abs(got[tok: tok + 1] - want) <= G.tc_error_bound(host, xt, oidx))
+        # a decode step on the residual: x_hat, list and update against the oracle
+        x0 = W.decode_inputs(cfg, B, 44)
+        xd = t.from_numpy(x0.copy()).cuda()
+        txh = t.zeros((1, B, cfg.d), dtype=t.int16, device="cuda")
+        tidx = t.full((1, cfg.n), -1, dtype=t.int32, device="cuda")
+        tcnt = t.zeros(1, dtype=t.int32, device="cuda")
+        c.set_trace(None, txh, tidx, tcnt)
+        c.decode_step(xd)
+        c.check()
+        c.set_trace(None, None, None, None)
+        xh = G.host16(txh)[0]
+        want_xh = O.rmsnorm(x0.astype(np.float32), cfg.act_dtype)
+        assert np.abs(xh.astype(np.int32) - want_xh.astype(np.int32)).max() <= 1
+        m = int(tcnt[0].item())
+        sel = np.sort(perm[tidx[0, :m].cpu().numpy()])
+        assert np.array_equal(sel, O.union(O.layer_predict(host, xh)["mask"]))
+        upd = xd.cpu().numpy().astype(np.float64) - x0.astype(np.float64)
+        for tok in ([0] if B == 1 else [0, 63]):
+            xt = xh[tok: tok + 1]
+            want = O.masked_ffn(host, xt, sel)
+            if B == 1:
+                assert max_rel_err(upd[tok: tok + 1], want) <= G.tol(host)
+            else:
+                assert np.all(np.abs(upd[tok: tok + 1] - want) <= G.tc_error_bound(host, xt, sel))
+    c.close()
