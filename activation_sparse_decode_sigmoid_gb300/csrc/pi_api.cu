@@ -706,13 +706,44 @@ static pi_status step_common(pi_ctx *c, float *x, int32_t B, int mode)
     int nmax = 0;
     for (int l = 0; l < L; ++l) nmax = std::max(nmax, c->layers[l].desc.d_ffn);
     p.tr_n = nmax;
-    if (!use_mma(c, 0, B)) return launch(c, 0, L, B, mode, p);
-    // Large batch, per layer: x_hat = RMSNorm(x) into the workspace, the
-    // predicted list (or the whole list), then the tensor-core FFN adds the
-    // layer's output into x.
     const int d = c->layers[0].desc.d_model;
     const bool dense = (mode & pi::M_DENSE) != 0;
     const bool bf16 = c->layers[0].desc.act_dtype == PI_BF16;
+    if (!use_mma(c, 0, B)) {
+        if (dense || !use_pred_batch(c, B)) return launch(c, 0, L, B, mode, p);
+        // Q4_0 batches, per layer: x_hat = RMSNorm(x), the batched predictor,
+        // then the step kernel's FFN on that list adds the layer into x
+        for (int l = 0; l < L; ++l) {
+            pi::PredParams q = pred_params(c, l, B);
+            q.x = x;
+            q.tr_x = c->tr_x ? c->tr_x + (size_t)l * B * d : nullptr;
+            q.xhat = c->xhat_ws;
+            q.idx = c->lidx;
+            q.count = c->lidx + pi::kMaxN;
+            q.tr_idx = c->tr_idx ? c->tr_idx + (size_t)l * nmax : nullptr;
+            q.tr_cnt = c->tr_cnt ? c->tr_cnt + l : nullptr;
+            const cudaError_t e = pi::launch_rmsnorm_rows(q, bf16, c->stream);
+            if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "RMSNorm launch: %s", cudaGetErrorString(e));
+            st = pred_batch(c, q, l);
+            if (st) return st;
+            if (c->tr_xhat) {
+                const cudaError_t e2 = cudaMemcpyAsync((uint16_t *)c->tr_xhat + (size_t)l * B * d, c->xhat_ws,
+                                                       (size_t)B * d * 2, cudaMemcpyDeviceToDevice, c->stream);
+                if (e2 != cudaSuccess) return fail(c, PI_ERR_CUDA, "x_hat trace: %s", cudaGetErrorString(e2));
+            }
+            StepParams f{};
+            f.x = x;
+            f.xhat_in = c->xhat_ws;
+            f.idx_in = c->lidx;
+            f.count_in = c->lidx + pi::kMaxN;
+            st = launch(c, l, 1, B, pi::M_IDX_IN | pi::M_FFN | pi::M_RESID, f);
+            if (st) return st;
+        }
+        return PI_OK;
+    }
+    // Large batch, per layer: x_hat = RMSNorm(x) into the workspace, the
+    // predicted list (or the whole list), then the tensor-core FFN adds the
+    // layer's output into x.
     for (int l = 0; l < L; ++l) {
         pi::PredParams q = pred_params(c, l, B);
         q.x = x;
