@@ -223,5 +223,12 @@ cudaError_t launch_transpose_permute16(const uint16_t *src, uint16_t *dst, const
 cudaError_t launch_q4_split(const uint8_t *src, uint8_t *dst, const int32_t *perm, int n, int d, int scB,
                             cudaStream_t s, size_t dstStride = 0);
 cudaError_t launch_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int n, cudaStream_t s);
+// The rows of the listed neurons of a Q4_0 layer L (idx NULL: every neuron;
+// count NULL: n) dequantised to f16 at list position k -> row k of `to`, a
+// 16-bit layer of the same shape (W_up rows with their bias tail), for the
+// tensor-core FFN.  An id outside [0, n) is flagged in *status and its rows
+// are zero.
+cudaError_t launch_q4_to_f16_rows(const LayerDev &L, const LayerDev &to, const int32_t *idx, const int32_t *count,
+                                  int *status, int *abort_flag, cudaStream_t s);
 
 } // namespace pi
