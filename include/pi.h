@@ -17,7 +17,8 @@
  *     whole model is resident in HBM; the hot/cold split becomes an offline
  *     neuron permutation (hot neurons first) and the merge is a split-K
  *     reduction in fp32.
- *   - de.news.hada.io summary: ReLU / ReGLU activations, Q4_0 INT4 weights.
+ *   - de.news.hada.io summary: ReLU / ReGLU / squared-ReLU activations,
+ *     Q4_0 INT4 weights.
  * The pages print no formulas; the readings used (z > 0 for "sigmoid > 0.5",
  * the canonical fp32 predictor order, Q4_0 block layout, weightless RMSNorm
  * between layers, union of per-token sets for a batch) are documented with
@@ -123,6 +124,11 @@ pi_status pi_set_stream(pi_ctx *ctx, void *stream);
  * WdT (one contiguous row per neuron) and splitting Q4_0 rows into separate
  * scale and nibble arrays.  This is the offline placement step of the
  * "CPU/GPU混合推理设计" section, mapped to one device: hot neurons first.
+ * In a context with max_batch >= 2, a Q4_0 layer also sizes the context's
+ * 16-bit scratch, into which batches dequantise their listed rows for the
+ * tensor cores (n * (4 d + 16) bytes, plus n * 2 d for ReGLU, for the
+ * largest Q4_0 layer loaded); if it cannot be allocated, that layer's
+ * batches stay on the CUDA cores.
  * Synchronous: returns when the copy is done; the caller keeps its buffers. */
 pi_status pi_load_layer(pi_ctx *ctx, int32_t layer, const pi_layer_desc *desc,
                         const pi_layer_weights *w, const int32_t *perm);
@@ -292,9 +298,10 @@ pi_status pi_debug_set_tuning(pi_ctx *ctx, int32_t prefetch, int32_t prefetch_ns
 pi_status pi_debug_copy_hidden(pi_ctx *ctx, float *dst, int32_t count);
 
 /* Smallest batch (tokens) that runs layer by layer (default 2): the
- * predictor as batched launches and, with 16-bit weights, the FFN on the
- * tensor cores (tcgen05 gather-GEMM).  0 keeps every batch on the persistent
- * step kernel (CUDA cores).  For comparing the two paths. */
+ * predictor as batched launches and the FFN on the tensor cores (tcgen05
+ * gather-GEMM; Q4_0 rows dequantised to f16 into a context scratch first).
+ * 0 keeps every batch on the persistent step kernel (CUDA cores).  For
+ * comparing the two paths. */
 pi_status pi_debug_set_mma_min_batch(pi_ctx *ctx, int32_t min_batch);
 
 #ifdef __cplusplus
