@@ -189,6 +189,35 @@ cudaError_t occupancy_step_q4(int tgf, int smem_bytes, int *blocks);
 // the union-mask FFN on tcgen05: up/gate kernel on `grid` SMs, then the down kernel
 cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, cudaStream_t s);
 
+// Programmatic dependent launch for the layer-by-layer path: each kernel is
+// launched so that it may be scheduled while its predecessor in the stream
+// finishes.  It first waits for the predecessor's results (a no-op when it
+// was launched without the attribute), then lets its own successor be
+// scheduled; a successor can only start once every CTA of this grid is
+// resident, so the two never wait on each other's resources.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+template <typename... P, typename... A>
+cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, A... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // The predictor of one layer for a batch of several tokens (pi_pred.cu).
 struct PredParams {
     LayerDev L;               // the layer (device pointers)

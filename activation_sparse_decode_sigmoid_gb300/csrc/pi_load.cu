@@ -131,6 +131,7 @@ cudaError_t launch_q4_split(const uint8_t *src, uint8_t *dst, const int32_t *per
 __global__ void q4_to_f16_rows_kernel(const LayerDev L, const LayerDev to, const int32_t *__restrict__ idx,
                                       const int32_t *__restrict__ count, int *status, int *abort_flag)
 {
+    pdl_enter();
     if (*(volatile int *)abort_flag) return;
     int m = count ? *count : L.n;
     if (m < 0 || m > L.n) m = 0; // (the FFN kernels flag it)
@@ -175,8 +176,7 @@ __global__ void q4_to_f16_rows_kernel(const LayerDev L, const LayerDev to, const
 cudaError_t launch_q4_to_f16_rows(const LayerDev &L, const LayerDev &to, const int32_t *idx, const int32_t *count,
                                   int *status, int *abort_flag, cudaStream_t s)
 {
-    q4_to_f16_rows_kernel<<<4 * 152, 256, 0, s>>>(L, to, idx, count, status, abort_flag);
-    return cudaGetLastError();
+    return launch_pdl(q4_to_f16_rows_kernel, dim3(4 * 152), dim3(256), 0, s, L, to, idx, count, status, abort_flag);
 }
 
 cudaError_t launch_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int n, cudaStream_t s)

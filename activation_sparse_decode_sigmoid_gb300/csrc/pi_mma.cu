@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     using H = H16<T>;
+    pdl_enter();
     const LayerDev &L = *p.layer;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = L.d, n = L.n, B = p.B, Np = p.Npad;
@@ -369,6 +370,7 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     using H = H16<T>;
+    pdl_enter();
     const LayerDev &L = *p.layer;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = L.d, n = L.n, B = p.B, Np = p.Npad;
@@ -503,6 +505,7 @@ template <typename T>
 __global__ void ffn_merge(const __grid_constant__ MmaParams p, int nks)
 {
     using H = H16<T>;
+    pdl_enter();
     const LayerDev &L = *p.layer;
     const int d = L.d;
     const size_t total = (size_t)p.B * d;
@@ -524,8 +527,7 @@ cudaError_t launch_up(const MmaParams &p, int grid, cudaStream_t s)
     auto kern = ffn_up_mma<T, REGLU, st, rp>;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kMT, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kMT), smem, s, p);
 }
 
 template <typename T>
@@ -540,11 +542,9 @@ cudaError_t launch_down(const MmaParams &p, int grid, cudaStream_t s)
     const int ncb = (p.d + 255) / 256;
     const int nks = grid / ncb > 8 ? 8 : (grid / ncb < 1 ? 1 : grid / ncb);
     const int units = ncb * nks;
-    kern<<<units < grid ? units : grid, kMT, smem, s>>>(p, nks);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3(units < grid ? units : grid), dim3(kMT), smem, s, p, nks);
     if (e != cudaSuccess || nks == 1) return e;
-    ffn_merge<T><<<grid * 4, 256, 0, s>>>(p, nks);
-    return cudaGetLastError();
+    return launch_pdl(ffn_merge<T>, dim3(grid * 4), dim3(256), 0, s, p, nks);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,

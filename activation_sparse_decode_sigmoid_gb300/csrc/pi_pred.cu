@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(512) rmsnorm_rows(const PredParams p)
     __shared__ float part[16];
     __shared__ float inv_s;
     const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_enter();
     if (cta_aborted(p)) return;
     const int d = p.L.d, n4 = d / 4;
     const float4 *xr = reinterpret_cast<const float4 *>(p.x + (size_t)t * d);
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(kPT, 1) pred_hidden(const PredParams p)
 {
     using F = F16T<T>;
     extern __shared__ __align__(128) uint8_t smem[];
+    pdl_enter();
     if (cta_aborted(p)) return;
     const LayerDev &L = p.L;
     const int d = L.d, r = L.r, B = p.B;
@@ -296,6 +298,7 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
     float *hbuf = reinterpret_cast<float *>(smem + 8 * (size_t)WS * wB);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 8 * (size_t)WS * wB + 2 * (size_t)TT * Kp * 4);
     uint32_t *smask = reinterpret_cast<uint32_t *>(bar + 8 * WS);
+    pdl_enter();
     if (threadIdx.x < 8 * WS) mbar_init(bar + threadIdx.x, 1);
     if (threadIdx.x < (RT + 31) / 32) smask[threadIdx.x] = 0u;
     fence_barrier_init();
@@ -438,6 +441,7 @@ __global__ void __launch_bounds__(256) pred_compact(const PredParams p)
 {
     __shared__ int red[8];
     __shared__ int wsum[8];
+    pdl_enter();
     if (cta_aborted(p)) return;
     const int n = p.L.n, nwords = (n + 31) >> 5;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -511,8 +515,7 @@ cudaError_t launch_hidden(const PredParams &p, int sms, cudaStream_t s)
     const int nrg = (p.L.r + 8 * R - 1) / (8 * R);
     int grid = std::min(ntb * nrg, std::max(1, per_sm) * sms);
     grid = std::max(ntb, grid / ntb * ntb); // every token block gets the same number of CTAs
-    kern<<<grid, kPT, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kPT), smem, s, p);
 }
 
 template <typename T, int R, int WS, int TT>
@@ -523,8 +526,7 @@ cudaError_t launch_out(const PredParams &p, int sms, cudaStream_t s)
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nrt = (p.L.n + 8 * R - 1) / (8 * R);
-    kern<<<std::min(nrt, sms), kPT, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(std::min(nrt, sms)), dim3(kPT), smem, s, p);
 }
 
 template <typename T>
@@ -546,25 +548,22 @@ cudaError_t launch_all(const PredParams &p, int sms, cudaStream_t s)
     else if (B <= 16) e = launch_out<T, 4, 2, 8>(p, sms, s);
     else e = launch_out<T, 8, 1, 8>(p, sms, s);
     if (e != cudaSuccess) return e;
-    pred_compact<<<compact_grid(p.L.n), 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(pred_compact, dim3(compact_grid(p.L.n)), dim3(256), 0, s, p);
 }
 
 } // namespace
 
 cudaError_t launch_rmsnorm_rows(const PredParams &p, bool bf16, cudaStream_t s)
 {
-    if (bf16) rmsnorm_rows<__nv_bfloat16><<<p.B, 512, 0, s>>>(p);
-    else rmsnorm_rows<__half><<<p.B, 512, 0, s>>>(p);
-    return cudaGetLastError();
+    return bf16 ? launch_pdl(rmsnorm_rows<__nv_bfloat16>, dim3(p.B), dim3(512), 0, s, p)
+                : launch_pdl(rmsnorm_rows<__half>, dim3(p.B), dim3(512), 0, s, p);
 }
 
 cudaError_t launch_list_all(const PredParams &p, cudaStream_t s)
 {
     PredParams q = p;
     q.dense = 1;
-    pred_compact<<<compact_grid(p.L.n), 256, 0, s>>>(q);
-    return cudaGetLastError();
+    return launch_pdl(pred_compact, dim3(compact_grid(p.L.n)), dim3(256), 0, s, q);
 }
 
 cudaError_t launch_predict_batch(const PredParams &p, bool bf16, int sms, cudaStream_t s)
