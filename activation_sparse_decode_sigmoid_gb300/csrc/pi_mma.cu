@@ -227,7 +227,6 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     using H = H16<T>;
-    pdl_enter();
     const LayerDev &L = *p.layer;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = L.d, n = L.n, B = p.B, Np = p.Npad;
@@ -245,6 +244,7 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
     }
     // TMEM: tile j (0, 1) of U at columns [j Np, (j+1) Np), of the gate at [(2+j) Np, ...)
     const uint32_t tmem = tmem_alloc(tslot, 256);
+    pdl_enter(); // (the barriers and tensor memory above were set up while the list was finished)
     const int m = list_len(p, n);
     const int s0 = slice_at(m, blockIdx.x, gridDim.x), s1 = slice_at(m, blockIdx.x + 1, gridDim.x);
     const int KT = (d + kBK - 1) / kBK;
@@ -370,7 +370,6 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     using H = H16<T>;
-    pdl_enter();
     const LayerDev &L = *p.layer;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = L.d, n = L.n, B = p.B, Np = p.Npad;
@@ -388,6 +387,7 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     const uint32_t tmem = tmem_alloc(tslot, 128); // tile j at columns [j Np, (j+1) Np)
+    pdl_enter(); // (the barriers and tensor memory above were set up while the up kernel finished)
     const int m = list_len(p, n);
     const int KTall = (m + kBK - 1) / kBK;
     const int ncb = (d + 255) / 256;

@@ -212,8 +212,6 @@ __global__ void __launch_bounds__(kPT, 1) pred_hidden(const PredParams p)
 {
     using F = F16T<T>;
     extern __shared__ __align__(128) uint8_t smem[];
-    pdl_enter();
-    if (cta_aborted(p)) return;
     const LayerDev &L = p.L;
     const int d = L.d, r = L.r, B = p.B;
     const int ntb = (B + TT - 1) / TT;
@@ -222,11 +220,16 @@ __global__ void __launch_bounds__(kPT, 1) pred_hidden(const PredParams p)
     const int t0 = tb * TT, nch = d >> 3;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nrg = (r + 8 * R - 1) / (8 * R);
-    if (lane == 0) // this warp's rows of every unit start for L2 now: the loads below then wait on L2, not HBM
+    // this warp's rows of every unit start for L2 now, while the previous
+    // launch finishes (they do not depend on it): the loads below then wait
+    // on L2, not HBM
+    if (lane == 0)
         for (int rg = cta; rg < nrg; rg += ncta) {
             const int i0 = rg * 8 * R + warp * R, nr = min(R, r - i0);
             if (nr > 0) bulk_prefetch_l2(L.w1 + (size_t)i0 * d, (uint32_t)nr * d * 2, policy_evict_normal());
         }
+    pdl_enter();
+    if (cta_aborted(p)) return;
     for (int k = blockIdx.x * kPT + threadIdx.x; k < (L.n + 31) >> 5; k += (int)gridDim.x * kPT) p.mask[k] = 0u;
     for (int q = threadIdx.x; q < TT * nch; q += kPT) {
         const int t = q / nch, ch = q - t * nch;
@@ -298,11 +301,13 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
     float *hbuf = reinterpret_cast<float *>(smem + 8 * (size_t)WS * wB);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 8 * (size_t)WS * wB + 2 * (size_t)TT * Kp * 4);
     uint32_t *smask = reinterpret_cast<uint32_t *>(bar + 8 * WS);
-    pdl_enter();
     if (threadIdx.x < 8 * WS) mbar_init(bar + threadIdx.x, 1);
     if (threadIdx.x < (RT + 31) / 32) smask[threadIdx.x] = 0u;
     fence_barrier_init();
-    if (cta_aborted(p)) return; // (its barrier also publishes the initialised mbarriers)
+    // (an earlier launch's failure; one the hidden-layer launch raises while
+    // this one starts stays in the status word.  The barrier also publishes
+    // the initialised mbarriers)
+    if (cta_aborted(p)) return;
     const int ntb = (B + TT - 1) / TT;
     const int nrt = (n + RT - 1) / RT;
     const int nwords = (n + 31) >> 5;
@@ -329,16 +334,19 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
                      policy_evict_first());
         }
     };
+    // the first unit's rows do not depend on the hidden layer: they start
+    // while it finishes
+    if (blockIdx.x < nrt) load_rows(blockIdx.x, 0);
+    pdl_enter();
     if (ntb == 1) stage_h(0, 0); // one block serves every unit
     bool ok = true;
     uint32_t it = 0;
-    if (WS == 2 && blockIdx.x < nrt) load_rows(blockIdx.x, 0);
     for (int u = blockIdx.x; u < nrt; u += gridDim.x, ++it) {
         const int sl = WS == 2 ? (int)(it & 1) : 0;
         const uint32_t par = WS == 2 ? (it >> 1) & 1 : it & 1;
         if (WS == 2) {
             if (u + (int)gridDim.x < nrt) load_rows(u + gridDim.x, sl ^ 1); // slot sl ^ 1 was read by the last unit
-        } else {
+        } else if (it > 0) {
             load_rows(u, 0);
         }
         const int i0 = u * RT + warp * R;
