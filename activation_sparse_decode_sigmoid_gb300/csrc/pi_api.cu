@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -607,6 +608,55 @@ pi_status pi_perm_from_counts(const int32_t *counts, int32_t n, int32_t *perm)
     if (!counts || !perm || n < 1) return PI_ERR_ARG;
     for (int i = 0; i < n; ++i) perm[i] = i;
     std::stable_sort(perm, perm + n, [&](int32_t a, int32_t b) { return counts[a] > counts[b]; });
+    return PI_OK;
+}
+
+pi_status pi_hot_prefix_crossover(const int32_t *counts, int32_t n, int32_t T, int32_t B, double pred_bytes,
+                                  double ffn_bytes, int32_t *hot)
+{
+    if (!counts || !hot || n < 1 || T < 1 || B < 1 || !(pred_bytes > 0.0) || !(ffn_bytes > 0.0)) return PI_ERR_ARG;
+    for (int i = 0; i < n; ++i)
+        if (counts[i] < 0 || counts[i] > T) return PI_ERR_ARG;
+    // computing neuron i unconditionally saves its predictor bytes P and costs
+    // F (1 - q_i) more FFN bytes, q_i = 1 - (1 - c_i / T)^B the chance that the
+    // union over B tokens selects it: the prefix runs while (1 - q_i) F < P
+    const double keep = pred_bytes / ffn_bytes;
+    int h = 0;
+    while (h < n && std::pow((double)(T - counts[h]) / (double)T, (double)B) < keep) ++h;
+    *hot = h;
+    return PI_OK;
+}
+
+static void neuron_cost(const pi_layer_desc &d, double &pred, double &ffn)
+{
+    const double w = d.w_dtype == PI_Q4_0 ? 18.0 / 32.0 : 2.0;
+    pred = 2.0 * d.rank + 2.0;                                              // W2 row + b2
+    ffn = (d.act == PI_REGLU ? 2.0 : 1.0) * d.d_model * w + 2.0 + d.d_model * w; // up (+ gate) + bias + down
+}
+
+pi_status pi_choose_hot_prefix(pi_ctx *c, int32_t layer, const int32_t *counts, int32_t T, int32_t B, int32_t *hot)
+{
+    if (!c) return PI_ERR_ARG;
+    pi_status st = check_layer(c, layer);
+    if (st) return st;
+    double pred, ffn;
+    neuron_cost(c->layers[layer].desc, pred, ffn);
+    st = pi_hot_prefix_crossover(counts, c->layers[layer].desc.d_ffn, T, B, pred, ffn, hot);
+    return st ? fail(c, st, "counts/hot NULL, T or B < 1, or a count outside [0, T]") : PI_OK;
+}
+
+pi_status pi_set_hot_prefix(pi_ctx *c, int32_t layer, int32_t hot)
+{
+    if (!c) return PI_ERR_ARG;
+    pi_status st = check_layer(c, layer);
+    if (st) return st;
+    LayerSlot &s = c->layers[layer];
+    if (hot < 0 || hot > s.desc.d_ffn) return fail(c, PI_ERR_ARG, "hot prefix %d outside [0, %d]", hot, s.desc.d_ffn);
+    DeviceGuard g(c->device);
+    // steps in flight read the layer's descriptor
+    CU(cudaStreamSynchronize(c->stream));
+    s.dev.hot = hot;
+    CU(cudaMemcpy(c->d_layers + layer, &s.dev, sizeof(LayerDev), cudaMemcpyHostToDevice));
     return PI_OK;
 }
 

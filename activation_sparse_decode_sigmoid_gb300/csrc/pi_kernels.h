@@ -51,6 +51,8 @@ struct LayerDev {
     int upB;                // bytes of one W_up row in `up`: rowB, or rowB + 16 with the bias tail
     int bias_tail;          // 1: neuron i's bias (16-bit) sits at up row i + rowB, so it arrives
                             //    with the row; 0: read from b[]
+    int hot;                // neurons [0, hot) are always active: their predictor rows are not
+                            // evaluated (0 = every neuron predicted)
     const uint16_t *w1;     // [r][d]
     const uint16_t *b1;     // [r]
     const uint16_t *w2;     // [n][r]   rows in physical order
@@ -195,6 +197,17 @@ cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, 
 // was launched without the attribute), then lets its own successor be
 // scheduled; a successor can only start once every CTA of this grid is
 // resident, so the two never wait on each other's resources.
+// The bits of mask word w (neurons [32 w, 32 w + 32)) that a hot prefix of
+// h neurons sets.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline unsigned hot_bits(int w, int h)
+{
+    const int k = h - 32 * w;
+    return k >= 32 ? ~0u : (k <= 0 ? 0u : (1u << k) - 1u);
+}
+
 #ifdef __CUDACC__
 __device__ __forceinline__ void pdl_enter()
 {

@@ -285,7 +285,9 @@ __device__ __forceinline__ int hpos(int ch, int hf) { return (ch >> 5) * 256 + h
 // of the tile and stay while the batch's h passes through in blocks of 8
 // tokens (two buffers).  With WS = 2 tile slots, a warp issues the copy of
 // its rows of the next unit before it computes this one (small batches,
-// where the rows' transfer, not the arithmetic, is the longer part).
+// where the rows' transfer, not the arithmetic, is the longer part).  Units
+// wholly inside the layer's hot prefix are skipped: the compaction sets the
+// prefix's bits.
 template <typename T, int R, int WS, int TT>
 __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
 {
@@ -310,6 +312,7 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
     if (cta_aborted(p)) return;
     const int ntb = (B + TT - 1) / TT;
     const int nrt = (n + RT - 1) / RT;
+    const int u0 = min(L.hot, n) / RT; // units wholly inside the hot prefix are not evaluated
     const int nwords = (n + 31) >> 5;
     // h block tb into buffer b (zeros past B), in the conflict-free layout
     const auto stage_h = [&](int tb, int b) {
@@ -336,12 +339,12 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
     };
     // the first unit's rows do not depend on the hidden layer: they start
     // while it finishes
-    if (blockIdx.x < nrt) load_rows(blockIdx.x, 0);
+    if (u0 + (int)blockIdx.x < nrt) load_rows(u0 + blockIdx.x, 0);
     pdl_enter();
     if (ntb == 1) stage_h(0, 0); // one block serves every unit
     bool ok = true;
     uint32_t it = 0;
-    for (int u = blockIdx.x; u < nrt; u += gridDim.x, ++it) {
+    for (int u = u0 + blockIdx.x; u < nrt; u += gridDim.x, ++it) {
         const int sl = WS == 2 ? (int)(it & 1) : 0;
         const uint32_t par = WS == 2 ? (it >> 1) & 1 : it & 1;
         if (WS == 2) {
@@ -465,13 +468,14 @@ __global__ void __launch_bounds__(256) pred_compact(const PredParams p)
         return;
     }
     const int w0 = blockIdx.x * 256;
+    const int hot = p.L.hot; // neurons [0, hot) are on whatever their mask bits say
     int before = 0;
-    for (int k = tid; k < w0; k += 256) before += __popc(p.mask[k]);
+    for (int k = tid; k < w0; k += 256) before += __popc(p.mask[k] | hot_bits(k, hot));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
     if (lane == 0) red[warp] = before;
     const int wi = w0 + tid;
-    const uint32_t m = wi < nwords ? p.mask[wi] : 0u;
+    const uint32_t m = wi < nwords ? p.mask[wi] | hot_bits(wi, hot) : 0u;
     const int c = __popc(m);
     int incl = c;
 #pragma unroll
@@ -533,8 +537,8 @@ cudaError_t launch_out(const PredParams &p, int sms, cudaStream_t s)
     auto kern = pred_out<T, R, WS, TT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int nrt = (p.L.n + 8 * R - 1) / (8 * R);
-    return launch_pdl(kern, dim3(std::min(nrt, sms)), dim3(kPT), smem, s, p);
+    const int nrt = (p.L.n + 8 * R - 1) / (8 * R) - std::min(p.L.hot, p.L.n) / (8 * R);
+    return launch_pdl(kern, dim3(std::max(1, std::min(nrt, sms))), dim3(kPT), smem, s, p);
 }
 
 template <typename T>

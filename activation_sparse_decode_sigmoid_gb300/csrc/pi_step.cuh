@@ -125,11 +125,22 @@ static __device__ __forceinline__ int word_row_start(int n, int c, int G)
     return min(n, 32 * slice_lo(nw, c, G));
 }
 
+// Neurons [0, hot) are active without prediction (the hot prefix); counting
+// the predictor's selections for calibration evaluates every row.
+static __device__ __forceinline__ int hot_rows(const LayerDev &L, const StepParams &p)
+{
+    return (p.mode & M_COUNTS) ? 0 : L.hot;
+}
+
+// Phase B evaluates rows [h0, n), h0 = the hot prefix rounded down to a whole
+// mask word; the rows of the boundary word below the prefix are evaluated and
+// then forced on.
 static __device__ __forceinline__ SliceB slice_b(const LayerDev &L, const StepParams &p)
 {
     SliceB b;
-    b.i0 = word_row_start(L.n, blockIdx.x, gridDim.x);
-    b.i1 = word_row_start(L.n, blockIdx.x + 1, gridDim.x);
+    const int h0 = hot_rows(L, p) & ~31;
+    b.i0 = h0 + word_row_start(L.n - h0, blockIdx.x, gridDim.x);
+    b.i1 = h0 + word_row_start(L.n - h0, blockIdx.x + 1, gridDim.x);
     b.rps = max(1, p.slotB / (L.r * 2));
     b.nst = (b.i1 - b.i0 + b.rps - 1) / b.rps;
     return b;
@@ -700,6 +711,7 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
         const int nw = (L.n + 31) >> 5;
         const int wpt = (nw + kConsumerThreads - 1) / kConsumerThreads; // <= 4 for n <= 65536
         const int wb = min(nw, tid * wpt), we = min(nw, wb + wpt);
+        const int hot = hot_rows(L, p), hw = hot >> 5; // words below hw: the hot prefix, never written
         // the mask words, straight from the writers' tagged words (phase B
         // of every SM), polled until all carry this layer's epoch
         unsigned wv[4];
@@ -709,7 +721,8 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
             const auto reload = [&]() {
                 const uint64_t *stale = nullptr;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) raw[q] = (wb + q < we) ? ld_tagged(p.bmx + wb + q) : ((uint64_t)ew << 32);
+                for (int q = 0; q < 4; ++q)
+                    raw[q] = (wb + q < we && wb + q >= hw) ? ld_tagged(p.bmx + wb + q) : ((uint64_t)ew << 32);
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     if (!tag_is(raw[q], ew)) stale = p.bmx + wb + q;
@@ -717,7 +730,7 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
             };
             poll_tags(p, fail_word(S), ew, reload(), reload);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) wv[q] = (uint32_t)raw[q];
+            for (int q = 0; q < 4; ++q) wv[q] = (uint32_t)raw[q] | (wb + q < we ? hot_bits(wb + q, hot) : 0u);
         }
         if (!cons_sync_ok(fail_word(S))) return false;
         int cnt = 0;

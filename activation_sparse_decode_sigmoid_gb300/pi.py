@@ -32,7 +32,7 @@ EXPORTS = ("pi_create", "pi_destroy", "pi_set_stream", "pi_load_layer", "pi_laye
            "pi_dense_step", "pi_set_trace", "pi_sync_status", "pi_last_error", "pi_grid_size",
            "pi_debug_set_wait_limit", "pi_debug_barrier_extra", "pi_debug_set_timeline",
            "pi_debug_set_tuning", "pi_debug_copy_hidden", "pi_debug_set_mma_min_batch",
-           "pi_sparse_ffn_noalloc")
+           "pi_sparse_ffn_noalloc", "pi_set_hot_prefix", "pi_hot_prefix_crossover", "pi_choose_hot_prefix")
 
 
 class PiError(RuntimeError):
@@ -95,6 +95,9 @@ def load_library(path: str = LIB_PATH):
         "pi_debug_copy_hidden": (st, [P, P, I32]),
         "pi_debug_set_mma_min_batch": (st, [P, I32]),
         "pi_sparse_ffn_noalloc": (st, [ctypes.POINTER(pi_ffn_rows), P, I32, P, P, P, P, P]),
+        "pi_set_hot_prefix": (st, [P, I32, I32]),
+        "pi_hot_prefix_crossover": (st, [P, I32, I32, I32, ctypes.c_double, ctypes.c_double, P]),
+        "pi_choose_hot_prefix": (st, [P, I32, P, I32, I32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -158,6 +161,26 @@ def pi_perm_from_counts(counts) -> np.ndarray:
     if rc:
         raise PiError(rc, "pi_perm_from_counts")
     return perm
+
+
+def pi_set_hot_prefix(ctx: int, layer: int, hot: int) -> None:
+    _check(ctx, load_library().pi_set_hot_prefix(ctx, layer, hot), "pi_set_hot_prefix")
+
+
+def pi_hot_prefix_crossover(counts, T: int, B: int, pred_bytes: float, ffn_bytes: float) -> int:
+    c = np.ascontiguousarray(counts, dtype=np.int32)
+    hot = np.zeros(1, np.int32)
+    rc = load_library().pi_hot_prefix_crossover(_ptr(c), c.size, T, B, pred_bytes, ffn_bytes, _ptr(hot))
+    if rc:
+        raise PiError(rc, "pi_hot_prefix_crossover")
+    return int(hot[0])
+
+
+def pi_choose_hot_prefix(ctx: int, layer: int, counts, T: int, B: int) -> int:
+    c = np.ascontiguousarray(counts, dtype=np.int32)
+    hot = np.zeros(1, np.int32)
+    _check(ctx, load_library().pi_choose_hot_prefix(ctx, layer, _ptr(c), T, B, _ptr(hot)), "pi_choose_hot_prefix")
+    return int(hot[0])
 
 
 def pi_predict(ctx: int, layer: int, x_hat, B: int, idx, count) -> None:
@@ -254,6 +277,7 @@ class Context:
         self.max_layers, self.max_batch = max_layers, max_batch
         self.handle = pi_create(device, _stream_ptr(self.torch_device), max_layers, max_batch)
         self.descs: dict[int, pi_layer_desc] = {}
+        self.hot: dict[int, int] = {}  # each layer's always-active prefix
 
     def close(self):
         if self.handle:
@@ -301,6 +325,7 @@ class Context:
         self._s()
         pi_load_layer(self.handle, layer, desc, w, perm)
         self.descs[layer] = desc
+        self.hot[layer] = 0
 
     def layer_counts(self, layer: int, x_hat):
         import torch
@@ -309,6 +334,17 @@ class Context:
         self._s()
         pi_layer_counts(self.handle, layer, x_hat, x_hat.shape[0], counts)
         return counts
+
+    def set_hot_prefix(self, layer: int, hot: int) -> None:
+        self._s()
+        pi_set_hot_prefix(self.handle, layer, hot)
+        self.hot[layer] = hot
+
+    def choose_hot_prefix(self, layer: int, counts, T: int, B: int) -> int:
+        """Crossover prefix length from calibration counts (host or device, physical order)."""
+        if not isinstance(counts, np.ndarray):
+            counts = counts.cpu().numpy()
+        return pi_choose_hot_prefix(self.handle, layer, counts, T, B)
 
     # -- hot path
     def predict(self, layer: int, x_hat, idx=None, count=None):

@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (0 = the config's)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-extras", action="store_true", help="skip dense, e2e and CPU legs")
+    ap.add_argument("--hot-prefix", action="store_true",
+                    help="give every layer its always-active prefix at the byte crossover for the batch")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
     ap.add_argument("--mode", choices=["step", "ffn"], default="step",
                     help="step: the decode step over the stack (the headline); ffn: the sparse FFN of one "
@@ -190,21 +192,23 @@ def profiled_traffic(workload: str):
 
 
 # ------------------------------------------------------------------ workload
-def algorithmic_bytes(cfg, L, B, counts):
-    """Bytes a step must move: predictor weights + biases, the rows of the
-    active neurons (W_up [+ W_gate] + W_down^T + bias), x_hat / x traffic."""
+def algorithmic_bytes(cfg, L, B, counts, hot=None):
+    """Bytes a step must move: predictor weights + biases (the rows of the
+    neurons past each layer's hot prefix), the rows of the active neurons
+    (W_up [+ W_gate] + W_down^T + bias), x_hat / x traffic."""
     from activation_sparse_decode_sigmoid_gb300 import workload as W
     d, n, r = cfg.d, cfg.n, cfg.r
     rows = 3 if cfg.act == W.REGLU else 2
     row = d * 18 / 32 if cfg.w_dtype == W.Q4_0 else d * 2
-    pred = r * d * 2 + n * r * 2 + (r + n) * 2
     total = 0.0
-    for m in counts:
+    for l, m in enumerate(counts):
+        h = hot[l] if hot else 0
+        pred = r * d * 2 + (n - h) * r * 2 + (r + n - h) * 2
         total += pred + m * (rows * row + 2) + B * d * (2 + 4 + 4)
     return total
 
 
-def cpu_oracle_sample(cfg, L, host_layers, seed, budget_s):
+def cpu_oracle_sample(cfg, L, host_layers, seed, budget_s, hot=None):
     """Time the oracle (as it stands, all host cores) on layer-token pairs of
     the workload until the budget is used; returns tokens/s for the stack."""
     import numpy as np
@@ -216,10 +220,11 @@ def cpu_oracle_sample(cfg, L, host_layers, seed, budget_s):
     times, pairs = [], 0
     t_start = time.perf_counter()
     for tok in range(8):
-        for l, (lw, _perm) in host_layers.items():
+        for l, (lw, perm) in host_layers.items():
             x = xs[tok: tok + 1]
+            h = hot.get(l, 0) if hot else 0
             t0 = time.perf_counter()
-            res = O.layer_predict(lw, x, threads)
+            res = O.layer_predict(lw, x, threads, hot=perm[:h] if h else None)
             idx = O.union(res["mask"])
             O.masked_ffn(lw, x, idx, threads)
             times.append(time.perf_counter() - t0)
@@ -298,7 +303,7 @@ def needs_l2_flush(cfg, L) -> bool:
     return stack_weight_bytes(cfg, L) < 2 * L2_BYTES
 
 
-def config_block(cfg, L, B):
+def config_block(cfg, L, B, hot=None):
     from activation_sparse_decode_sigmoid_gb300 import workload as W
     l2 = ("flushed: the stack fits in L2, so a buffer of twice the L2 size is written before every "
           "timed step, outside that step's CUDA events" if needs_l2_flush(cfg, L)
@@ -307,7 +312,10 @@ def config_block(cfg, L, B):
                         f"{ACT_NAMES[cfg.act]}, weights {W.DTYPE_NAMES[cfg.w_dtype]}, "
                         f"Zipf alpha {cfg.alpha}, mean activation {cfg.rho}",
             "batch": B, "seq_len": 1, "parallelism": "replicas (one independent stack per GPU)",
-            "l2": l2, "seed": 0}
+            "l2": l2, "seed": 0,
+            **({"hot_prefix": f"neurons [0, H) always active, H at the byte crossover for {B} tokens: "
+                              f"mean H {sum(hot) / len(hot):.0f} of {cfg.n} (min {min(hot)}, max {max(hot)})"}
+               if hot and any(hot) else {})}
 
 
 def run_ours(args, world, rank, local):
@@ -327,7 +335,9 @@ def run_ours(args, world, rank, local):
     do_extras = not args.no_extras
     do_cpu = do_extras and rank == 0 and world == 1
     from activation_sparse_decode_sigmoid_gb300.calibrate import load_synthetic_stack
-    ctx, host = load_synthetic_stack(cfg, L, args.seed, device, max(B, 1), keep_host=(0, L // 2) if do_cpu else ())
+    ctx, host = load_synthetic_stack(cfg, L, args.seed, device, max(B, 1), keep_host=(0, L // 2) if do_cpu else (),
+                                     hot_batch=B if args.hot_prefix else 0)
+    hot = [ctx.hot.get(l, 0) for l in range(L)]
     d = cfg.d
     xbuf = torch.from_numpy(W.decode_inputs(cfg, (K + Wm) * B, args.seed)).cuda(device).view(K + Wm, B, d)
     cnt = torch.zeros((K + Wm, L), dtype=torch.int32, device=device)
@@ -373,7 +383,7 @@ def run_ours(args, world, rank, local):
         ms = ev[0].elapsed_time(ev[K])
     ms = allreduce_max(world, ms, torch.device("cuda", device))
     counts = cnt[Wm:].cpu().numpy()  # [K][L] active neurons per layer
-    bytes_per_step = [algorithmic_bytes(cfg, L, B, counts[k]) for k in range(K)]
+    bytes_per_step = [algorithmic_bytes(cfg, L, B, counts[k], hot) for k in range(K)]
     mean_launch_s = statistics.mean(per_launch) / 1e3
     achieved = statistics.mean(bytes_per_step) / mean_launch_s / 1e9
     peak, peak_kind = measured_hbm()
@@ -391,7 +401,7 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": W.DTYPE_NAMES[cfg.w_dtype], "data": "synthetic", "config": config_block(cfg, L, B),
+        "dtype": W.DTYPE_NAMES[cfg.w_dtype], "data": "synthetic", "config": config_block(cfg, L, B, hot),
         "effective_hbm_gbs": achieved, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
         "mean_active_neurons_per_layer": float(counts.mean()), "mean_active_fraction": float(counts.mean() / cfg.n),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -443,7 +453,7 @@ def run_ours(args, world, rank, local):
     if clocks:
         line["clocks"] = clocks.stop()
     if do_cpu:
-        line["cpu_baseline"] = cpu_oracle_sample(cfg, L, host, args.seed, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_oracle_sample(cfg, L, host, args.seed, args.cpu_seconds, dict(enumerate(hot)))
     ctx.close()
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -143,6 +143,36 @@ pi_status pi_layer_counts(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t
  * the lower id -- the permutation that makes hot neurons contiguous. */
 pi_status pi_perm_from_counts(const int32_t *counts, int32_t n, int32_t *perm);
 
+/* Hot prefix: the one-device analog of the hot/cold split of the
+ * "CPU/GPU混合推理设计" section (CSDN page "2080 Ti就能跑70B大模型..."): after
+ * the calibrated permutation the hottest neurons are the first physical ones,
+ * and neurons [0, hot) of `layer` are then always active -- their predictor
+ * rows are not evaluated, and every list (pi_predict, the decode steps)
+ * holds them, followed by the predicted neurons >= hot.  hot = 0 (the
+ * default after pi_load_layer) predicts every neuron; hot = n is the dense
+ * FFN.  pi_layer_counts still evaluates every row.  Synchronises the
+ * context's stream before it changes the layer; a CUDA graph captured before
+ * the change keeps the old prefix.  PI_ERR_ARG if hot is outside [0, n]. */
+pi_status pi_set_hot_prefix(pi_ctx *ctx, int32_t layer, int32_t hot);
+
+/* Host helper: the hot-prefix length at which always computing a neuron
+ * costs no more HBM bytes than predicting it.  Predicting neuron i costs
+ * pred_bytes (its W2 row and b2); when the union over B tokens misses it,
+ * which happens with probability (1 - counts[i] / T)^B, that saves its
+ * ffn_bytes (its FFN rows and bias).  *hot = the length of the longest prefix
+ * of counts (host int32 [n], physical order; counts[i] = tokens out of T for
+ * which the predictor selected neuron i) whose every neuron has
+ * (1 - counts[i]/T)^B < pred_bytes / ffn_bytes.  PI_ERR_ARG for NULL
+ * pointers, n, T or B < 1, bytes <= 0, or a count outside [0, T]. */
+pi_status pi_hot_prefix_crossover(const int32_t *counts, int32_t n, int32_t T, int32_t B, double pred_bytes,
+                                  double ffn_bytes, int32_t *hot);
+
+/* pi_hot_prefix_crossover with the bytes of the loaded layer: pred_bytes =
+ * 2 r + 2; ffn_bytes = (2 with ReGLU, else 1) d w + 2 + d w, w = 2 bytes per
+ * 16-bit weight or 18/32 for Q4_0.  counts: host int32 [n], as above. */
+pi_status pi_choose_hot_prefix(pi_ctx *ctx, int32_t layer, const int32_t *counts, int32_t T, int32_t B,
+                               int32_t *hot);
+
 /* Predictor ("充分利用模型和硬件特点": a small per-layer routing module
  * predicts the neurons each input activates).  For B tokens x_hat (dev
  * [B][d], act_dtype):
@@ -155,7 +185,8 @@ pi_status pi_perm_from_counts(const int32_t *counts, int32_t n, int32_t *perm);
  * distances 16, 8, 4, 2, 1; it makes the index list a deterministic function
  * of the input bytes.
  * Output: idx (dev int32, capacity n) = ascending physical ids of the union
- * over the B tokens; *count (dev int32) = its length. */
+ * over the B tokens, together with the layer's hot prefix (pi_set_hot_prefix);
+ * *count (dev int32) = its length. */
 pi_status pi_predict(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t B, int32_t *idx, int32_t *count);
 
 /* Neuron-aware sparse FFN on the listed neurons only.  x_hat dev [B][d];

@@ -13,6 +13,9 @@ GPU; blog.csdn.net QbitAI/IPADS article and de.news.hada.io summary):
   a small MLP decides which neurons fire; here d -> r -> n with ReLU, then
   sigmoid(z) > 0.5, i.e. z > 0, evaluated in the canonical fp32 order CDOT.
 * ``union``        -- the batch's active set: union of the per-token sets.
+* ``predict(..., hot=ids)`` -- the one-device reading of the hot/cold split
+  ("CPU/GPU混合推理设计"): the hot neurons (the first ones of the calibrated
+  order) are active for every token, the rest as predicted.
 * ``ffn_act``      -- ReLU / ReGLU / squared-ReLU activations of every neuron
   (fp64; the three families the pages name, de.news.hada.io summary,
   "Einschränkungen und FAQ").
@@ -74,6 +77,8 @@ def _load():
             lib.or_q4_dequant.argtypes = [P, ctypes.c_long, P]
             lib.or_predict.restype = i32
             lib.or_predict.argtypes = [i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, i32]
+            lib.or_force_active.restype = i32
+            lib.or_force_active.argtypes = [P, i32, i32, P, i32]
             lib.or_union.restype = i32
             lib.or_union.argtypes = [P, i32, i32, P, P]
             lib.or_ffn_act.restype = i32
@@ -143,13 +148,14 @@ def cdot(w, dt: int, v) -> np.float32:
     return np.float32(lib.or_cdot(_p(w), dt, _p(v), w.size))
 
 
-def predict(W1, b1, W2, b2, xhat, dt: int, nthreads: int | None = None):
+def predict(W1, b1, W2, b2, xhat, dt: int, nthreads: int | None = None, hot=None):
     """Per-token predicted masks.
 
     W1 [r,d], b1 [r] or None, W2 [n,r], b2 [n] or None, xhat [B,d] as 16-bit
     bit patterns (uint16) of dtype ``dt``.  Returns dict with ``mask`` (bool
     [B,n]), ``z`` (fp32 canonical logits), ``z64`` (fp64 logits), ``h`` (fp32
-    hidden [B,r])."""
+    hidden [B,r]).  ``hot``: ids of hot neurons, active for every token
+    whatever their logits (``z`` still holds those)."""
     lib = _load()
     W1, W2, xhat = _u16(W1), _u16(W2), _u16(xhat)
     b1, b2 = _u16(b1), _u16(b2)
@@ -165,6 +171,9 @@ def predict(W1, b1, W2, b2, xhat, dt: int, nthreads: int | None = None):
     rc = lib.or_predict(d, n, r, dt, _p(W1), _p(b1), _p(W2), _p(b2), _p(xhat), B,
                         _p(h), _p(z), _p(z64), _p(mask), nthreads or default_threads())
     _check(rc, "predict")
+    if hot is not None:
+        ids = np.ascontiguousarray(hot, dtype=np.int32)
+        _check(lib.or_force_active(_p(mask), B, n, _p(ids) if ids.size else None, int(ids.size)), "force_active")
     return {"mask": mask.astype(bool), "z": z, "z64": z64, "h": h}
 
 
@@ -237,9 +246,9 @@ def masked_ffn(layer: dict, xhat, idx, nthreads: int | None = None):
                     layer["act_dtype"], nthreads)
 
 
-def layer_predict(layer: dict, xhat, nthreads: int | None = None):
+def layer_predict(layer: dict, xhat, nthreads: int | None = None, hot=None):
     return predict(layer["p_w1"], layer.get("p_b1"), layer["p_w2"], layer.get("p_b2"), xhat,
-                   layer["act_dtype"], nthreads)
+                   layer["act_dtype"], nthreads, hot)
 
 
 # ---------------------------------------------------------------- stack / load

@@ -281,6 +281,20 @@ int or_predict(int d, int n, int r, int dt, const uint16_t *W1, const uint16_t *
     return OR_OK;
 }
 
+/* Hot neurons: the one-device reading of the hot/cold split ("CPU/GPU混合推理设计",
+ * CSDN page): the listed neurons (the first ones of the calibrated order) are
+ * active for every token, whatever the predictor says; the others keep their
+ * predicted bit. */
+int or_force_active(uint8_t *mask, int B, int n, const int32_t *ids, int nids)
+{
+    if (!mask || B < 1 || n < 1 || nids < 0 || (nids > 0 && !ids)) return OR_EARG;
+    for (int k = 0; k < nids; ++k)
+        if (ids[k] < 0 || ids[k] >= n) return OR_EARG;
+    for (int t = 0; t < B; ++t)
+        for (int k = 0; k < nids; ++k) mask[(long)t * n + ids[k]] = 1;
+    return OR_OK;
+}
+
 /* Union over B tokens of the per-token masks, as an ascending index list. */
 int or_union(const uint8_t *mask, int B, int n, int32_t *idx, int32_t *count)
 {

@@ -46,8 +46,9 @@ def ctx(max_layers=1, max_batch=8) -> pi.Context:
     return pi.Context(0, max_layers=max_layers, max_batch=max_batch)
 
 
-def predict_checked(c: pi.Context, slot: int, layer_host: dict, xhat: np.ndarray, perm=None):
-    """GPU predictor vs oracle: ascending physical list, bit-exact set."""
+def predict_checked(c: pi.Context, slot: int, layer_host: dict, xhat: np.ndarray, perm=None, hot=None):
+    """GPU predictor vs oracle: ascending physical list, bit-exact set.
+    ``hot``: original ids of the neurons the loaded layer keeps always active."""
     t = torch()
     n = layer_host["n"]
     idx, cnt = c.predict(slot, dev16(xhat))
@@ -56,7 +57,7 @@ def predict_checked(c: pi.Context, slot: int, layer_host: dict, xhat: np.ndarray
     gidx = idx[:m].cpu().numpy()
     assert np.all(np.diff(gidx) > 0), "index list not strictly ascending"
     assert gidx.size == 0 or (gidx.min() >= 0 and gidx.max() < n)
-    ref = O.layer_predict(layer_host, xhat)
+    ref = O.layer_predict(layer_host, xhat, hot=hot)
     oidx = O.union(ref["mask"])
     orig = gidx if perm is None else np.asarray(perm)[gidx]
     assert np.array_equal(np.sort(orig), oidx), (

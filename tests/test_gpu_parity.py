@@ -317,6 +317,83 @@ def test_batched_predictor_matches_oracle_and_step_kernel(c64, name, B):
     assert np.array_equal(idx[:m].cpu().numpy(), idx2[:m].cpu().numpy())
 
 
+@pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4", "ring_wrap"])
+@pytest.mark.parametrize("B", [1, 3, 8, 64])
+@pytest.mark.parametrize("path", ["default", "step kernel"], indirect=True)
+def test_hot_prefix_lists_and_ffn_match_oracle(c64, name, B, path):
+    """Neurons [0, hot) of the physical order are always active and their
+    predictor rows are skipped: the list equals the oracle's with those
+    neurons forced on, for a prefix inside a mask word, on a word boundary,
+    past whole output tiles of the batched predictor, and all but one or
+    every neuron; the FFN on that list matches."""
+    cfg, layer = _layer(name)
+    if name == "ring_wrap" and B == 64:
+        pytest.skip("the oracle's predictor at r = 2048 and 64 tokens is slow; B <= 8 covers the narrow tile")
+    perm = np.random.default_rng(5).permutation(cfg.n).astype(np.int32)
+    c64.load_layer(0, layer, perm)
+    x = W.xhat_inputs(cfg, B, 41 + B)
+    try:
+        for hot in (0, 1, 31, 32, 33, 200, cfg.n - 1, cfg.n):
+            c64.set_hot_prefix(0, hot)
+            idx, cnt, oidx = G.predict_checked(c64, 0, layer, x, perm, hot=perm[:hot])
+            assert np.array_equal(idx[:hot].cpu().numpy(), np.arange(hot))
+            if hot == 200:
+                G.ffn_checked(c64, 0, layer, x, idx, cnt, oidx)
+    finally:
+        c64.set_hot_prefix(0, 0)
+    with pytest.raises(pi.PiError):
+        c64.set_hot_prefix(0, cfg.n + 1)
+
+
+@pytest.mark.parametrize("layerwise", [True, False])
+def test_decode_stack_with_crossover_hot_prefix(layerwise):
+    """A three-layer stack whose hot prefixes come from the calibration
+    counts at the crossover for the batch (pi_choose_hot_prefix): every layer's
+    list equals the oracle's with the calibrated order's first neurons forced
+    on, and the update matches."""
+    t = G.torch()
+    cfg = CFGS["relu_f16"]
+    B, L, T = 8, 3, 64
+    c = G.ctx(max_layers=L, max_batch=B)
+    if not layerwise:
+        pi.pi_debug_set_mma_min_batch(c.handle, 0)
+    layers, perms, hots = [], [], []
+    for l in range(L):
+        lw = W.make_layer(cfg, l, 0, random_b1=True, random_bdown=True)
+        c.load_layer(l, lw)
+        cal = W.calibration_inputs(cfg, l, 0, T=T)
+        perm = pi.pi_perm_from_counts(c.layer_counts(l, G.dev16(cal)).cpu().numpy())
+        c.load_layer(l, lw, perm)
+        counts = c.layer_counts(l, G.dev16(cal)).cpu().numpy()  # physical order, descending
+        hot = c.choose_hot_prefix(l, counts, T, B)
+        assert 0 < hot < cfg.n
+        c.set_hot_prefix(l, hot)
+        layers.append(lw)
+        perms.append(perm)
+        hots.append(hot)
+    assert len(set(hots)) > 1 or hots[0] > 32
+    x0 = W.decode_inputs(cfg, B, 6)
+    x = t.from_numpy(x0.copy()).cuda()
+    tx = t.zeros((L, B, cfg.d), dtype=t.float32, device="cuda")
+    txh = t.zeros((L, B, cfg.d), dtype=t.int16, device="cuda")
+    tidx = t.full((L, cfg.n), -1, dtype=t.int32, device="cuda")
+    tcnt = t.zeros(L, dtype=t.int32, device="cuda")
+    c.set_trace(tx, txh, tidx, tcnt)
+    c.decode_step(x)
+    c.check()
+    xs = np.concatenate([tx.cpu().numpy(), x.cpu().numpy()[None]], 0).astype(np.float64)
+    xh = G.host16(txh)
+    for l in range(L):
+        m = int(tcnt[l].item())
+        gidx = tidx[l, :m].cpu().numpy()
+        assert np.array_equal(gidx[:hots[l]], np.arange(hots[l]))
+        oidx = O.union(O.layer_predict(layers[l], xh[l], hot=perms[l][:hots[l]])["mask"])
+        assert np.array_equal(np.sort(perms[l][gidx]), oidx)
+        err = max_rel_err(xs[l + 1] - xs[l], O.masked_ffn(layers[l], xh[l], oidx))
+        assert err <= G.tol(layers[l]), f"layer {l}: {err:.3g}"
+    c.close()
+
+
 def test_large_batch_decode_x_hat_and_list_match_fused_kernel():
     """A batch of 8 decodes layer by layer (RMSNorm launch, batched
     predictor, tensor-core FFN); with the tensor cores off the same batch

@@ -225,6 +225,28 @@ def test_union_matches_flatnonzero():
     assert O.union(np.zeros((3, 10), bool)).size == 0
 
 
+@pytest.mark.parametrize("cfg", [SMALL, SMALL_REGLU])
+def test_hot_neurons_are_active_for_every_token_and_the_rest_as_predicted(cfg):
+    """Hot neurons (the hot/cold split mapped to one device): the forced ids
+    are on for every token, every other bit is the plain prediction, and the
+    logits are untouched; every neuron hot is the dense FFN's list."""
+    layer = W.make_layer(cfg, 0, 0, random_b1=True)
+    x = W.xhat_inputs(cfg, 5, 3)
+    plain = O.layer_predict(layer, x)
+    rng = np.random.default_rng(8)
+    for hot in (np.arange(0), np.arange(1), np.arange(33), rng.permutation(cfg.n)[:50], np.arange(cfg.n)):
+        res = O.layer_predict(layer, x, hot=hot)
+        assert res["mask"][:, hot].all()
+        rest = np.setdiff1d(np.arange(cfg.n), hot)
+        assert np.array_equal(res["mask"][:, rest], plain["mask"][:, rest])
+        assert np.array_equal(res["z"], plain["z"])
+        # the batch's list is the hot ids together with the union of the predictions (brute force)
+        assert np.array_equal(O.union(res["mask"]), np.union1d(hot, np.flatnonzero(plain["mask"].any(0))))
+    assert np.array_equal(O.union(O.layer_predict(layer, x, hot=np.arange(cfg.n))["mask"]), np.arange(cfg.n))
+    with pytest.raises(ValueError):
+        O.layer_predict(layer, x, hot=np.array([cfg.n], np.int32))
+
+
 # ------------------------------------------------------------------ FFN
 @pytest.mark.parametrize("cfg", [SMALL, SMALL_REGLU, SMALL_Q4, SMALL_SQ])
 def test_dense_ffn_matches_numpy(cfg):
