@@ -80,7 +80,7 @@ struct pi_ctx {
     // Batches of at least this many tokens run layer by layer: batched predictor launches and the
     // tensor-core FFN (0: never).  Measured on GB300: from 2 tokens on LLaMA-70B-shaped (ReGLU)
     // layers, from 3 on OPT-30B-shaped ones (equal at 2), the step kernel's per-group passes lose.
-    int mma_min_b = 2;
+    int mma_min_b = -1; // smallest batch run layer by layer; -1: by layer kind (layerwise_min_b)
     int *ctl = nullptr; // [0..1] grid-barrier counter (u64), [2] status, [3] abort
     // trace
     float *tr_x = nullptr;
@@ -188,7 +188,9 @@ pi_status plan(pi_ctx *c, StepParams &p, int l0, int L, int B, int mode, int *tg
     }
     const bool pred = (mode & (pi::M_PREDICT | pi::M_COUNTS)) != 0;
     const bool ffn = (mode & pi::M_FFN) != 0;
-    const int tgf = B == 1 ? 1 : 4;
+    // token-group width of the FFN phase: 1, 2 or 4 tokens (the y accumulators
+    // of a wider group do not fit the registers of 576 threads and spill)
+    const int tgf = B == 1 ? 1 : (B == 2 ? 2 : 4);
     p.d = d;
     p.B = B;
     p.tg = std::min(B, tgf);
@@ -682,9 +684,20 @@ pi_status pi_layer_counts(pi_ctx *c, int32_t layer, const void *x_hat, int32_t T
 // Batches of at least mma_min_b tokens take the tensor-core gather-GEMM
 // (pi_mma.cu; Q4_0 rows dequantised to f16 first); smaller ones the step kernel.
 // A layer without tensor maps (none could be made) stays on the step kernel.
+// The smallest batch that runs layer by layer.  Unless set, 2 tokens for
+// gated (ReGLU) layers and 3 for the others: at 2 tokens the persistent
+// kernel's two-token groups stream the rows of a ReLU layer faster than the
+// short launches, and those of a ReGLU layer (three rows a neuron) slower.
+static int layerwise_min_b(const pi_ctx *c, int layer)
+{
+    if (c->mma_min_b >= 0) return c->mma_min_b;
+    return c->layers[layer].desc.act == PI_REGLU ? 2 : 3;
+}
+
 static bool use_mma(const pi_ctx *c, int layer, int B)
 {
-    return c->mma_min_b > 0 && B >= c->mma_min_b && c->layers[layer].maps;
+    const int mb = layerwise_min_b(c, layer);
+    return mb > 0 && B >= mb && c->layers[layer].maps;
 }
 
 // The FFN of one layer on the tensor cores: into y (16-bit), or added into
@@ -735,7 +748,11 @@ static pi_status mma_ffn(pi_ctx *c, int layer, const uint16_t *xhat, int B, cons
 
 // Batches of at least mma_min_b tokens run the predictor as short launches
 // of register-tiled dot products (pi_pred.cu) instead of the step kernel.
-static bool use_pred_batch(const pi_ctx *c, int B) { return c->mma_min_b > 0 && B >= c->mma_min_b; }
+static bool use_pred_batch(const pi_ctx *c, int layer, int B)
+{
+    const int mb = layerwise_min_b(c, layer);
+    return mb > 0 && B >= mb;
+}
 
 static pi::PredParams pred_params(pi_ctx *c, int layer, int B)
 {
@@ -767,7 +784,7 @@ pi_status pi_predict(pi_ctx *c, int32_t layer, const void *x_hat, int32_t B, int
     if (st) return st;
     if (!x_hat || !idx || !count) return fail(c, PI_ERR_ARG, "x_hat/idx/count NULL");
     DeviceGuard g(c->device);
-    if (use_pred_batch(c, B)) {
+    if (use_pred_batch(c, layer, B)) {
         if (reinterpret_cast<uintptr_t>(x_hat) & 15u) return fail(c, PI_ERR_ARG, "x_hat must be 16-byte aligned");
         pi::PredParams q = pred_params(c, layer, B);
         q.xhat = (uint16_t *)x_hat;
@@ -838,7 +855,7 @@ static pi_status step_common(pi_ctx *c, float *x, int32_t B, int mode)
     const bool dense = (mode & pi::M_DENSE) != 0;
     const bool bf16 = c->layers[0].desc.act_dtype == PI_BF16;
     if (!use_mma(c, 0, B)) {
-        if (dense || !use_pred_batch(c, B)) return launch(c, 0, L, B, mode, p);
+        if (dense || !use_pred_batch(c, 0, B)) return launch(c, 0, L, B, mode, p);
         // Q4_0 batches, per layer: x_hat = RMSNorm(x), the batched predictor,
         // then the step kernel's FFN on that list adds the layer into x
         for (int l = 0; l < L; ++l) {
@@ -1010,8 +1027,19 @@ pi_status pi_debug_copy_hidden(pi_ctx *c, float *dst, int32_t count)
 
 pi_status pi_debug_set_mma_min_batch(pi_ctx *c, int32_t min_batch)
 {
-    if (!c || min_batch < 0) return PI_ERR_ARG;
+    if (!c || min_batch < -1) return PI_ERR_ARG;
     c->mma_min_b = min_batch;
+    return PI_OK;
+}
+
+pi_status pi_layerwise_min_batch(pi_ctx *c, int32_t layer, int32_t *min_batch)
+{
+    if (!c) return PI_ERR_ARG;
+    pi_status st = check_layer(c, layer);
+    if (st) return st;
+    if (!min_batch) return fail(c, PI_ERR_ARG, "min_batch NULL");
+    const int mb = layerwise_min_b(c, layer);
+    *min_batch = mb > 0 && c->layers[layer].maps ? mb : 0;
     return PI_OK;
 }
 

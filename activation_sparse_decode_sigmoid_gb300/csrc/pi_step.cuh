@@ -425,6 +425,63 @@ static __device__ __forceinline__ void cdot_rows(const uint8_t *w, size_t rstrid
     }
 }
 
+// acc0[r] = CDOT(w_r, v0), acc1[r] = CDOT(w_r, v1) for NR 16-bit rows and two
+// fp32 vectors in shared memory: each row chunk is loaded and widened once
+// for both tokens; each chain keeps the canonical per-lane order.
+template <typename T, int NR>
+static __device__ __forceinline__ void cdot_rows_2t(const uint8_t *w, size_t rstride, const float *v0, const float *v1,
+                                                    int K, int lane, float (&acc0)[NR], float (&acc1)[NR])
+{
+    using F = F16T<T>;
+#pragma unroll
+    for (int r = 0; r < NR; ++r) acc0[r] = acc1[r] = 0.f;
+    const int nch = K >> 3;
+    for (int ch = lane; ch < nch; ch += 32) {
+        const float4 a0 = *reinterpret_cast<const float4 *>(v0 + (size_t)ch * 8);
+        const float4 b0 = *reinterpret_cast<const float4 *>(v0 + (size_t)ch * 8 + 4);
+        const float4 a1 = *reinterpret_cast<const float4 *>(v1 + (size_t)ch * 8);
+        const float4 b1 = *reinterpret_cast<const float4 *>(v1 + (size_t)ch * 8 + 4);
+        const float x0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
+        const float x1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const uint4 wv = *reinterpret_cast<const uint4 *>(w + r * rstride + (size_t)ch * 16);
+            const float2 p[4] = {F::pair(wv.x), F::pair(wv.y), F::pair(wv.z), F::pair(wv.w)};
+            float s0 = acc0[r], s1 = acc1[r];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                s0 = __fmaf_rn(p[e].x, x0[2 * e], s0);
+                s1 = __fmaf_rn(p[e].x, x1[2 * e], s1);
+                s0 = __fmaf_rn(p[e].y, x0[2 * e + 1], s0);
+                s1 = __fmaf_rn(p[e].y, x1[2 * e + 1], s1);
+            }
+            acc0[r] = s0, acc1[r] = s1;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) acc0[r] = butterfly_sum(acc0[r]), acc1[r] = butterfly_sum(acc1[r]);
+}
+
+// Rows [0, nrows) of a static stage against two fp32 vectors, 4 rows at a
+// time, then one by one; emit(row, acc0, acc1) gets both CDOTs of each row.
+template <typename T, typename Emit>
+static __device__ __forceinline__ void stage_rows_2t(const uint8_t *base, size_t rstride, int nrows, const float *v0,
+                                                     const float *v1, int K, int lane, Emit emit)
+{
+    int r = 0;
+    for (; r + 4 <= nrows; r += 4) {
+        float a0[4], a1[4];
+        cdot_rows_2t<T, 4>(base + (size_t)r * rstride, rstride, v0, v1, K, lane, a0, a1);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) emit(r + u, a0[u], a1[u]);
+    }
+    for (; r < nrows; ++r) {
+        float a0[1], a1[1];
+        cdot_rows_2t<T, 1>(base + (size_t)r * rstride, rstride, v0, v1, K, lane, a0, a1);
+        emit(r, a0[0], a1[0]);
+    }
+}
+
 // Rows [0, nrows) of a static stage (row stride rstride), 4 independent rows
 // at a time, then the remainder one by one; emit(row, acc) gets each CDOT.
 template <typename T, bool VF, typename Emit>
@@ -661,15 +718,19 @@ static __device__ bool phase_b(const StepParams &p, const Shm &S, const LayerDev
             for (int r0 = 0; r0 < nr; r0 += 32) {
                 const int nrr = min(32, nr - r0);
                 unsigned bits = 0; // bit r: row ir0 + r0 + r selected for some token of the group
-                for (int t = 0; t < nt; ++t) {
-                    stage_rows<T, true>(base + (size_t)r0 * L.r * 2, (size_t)L.r * 2, nrr, hs + (size_t)t * L.r, L.r,
-                                        lane, [&](int r, float acc) {
-                                            if (__fadd_rn(acc, F::one(b2s[ir0 + r0 + r - Bs.i0])) > 0.f) {
-                                                bits |= 1u << r;
-                                                if (lane == 0 && (p.mode & M_COUNTS))
-                                                    atomicAdd(p.counts_out + ir0 + r0 + r, 1);
-                                            }
-                                        });
+                const auto pick = [&](int r, float acc) {
+                    if (__fadd_rn(acc, F::one(b2s[ir0 + r0 + r - Bs.i0])) > 0.f) {
+                        bits |= 1u << r;
+                        if (lane == 0 && (p.mode & M_COUNTS)) atomicAdd(p.counts_out + ir0 + r0 + r, 1);
+                    }
+                };
+                if (nt == 2) { // two tokens share every row chunk's load and widening
+                    stage_rows_2t<T>(base + (size_t)r0 * L.r * 2, (size_t)L.r * 2, nrr, hs, hs + L.r, L.r, lane,
+                                     [&](int r, float a0, float a1) { pick(r, a0), pick(r, a1); });
+                } else {
+                    for (int t = 0; t < nt; ++t)
+                        stage_rows<T, true>(base + (size_t)r0 * L.r * 2, (size_t)L.r * 2, nrr, hs + (size_t)t * L.r,
+                                            L.r, lane, pick);
                 }
                 if (lane == 0 && (p.mode & M_PREDICT) && bits) {
                     const int rel = ir0 + r0 - Bs.i0; // rows relative to the word-aligned i0

@@ -27,13 +27,15 @@ template <int TGF> static cudaError_t launch_tgf(const StepParams &p, int grid, 
 
 cudaError_t launch_step_bf16(const StepParams &p, int tgf, int grid, cudaStream_t s)
 {
-    return tgf == 1 ? launch_tgf<1>(p, grid, s) : launch_tgf<4>(p, grid, s);
+    return tgf == 1 ? launch_tgf<1>(p, grid, s) : tgf == 2 ? launch_tgf<2>(p, grid, s) : launch_tgf<4>(p, grid, s);
 }
 
 cudaError_t occupancy_step_bf16(int tgf, int smem_bytes, int *blocks)
 {
     if (tgf == 1)
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<__nv_bfloat16, false, 1>, kThreads, smem_bytes);
+    if (tgf == 2)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<__nv_bfloat16, false, 2>, kThreads, smem_bytes);
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<__nv_bfloat16, false, 4>, kThreads, smem_bytes);
 }
 

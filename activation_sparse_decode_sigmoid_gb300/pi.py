@@ -32,7 +32,8 @@ EXPORTS = ("pi_create", "pi_destroy", "pi_set_stream", "pi_load_layer", "pi_laye
            "pi_dense_step", "pi_set_trace", "pi_sync_status", "pi_last_error", "pi_grid_size",
            "pi_debug_set_wait_limit", "pi_debug_barrier_extra", "pi_debug_set_timeline",
            "pi_debug_set_tuning", "pi_debug_copy_hidden", "pi_debug_set_mma_min_batch",
-           "pi_sparse_ffn_noalloc", "pi_set_hot_prefix", "pi_hot_prefix_crossover", "pi_choose_hot_prefix")
+           "pi_sparse_ffn_noalloc", "pi_set_hot_prefix", "pi_hot_prefix_crossover", "pi_choose_hot_prefix",
+           "pi_layerwise_min_batch")
 
 
 class PiError(RuntimeError):
@@ -96,6 +97,7 @@ def load_library(path: str = LIB_PATH):
         "pi_debug_set_mma_min_batch": (st, [P, I32]),
         "pi_sparse_ffn_noalloc": (st, [ctypes.POINTER(pi_ffn_rows), P, I32, P, P, P, P, P]),
         "pi_set_hot_prefix": (st, [P, I32, I32]),
+        "pi_layerwise_min_batch": (st, [P, I32, P]),
         "pi_hot_prefix_crossover": (st, [P, I32, I32, I32, ctypes.c_double, ctypes.c_double, P]),
         "pi_choose_hot_prefix": (st, [P, I32, P, I32, I32, P]),
     }
@@ -260,6 +262,12 @@ def pi_debug_copy_hidden(ctx: int, dst, count: int) -> None:
 
 def pi_debug_set_mma_min_batch(ctx: int, min_batch: int) -> None:
     _check(ctx, load_library().pi_debug_set_mma_min_batch(ctx, min_batch), "pi_debug_set_mma_min_batch")
+
+
+def pi_layerwise_min_batch(ctx: int, layer: int) -> int:
+    mb = np.zeros(1, np.int32)
+    _check(ctx, load_library().pi_layerwise_min_batch(ctx, layer, _ptr(mb)), "pi_layerwise_min_batch")
+    return int(mb[0])
 
 
 def pi_debug_barrier_extra(ctx: int, extra: int) -> None:

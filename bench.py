@@ -151,11 +151,6 @@ class ClockSampler:
 
 ACT_NAMES = ("ReLU", "ReGLU", "squared ReLU")  # by the workload's activation ids 0, 1, 2
 
-# The library's default: batches of this many tokens or more run layer by
-# layer (batched predictor launches, tensor-core FFN) instead of in the
-# persistent step kernel.
-LAYERWISE_MIN_BATCH = 2
-
 # The sources the persistent step kernel is built from, with the host plan
 # that sizes its rings (pi_api.cu): a profile's DRAM counters stand for the
 # kernel only while these files are unchanged.
@@ -388,15 +383,18 @@ def run_ours(args, world, rank, local):
     achieved = statistics.mean(bytes_per_step) / mean_launch_s / 1e9
     peak, peak_kind = measured_hbm()
     value = world * K * B / (ms / 1e3)
-    # batches of LAYERWISE_MIN_BATCH+ tokens with 16-bit weights run layer by layer: per layer
-    # RMSNorm, the predictor's hidden layer, output layer and compaction, the FFN's up and down
-    # kernels and the share merge; everything else is one persistent launch per step
-    layerwise = B >= LAYERWISE_MIN_BATCH
+    # batches from the library's layer-by-layer threshold on run per layer: RMSNorm, the
+    # predictor's hidden layer, output layer and compaction, (Q4_0: the listed rows to f16,)
+    # the FFN's up and down kernels and the share merge; smaller ones are one persistent
+    # launch per step
+    mb = pi.pi_layerwise_min_batch(ctx.handle, 0)
+    layerwise = 0 < mb <= B
     q4 = cfg.w_dtype == W.Q4_0
-    kernel = ("per-layer launches: RMSNorm, batched predictor (3), tensor-core FFN (3)" if layerwise and not q4
-              else "per-layer launches: RMSNorm, batched predictor (3), step kernel FFN" if layerwise
+    kernel = ("per-layer launches: RMSNorm, batched predictor (3), Q4_0 rows to f16, tensor-core FFN (3)"
+              if layerwise and q4 else
+              "per-layer launches: RMSNorm, batched predictor (3), tensor-core FFN (3)" if layerwise
               else "step_kernel (one persistent launch per step)")
-    launches_per_step = (5 if q4 else 7) * L if layerwise else 1
+    launches_per_step = (8 if q4 else 7) * L if layerwise else 1
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
@@ -461,8 +459,9 @@ def run_ours(args, world, rank, local):
 
 def run_ffn(args, world, rank, local):
     """pi_sparse_ffn on one calibrated full-size layer with the tokens' predicted
-    union list: batches of 8+ run the tensor-core kernels, smaller ones the
-    step kernel's FFN phase.  Bytes = the rows of the listed neurons."""
+    union list: batches from the layer-by-layer threshold on run the
+    tensor-core kernels, smaller ones the step kernel's FFN phase.  Bytes =
+    the rows of the listed neurons."""
     import numpy as np
     import torch
     from activation_sparse_decode_sigmoid_gb300 import build as libbuild
@@ -497,6 +496,8 @@ def run_ffn(args, world, rank, local):
     ctx.check()
     ms = allreduce_max(world, e0.elapsed_time(e1) / K, dev)
     m = int(cnt.item())
+    mb = pi.pi_layerwise_min_batch(ctx.handle, 0)
+    tc = 0 < mb <= B  # the tensor-core FFN: (Q4_0: rows to f16,) up, down, merge
     rows = 3 if cfg.act == W.REGLU else 2
     row = cfg.d * 18 / 32 if cfg.w_dtype == W.Q4_0 else cfg.d * 2
     byts = m * (rows * row + 2) + B * cfg.d * 4
@@ -510,11 +511,10 @@ def run_ffn(args, world, rank, local):
             "scaling": "weak", "vs_baseline": None, "dtype": W.DTYPE_NAMES[cfg.w_dtype], "data": "synthetic",
             "config": {"workload": f"{cfg.name}: one layer, d_model {cfg.d}, d_ffn {cfg.n}, batch {B}, "
                                    f"{m} listed neurons ({m / cfg.n:.3f} of d_ffn)",
-                       "path": "tensor cores (tcgen05)" if B >= LAYERWISE_MIN_BATCH and cfg.w_dtype != W.Q4_0
-                       else "step kernel"},
+                       "path": "tensor cores (tcgen05)" if tc else "step kernel"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "peak_source": f"{kind} copy bandwidth (hbm_gbs)", "traffic": None},
-            "gpu_launches": K * (3 if B >= LAYERWISE_MIN_BATCH and cfg.w_dtype != W.Q4_0 else 1)}), flush=True)
+            "gpu_launches": K * ((4 if cfg.w_dtype == W.Q4_0 else 3) if tc else 1)}), flush=True)
 
 
 def main():

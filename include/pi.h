@@ -328,12 +328,20 @@ pi_status pi_debug_set_tuning(pi_ctx *ctx, int32_t prefetch, int32_t prefetch_ns
  * most max_batch * 2048. */
 pi_status pi_debug_copy_hidden(pi_ctx *ctx, float *dst, int32_t count);
 
-/* Smallest batch (tokens) that runs layer by layer (default 2): the
- * predictor as batched launches and the FFN on the tensor cores (tcgen05
- * gather-GEMM; Q4_0 rows dequantised to f16 into a context scratch first).
- * 0 keeps every batch on the persistent step kernel (CUDA cores).  For
- * comparing the two paths. */
+/* Smallest batch (tokens) that runs layer by layer: the predictor as
+ * batched launches and the FFN on the tensor cores (tcgen05 gather-GEMM;
+ * Q4_0 rows dequantised to f16 into a context scratch first).  Smaller
+ * batches run in the persistent step kernel (CUDA cores).  -1 (the default)
+ * chooses by layer kind: 2 tokens for ReGLU layers, 3 for the others.  0
+ * keeps every batch on the step kernel.  For comparing the two paths.
+ * PI_ERR_ARG below -1. */
 pi_status pi_debug_set_mma_min_batch(pi_ctx *ctx, int32_t min_batch);
+
+/* *min_batch = the smallest batch for which `layer`'s FFN runs layer by
+ * layer, as set by pi_debug_set_mma_min_batch (0: never, e.g. when the
+ * layer's rows could not be mapped for the tensor cores).  A decode step
+ * takes the path of layer 0 for the whole stack. */
+pi_status pi_layerwise_min_batch(pi_ctx *ctx, int32_t layer, int32_t *min_batch);
 
 #ifdef __cplusplus
 }

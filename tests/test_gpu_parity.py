@@ -14,8 +14,9 @@ from tests._helpers import max_rel_err, worked_example_layer
 
 pytestmark = pytest.mark.gpu
 
-# the library's default: batches of this many tokens or more run layer by layer
-LAYERWISE_MIN_BATCH = 2
+# pi_debug_set_mma_min_batch: the library's own choice of the smallest batch
+# that runs layer by layer (2 tokens for ReGLU layers, 3 for the others)
+AUTO = -1
 
 # small layers spanning several tiles with ragged tails (n not a multiple of
 # 32, d not a multiple of 256), every activation / weight kind
@@ -59,8 +60,8 @@ def test_predict_and_sparse_ffn(c64, name, B):
 @pytest.mark.parametrize("B", [1, 2, 7, 9, 64])
 @pytest.mark.parametrize("path", ["default", "step kernel"], indirect=True)
 def test_batch_sizes(c64, name, B, path):
-    """Every batch size on the default path (layer by layer from 2 tokens)
-    and on the persistent step kernel (its multi-token groups)."""
+    """Every batch size on the default path (layer by layer from 2 or 3
+    tokens) and on the persistent step kernel (its token groups of 1, 2 and 4)."""
     cfg, layer = _layer(name)
     c64.load_layer(0, layer)
     x = W.xhat_inputs(cfg, B, 11)
@@ -74,7 +75,7 @@ def path(c64, request):
     if request.param == "step kernel":
         pi.pi_debug_set_mma_min_batch(c64.handle, 0)
     yield request.param
-    pi.pi_debug_set_mma_min_batch(c64.handle, LAYERWISE_MIN_BATCH)
+    pi.pi_debug_set_mma_min_batch(c64.handle, AUTO)
 
 
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4", "sqrelu_bf16"])
@@ -278,7 +279,7 @@ def test_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
     pi.pi_debug_set_mma_min_batch(c64.handle, 0)
     y_cc = c64.sparse_ffn(0, xd, idx, cnt)
     c64.check()
-    pi.pi_debug_set_mma_min_batch(c64.handle, LAYERWISE_MIN_BATCH)
+    pi.pi_debug_set_mma_min_batch(c64.handle, AUTO)
     m = int(cnt.item())
     oidx = np.sort(idx[:m].cpu().numpy())
     got = G.y_to_f64(y_tc, cfg.act_dtype)
@@ -297,21 +298,23 @@ def test_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "ring_wrap", "opt_1layer"])
 @pytest.mark.parametrize("B", [2, 5, 8, 9, 16, 17, 40, 64])
 def test_batched_predictor_matches_oracle_and_step_kernel(c64, name, B):
-    """From 2 tokens the predictor runs as register-tiled launches (8-token
-    blocks, a halving butterfly over R x 8 dot products per warp); its lists
-    equal the oracle's and, entry for entry, the step kernel's on the same
-    x_hat (one, two and several token blocks; r = 2048 takes the narrow
-    output tile that shares mask words between CTAs)."""
+    """Layer by layer (forced from 2 tokens here) the predictor runs as
+    register-tiled launches (8-token blocks, a halving butterfly over R x 8
+    dot products per warp); its lists equal the oracle's and, entry for
+    entry, the step kernel's on the same x_hat (one, two and several token
+    blocks; r = 2048 takes the narrow output tile that shares mask words
+    between CTAs)."""
     cfg, layer = _layer(name)
     c64.load_layer(0, layer)
     x = W.xhat_inputs(cfg, B, 31 + B)
-    idx, cnt, _ = G.predict_checked(c64, 0, layer, x)
-    pi.pi_debug_set_mma_min_batch(c64.handle, 0)
     try:
+        pi.pi_debug_set_mma_min_batch(c64.handle, 2)
+        idx, cnt, _ = G.predict_checked(c64, 0, layer, x)
+        pi.pi_debug_set_mma_min_batch(c64.handle, 0)
         idx2, cnt2 = c64.predict(0, G.dev16(x))
         c64.check()
     finally:
-        pi.pi_debug_set_mma_min_batch(c64.handle, LAYERWISE_MIN_BATCH)
+        pi.pi_debug_set_mma_min_batch(c64.handle, AUTO)
     m = int(cnt.item())
     assert m == int(cnt2.item())
     assert np.array_equal(idx[:m].cpu().numpy(), idx2[:m].cpu().numpy())
@@ -408,7 +411,7 @@ def test_large_batch_decode_x_hat_and_list_match_fused_kernel():
         c.load_layer(l, W.make_layer(cfg, l, 0, random_b1=True, random_bdown=True))
     x0 = W.decode_inputs(cfg, B, 8)
     out = []
-    for mma in (LAYERWISE_MIN_BATCH, 0):
+    for mma in (2, 0):
         pi.pi_debug_set_mma_min_batch(c.handle, mma)
         x = t.from_numpy(x0.copy()).cuda()
         tx = t.zeros((L, B, cfg.d), dtype=t.float32, device="cuda")
@@ -424,6 +427,24 @@ def test_large_batch_decode_x_hat_and_list_match_fused_kernel():
     assert np.array_equal(out[0][2], out[1][2]) and np.array_equal(out[0][2], x0)
     assert np.array_equal(out[0][0], out[1][0])
     assert np.array_equal(out[0][1], out[1][1])
+    c.close()
+
+
+def test_layerwise_threshold_follows_the_layer_kind():
+    """By default a ReGLU layer runs layer by layer from 2 tokens, the other
+    kinds from 3; a set threshold overrides both until -1 restores them."""
+    c = G.ctx(max_layers=2, max_batch=8)
+    c.load_layer(0, _layer("relu_f16")[1])
+    c.load_layer(1, _layer("reglu_bf16")[1])
+    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in (0, 1)] == [3, 2]
+    pi.pi_debug_set_mma_min_batch(c.handle, 0)
+    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in (0, 1)] == [0, 0]
+    pi.pi_debug_set_mma_min_batch(c.handle, 5)
+    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in (0, 1)] == [5, 5]
+    pi.pi_debug_set_mma_min_batch(c.handle, AUTO)
+    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in (0, 1)] == [3, 2]
+    with pytest.raises(pi.PiError):
+        pi.pi_debug_set_mma_min_batch(c.handle, -2)
     c.close()
 
 
