@@ -78,9 +78,8 @@ struct pi_ctx {
     size_t q4s_cap_up = 0, q4s_cap_gate = 0, q4s_cap_dn = 0; // bytes
     LayerDev *q4s_layers = nullptr; // device [max_layers]: each Q4_0 layer's 16-bit view of those rows
     // Batches of at least this many tokens run layer by layer: batched predictor launches and the
-    // tensor-core FFN (0: never).  Measured on GB300: from 2 tokens on LLaMA-70B-shaped (ReGLU)
-    // layers, from 3 on OPT-30B-shaped ones (equal at 2), the step kernel's per-group passes lose.
-    int mma_min_b = -1; // smallest batch run layer by layer; -1: by layer kind (layerwise_min_b)
+    // tensor-core FFN (0: never; -1: by layer kind, see layerwise_min_b).
+    int mma_min_b = -1;
     int *ctl = nullptr; // [0..1] grid-barrier counter (u64), [2] status, [3] abort
     // trace
     float *tr_x = nullptr;
