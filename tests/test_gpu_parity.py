@@ -370,6 +370,8 @@ def test_decode_stack_with_crossover_hot_prefix(layerwise):
         counts = c.layer_counts(l, G.dev16(cal)).cpu().numpy()  # physical order, descending
         hot = c.choose_hot_prefix(l, counts, T, B)
         assert 0 < hot < cfg.n
+        # the layer's bytes: W2 row and b2 predicted; W_up row, bias and W_down^T row computed
+        assert hot == pi.pi_hot_prefix_crossover(counts, T, B, 2.0 * cfg.r + 2, 2 * cfg.d * 2.0 + 2)
         c.set_hot_prefix(l, hot)
         layers.append(lw)
         perms.append(perm)
