@@ -399,6 +399,57 @@ def test_decode_stack_with_crossover_hot_prefix(layerwise):
     c.close()
 
 
+@pytest.mark.parametrize("B", [1, 2, 8])
+def test_distilled_predictor_runs_unchanged_on_the_gpu(c64, B):
+    """A predictor fitted offline to the layer's fired sets (another rank than
+    the layer's own) loads like any other: the lists equal the oracle's."""
+    pytest.importorskip("torch")
+    from activation_sparse_decode_sigmoid_gb300 import distill as D
+    cfg, layer = _layer("relu_f16")
+    fitted = D.distill(layer, W.calibration_inputs(cfg, 0, 0, T=1024), 48, steps=100)
+    c64.load_layer(0, fitted)
+    x = W.xhat_inputs(cfg, B, 51 + B)
+    idx, cnt, oidx = G.predict_checked(c64, 0, fitted, x)
+    G.ffn_checked(c64, 0, fitted, x, idx, cnt, oidx)
+
+
+@pytest.mark.parametrize("B", [1, 2, 8])
+def test_stack_with_a_rank_per_layer(B):
+    """Distilled predictors of different ranks per layer (16, 48, 32) in one
+    stack: each layer's list equals the oracle's on the GPU's x_hat, and the
+    update matches."""
+    pytest.importorskip("torch")
+    from activation_sparse_decode_sigmoid_gb300 import distill as D
+    t = G.torch()
+    cfg = CFGS["relu_f16"]
+    L = 3
+    c = G.ctx(max_layers=L, max_batch=8)
+    layers = []
+    for l, rank in enumerate((16, 48, 32)):
+        lw = W.make_layer(cfg, l, 0, random_bdown=True)
+        fitted = D.distill(lw, W.calibration_inputs(cfg, l, 0, T=512), rank, steps=50, seed=l)
+        c.load_layer(l, fitted)
+        layers.append(fitted)
+    x0 = W.decode_inputs(cfg, B, 12)
+    x = t.from_numpy(x0.copy()).cuda()
+    tx = t.zeros((L, B, cfg.d), dtype=t.float32, device="cuda")
+    txh = t.zeros((L, B, cfg.d), dtype=t.int16, device="cuda")
+    tidx = t.full((L, cfg.n), -1, dtype=t.int32, device="cuda")
+    tcnt = t.zeros(L, dtype=t.int32, device="cuda")
+    c.set_trace(tx, txh, tidx, tcnt)
+    c.decode_step(x)
+    c.check()
+    xs = np.concatenate([tx.cpu().numpy(), x.cpu().numpy()[None]], 0).astype(np.float64)
+    xh = G.host16(txh)
+    for l in range(L):
+        m = int(tcnt[l].item())
+        oidx = O.union(O.layer_predict(layers[l], xh[l])["mask"])
+        assert np.array_equal(tidx[l, :m].cpu().numpy(), oidx)
+        err = max_rel_err(xs[l + 1] - xs[l], O.masked_ffn(layers[l], xh[l], oidx))
+        assert err <= G.tol(layers[l]), f"layer {l}: {err:.3g}"
+    c.close()
+
+
 def test_large_batch_decode_x_hat_and_list_match_fused_kernel():
     """A batch of 8 decodes layer by layer (RMSNorm launch, batched
     predictor, tensor-core FFN); with the tensor cores off the same batch
