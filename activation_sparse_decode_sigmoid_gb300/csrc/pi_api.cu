@@ -684,13 +684,13 @@ pi_status pi_layer_counts(pi_ctx *c, int32_t layer, const void *x_hat, int32_t T
 // (pi_mma.cu; Q4_0 rows dequantised to f16 first); smaller ones the step kernel.
 // A layer without tensor maps (none could be made) stays on the step kernel.
 // The smallest batch that runs layer by layer.  Unless set, 2 tokens for
-// gated (ReGLU) layers and 3 for the others: at 2 tokens the persistent
-// kernel's two-token groups stream the rows of a ReLU layer faster than the
-// short launches, and those of a ReGLU layer (three rows a neuron) slower.
+// 16-bit layers and 3 for Q4_0 ones: at 2 tokens the persistent kernel's
+// two-token groups beat the short launches only where those first
+// dequantise the listed rows.
 static int layerwise_min_b(const pi_ctx *c, int layer)
 {
     if (c->mma_min_b >= 0) return c->mma_min_b;
-    return c->layers[layer].desc.act == PI_REGLU ? 2 : 3;
+    return c->layers[layer].desc.w_dtype == PI_Q4_0 ? 3 : 2;
 }
 
 static bool use_mma(const pi_ctx *c, int layer, int B)

@@ -181,7 +181,7 @@ struct MmaParams {
 };
 
 // Launchers (host side of the kernels), in the step/load translation units.
-// tgf: 1 (single-token kernel) or 4 (up to four tokens per FFN pass)
+// tgf: tokens per FFN pass of the step kernel: 1, 2 or 4
 cudaError_t launch_step_f16(const StepParams &p, int tgf, int grid, cudaStream_t s);
 cudaError_t launch_step_bf16(const StepParams &p, int tgf, int grid, cudaStream_t s);
 cudaError_t launch_step_q4(const StepParams &p, int tgf, int grid, cudaStream_t s);

@@ -36,6 +36,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "pi_kernels.h"
 
 namespace pi {
@@ -358,6 +360,196 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
     tmem_free(tmem, 256);
 }
 
+// ------------------------------------------------------------------ up / gate kernel, few tokens
+// For a few tokens the rows are streamed whole instead: each neuron's W_up
+// row (with its bias tail) and W_gate row arrive by bulk copies into one
+// stage of a ring, and a consumer warp computes the neuron's dot products
+// with every token's x_hat (shared memory) on the CUDA cores, then the
+// activation, written to A^T as the tensor-core kernel writes it.  A 4-row
+// gather per TMA instruction limits that kernel at small batches; here one
+// bulk copy brings a whole row and the ring holds many neurons.
+// Every stage slot has one consumer warp, which takes the slot's stages in
+// order, so it never waits on a slot more than one phase ahead (a parity
+// wait cannot tell phase j from phase j + 2): with nst slots, W = nst warps
+// when nst <= 16, else W = 16 and nst a multiple of 16; warp w takes the
+// SM's neurons w, w + W, w + 2W, ...
+constexpr int kRowWarps = 16;               // consumer warps
+constexpr int kRowT = 32 * (kRowWarps + 1); // + the producer warp
+constexpr int kRowMaxB = 4;                 // tokens up to which the row kernel runs
+constexpr int kRowMinStages = 6;            // fewer stages than this: the tensor-core kernel
+
+__device__ __forceinline__ void cp16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_row(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+                 "%4;" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_one(uint64_t *b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds16(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// c + the eight products of a 16-bit chunk pair, in element order (the
+// mixed-precision fma multiplies the exactly widened operands, rounds once)
+template <typename T> __device__ __forceinline__ float fma8(const uint4 &w, const uint4 &x, float c);
+template <> __device__ __forceinline__ float fma8<__half>(const uint4 &w, const uint4 &x, float c)
+{
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w}, b[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{ .reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;"
+            " fma.rn.f32.f16 %0, al, bl, %0; fma.rn.f32.f16 %0, ah, bh, %0; }"
+            : "+f"(c)
+            : "r"(a[i]), "r"(b[i]));
+    return c;
+}
+template <> __device__ __forceinline__ float fma8<__nv_bfloat16>(const uint4 &w, const uint4 &x, float c)
+{
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w}, b[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{ .reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;"
+            " fma.rn.f32.bf16 %0, al, bl, %0; fma.rn.f32.bf16 %0, ah, bh, %0; }"
+            : "+f"(c)
+            : "r"(a[i]), "r"(b[i]));
+    return c;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// shared memory of the row kernel: x_hat [B][d], then nst stages of stageB, then 2 nst mbarriers
+__host__ __device__ inline uint32_t row_xs_bytes(int B, int d) { return ((uint32_t)B * d * 2 + 127u) / 128u * 128u; }
+
+template <typename T, bool REGLU>
+__global__ void __launch_bounds__(kRowT, 1) ffn_up_rows(const __grid_constant__ MmaParams p, int nst, uint32_t stageB)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    using H = H16<T>;
+    const LayerDev &L = *p.layer;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int d = L.d, n = L.n, B = p.B;
+    const uint32_t xs = smem_addr(smem);
+    const uint32_t ring = xs + row_xs_bytes(B, d);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + row_xs_bytes(B, d) + (size_t)nst * stageB);
+    uint64_t *empty = full + nst;
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) mbar_init1(full + s), mbar_init1(empty + s);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_enter(); // (the barriers above were set up while the list was finished)
+    const int m = list_len(p, n);
+    const int s0 = slice_at(m, blockIdx.x, gridDim.x), cnt = slice_at(m, blockIdx.x + 1, gridDim.x) - s0;
+    const uint32_t upB = (uint32_t)L.upB, rowB = (uint32_t)L.rowB;
+    if (warp == kRowWarps) {
+        // producer: the slice's rows in list order, one neuron per stage
+        if (lane == 0) {
+            const uint64_t pol = []() {
+                uint64_t q;
+                asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(q));
+                return q;
+            }();
+            int k = 0;
+            for (; k < cnt; ++k) {
+                const int st = k % nst;
+                if (k >= nst && !mbar_wait_bounded(empty + st, ((k / nst) - 1) & 1, p)) break;
+                const int id = p.idx ? __ldg(p.idx + s0 + k) : s0 + k;
+                const bool v = id >= 0 && id < n; // (a bad id is flagged by its consumer)
+                mbar_expect(full + st, v ? upB + (REGLU ? rowB : 0u) : 0u);
+                if (v) {
+                    const uint32_t dst = ring + (uint32_t)st * stageB;
+                    bulk_row(dst, L.up + (size_t)id * upB, upB, full + st, pol);
+                    if (REGLU) bulk_row(dst + upB, L.gate + (size_t)id * rowB, rowB, full + st, pol);
+                }
+            }
+            // no copy may still be in flight when the CTA exits
+            for (int j = max(0, k - nst); j < k; ++j) mbar_wait_bounded(full + j % nst, (j / nst) & 1, p);
+        }
+        return;
+    }
+    // consumers: every token's x_hat into shared memory (rows are 16-byte multiples)
+    for (int q = tid; q < B * (d >> 3); q += kRowWarps * 32) {
+        const int t = q / (d >> 3), ch = q % (d >> 3);
+        cp16(xs + (uint32_t)(t * d + ch * 8) * 2, p.xhat + (size_t)t * d + ch * 8, 16u);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(kRowWarps * 32) : "memory");
+    const int nch = d >> 3;
+    const int W = nst < kRowWarps ? nst : kRowWarps; // (nst: a multiple of kRowWarps from kRowWarps up)
+    for (int k = warp; k < cnt && warp < W; k += W) {
+        const int st = k % nst, pos = s0 + k;
+        const int id = p.idx ? __ldg(p.idx + pos) : pos;
+        const bool v = id >= 0 && id < n;
+        if (!v && lane == 0) fail(p, PI_DEV_FLAG);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(full + st, (k / nst) & 1, p));
+        float au[kRowMaxB], ag[kRowMaxB];
+#pragma unroll
+        for (int t = 0; t < kRowMaxB; ++t) au[t] = ag[t] = 0.f;
+        const uint32_t a = ring + (uint32_t)st * stageB;
+        if (ok && v) {
+            for (int ch = lane; ch < nch; ch += 32) {
+                const uint4 wu = lds16(a + (uint32_t)ch * 16);
+                uint4 wg = make_uint4(0, 0, 0, 0);
+                if (REGLU) wg = lds16(a + upB + (uint32_t)ch * 16);
+#pragma unroll
+                for (int t = 0; t < kRowMaxB; ++t)
+                    if (t < B) {
+                        const uint4 xv = lds16(xs + (uint32_t)(t * d + ch * 8) * 2);
+                        au[t] = fma8<T>(wu, xv, au[t]);
+                        if (REGLU) ag[t] = fma8<T>(wg, xv, ag[t]);
+                    }
+            }
+        }
+        float bias = 0.f;
+        if (ok && v)
+            bias = L.bias_tail ? H::one(*reinterpret_cast<const uint16_t *>(smem + (a - xs) + rowB)) : H::one(L.b[id]);
+#pragma unroll
+        for (int t = 0; t < kRowMaxB; ++t) {
+            au[t] = warp_sum(au[t]);
+            if (REGLU) ag[t] = warp_sum(ag[t]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_one(empty + st); // the stage's rows are no longer read
+        if (lane < B && lane < kRowMaxB && ok) {
+            float u = 0.f, g = 0.f;
+#pragma unroll
+            for (int t = 0; t < kRowMaxB; ++t)
+                if (t == lane) u = au[t], g = ag[t];
+            const float rl = fmaxf((REGLU ? g : u) + bias, 0.f);
+            const float av = REGLU ? rl * u : (L.act == ACT_SQRELU ? rl * rl : rl);
+            p.actT[(size_t)lane * p.mstride + pos] = H::round(v ? av : 0.f);
+        }
+    }
+    // the list's tail up to a whole 64-neuron step reads as zeros in the down kernel
+    if (blockIdx.x == gridDim.x - 1) {
+        const int mp = (m + kBK - 1) / kBK * kBK;
+        for (int q = tid; q < (mp - m) * B; q += kRowWarps * 32) {
+            const int t = q / (mp - m), i = m + q % (mp - m);
+            p.actT[(size_t)t * p.mstride + i] = 0;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ down kernel
 // Work unit u = (256-column block cb, share ks of the list).  For each of the
 // block's two 128-column tiles, D[128 columns x Np tokens] = W_down^T (MN-
@@ -530,6 +722,24 @@ cudaError_t launch_up(const MmaParams &p, int grid, cudaStream_t s)
     return launch_pdl(kern, dim3(grid), dim3(kMT), smem, s, p);
 }
 
+// The row kernel for up to kRowMaxB tokens when its ring holds kRowMinStages
+// neurons or more; returns cudaErrorNotSupported otherwise.
+template <typename T, bool REGLU>
+cudaError_t launch_up_rows(const MmaParams &p, int grid, int smem_optin, cudaStream_t s)
+{
+    if (p.B > kRowMaxB) return cudaErrorNotSupported;
+    const uint32_t stageB = ((uint32_t)(p.d * 2 + 16) + (REGLU ? (uint32_t)p.d * 2 : 0u) + 127u) / 128u * 128u;
+    const int fixed = (int)row_xs_bytes(p.B, p.d);
+    int nst = std::min(32, (smem_optin - fixed - 2 * 32 * 8) / (int)stageB);
+    if (nst < kRowMinStages) return cudaErrorNotSupported;
+    if (nst > kRowWarps) nst = nst / kRowWarps * kRowWarps; // one consumer warp per slot
+    const int smem = fixed + nst * (int)stageB + 2 * nst * 8;
+    auto kern = ffn_up_rows<T, REGLU>;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(grid), dim3(kRowT), smem, s, p, nst, stageB);
+}
+
 template <typename T>
 cudaError_t launch_down(const MmaParams &p, int grid, cudaStream_t s)
 {
@@ -576,9 +786,18 @@ cudaError_t encode_map(CUtensorMap *map, const void *base, uint64_t cols, uint64
 
 cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, cudaStream_t s)
 {
-    cudaError_t e;
-    if (bf16) e = reglu ? launch_up<__nv_bfloat16, true>(p, grid, s) : launch_up<__nv_bfloat16, false>(p, grid, s);
-    else e = reglu ? launch_up<__half, true>(p, grid, s) : launch_up<__half, false>(p, grid, s);
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    // a few tokens: whole rows on the CUDA cores, if the ring holds enough neurons
+    if (bf16) e = reglu ? launch_up_rows<__nv_bfloat16, true>(p, grid, optin, s)
+                        : launch_up_rows<__nv_bfloat16, false>(p, grid, optin, s);
+    else e = reglu ? launch_up_rows<__half, true>(p, grid, optin, s) : launch_up_rows<__half, false>(p, grid, optin, s);
+    if (e == cudaErrorNotSupported) {
+        if (bf16) e = reglu ? launch_up<__nv_bfloat16, true>(p, grid, s) : launch_up<__nv_bfloat16, false>(p, grid, s);
+        else e = reglu ? launch_up<__half, true>(p, grid, s) : launch_up<__half, false>(p, grid, s);
+    }
     if (e != cudaSuccess) return e;
     return bf16 ? launch_down<__nv_bfloat16>(p, grid, s) : launch_down<__half>(p, grid, s);
 }

@@ -390,9 +390,10 @@ def run_ours(args, world, rank, local):
     mb = pi.pi_layerwise_min_batch(ctx.handle, 0)
     layerwise = 0 < mb <= B
     q4 = cfg.w_dtype == W.Q4_0
-    kernel = ("per-layer launches: RMSNorm, batched predictor (3), Q4_0 rows to f16, tensor-core FFN (3)"
-              if layerwise and q4 else
-              "per-layer launches: RMSNorm, batched predictor (3), tensor-core FFN (3)" if layerwise
+    ffn = ("FFN up/gate (whole rows on the CUDA cores up to 4 tokens, else tcgen05), down (tcgen05), "
+           "share merge")
+    kernel = (f"per-layer launches: RMSNorm, batched predictor (3), Q4_0 rows to f16, {ffn}" if layerwise and q4
+              else f"per-layer launches: RMSNorm, batched predictor (3), {ffn}" if layerwise
               else "step_kernel (one persistent launch per step)")
     launches_per_step = (8 if q4 else 7) * L if layerwise else 1
 

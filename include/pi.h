@@ -332,7 +332,7 @@ pi_status pi_debug_copy_hidden(pi_ctx *ctx, float *dst, int32_t count);
  * batched launches and the FFN on the tensor cores (tcgen05 gather-GEMM;
  * Q4_0 rows dequantised to f16 into a context scratch first).  Smaller
  * batches run in the persistent step kernel (CUDA cores).  -1 (the default)
- * chooses by layer kind: 2 tokens for ReGLU layers, 3 for the others.  0
+ * chooses by weight type: 2 tokens for 16-bit layers, 3 for Q4_0 layers.  0
  * keeps every batch on the step kernel.  For comparing the two paths.
  * PI_ERR_ARG below -1. */
 pi_status pi_debug_set_mma_min_batch(pi_ctx *ctx, int32_t min_batch);

@@ -15,7 +15,7 @@ from tests._helpers import max_rel_err, worked_example_layer
 pytestmark = pytest.mark.gpu
 
 # pi_debug_set_mma_min_batch: the library's own choice of the smallest batch
-# that runs layer by layer (2 tokens for ReGLU layers, 3 for the others)
+# that runs layer by layer (2 tokens for 16-bit layers, 3 for Q4_0 layers)
 AUTO = -1
 
 # small layers spanning several tiles with ragged tails (n not a multiple of
@@ -29,6 +29,8 @@ CFGS = {
     "opt_1layer": W.CONFIGS["opt_1layer_relu_f16"],
     # enough W1 / W2 rows per SM that both static-ring passes wrap several times
     "ring_wrap": W.LayerConfig("ring_wrap", 4096, 12000, 2048, 2, W.RELU, W.F16, W.F16, alpha=0.9, cfg_id=205),
+    # wide ReGLU rows: the few-token row kernel's ring holds only 4 to 6 neurons
+    "reglu_wide": W.LayerConfig("reglu_wide", 8192, 16384, 64, 1, W.REGLU, W.BF16, W.BF16, alpha=0.7, cfg_id=207),
 }
 
 
@@ -57,11 +59,13 @@ def test_predict_and_sparse_ffn(c64, name, B):
 
 
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4", "sqrelu_bf16"])
-@pytest.mark.parametrize("B", [1, 2, 7, 9, 64])
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 7, 9, 64])
 @pytest.mark.parametrize("path", ["default", "step kernel"], indirect=True)
 def test_batch_sizes(c64, name, B, path):
     """Every batch size on the default path (layer by layer from 2 or 3
-    tokens) and on the persistent step kernel (its token groups of 1, 2 and 4)."""
+    tokens; up to 4 tokens the up/gate rows stream whole on the CUDA cores,
+    from 5 through the tensor cores) and on the persistent step kernel (its
+    token groups of 1, 2 and 4)."""
     cfg, layer = _layer(name)
     c64.load_layer(0, layer)
     x = W.xhat_inputs(cfg, B, 11)
@@ -76,6 +80,25 @@ def path(c64, request):
         pi.pi_debug_set_mma_min_batch(c64.handle, 0)
     yield request.param
     pi.pi_debug_set_mma_min_batch(c64.handle, AUTO)
+
+
+@pytest.mark.parametrize("name", ["ring_wrap", "reglu_wide"])
+@pytest.mark.parametrize("B", [2, 3, 4])
+def test_few_token_row_kernel_wraps_its_ring(c64, name, B):
+    """Up to 4 tokens the up/gate rows stream whole through a ring of stages
+    with one consumer warp per stage slot; with far more neurons per SM than
+    slots (16 slots of 8 KB rows; 4 to 6 slots of 32 KB ReGLU rows) every
+    slot is refilled many times, and the FFN still matches the oracle."""
+    cfg, layer = _layer(name)
+    c64.load_layer(0, layer)
+    x = W.xhat_inputs(cfg, B, 61 + B)
+    try:
+        pi.pi_debug_set_mma_min_batch(c64.handle, 2)
+        idx, cnt, oidx = G.predict_checked(c64, 0, layer, x)
+        assert oidx.size > 4 * c64.grid  # many neurons per SM
+        G.ffn_checked(c64, 0, layer, x, idx, cnt, oidx)
+    finally:
+        pi.pi_debug_set_mma_min_batch(c64.handle, AUTO)
 
 
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4", "sqrelu_bf16"])
@@ -484,18 +507,20 @@ def test_large_batch_decode_x_hat_and_list_match_fused_kernel():
 
 
 def test_layerwise_threshold_follows_the_layer_kind():
-    """By default a ReGLU layer runs layer by layer from 2 tokens, the other
-    kinds from 3; a set threshold overrides both until -1 restores them."""
-    c = G.ctx(max_layers=2, max_batch=8)
+    """By default a 16-bit layer runs layer by layer from 2 tokens, a Q4_0
+    layer from 3; a set threshold overrides both until -1 restores them."""
+    c = G.ctx(max_layers=3, max_batch=8)
     c.load_layer(0, _layer("relu_f16")[1])
     c.load_layer(1, _layer("reglu_bf16")[1])
-    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in (0, 1)] == [3, 2]
+    c.load_layer(2, _layer("relu_q4")[1])
+    ls = (0, 1, 2)
+    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in ls] == [2, 2, 3]
     pi.pi_debug_set_mma_min_batch(c.handle, 0)
-    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in (0, 1)] == [0, 0]
+    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in ls] == [0, 0, 0]
     pi.pi_debug_set_mma_min_batch(c.handle, 5)
-    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in (0, 1)] == [5, 5]
+    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in ls] == [5, 5, 5]
     pi.pi_debug_set_mma_min_batch(c.handle, AUTO)
-    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in (0, 1)] == [3, 2]
+    assert [pi.pi_layerwise_min_batch(c.handle, l) for l in ls] == [2, 2, 3]
     with pytest.raises(pi.PiError):
         pi.pi_debug_set_mma_min_batch(c.handle, -2)
     c.close()
