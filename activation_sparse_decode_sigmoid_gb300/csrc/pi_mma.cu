@@ -25,6 +25,9 @@
 //                 epilogue adds b_down and writes y (16-bit) or adds into the
 //                 fp32 residual x, or, when a block has several shares, fp32
 //                 partials that ffn_merge adds in share order.
+//   ffn_up_rows   up to 4 tokens, in place of ffn_up_mma: whole W_up / W_gate
+//                 rows by bulk copy through a ring, dot products on the CUDA
+//                 cores, the same A^T.
 // Between the kernels A^T goes through global memory (m * B * 2 bytes, small
 // next to the rows); stream order separates them.
 //

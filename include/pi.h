@@ -194,6 +194,7 @@ pi_status pi_predict(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t B, i
  * [0, n)); count dev int32.  Every token uses the whole list.
  *   a_{t,i} = ReLU:  max(W_up[i].x_t + b_i, 0)
  *             ReGLU: max(W_gate[i].x_t + b_i, 0) * (W_up[i].x_t)
+ *             squared ReLU: max(W_up[i].x_t + b_i, 0)^2
  *   y_t = sum_i a_{t,i} W_down[:, i] + b_down        (fp32 accumulate)
  * y: dev [B][d] act_dtype.  An id outside [0, n) or a count outside [0, n]
  * sets PI_ERR_DEVICE_FLAG (returned by pi_sync_status) and that entry or the
@@ -329,8 +330,10 @@ pi_status pi_debug_set_tuning(pi_ctx *ctx, int32_t prefetch, int32_t prefetch_ns
 pi_status pi_debug_copy_hidden(pi_ctx *ctx, float *dst, int32_t count);
 
 /* Smallest batch (tokens) that runs layer by layer: the predictor as
- * batched launches and the FFN on the tensor cores (tcgen05 gather-GEMM;
- * Q4_0 rows dequantised to f16 into a context scratch first).  Smaller
+ * batched launches and the FFN as a gather-GEMM (up to 4 tokens the up/gate
+ * rows stream whole through the CUDA cores, else tcgen05; the down
+ * projection on tcgen05; Q4_0 rows dequantised to f16 into a context scratch
+ * first).  Smaller
  * batches run in the persistent step kernel (CUDA cores).  -1 (the default)
  * chooses by weight type: 2 tokens for 16-bit layers, 3 for Q4_0 layers.  0
  * keeps every batch on the step kernel.  For comparing the two paths.
