@@ -394,6 +394,22 @@ __device__ __forceinline__ void bulk_row(uint32_t dst, const void *src, uint32_t
                  : "memory");
 }
 
+// Bounded wait that ignores the abort flag: a CTA lets its own copies land
+// before it exits, even after a failure elsewhere.
+__device__ __forceinline__ void mbar_drain(uint64_t *b, uint32_t parity, unsigned long long ns)
+{
+    const uint64_t t0 = gtimer();
+    for (;;) {
+        uint32_t ok;
+        asm volatile("{ .reg .pred q; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 q, [%1], %2; "
+                     "selp.u32 %0, 1, 0, q; }"
+                     : "=r"(ok)
+                     : "r"(smem_addr(b)), "r"(parity)
+                     : "memory");
+        if (ok || gtimer() - t0 > ns) return;
+    }
+}
+
 __device__ __forceinline__ void mbar_arrive_one(uint64_t *b)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
@@ -474,6 +490,7 @@ __global__ void __launch_bounds__(kRowT, 1) ffn_up_rows(const __grid_constant__ 
             int k = 0;
             for (; k < cnt; ++k) {
                 const int st = k % nst;
+                if (*(volatile const int *)p.abort_flag) break; // (consumers stop waiting for stages)
                 if (k >= nst && !mbar_wait_bounded(empty + st, ((k / nst) - 1) & 1, p)) break;
                 const int id = p.idx ? __ldg(p.idx + s0 + k) : s0 + k;
                 const bool v = id >= 0 && id < n; // (a bad id is flagged by its consumer)
@@ -485,7 +502,7 @@ __global__ void __launch_bounds__(kRowT, 1) ffn_up_rows(const __grid_constant__ 
                 }
             }
             // no copy may still be in flight when the CTA exits
-            for (int j = max(0, k - nst); j < k; ++j) mbar_wait_bounded(full + j % nst, (j / nst) & 1, p);
+            for (int j = max(0, k - nst); j < k; ++j) mbar_drain(full + j % nst, (j / nst) & 1, p.wait_ns);
         }
         return;
     }
