@@ -65,7 +65,7 @@ struct pi_ctx {
     uint64_t *xx = nullptr;    // tagged residual between layers [max_batch][kMaxD]
     float *xstage = nullptr; // [max_batch][kMaxD] residual staging of pi_decode_step_host
     // tensor-core FFN of large batches: activations, x_hat and the list of one layer
-    uint16_t *actT = nullptr;    // [max_batch][kMaxN]
+    uint16_t *actT = nullptr;    // [2][max_batch][kMaxN]: hi, then lo parts of the activations
     uint16_t *xhat_ws = nullptr; // [max_batch][kMaxD]
     int32_t *lidx = nullptr;     // [kMaxN] list, then [1] its count
     float *mpart = nullptr;      // [8][max_batch][kMaxD] partials of the tensor-core down-projection
@@ -315,7 +315,7 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
                      sizeof(uint64_t) * (size_t)c->G * max_batch * pi::kMaxD,
                      sizeof(uint64_t) * (size_t)max_batch * pi::kMaxD,
                      sizeof(int) * 64,
-                     sizeof(uint16_t) * (size_t)max_batch * pi::kMaxN,
+                     2 * sizeof(uint16_t) * (size_t)max_batch * pi::kMaxN,
                      sizeof(uint16_t) * (size_t)max_batch * pi::kMaxD,
                      sizeof(int32_t) * ((size_t)pi::kMaxN + 64),
                      sizeof(float) * 8 * (size_t)max_batch * pi::kMaxD,
@@ -713,8 +713,11 @@ static pi_status mma_ffn(pi_ctx *c, int layer, const uint16_t *xhat, int B, cons
     const int np = (B + 15) / 16 * 16;
     if (reinterpret_cast<uintptr_t>(xhat) & 15u) return fail(c, PI_ERR_ARG, "x_hat must be 16-byte aligned");
     cudaError_t me = pi::encode_map(&q.tm_x, xhat, (uint64_t)dsc.d_model, (uint64_t)B, (uint64_t)dsc.d_model * 2, np);
+    uint16_t *actL = c->actT + (size_t)c->max_batch * pi::kMaxN;
     if (me == cudaSuccess)
         me = pi::encode_map(&q.tm_act, c->actT, (uint64_t)pi::kMaxN, (uint64_t)B, (uint64_t)pi::kMaxN * 2, np);
+    if (me == cudaSuccess)
+        me = pi::encode_map(&q.tm_act_lo, actL, (uint64_t)pi::kMaxN, (uint64_t)B, (uint64_t)pi::kMaxN * 2, np);
     if (me != cudaSuccess) return fail(c, PI_ERR_CUDA, "tensor map: %s", cudaGetErrorString(me));
     q.layer = c->d_layers + layer;
     if (dsc.w_dtype == PI_Q4_0) {
@@ -733,6 +736,7 @@ static pi_status mma_ffn(pi_ctx *c, int layer, const uint16_t *xhat, int B, cons
     q.idx = idx;
     q.count = count;
     q.actT = c->actT;
+    q.actL = actL;
     q.mstride = pi::kMaxN;
     q.y = y;
     q.x = x;

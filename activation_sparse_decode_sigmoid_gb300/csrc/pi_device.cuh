@@ -237,6 +237,7 @@ template <typename F>
 __device__ __forceinline__ bool poll_tags(const StepParams &p, volatile int *fail, unsigned epoch,
                                           const uint64_t *stale, F reload)
 {
+    if (!stale) return true; // (the clock is read only once a word has to be polled)
     const uint64_t t0 = globaltimer();
     unsigned it = 0;
     while (stale) {

@@ -163,15 +163,22 @@ __host__ __device__ inline MiscLayout misc_layout(int nss, int nsd, int lcap, in
 struct MmaParams {
     // TMA maps (16-bit elements, 64-column boxes, 128-byte swizzle): the
     // layer's W_up / W_gate / W_down^T rows (one-row boxes, for gather4),
-    // x_hat and A^T (tile boxes of Npad rows; rows past B read as zeros)
-    CUtensorMap tm_up, tm_gate, tm_dn, tm_x, tm_act;
+    // x_hat and the two 16-bit parts of A^T (tile boxes of Npad rows; rows
+    // past B read as zeros)
+    CUtensorMap tm_up, tm_gate, tm_dn, tm_x, tm_act, tm_act_lo;
     const LayerDev *layer;   // device pointer to the layer's descriptor
     const uint16_t *xhat;    // [B][d] 16-bit
     int B, Npad, d;          // tokens, tokens rounded up to 16, d_model
     const int32_t *idx;      // [m] physical neuron ids, ascending; NULL = all n neurons (dense)
     const int32_t *count;    // device m; NULL = n
-    uint16_t *actT;          // [B][mstride] activations, rounded to the weights' type
-    size_t mstride;          // row stride of actT (multiple of 64, >= m rounded up to 64)
+    // The activations A^T as two 16-bit parts in the weights' type: hi =
+    // round(a), lo = round(a - hi).  The down-projection multiplies both with
+    // the same W_down^T tile into one fp32 accumulator, so a reaches it with
+    // about twice the 16-bit precision (a 16-bit tensor-core product takes
+    // both operands in one type).
+    uint16_t *actT;          // [B][mstride] hi parts
+    uint16_t *actL;          // [B][mstride] lo parts
+    size_t mstride;          // row stride of actT / actL (multiple of 64, >= m rounded up to 64)
     uint16_t *y;             // [B][d] 16-bit output, or NULL when x is set
     float *x;                // [B][d] fp32 residual to add into, or NULL
     float *part;             // [8][B][d] fp32 partials of column blocks split over list shares
@@ -185,9 +192,6 @@ struct MmaParams {
 cudaError_t launch_step_f16(const StepParams &p, int tgf, int grid, cudaStream_t s);
 cudaError_t launch_step_bf16(const StepParams &p, int tgf, int grid, cudaStream_t s);
 cudaError_t launch_step_q4(const StepParams &p, int tgf, int grid, cudaStream_t s);
-cudaError_t occupancy_step_f16(int tgf, int smem_bytes, int *blocks);
-cudaError_t occupancy_step_bf16(int tgf, int smem_bytes, int *blocks);
-cudaError_t occupancy_step_q4(int tgf, int smem_bytes, int *blocks);
 // the union-mask FFN on tcgen05: up/gate kernel on `grid` SMs, then the down kernel
 cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, cudaStream_t s);
 

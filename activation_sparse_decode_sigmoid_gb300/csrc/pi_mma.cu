@@ -16,12 +16,15 @@
 //                 128-byte swizzle), D = W_rows (two M = 128 tiles, K-major) x X_hat^T
 //                 (N = B rounded up to 16, K-major), K = d_model in steps of
 //                 64; the epilogue applies the activation and writes A^T
-//                 [B][m] rounded to the weights' 16-bit type (the product of a
-//                 16-bit GEMM takes both operands in one type).
+//                 [B][m] as two parts in the weights' 16-bit type, hi =
+//                 round(a) and lo = round(a - hi) (the product of a 16-bit
+//                 GEMM takes both operands in one type; the two parts carry a
+//                 to about twice that precision).
 //   ffn_down_mma  column blocks of 256 x shares of the list: D = W_down^T
 //                 (M = 128 columns per tile, MN-major: 512-byte segments of
 //                 the gathered rows, by gather4) x A^T (N = B rounded up to 16, K-major),
-//                 K = the share of the list in steps of 64 neurons; the
+//                 once with the hi and once with the lo part into the same
+//                 fp32 accumulator, K = the share of the list in steps of 64 neurons; the
 //                 epilogue adds b_down and writes y (16-bit) or adds into the
 //                 fp32 residual x, or, when a block has several shares, fp32
 //                 partials that ffn_merge adds in share order.
@@ -34,6 +37,20 @@
 // Shared-memory operand layouts are the canonical 128-byte-swizzle layouts:
 // a "row" of 128 bytes (64 16-bit elements) at 128-byte pitch, 16-byte chunk
 // c of row r stored at chunk c ^ (r & 7), 8-row groups at 1024 bytes.
+//
+// Failure handling: every wait is bounded and also gives up once another CTA
+// or launch has raised the abort flag.  A CTA that gives up still lets its
+// own asynchronous work finish before it exits:
+//   * the MMA lane always commits `done`, which every thread waits for
+//     (bounded, ignoring the flag) before tensor memory is read or freed;
+//   * a stage's full barrier counts one arrival per producer, so a producer
+//     that stopped early would leave it incomplete forever.  At the end the
+//     producers publish how many stages they issued; each one then arrives,
+//     without copies, on the stages it skipped up to the furthest any of them
+//     reached (stage by stage, each after the slot's previous round has
+//     completed), and finally waits (bounded, ignoring the flag) for the last
+//     round of every slot.  Rounds of a slot complete in order, so every
+//     copy the CTA issued has then landed.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -92,26 +109,92 @@ __device__ __forceinline__ void mbar_init1(uint64_t *b) { mbar_init(b, 1); }
 // are needed to keep enough bytes in flight.
 __device__ __forceinline__ int issuer_index(int warp) { return warp == 0 ? 0 : (warp >= 2 ? warp - 1 : -1); }
 
-// bounded wait for the phase of the given parity; false after the wait limit or an abort
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{ .reg .pred q; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 q, [%1], %2; "
+                 "selp.u32 %0, 1, 0, q; }"
+                 : "=r"(ok)
+                 : "r"(smem_addr(b)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// bounded wait for the phase of the given parity; false after the wait limit
+// or an abort.  A phase that has completed costs one try_wait.  Once the
+// wait has to spin, the clock is read after every try_wait (each may suspend
+// the thread for a while, so the limit holds however short it is) and the
+// abort flag, an L2 read, after every 16th.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *b, uint32_t parity, const MmaParams &p)
 {
+    if (mbar_try(b, parity)) return true;
     const uint64_t t0 = gtimer();
-    for (unsigned it = 0;; ++it) {
-        uint32_t ok;
-        asm volatile("{ .reg .pred q; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 q, [%1], %2; "
-                     "selp.u32 %0, 1, 0, q; }"
-                     : "=r"(ok)
-                     : "r"(smem_addr(b)), "r"(parity)
-                     : "memory");
-        if (ok) return true;
-        if ((it & 15) == 15) {
-            if (*(volatile int *)p.abort_flag) return false;
-            if (gtimer() - t0 > p.wait_ns) {
-                fail(p, PI_DEV_TIMEOUT);
-                return false;
-            }
+    for (unsigned it = 1;; ++it) {
+        if (mbar_try(b, parity)) return true;
+        if (gtimer() - t0 > p.wait_ns) {
+            fail(p, PI_DEV_TIMEOUT);
+            return false;
         }
+        if ((it & 15) == 0 && *(volatile int *)p.abort_flag) return false;
     }
+}
+
+// Bounded wait that ignores the abort flag: a CTA lets its own copies land
+// before it exits, even after a failure elsewhere.  Copies land within
+// microseconds; the limit only guards against a device that stopped.
+constexpr unsigned long long kDrainNs = 100000000ull; // 100 ms
+
+__device__ __forceinline__ bool mbar_drain(uint64_t *b, uint32_t parity, unsigned long long ns)
+{
+    if (mbar_try(b, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (;;) {
+        if (mbar_try(b, parity)) return true;
+        if (gtimer() - t0 > ns) return false;
+    }
+}
+
+// Wait for `done` (committed by the MMA lane after its last MMA of a pass,
+// whatever happened before): ignores the abort flag, so tensor memory is
+// never read or freed while an MMA runs; a timeout past the MMA lane's own
+// bounded waits is reported.
+__device__ __forceinline__ bool mbar_settle(uint64_t *b, uint32_t parity, const MmaParams &p)
+{
+    if (mbar_drain(b, parity, p.wait_ns + kDrainNs)) return true;
+    fail(p, PI_DEV_TIMEOUT);
+    return false;
+}
+
+// End of a kernel, producer lanes (iss >= 0, lane 0): complete every round of
+// the full barriers (count kIssuers each, nst slots) up to the furthest stage
+// any producer issued, then wait for the last round of each slot.  pub
+// [kIssuers] is shared memory; `gp` = the stages this producer issued.  Every
+// thread of the CTA must call it (it holds a CTA barrier).
+__device__ __forceinline__ void settle_producers(uint64_t *full, int nst, int *pub, int iss, int lane, uint32_t gp)
+{
+    if (iss >= 0 && lane == 0) pub[iss] = (int)gp;
+    __syncthreads();
+    if (iss < 0 || lane != 0) return;
+    uint32_t gmax = 0;
+    for (int i = 0; i < kIssuers; ++i) gmax = max(gmax, (uint32_t)pub[i]);
+    for (uint32_t g = gp; g < gmax; ++g) {
+        const uint32_t st = g % (uint32_t)nst, r = g / (uint32_t)nst;
+        // this producer saw round r - 2 of the slot complete (it issued or
+        // filled in stage g - nst after it), so a parity wait here is exact
+        if (r > 0) mbar_drain(full + st, (r - 1) & 1, kDrainNs);
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(full + st)) : "memory");
+    }
+    for (uint32_t g = gmax > (uint32_t)nst ? gmax - nst : 0u; g < gmax; ++g)
+        mbar_drain(full + g % (uint32_t)nst, (g / (uint32_t)nst) & 1, kDrainNs);
+}
+
+// a = hi + lo to about twice the 16-bit precision: hi = round(a), lo =
+// round(a - hi) (the difference is exact in fp32)
+template <typename H>
+__device__ __forceinline__ void split16(float a, uint16_t &hi, uint16_t &lo)
+{
+    hi = H::round(a);
+    lo = H::round(a - H::one(hi));
 }
 
 // shared-memory matrix descriptor, 128-byte swizzle
@@ -237,11 +320,12 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
     const int d = L.d, n = L.n, B = p.B, Np = p.Npad;
     constexpr uint32_t kW = RP / 128 * kTileA; // RP rows x 128 bytes of one weight matrix
     constexpr uint32_t kStage = kW * (REGLU ? 2 : 1) + kTileX;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * kStage);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * kStage); // one arrival per producer
     uint64_t *empty = full + STAGES;
     uint64_t *done = empty + STAGES;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
     int *sid = reinterpret_cast<int *>(tslot + 4); // [RP] row ids of the current pass
+    int *pub = sid + RP;                           // [kIssuers] stages each producer issued
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(full + s, kIssuers), mbar_init1(empty + s);
         mbar_init1(done);
@@ -255,7 +339,8 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
     const int KT = (d + kBK - 1) / kBK;
     const uint32_t base = smem_addr(smem);
     const uint32_t id_up = idesc(H::fmt, 0, 0, 128, (uint32_t)Np);
-    uint32_t gp = 0, gc = 0, pass = 0; // stages produced / consumed, passes
+    const int iss = issuer_index(warp);
+    uint32_t gp = 0, gc = 0, pass = 0; // stages produced (by this producer lane) / consumed, passes
     bool ok = true;
 
     for (int r0 = s0; r0 < s1; r0 += RP, ++pass) {
@@ -273,7 +358,6 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
             sid[r] = id;
         }
         __syncthreads();
-        const int iss = issuer_index(warp);
         if (iss >= 0 && lane == 0) {
             const int nq = (rows + 3) / 4;
             const int mine = (nq - iss + kIssuers - 1) / kIssuers; // gathers q = iss, iss + kIssuers, ...
@@ -281,18 +365,19 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
             for (int kt = 0; kt < KT && ok; ++kt, ++gp) {
                 const uint32_t st = gp % STAGES;
                 if (gp >= STAGES && !mbar_wait_bounded(empty + st, ((gp / STAGES) - 1) & 1, p)) {
-                    ok = false;
+                    ok = false; // (nothing issued for this stage)
                     break;
                 }
                 const uint32_t sb = base + st * kStage;
-                mbar_expect(full + st, bytes);
+                uint64_t *fb = full + st;
+                mbar_expect(fb, bytes);
                 for (int q = iss; q < nq; q += kIssuers) {
                     const int r = 4 * q;
                     const uint32_t dst = sb + (uint32_t)(r >> 7) * kTileA + (uint32_t)(r & 127) * 128u;
-                    gather4(dst, &p.tm_up, kt * kBK, sid[r], sid[r + 1], sid[r + 2], sid[r + 3], full + st);
-                    if (REGLU) gather4(dst + kW, &p.tm_gate, kt * kBK, sid[r], sid[r + 1], sid[r + 2], sid[r + 3], full + st);
+                    gather4(dst, &p.tm_up, kt * kBK, sid[r], sid[r + 1], sid[r + 2], sid[r + 3], fb);
+                    if (REGLU) gather4(dst + kW, &p.tm_gate, kt * kBK, sid[r], sid[r + 1], sid[r + 2], sid[r + 3], fb);
                 }
-                if (iss == 0) tile_load(sb + kW * (REGLU ? 2 : 1), &p.tm_x, kt * kBK, 0, full + st);
+                if (iss == 0) tile_load(sb + kW * (REGLU ? 2 : 1), &p.tm_x, kt * kBK, 0, fb);
             }
         } else if (warp == 1 && lane == 0) {
             for (int kt = 0; kt < KT && ok; ++kt, ++gc) {
@@ -317,13 +402,14 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
                 }
                 mma_commit(empty + st);
             }
-            mma_commit(done);
+            mma_commit(done); // always: the MMAs issued so far complete before `done` flips
         }
         __syncwarp(); // (gp lives in the producer lane, gc in the MMA lane)
-        if (!mbar_wait_bounded(done, pass & 1, p)) ok = false;
+        const bool settled = mbar_settle(done, pass & 1, p);
         tc_after();
         // epilogue (warps 0..3): thread = row r of tile j (TMEM lane), 16 token columns at a time
-        for (int j = 0; j < ntile && warp < 4; ++j) {
+        const bool live = ok && settled && !*(volatile int *)p.abort_flag;
+        for (int j = 0; j < ntile && warp < 4; ++j) { // (tcgen05.ld is warp-wide: no per-thread condition here)
             const int r = j * 128 + warp * 32 + lane;
             const int id = sid[r];
             float bias = 0.f;
@@ -335,14 +421,17 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
                 float u[16], gt[16];
                 tmem_ld16(lane_addr + (uint32_t)(j * Np + c0), u);
                 if (REGLU) tmem_ld16(lane_addr + (uint32_t)((2 + j) * Np + c0), gt);
-                if (r < rows && ok) {
+                if (r < rows && live) {
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
                         const int t = c0 + jj;
                         if (t < B) {
                             const float rl = fmaxf((REGLU ? gt[jj] : u[jj]) + bias, 0.f);
                             const float a = REGLU ? rl * u[jj] : (L.act == ACT_SQRELU ? rl * rl : rl);
-                            p.actT[(size_t)t * p.mstride + r0 + r] = H::round(id < n ? a : 0.f);
+                            uint16_t hi, lo;
+                            split16<H>(id < n ? a : 0.f, hi, lo);
+                            p.actT[(size_t)t * p.mstride + r0 + r] = hi;
+                            p.actL[(size_t)t * p.mstride + r0 + r] = lo;
                         }
                     }
                 }
@@ -358,8 +447,11 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
         for (int q = tid; q < (mp - m) * B; q += kMT) {
             const int t = q / (mp - m), i = m + q % (mp - m);
             p.actT[(size_t)t * p.mstride + i] = 0;
+            p.actL[(size_t)t * p.mstride + i] = 0;
         }
     }
+    // no copy of this CTA may be in flight when it exits
+    settle_producers(full, STAGES, pub, iss, lane, gp);
     tmem_free(tmem, 256);
 }
 
@@ -368,7 +460,8 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
 // row (with its bias tail) and W_gate row arrive by bulk copies into one
 // stage of a ring, and a consumer warp computes the neuron's dot products
 // with every token's x_hat (shared memory) on the CUDA cores, then the
-// activation, written to A^T as the tensor-core kernel writes it.  A 4-row
+// activation, written to A^T (hi and lo parts) as the tensor-core kernel
+// writes it.  A 4-row
 // gather per TMA instruction limits that kernel at small batches; here one
 // bulk copy brings a whole row and the ring holds many neurons.
 // Every stage slot has one consumer warp, which takes the slot's stages in
@@ -392,22 +485,6 @@ __device__ __forceinline__ void bulk_row(uint32_t dst, const void *src, uint32_t
                  "%4;" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
                  : "memory");
-}
-
-// Bounded wait that ignores the abort flag: a CTA lets its own copies land
-// before it exits, even after a failure elsewhere.
-__device__ __forceinline__ void mbar_drain(uint64_t *b, uint32_t parity, unsigned long long ns)
-{
-    const uint64_t t0 = gtimer();
-    for (;;) {
-        uint32_t ok;
-        asm volatile("{ .reg .pred q; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 q, [%1], %2; "
-                     "selp.u32 %0, 1, 0, q; }"
-                     : "=r"(ok)
-                     : "r"(smem_addr(b)), "r"(parity)
-                     : "memory");
-        if (ok || gtimer() - t0 > ns) return;
-    }
 }
 
 __device__ __forceinline__ void mbar_arrive_one(uint64_t *b)
@@ -502,7 +579,7 @@ __global__ void __launch_bounds__(kRowT, 1) ffn_up_rows(const __grid_constant__ 
                 }
             }
             // no copy may still be in flight when the CTA exits
-            for (int j = max(0, k - nst); j < k; ++j) mbar_drain(full + j % nst, (j / nst) & 1, p.wait_ns);
+            for (int j = max(0, k - nst); j < k; ++j) mbar_drain(full + j % nst, (j / nst) & 1, kDrainNs);
         }
         return;
     }
@@ -557,7 +634,10 @@ __global__ void __launch_bounds__(kRowT, 1) ffn_up_rows(const __grid_constant__ 
                 if (t == lane) u = au[t], g = ag[t];
             const float rl = fmaxf((REGLU ? g : u) + bias, 0.f);
             const float av = REGLU ? rl * u : (L.act == ACT_SQRELU ? rl * rl : rl);
-            p.actT[(size_t)lane * p.mstride + pos] = H::round(v ? av : 0.f);
+            uint16_t hi, lo;
+            split16<H>(v ? av : 0.f, hi, lo);
+            p.actT[(size_t)lane * p.mstride + pos] = hi;
+            p.actL[(size_t)lane * p.mstride + pos] = lo;
         }
     }
     // the list's tail up to a whole 64-neuron step reads as zeros in the down kernel
@@ -566,6 +646,7 @@ __global__ void __launch_bounds__(kRowT, 1) ffn_up_rows(const __grid_constant__ 
         for (int q = tid; q < (mp - m) * B; q += kRowWarps * 32) {
             const int t = q / (mp - m), i = m + q % (mp - m);
             p.actT[(size_t)t * p.mstride + i] = 0;
+            p.actL[(size_t)t * p.mstride + i] = 0;
         }
     }
 }
@@ -574,27 +655,38 @@ __global__ void __launch_bounds__(kRowT, 1) ffn_up_rows(const __grid_constant__ 
 // Work unit u = (256-column block cb, share ks of the list).  For each of the
 // block's two 128-column tiles, D[128 columns x Np tokens] = W_down^T (MN-
 // major A: per stage 64 neurons x 256 columns, four 64-column atoms filled by
-// gather4) x A^T (K-major B: a tile load of tokens x 64 neurons).  When the
-// list is split over several shares, the units write fp32 partials that
-// ffn_merge adds in share order; with one share the unit writes y or x.
-template <typename T, int STAGES>
-__global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ MmaParams p, int nks)
+// gather4) x A^T (K-major B: tile loads of tokens x 64 neurons, the hi and the
+// lo part, each multiplied into the same accumulator).  When the list is
+// split over several shares, the units write fp32 partials that ffn_merge
+// adds in share order; with one share the unit writes y or x.  A stage holds
+// 32 KB of rows and 2 x Np x 128 bytes of A^T: nst stages, as many as fit.
+constexpr uint32_t kDnAtom = 8192;        // 64 neurons x 64 columns (128 bytes)
+constexpr uint32_t kDnW = 4 * kDnAtom;    // 64 neurons x 256 columns
+__host__ __device__ constexpr uint32_t dn_stage_bytes(int Np) { return kDnW + 2u * (uint32_t)Np * 128u; }
+__host__ __device__ constexpr int dn_fixed_bytes() { return 16 + kIssuers * 65 * 4; }
+__host__ __device__ constexpr int dn_smem_bytes(int Np, int nst)
+{
+    return nst * (int)dn_stage_bytes(Np) + (2 * nst + 1) * 8 + dn_fixed_bytes();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ MmaParams p, int nks, int nst)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     using H = H16<T>;
     const LayerDev &L = *p.layer;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = L.d, n = L.n, B = p.B, Np = p.Npad;
-    constexpr uint32_t kAtom = 8192;   // 64 neurons x 64 columns (128 bytes)
-    constexpr uint32_t kW = 4 * kAtom; // 64 neurons x 256 columns
-    constexpr uint32_t kStage = kW + kTileX;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * kStage);
-    uint64_t *empty = full + STAGES;
-    uint64_t *done = empty + STAGES;
+    const uint32_t kX = (uint32_t)Np * 128u; // one A^T part of a stage
+    const uint32_t kStage = dn_stage_bytes(Np);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)nst * kStage); // one arrival per producer
+    uint64_t *empty = full + nst;
+    uint64_t *done = empty + nst;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
     int *sidd = reinterpret_cast<int *>(tslot + 4); // [kIssuers][64] ids of the stage each producer is on
+    int *pub = sidd + kIssuers * 64;                 // [kIssuers] stages each producer issued
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) mbar_init(full + s, kIssuers), mbar_init1(empty + s);
+        for (int s = 0; s < nst; ++s) mbar_init(full + s, kIssuers), mbar_init1(empty + s);
         mbar_init1(done);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -607,7 +699,7 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
     const uint32_t id_dn = idesc(H::fmt, 1, 0, 128, (uint32_t)Np);
     const int iss = issuer_index(warp);
     // 64 gathers per stage (4 column atoms x 16 groups of 4 neurons): g = iss, iss + kIssuers, ...
-    const uint32_t bytes = (uint32_t)((64 - iss + kIssuers - 1) / kIssuers) * 512u + (iss == 0 ? (uint32_t)Np * 128u : 0u);
+    const uint32_t bytes = (uint32_t)((64 - iss + kIssuers - 1) / kIssuers) * 512u + (iss == 0 ? 2u * kX : 0u);
     int *myids = sidd + (iss < 0 ? 0 : iss) * 64;
     uint32_t gp = 0, gc = 0, pass = 0;
     bool ok = true;
@@ -626,8 +718,8 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
             int f0[2], f1[2], f2[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) f0[h] = fetch(0, h), f1[h] = fetch(1, h), f2[h] = fetch(2, h);
-            for (int kt = 0; kt < KT; ++kt, ++gp) {
-                const uint32_t st = gp % STAGES;
+            for (int kt = 0; kt < KT; ++kt) {
+                const uint32_t st = gp % (uint32_t)nst;
                 const int k0 = (k_lo + kt) * kBK;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -640,27 +732,30 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
                 }
                 __syncwarp();
                 if (lane == 0 && ok) {
-                    if (gp >= STAGES && !mbar_wait_bounded(empty + st, ((gp / STAGES) - 1) & 1, p)) ok = false;
+                    if (gp >= (uint32_t)nst && !mbar_wait_bounded(empty + st, ((gp / nst) - 1) & 1, p)) ok = false;
                     if (ok) {
                         const uint32_t sb = base + st * kStage;
-                        mbar_expect(full + st, bytes);
+                        uint64_t *fb = full + st;
+                        mbar_expect(fb, bytes);
                         for (int gi = iss; gi < 64; gi += kIssuers) {
                             const int a = gi >> 4, q = gi & 15;
-                            gather4(sb + (uint32_t)a * kAtom + (uint32_t)q * 512u, &p.tm_dn, c0 + 64 * a,
-                                    myids[4 * q], myids[4 * q + 1], myids[4 * q + 2], myids[4 * q + 3], full + st);
+                            gather4(sb + (uint32_t)a * kDnAtom + (uint32_t)q * 512u, &p.tm_dn, c0 + 64 * a,
+                                    myids[4 * q], myids[4 * q + 1], myids[4 * q + 2], myids[4 * q + 3], fb);
                         }
-                        if (iss == 0) tile_load(sb + kW, &p.tm_act, k0, 0, full + st);
+                        if (iss == 0) {
+                            tile_load(sb + kDnW, &p.tm_act, k0, 0, fb);
+                            tile_load(sb + kDnW + kX, &p.tm_act_lo, k0, 0, fb);
+                        }
+                        ++gp; // (lane 0 counts the stages it issued)
                     }
                 }
                 __syncwarp(); // myids is rewritten for the next stage
             }
-        } else {
-            gp += (uint32_t)KT;
         }
         if (warp == 1 && lane == 0) {
             for (int kt = 0; kt < KT && ok; ++kt, ++gc) {
-                const uint32_t st = gc % STAGES;
-                if (!mbar_wait_bounded(full + st, (gc / STAGES) & 1, p)) {
+                const uint32_t st = gc % (uint32_t)nst;
+                if (!mbar_wait_bounded(full + st, (gc / nst) & 1, p)) {
                     ok = false;
                     break;
                 }
@@ -668,20 +763,22 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
                 const uint32_t sb = base + st * kStage;
 #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k) {
-                    const uint64_t bx = sdesc(sb + kW + k * 32, 16, 1024);
+                    const uint64_t bh = sdesc(sb + kDnW + k * 32, 16, 1024);
+                    const uint64_t bl = sdesc(sb + kDnW + kX + k * 32, 16, 1024);
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) // atoms 2j, 2j+1: LBO steps from one 64-column atom to the next
-                        mma(tmem + (uint32_t)(j * Np), sdesc(sb + (uint32_t)(2 * j) * kAtom + k * 16 * 128, kAtom, 1024),
-                            bx, id_dn, (kt | k) != 0);
+                    for (int j = 0; j < 2; ++j) { // atoms 2j, 2j+1: LBO steps from one 64-column atom to the next
+                        const uint64_t a = sdesc(sb + (uint32_t)(2 * j) * kDnAtom + k * 16 * 128, kDnAtom, 1024);
+                        mma(tmem + (uint32_t)(j * Np), a, bh, id_dn, (kt | k) != 0);
+                        mma(tmem + (uint32_t)(j * Np), a, bl, id_dn, 1u);
+                    }
                 }
                 mma_commit(empty + st);
             }
-            mma_commit(done);
-        } else {
-            gc += (uint32_t)KT;
+            mma_commit(done); // always: the MMAs issued so far complete before `done` flips
         }
-        if (!mbar_wait_bounded(done, pass & 1, p)) ok = false;
+        const bool settled = mbar_settle(done, pass & 1, p);
         tc_after();
+        const bool live = ok && settled && !*(volatile int *)p.abort_flag;
         // epilogue: thread = output column (TMEM lane) of tile j, 16 tokens at a time
         const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
         for (int j = 0; j < 2 && warp < 4; ++j) { // epilogue: warps 0..3
@@ -692,7 +789,7 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
                 if (KT > 0) tmem_ld16(lane_addr + (uint32_t)(j * Np + t0), v);
                 else
                     for (int i = 0; i < 16; ++i) v[i] = 0.f;
-                if (c < d && ok) {
+                if (c < d && live) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int t = t0 + i;
@@ -709,6 +806,8 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
         __syncthreads();
         tc_after();
     }
+    // no copy of this CTA may be in flight when it exits
+    settle_producers(full, nst, pub, iss, lane, gp);
     tmem_free(tmem, 128);
 }
 
@@ -734,8 +833,10 @@ template <typename T, bool REGLU>
 cudaError_t launch_up(const MmaParams &p, int grid, cudaStream_t s)
 {
     constexpr int st = REGLU ? 5 : 9, rp = 128;
-    // stages, then full[st], empty[st], done, the TMEM slot (16 bytes) and the row ids [rp]
-    const int smem = st * (int)(rp / 128 * kTileA * (REGLU ? 2 : 1) + kTileX) + (2 * st + 1) * 8 + 16 + rp * 4;
+    // stages, then full[st], empty[st], done, the TMEM slot (16 bytes), the row ids [rp] and the
+    // producers' stage counts [kIssuers]
+    const int smem = st * (int)(rp / 128 * kTileA * (REGLU ? 2 : 1) + kTileX) + (2 * st + 1) * 8 + 16 + rp * 4 +
+                     kIssuers * 4;
     auto kern = ffn_up_mma<T, REGLU, st, rp>;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -761,18 +862,21 @@ cudaError_t launch_up_rows(const MmaParams &p, int grid, int smem_optin, cudaStr
 }
 
 template <typename T>
-cudaError_t launch_down(const MmaParams &p, int grid, cudaStream_t s)
+cudaError_t launch_down(const MmaParams &p, int grid, int smem_optin, cudaStream_t s)
 {
-    constexpr int st = 5;
-    const int smem = st * (int)(4 * 8192 + kTileX) + 128 + kIssuers * 64 * 4;
-    auto kern = ffn_down_mma<T, st>;
+    // as many stages as shared memory holds (at most 6): 4 at 64 tokens, 6 at 16
+    int st = 6;
+    while (st > 2 && dn_smem_bytes(p.Npad, st) > smem_optin) --st;
+    const int smem = dn_smem_bytes(p.Npad, st);
+    if (smem > smem_optin) return cudaErrorInvalidValue;
+    auto kern = ffn_down_mma<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // as many shares of the list per 256-column block as keep every SM busy with one unit
     const int ncb = (p.d + 255) / 256;
     const int nks = grid / ncb > 8 ? 8 : (grid / ncb < 1 ? 1 : grid / ncb);
     const int units = ncb * nks;
-    e = launch_pdl(kern, dim3(units < grid ? units : grid), dim3(kMT), smem, s, p, nks);
+    e = launch_pdl(kern, dim3(units < grid ? units : grid), dim3(kMT), smem, s, p, nks, st);
     if (e != cudaSuccess || nks == 1) return e;
     return launch_pdl(ffn_merge<T>, dim3(grid * 4), dim3(256), 0, s, p, nks);
 }
@@ -819,7 +923,7 @@ cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, 
         else e = reglu ? launch_up<__half, true>(p, grid, s) : launch_up<__half, false>(p, grid, s);
     }
     if (e != cudaSuccess) return e;
-    return bf16 ? launch_down<__nv_bfloat16>(p, grid, s) : launch_down<__half>(p, grid, s);
+    return bf16 ? launch_down<__nv_bfloat16>(p, grid, optin, s) : launch_down<__half>(p, grid, optin, s);
 }
 
 } // namespace pi

@@ -49,25 +49,26 @@ unsigned char *g_ptr[kMaxDevices] = {};
 unsigned g_epoch[kMaxDevices] = {}; // epoch of the last call on each device (the array starts zeroed)
 
 // Device address of the scratch array on the current device.  The first call
-// on a device resolves it (cudaGetSymbolAddress may load the module) and
-// clears the array once; later calls only read the cache.
-cudaError_t noalloc_scratch(int dev, unsigned char **out, unsigned *epoch)
+// on a device resolves it (cudaGetSymbolAddress may load the module; the
+// array starts zeroed, as every device variable without an initialiser);
+// later calls only read the cache.
+cudaError_t noalloc_scratch(int dev, cudaStream_t s, unsigned char **out, unsigned *epoch)
 {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_ptr[dev]) {
         void *ptr = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        e = cudaMemset(ptr, 0, kScratchBytes);
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
         g_ptr[dev] = static_cast<unsigned char *>(ptr);
     }
     *out = g_ptr[dev];
     // every call writes its partials under a new epoch, so what earlier
-    // calls left in the array can never be taken for this call's
+    // calls left in the array can never be taken for this call's; before
+    // the 32-bit epoch could wrap, the tags are cleared on the caller's
+    // stream (ordered before this call's kernel)
     if (++g_epoch[dev] == 0xF0000000u) {
-        const cudaError_t e = cudaMemset(g_ptr[dev], 0, kScratchBytes);
+        const cudaError_t e = cudaMemsetAsync(g_ptr[dev] + kPartialOff, 0, kPartialWords * 8, s);
         if (e != cudaSuccess) return e;
         g_epoch[dev] = 1;
     }
@@ -105,7 +106,8 @@ extern "C" pi_status pi_sparse_ffn_noalloc(const pi_ffn_rows *w, const void *x_h
     if ((size_t)G * B * d > kPartialWords) return PI_ERR_SHAPE;
     unsigned char *scratch = nullptr;
     unsigned epoch = 0;
-    if (noalloc_scratch(dev, &scratch, &epoch) != cudaSuccess) return PI_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (noalloc_scratch(dev, s, &scratch, &epoch) != cudaSuccess) return PI_ERR_CUDA;
 
     // shared-memory plan of the FFN-only launch (no predictor phases)
     pi::StepParams p{};
@@ -152,7 +154,6 @@ extern "C" pi_status pi_sparse_ffn_noalloc(const pi_ffn_rows *w, const void *x_h
     L.bdown = w->b_down ? static_cast<const uint16_t *>(w->b_down)
                         : reinterpret_cast<const uint16_t *>(scratch + kZeroOff);
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the array keeps the previous call's contents: clear the status words,
     // then publish this call's layer descriptor
     if (cudaMemsetAsync(scratch + kCtlOff, 0, 16, s) != cudaSuccess) return PI_ERR_CUDA;

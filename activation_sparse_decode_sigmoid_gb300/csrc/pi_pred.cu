@@ -56,20 +56,19 @@ __device__ __forceinline__ void flag(const PredParams &p, int code)
     atomicExch(p.abort_flag, 1);
 }
 
-// bounded wait for a bulk copy; false after the wait limit or an abort
+// bounded wait for a bulk copy; false after the wait limit or an abort (the
+// clock after every try_wait that failed, the abort flag after every 16th)
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, const PredParams &p)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (unsigned it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15) == 0) {
-            if (*(volatile int *)p.abort_flag) return false;
-            if (globaltimer() - t0 > p.wait_ns) {
-                flag(p, PI_DEV_TIMEOUT);
-                return false;
-            }
+        if (globaltimer() - t0 > p.wait_ns) {
+            flag(p, PI_DEV_TIMEOUT);
+            return false;
         }
+        if ((it & 15) == 0 && *(volatile int *)p.abort_flag) return false;
     }
 }
 
@@ -326,15 +325,22 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
         }
         cp_commit();
     };
+    // copies issued into / waited for in each tile slot of this warp (warp-
+    // uniform counts): at most one is outstanding per slot, and the warp
+    // waits for it before the CTA exits, whatever happened
+    uint32_t n_iss[2] = {0u, 0u}, n_wt[2] = {0u, 0u};
     // warp-level: bring this warp's rows of unit u into tile slot sl
     const auto load_rows = [&](int u, int sl) {
         const int i0 = u * RT + warp * R;
         const int nr = max(0, min(R, n - i0));
-        if (lane == 0 && nr > 0) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar + warp * WS + sl, (uint32_t)nr * r * 2);
-            bulk_g2s(wtile + (size_t)sl * wB, L.w2 + (size_t)i0 * r, (uint32_t)nr * r * 2, bar + warp * WS + sl,
-                     policy_evict_first());
+        if (nr > 0) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar + warp * WS + sl, (uint32_t)nr * r * 2);
+                bulk_g2s(wtile + (size_t)sl * wB, L.w2 + (size_t)i0 * r, (uint32_t)nr * r * 2, bar + warp * WS + sl,
+                         policy_evict_first());
+            }
+            ++n_iss[sl];
         }
     };
     // the first unit's rows do not depend on the hidden layer: they start
@@ -347,9 +353,10 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
     for (int u = u0 + blockIdx.x; u < nrt; u += gridDim.x, ++it) {
         const int sl = WS == 2 ? (int)(it & 1) : 0;
         const uint32_t par = WS == 2 ? (it >> 1) & 1 : it & 1;
+        // (after a failed wait nothing more is issued: that slot's copy may still be in flight)
         if (WS == 2) {
-            if (u + (int)gridDim.x < nrt) load_rows(u + gridDim.x, sl ^ 1); // slot sl ^ 1 was read by the last unit
-        } else if (it > 0) {
+            if (ok && u + (int)gridDim.x < nrt) load_rows(u + gridDim.x, sl ^ 1); // slot sl ^ 1 was read by the last unit
+        } else if (it > 0 && ok) {
             load_rows(u, 0);
         }
         const int i0 = u * RT + warp * R;
@@ -372,6 +379,7 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
                 // every lane waits; the warp goes on only if all saw the rows (shuffles follow)
                 const bool got = ok && wait_bounded(bar + warp * WS + sl, par, p);
                 ok = __all_sync(0xffffffffu, got);
+                if (ok) ++n_wt[sl];
                 landed = true;
             }
             if (nr > 0 && ok) {
@@ -440,6 +448,14 @@ __global__ void __launch_bounds__(kPT, 1) pred_out(const PredParams p)
         // (the next unit's shared-mask atomics come after the barrier of its first block)
     }
     cp_wait<0>();
+    // no bulk copy of this CTA may be in flight when it exits (bounded, ignoring the abort flag)
+    for (int sl = 0; sl < WS; ++sl)
+        if (n_iss[sl] > n_wt[sl]) {
+            const uint32_t par = (n_iss[sl] - 1) & 1;
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(bar + warp * WS + sl, par) && globaltimer() - t0 < 100000000ull) {
+            }
+        }
 }
 
 // ------------------------------------------------------------------ compaction

@@ -1358,4 +1358,30 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
     }
 }
 
+// ------------------------------------------------------------------ launch
+// One cooperative launch of step_kernel<T, Q4, tgf> on `grid` CTAs of the
+// current device.  The dynamic shared-memory limit is a per-device attribute
+// of the kernel, so it is set before every launch (a cached value would be
+// wrong for a second device or for a host thread racing with this one; the
+// call costs microseconds next to a step of milliseconds).
+template <typename T, bool Q4>
+cudaError_t launch_step(const StepParams &p, int tgf, int grid, cudaStream_t s)
+{
+    void (*kern)(const StepParams) =
+        tgf == 1 ? step_kernel<T, Q4, 1> : (tgf == 2 ? step_kernel<T, Q4, 2> : step_kernel<T, Q4, 4>);
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = p.smem_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 } // namespace pi

@@ -1,42 +1,12 @@
-// Instantiation of the step kernel for __half weights and activations.
+// Instantiation of the step kernel for __half weights and activations
+// (one translation unit per type, so that the three compile in parallel).
 #include "pi_step.cuh"
 
 namespace pi {
 
-template <int TGF> static cudaError_t launch_tgf(const StepParams &p, int grid, cudaStream_t s)
-{
-    auto kern = step_kernel<__half, false, TGF>;
-    static int configured = -1; // dynamic shared memory the attribute was last set to
-    if (configured != p.smem_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
-        if (e != cudaSuccess) return e;
-        configured = p.smem_bytes;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = p.smem_bytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
 cudaError_t launch_step_f16(const StepParams &p, int tgf, int grid, cudaStream_t s)
 {
-    return tgf == 1 ? launch_tgf<1>(p, grid, s) : tgf == 2 ? launch_tgf<2>(p, grid, s) : launch_tgf<4>(p, grid, s);
-}
-
-cudaError_t occupancy_step_f16(int tgf, int smem_bytes, int *blocks)
-{
-    if (tgf == 1)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<__half, false, 1>, kThreads, smem_bytes);
-    if (tgf == 2)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<__half, false, 2>, kThreads, smem_bytes);
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_kernel<__half, false, 4>, kThreads, smem_bytes);
+    return launch_step<__half, false>(p, tgf, grid, s);
 }
 
 } // namespace pi

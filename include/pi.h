@@ -225,18 +225,23 @@ pi_status pi_sparse_ffn(pi_ctx *ctx, int32_t layer, const void *x_hat, int32_t B
  *    act_dtype PI_F16 or PI_BF16 for every tensor (no Q4_0 here);
  *    d_model in [8, 8192] and a multiple of 8, d_ffn in [1, 65536].
  * x_hat dev [B][d], idx/count dev int32 as for pi_sparse_ffn, y dev [B][d];
- * B in [1, 64] and SMs * B * d_model <= 2,063,360 (the partials of every SM
- * must fit the array: on a 152-SM GB300, B * d_model <= 13,574), else
- * PI_ERR_SHAPE.  Misaligned pointers give PI_ERR_ARG.
+ * B in [1, 64] and SMs * B * d_model <= 2,080,256 (the fp32 partials of
+ * every SM, 8 bytes each with their tag, must fit the array beside its
+ * 135,168 bytes of control words, descriptor and zeros: on a 152-SM GB300,
+ * B * d_model <= 13,685), else PI_ERR_SHAPE.  Misaligned pointers give
+ * PI_ERR_ARG.
  * dev_status: optional dev int32, set to 0, then to the first device-side
  * error (PI_ERR_DEVICE_FLAG for an index or count out of range,
  * PI_ERR_TIMEOUT); when NULL that word stays inside the array.
  * stream: cudaStream_t; the call runs on the current device.
- * The first call on a device resolves and clears the array (module load,
- * synchronous cudaMemset): make it before any stream capture.  Every call
- * shares the array and leaves its contents behind; calls whose kernels can
- * overlap on the GPU (other streams, other host threads) race on it, so
- * serialise them. */
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, which may load the module): make it before any
+ * stream capture.  Every call shares the array and leaves its contents
+ * behind: each call clears what must start at zero (its status words, on
+ * `stream`) and tags its partials with a new epoch; once in about four
+ * billion calls the tags are cleared on `stream` first.  Calls whose kernels
+ * can overlap on the GPU (other streams, other host threads) race on the
+ * array, so serialise them. */
 typedef struct {
     int32_t d_model, d_ffn;
     int32_t act;       /* pi_act */

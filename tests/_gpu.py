@@ -67,15 +67,17 @@ def predict_checked(c: pi.Context, slot: int, layer_host: dict, xhat: np.ndarray
 
 
 def tc_error_bound(layer: dict, xhat: np.ndarray, idx) -> np.ndarray:
-    """Per-output bound on the tensor-core FFN's error, from its arithmetic.
+    """Per-output bound on the tensor-core FFN's error, from its arithmetic
+    (an extra check beside the max relative error of 1e-2).
 
-    The path rounds every activation to the weights' 16-bit type before the
-    down-projection (a 16-bit tensor-core product takes both operands in one
-    type) and rounds y to the 16-bit type.  With u the type's unit roundoff
-    (2^-8 bf16, 2^-11 f16) and M_j = sum_i |a_i| |W_down[j, i]|:
-    |y_tc - y| <= u * M_j + u * |y_j| + g * M_j, where g = (m + d) 2^-23
-    covers the fp32 sums of the up-projection (d terms, entering a squared
-    activation at most twice) and of the down-projection (m terms)."""
+    The path passes every activation to the down-projection as two parts in
+    the weights' 16-bit type, hi = round(a) and lo = round(a - hi) (a 16-bit
+    tensor-core product takes both operands in one type), so a reaches it
+    within u^2 |a|, and rounds y to the 16-bit type.  With u the type's unit
+    roundoff (2^-8 bf16, 2^-11 f16) and M_j = sum_i |a_i| |W_down[j, i]|:
+    |y_tc - y| <= 2 u^2 M_j + u |y_j| + g M_j, where g = (m + d) 2^-23 covers
+    the fp32 sums of the up-projection (d terms, entering a squared
+    activation at most twice) and of the down-projection (2 m terms)."""
     from tests._helpers import layer_dense_f64
     u = 2.0 ** -8 if layer["act_dtype"] == W.BF16 else 2.0 ** -11
     a = O.ffn_act(layer["w_up"], layer.get("w_gate"), layer["b"], xhat, layer["act"], layer["w_dtype"],
@@ -84,8 +86,8 @@ def tc_error_bound(layer: dict, xhat: np.ndarray, idx) -> np.ndarray:
     sel = np.asarray(idx, dtype=np.int64)
     mag = np.abs(a[:, sel]) @ np.abs(wd[:, sel]).T
     y = O.masked_ffn(layer, xhat, np.asarray(idx, dtype=np.int32))
-    g = (sel.size + layer["d"]) * 2.0 ** -23
-    return (u + g) * mag + u * np.abs(y) + 1e-6
+    g = (2 * sel.size + layer["d"]) * 2.0 ** -23
+    return (2 * u * u + g) * mag + u * np.abs(y) + 1e-6
 
 
 def ffn_checked(c: pi.Context, slot: int, layer_host: dict, xhat: np.ndarray, idx, cnt, oidx):

@@ -288,9 +288,11 @@ def test_predictor_hidden_layer_bit_exact(c64, name, path):
 @pytest.mark.parametrize("B", [8, 16, 40, 64])
 def test_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
     """Batches of several tokens run the FFN as a gather-GEMM on tcgen05 (A^T
-    rounded to the weights' 16-bit type between the two GEMMs); it must match
-    the oracle within the usual tolerance, and the CUDA-core path of the step
-    kernel on the same list within twice it."""
+    passed between the two GEMMs as hi and lo 16-bit parts); it must match
+    the oracle within the usual tolerance (and within the error bound of its
+    arithmetic, output by output), and the CUDA-core path of the step kernel
+    on the same list within twice the tolerance -- for every activation
+    family, the dense variant included."""
     t = G.torch()
     cfg, layer = _layer(name)
     c64.load_layer(0, layer)
@@ -307,6 +309,7 @@ def test_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
     oidx = np.sort(idx[:m].cpu().numpy())
     got = G.y_to_f64(y_tc, cfg.act_dtype)
     want = O.masked_ffn(layer, x, oidx)
+    assert max_rel_err(got, want) <= G.tol(layer)
     # within the error bound of the path's arithmetic, output by output
     assert np.all(np.abs(got - want) <= G.tc_error_bound(layer, x, oidx))
     assert max_rel_err(got, G.y_to_f64(y_cc, cfg.act_dtype)) <= 2 * G.tol(layer)
@@ -314,8 +317,9 @@ def test_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
     yd = c64.dense_ffn(0, xd)
     c64.check()
     every = np.arange(cfg.n)
-    assert np.all(np.abs(G.y_to_f64(yd, cfg.act_dtype) - O.masked_ffn(layer, x, every))
-                  <= G.tc_error_bound(layer, x, every))
+    got_d, want_d = G.y_to_f64(yd, cfg.act_dtype), O.masked_ffn(layer, x, every)
+    assert max_rel_err(got_d, want_d) <= G.tol(layer)
+    assert np.all(np.abs(got_d - want_d) <= G.tc_error_bound(layer, x, every))
 
 
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "ring_wrap", "opt_1layer"])
@@ -605,6 +609,66 @@ def test_timeout_is_reported_and_context_recovers():
     c.decode_step(again)
     c.check()
     assert t.equal(again, ref)  # deterministic and unaffected by the failed launch
+    c.close()
+
+
+def _until_timeout(run, c, tries=5):
+    """Run `run` (a call under a one-nanosecond wait limit) until a bounded
+    wait runs out; returns the last status."""
+    st = pi.PI_OK
+    for _ in range(tries):
+        run()
+        st = c.sync_status()
+        if st == pi.PI_ERR_TIMEOUT:
+            break
+    return st
+
+
+@pytest.mark.parametrize("call", ["sparse_ffn", "decode_step"])
+def test_layerwise_timeout_is_reported_and_next_call_is_unchanged(call):
+    """Eight tokens run layer by layer: the batched predictor's launches and
+    the tensor-core FFN (ffn_up_mma, ffn_down_mma).  With a wait limit of one
+    nanosecond every bounded wait that has to spin runs out: the call reports
+    PI_ERR_TIMEOUT, and every CTA lets its own bulk copies and MMAs finish
+    before it exits (the producers that stopped early complete the stages
+    they skipped).  The same call afterwards gives the clean result bit for
+    bit."""
+    t = G.torch()
+    cfg = CFGS["ring_wrap"]  # d 4096: 64 pipeline stages per row pass, waits are not instant
+    B, L = 8, 2
+    c = G.ctx(max_layers=L, max_batch=B)
+    for l in range(L):
+        c.load_layer(l, W.make_layer(cfg, l, 0, random_b1=True, random_bdown=True))
+    assert pi.pi_layerwise_min_batch(c.handle, 0) <= B
+    if call == "sparse_ffn":
+        x = G.dev16(W.xhat_inputs(cfg, B, 71))
+        idx, cnt = c.predict(0, x)
+        ref = c.sparse_ffn(0, x, idx, cnt)
+        c.check()
+        run = lambda: c.sparse_ffn(0, x, idx, cnt)  # noqa: E731
+        again = lambda: c.sparse_ffn(0, x, idx, cnt)  # noqa: E731
+    else:
+        x0 = t.from_numpy(W.decode_inputs(cfg, B, 72)).cuda()
+        ref = x0.clone()
+        c.decode_step(ref)
+        c.check()
+
+        def run():
+            c.decode_step(x0.clone())
+
+        def again():
+            y = x0.clone()
+            c.decode_step(y)
+            return y
+    pi.pi_debug_set_wait_limit(c.handle, 1)  # 1 ns
+    try:
+        st = _until_timeout(run, c)
+    finally:
+        pi.pi_debug_set_wait_limit(c.handle, 2_000_000_000)
+    assert st == pi.PI_ERR_TIMEOUT
+    got = again()
+    c.check()
+    assert t.equal(got, ref)
     c.close()
 
 

@@ -1,17 +1,20 @@
-"""The allocation-free sparse FFN entry point against the context-based one.
+"""The allocation-free sparse FFN entry point against the CPU oracle and the
+context-based entry point.
 
 pi_sparse_ffn_noalloc serves callers that may not allocate device memory
 (pre-allocated buffers only, a fixed memory budget, a server-owned pool): it
-keeps its scratch in a fixed array inside the library.  Here it must give the
-same output as pi_sparse_ffn (max relative error within 1e-2, the tolerance of
-the other parity tests) on two calls in a row, since every call reuses what
-the previous one left in that array.  This file is collected last so that a
-run stopping at its first failure has run everything else already."""
+keeps its scratch in a fixed array inside the library.  Here its output must
+match the oracle's masked FFN on the same list and the output of
+pi_sparse_ffn (max relative error within 1e-2, the tolerance of the other
+parity tests) on two calls in a row, since every call reuses what the
+previous one left in that array.  This file is collected last so that a run
+stopping at its first failure has run everything else already."""
 from __future__ import annotations
 
 import numpy as np
 import pytest
 
+import oracle as O
 from activation_sparse_decode_sigmoid_gb300 import pi
 from activation_sparse_decode_sigmoid_gb300 import workload as W
 from tests import _gpu as G
@@ -39,7 +42,7 @@ def _rows(layer: dict, keep: list) -> pi.pi_ffn_rows:
 
 
 @pytest.mark.parametrize("name", list(CFGS))
-def test_noalloc_matches_context_path_on_consecutive_calls(name):
+def test_noalloc_matches_oracle_and_context_path_on_consecutive_calls(name):
     t = G.torch()
     cfg = CFGS[name]
     layer = W.make_layer(cfg, 0, 0, random_bdown=True)
@@ -48,7 +51,8 @@ def test_noalloc_matches_context_path_on_consecutive_calls(name):
     keep: list = []
     rows = _rows(layer, keep)
     for call, B in enumerate((3, 1)):
-        x = G.dev16(W.xhat_inputs(cfg, B, 40 + call))
+        xh = W.xhat_inputs(cfg, B, 40 + call)
+        x = G.dev16(xh)
         idx, cnt = c.predict(0, x)
         y_ref = c.sparse_ffn(0, x, idx, cnt)
         c.check()
@@ -58,8 +62,12 @@ def test_noalloc_matches_context_path_on_consecutive_calls(name):
         assert rc == pi.PI_OK, rc
         t.cuda.synchronize()
         assert int(status.item()) == 0
-        err = max_rel_err(G.y_to_f64(y, cfg.act_dtype), G.y_to_f64(y_ref, cfg.act_dtype))
-        assert err <= 1e-2, f"call {call}: max rel err {err:.3g}"
+        got = G.y_to_f64(y, cfg.act_dtype)
+        oidx = np.sort(idx[: int(cnt.item())].cpu().numpy())
+        err_o = max_rel_err(got, O.masked_ffn(layer, xh, oidx))
+        assert err_o <= 1e-2, f"call {call}: max rel err vs the oracle {err_o:.3g}"
+        err = max_rel_err(got, G.y_to_f64(y_ref, cfg.act_dtype))
+        assert err <= 1e-2, f"call {call}: max rel err vs pi_sparse_ffn {err:.3g}"
     c.close()
 
 
