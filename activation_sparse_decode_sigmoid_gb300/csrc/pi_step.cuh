@@ -912,12 +912,28 @@ static __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8])
     f[0] = a.x, f[1] = a.y, f[2] = b.x, f[3] = b.y, f[4] = c.x, f[5] = c.y, f[6] = d.x, f[7] = d.y;
 }
 
-// 16 nibbles of a Q4_0 half-block (low nibbles if sh == 0, high if sh == 4) as q - 8
-static __device__ __forceinline__ void unpack_q4(const uint4 v, int sh, float (&f)[16])
+// 16 nibbles of a Q4_0 half-block (the low nibbles of its 16 bytes, or the
+// high ones) as q - 8, exactly, in eight f16 pairs: element e in half (e & 1)
+// of pair e / 2.  A byte permute puts bytes e and e + 1 in the two halves;
+// masking a nibble into the mantissa under the exponent of 1024 gives the f16
+// value 1024 + q (low nibble) or 1024 + 16 q (high nibble), and one f16-pair
+// add or fma takes that to q - 8 (every step is exact in f16).
+static __device__ __forceinline__ void q4_pairs(const uint4 v, bool high, uint32_t (&h)[8])
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int e = 0; e < 16; ++e) f[e] = (float)((int)((w[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8);
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t t = __byte_perm(w[i], 0u, j == 0 ? 0x4140u : 0x4342u); // bytes 4i+2j, 4i+2j+1
+            uint32_t m = (t & (high ? 0x00F000F0u : 0x000F000Fu)) | 0x64006400u;
+            __half2 x;
+            memcpy(&x, &m, 4);
+            x = high ? __hfma2(x, __float2half2_rn(0.0625f), __float2half2_rn(-72.f)) // (1024 + 16q)/16 - 72
+                     : __hsub2(x, __float2half2_rn(1032.f));                           // 1024 + q - 1032
+            memcpy(&h[2 * i + j], &x, 4);
+        }
+    }
 }
 
 // One warp: the dot products of one neuron's W_up row (at a) and, for ReGLU,
@@ -962,33 +978,31 @@ static __device__ __forceinline__ void row_dots(const LayerDev &L, uint32_t a, u
 #pragma unroll
         for (int t = 0; t < TGF; ++t) au[t] += bu[t], ag[t] += bg[t];
     } else {
+        // (Q4_0 layers take f16 activations: x_hat pairs and the q - 8 pairs
+        // meet in the mixed-precision fma, an exact product rounded once)
         const int nhb = d >> 4;
         for (int hb = lane; hb < nhb; hb += 32) {
-            const int blk = hb >> 1, sh = (hb & 1) * 4;
-            float qu[16], qg[16];
-            unpack_q4(ld_shared_v4(a + L.scB + blk * 16), sh, qu);
+            const int blk = hb >> 1;
+            const bool high = (hb & 1) != 0;
+            uint32_t qu[8], qg[8];
+            q4_pairs(ld_shared_v4(a + L.scB + blk * 16), high, qu);
             const float su = __half2float(__ushort_as_half(ld_shared_u16(a + blk * 2)));
             float sg = 0.f;
             if (REGLU) {
-                unpack_q4(ld_shared_v4(a + upB + L.scB + blk * 16), sh, qg);
+                q4_pairs(ld_shared_v4(a + upB + L.scB + blk * 16), high, qg);
                 sg = __half2float(__ushort_as_half(ld_shared_u16(a + upB + blk * 2)));
             }
 #pragma unroll
             for (int t = 0; t < TGF; ++t) {
                 if (t < nt) {
                     const uint32_t xb = xs + (uint32_t)(t * d + blk * 32 + (hb & 1) * 16) * 2;
-                    float x0[8], x1[8];
-                    unpack8<T>(ld_shared_v4(xb), x0);
-                    unpack8<T>(ld_shared_v4(xb + 16), x1);
+                    const uint4 x0 = ld_shared_v4(xb), x1 = ld_shared_v4(xb + 16);
+                    const uint32_t xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
                     float pu = 0.f, pg = 0.f;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        pu = fmaf(qu[e], x0[e], pu);
-                        pu = fmaf(qu[8 + e], x1[e], pu);
-                        if (REGLU) {
-                            pg = fmaf(qg[e], x0[e], pg);
-                            pg = fmaf(qg[8 + e], x1[e], pg);
-                        }
+                        pu = fma_pair<__half>(qu[e], xv[e], pu);
+                        if (REGLU) pg = fma_pair<__half>(qg[e], xv[e], pg);
                     }
                     au[t] = fmaf(su, pu, au[t]);
                     if (REGLU) ag[t] = fmaf(sg, pg, ag[t]);
@@ -1093,10 +1107,16 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
                     } else {
                         const int hb = tid;
                         if (hb < nhb) {
-                            const int blk = hb >> 1, sh = (hb & 1) * 4;
-                            float qf[16];
-                            unpack_q4(ld_shared_v4(dn + L.scB + blk * 16), sh, qf);
+                            const int blk = hb >> 1;
+                            uint32_t qh[8];
+                            q4_pairs(ld_shared_v4(dn + L.scB + blk * 16), (hb & 1) != 0, qh);
                             const float s = __half2float(__ushort_as_half(ld_shared_u16(dn + blk * 2)));
+                            float qf[16];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float2 f2 = F16T<__half>::pair(qh[e]);
+                                qf[2 * e] = f2.x, qf[2 * e + 1] = f2.y;
+                            }
 #pragma unroll
                             for (int t = 0; t < TGF; ++t) {
                                 const float as = a[t] * s;
