@@ -23,6 +23,7 @@ namespace {
 
 struct LayerSlot {
     bool loaded = false;
+    int shard = 0, nshards = 1; // neurons shard, shard + nshards, ... of the layer (pi_load_layer_shard)
     pi_layer_desc desc{};
     LayerDev dev{};
     std::vector<void *> bufs;
@@ -448,6 +449,14 @@ static pi_status q4_scratch(pi_ctx *c, int layer)
     return PI_OK;
 }
 
+// Load the neurons sel[0..nl) (host, original ids in [0, desc->d_ffn); NULL =
+// all of them in order, nl = d_ffn) into slot `layer`: physical neuron i of
+// the slot is original neuron sel[i].  The predictor's hidden layer (W1, b1)
+// is copied whole; W2 rows, b2, the FFN rows and their biases only for the
+// selected neurons; b_down when with_bdown, else zeros.
+static pi_status load_rows(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, const pi_layer_weights *w,
+                           const int32_t *sel, int nl, bool with_bdown);
+
 pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, const pi_layer_weights *w,
                         const int32_t *perm)
 {
@@ -455,9 +464,7 @@ pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, con
     if (layer < 0 || layer >= c->max_layers) return fail(c, PI_ERR_ARG, "layer %d outside [0, %d)", layer, c->max_layers);
     pi_status st = check_desc(c, desc);
     if (st) return st;
-    if (!w || !w->w_up || !w->w_down || !w->p_w1 || !w->p_w2) return fail(c, PI_ERR_ARG, "missing weight pointer");
-    if (desc->act == PI_REGLU && !w->w_gate) return fail(c, PI_ERR_ARG, "ReGLU needs w_gate");
-    const int d = desc->d_model, n = desc->d_ffn, r = desc->rank;
+    const int n = desc->d_ffn;
     if (perm) {
         std::vector<char> seen(n, 0);
         for (int i = 0; i < n; ++i) {
@@ -465,6 +472,42 @@ pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, con
             seen[perm[i]] = 1;
         }
     }
+    st = load_rows(c, layer, desc, w, perm, n, true);
+    if (!st) c->layers[layer].shard = 0, c->layers[layer].nshards = 1;
+    return st;
+}
+
+pi_status pi_load_layer_shard(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, const pi_layer_weights *w,
+                              const int32_t *perm, int32_t shard, int32_t nshards)
+{
+    if (!c) return PI_ERR_ARG;
+    if (layer < 0 || layer >= c->max_layers) return fail(c, PI_ERR_ARG, "layer %d outside [0, %d)", layer, c->max_layers);
+    pi_status st = check_desc(c, desc);
+    if (st) return st;
+    const int n = desc->d_ffn;
+    if (nshards < 1 || shard < 0 || shard >= nshards || nshards > n)
+        return fail(c, PI_ERR_ARG, "shard %d of %d invalid for %d neurons", shard, nshards, n);
+    std::vector<int32_t> sel;
+    for (int i = shard; i < n; i += nshards) sel.push_back(perm ? perm[i] : i);
+    if (perm) {
+        std::vector<char> seen(n, 0);
+        for (int i = 0; i < n; ++i) {
+            if (perm[i] < 0 || perm[i] >= n || seen[perm[i]]) return fail(c, PI_ERR_ARG, "perm is not a permutation of 0..%d", n - 1);
+            seen[perm[i]] = 1;
+        }
+    }
+    st = load_rows(c, layer, desc, w, sel.data(), (int)sel.size(), shard == 0);
+    if (!st) c->layers[layer].shard = shard, c->layers[layer].nshards = nshards;
+    return st;
+}
+
+static pi_status load_rows(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, const pi_layer_weights *w,
+                           const int32_t *perm, int nl, bool with_bdown)
+{
+    if (!w || !w->w_up || !w->w_down || !w->p_w1 || !w->p_w2) return fail(c, PI_ERR_ARG, "missing weight pointer");
+    if (desc->act == PI_REGLU && !w->w_gate) return fail(c, PI_ERR_ARG, "ReGLU needs w_gate");
+    const int d = desc->d_model, nsrc = desc->d_ffn, r = desc->rank;
+    const int n = nl; // neurons held by the slot
     DeviceGuard g(c->device);
     CU(cudaStreamSynchronize(c->stream));
     LayerSlot &s = c->layers[layer];
@@ -530,15 +573,15 @@ pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, con
     const void *s_up, *s_gate, *s_b, *s_dn, *s_bd, *s_w1, *s_b1, *s_w2, *s_b2;
     int32_t *dperm = nullptr;
     pi_status rc = PI_OK;
-    if (!rc) rc = src(w->w_up, n * srcRow, &s_up);
-    if (!rc) rc = src(w->w_gate, n * srcRow, &s_gate);
-    if (!rc) rc = src(w->b, (size_t)n * 2, &s_b);
-    if (!rc) rc = src(w->w_down, q4 ? n * srcRow : (size_t)d * n * 2, &s_dn);
-    if (!rc) rc = src(w->b_down, (size_t)d * 2, &s_bd);
+    if (!rc) rc = src(w->w_up, nsrc * srcRow, &s_up);
+    if (!rc) rc = src(w->w_gate, nsrc * srcRow, &s_gate);
+    if (!rc) rc = src(w->b, (size_t)nsrc * 2, &s_b);
+    if (!rc) rc = src(w->w_down, q4 ? nsrc * srcRow : (size_t)d * nsrc * 2, &s_dn);
+    if (!rc) rc = src(with_bdown ? w->b_down : nullptr, (size_t)d * 2, &s_bd);
     if (!rc) rc = src(w->p_w1, (size_t)r * d * 2, &s_w1);
     if (!rc) rc = src(w->p_b1, (size_t)r * 2, &s_b1);
-    if (!rc) rc = src(w->p_w2, (size_t)n * r * 2, &s_w2);
-    if (!rc) rc = src(w->p_b2, (size_t)n * 2, &s_b2);
+    if (!rc) rc = src(w->p_w2, (size_t)nsrc * r * 2, &s_w2);
+    if (!rc) rc = src(w->p_b2, (size_t)nsrc * 2, &s_b2);
     if (!rc && perm) {
         cudaError_t e = cudaMalloc((void **)&dperm, (size_t)n * 4);
         if (e == cudaSuccess) {
@@ -560,7 +603,7 @@ pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, con
         } else {
             chk(pi::launch_permute_rows(s_up, pup, dperm, n, (size_t)rowB, st0, (size_t)rowB + 16));
             if (reglu) chk(pi::launch_permute_rows(s_gate, pgate, dperm, n, (size_t)rowB, st0));
-            chk(pi::launch_transpose_permute16((const uint16_t *)s_dn, (uint16_t *)pdn, dperm, d, n, st0));
+            chk(pi::launch_transpose_permute16((const uint16_t *)s_dn, (uint16_t *)pdn, dperm, d, n, nsrc, st0));
         }
         if (s_b) chk(pi::launch_permute16((const uint16_t *)s_b, (uint16_t *)pb, dperm, n, st0));
         else chk(cudaMemsetAsync(pb, 0, (size_t)n * 2, st0));
@@ -596,6 +639,7 @@ pi_status pi_load_layer(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, con
         return fail(c, PI_ERR_CUDA, "layer table: %s", cudaGetErrorString(e));
     }
     s.desc = *desc;
+    s.desc.d_ffn = n; // the neurons this slot holds
     s.loaded = true;
     s.maps = false;
     if (q4 && c->max_batch >= 2) return q4_scratch(c, layer); // batches reach the tensor cores dequantised
@@ -956,6 +1000,86 @@ pi_status pi_decode_step_host(pi_ctx *c, const float *x_in, float *x_out, int32_
 pi_status pi_dense_step(pi_ctx *c, float *x, int32_t B)
 {
     return step_common(c, x, B, pi::M_RMSNORM | pi::M_DENSE | pi::M_FFN | pi::M_RESID);
+}
+
+pi_status pi_layer_partial(pi_ctx *c, int32_t layer, const float *x, int32_t B, float *u)
+{
+    if (!c) return PI_ERR_ARG;
+    pi_status st = check_layer(c, layer);
+    if (!st) st = check_batch(c, B);
+    if (st) return st;
+    if (!x || !u) return fail(c, PI_ERR_ARG, "x/u NULL");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(u)) & 15u)
+        return fail(c, PI_ERR_ARG, "x and u must be 16-byte aligned");
+    DeviceGuard g(c->device);
+    const pi_layer_desc &dsc = c->layers[layer].desc;
+    const int d = dsc.d_model;
+    const bool bf16 = dsc.act_dtype == PI_BF16;
+    if (!use_pred_batch(c, layer, B)) {
+        // one persistent launch: RMSNorm, predictor, list, FFN, merge into u
+        StepParams p{};
+        p.x = const_cast<float *>(x); // (read only: M_RESID is not set)
+        p.yf_out = u;
+        p.tr_x = c->tr_x;
+        p.tr_xhat = (uint16_t *)c->tr_xhat;
+        p.tr_idx = c->tr_idx;
+        p.tr_cnt = c->tr_cnt;
+        p.tr_n = dsc.d_ffn;
+        return launch(c, layer, 1, B, pi::M_RMSNORM | pi::M_PREDICT | pi::M_FFN | pi::M_YF32, p);
+    }
+    // layer by layer: RMSNorm, the batched predictor, then the FFN adds into u = 0
+    pi::PredParams q = pred_params(c, layer, B);
+    q.x = x;
+    q.tr_x = c->tr_x;
+    q.xhat = c->xhat_ws;
+    q.idx = c->lidx;
+    q.count = c->lidx + pi::kMaxN;
+    q.tr_idx = c->tr_idx;
+    q.tr_cnt = c->tr_cnt;
+    cudaError_t e = pi::launch_rmsnorm_rows(q, bf16, c->stream);
+    if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "RMSNorm launch: %s", cudaGetErrorString(e));
+    st = pred_batch(c, q, layer);
+    if (st) return st;
+    if (c->tr_xhat) {
+        e = cudaMemcpyAsync(c->tr_xhat, c->xhat_ws, (size_t)B * d * 2, cudaMemcpyDeviceToDevice, c->stream);
+        if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "x_hat trace: %s", cudaGetErrorString(e));
+    }
+    e = cudaMemsetAsync(u, 0, sizeof(float) * (size_t)B * d, c->stream);
+    if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "update clear: %s", cudaGetErrorString(e));
+    if (use_mma(c, layer, B)) return mma_ffn(c, layer, c->xhat_ws, B, c->lidx, c->lidx + pi::kMaxN, nullptr, u);
+    StepParams f{};
+    f.x = u;
+    f.xhat_in = c->xhat_ws;
+    f.idx_in = c->lidx;
+    f.count_in = c->lidx + pi::kMaxN;
+    return launch(c, layer, 1, B, pi::M_IDX_IN | pi::M_FFN | pi::M_RESID, f);
+}
+
+pi_status pi_residual_add(pi_ctx *c, float *x, const float *u, int32_t B)
+{
+    if (!c) return PI_ERR_ARG;
+    pi_status st = check_batch(c, B);
+    if (st) return st;
+    if (!x || !u) return fail(c, PI_ERR_ARG, "x/u NULL");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(u)) & 15u)
+        return fail(c, PI_ERR_ARG, "x and u must be 16-byte aligned");
+    int L = 0;
+    st = stack_layers(c, &L);
+    if (st) return st;
+    DeviceGuard g(c->device);
+    const cudaError_t e = pi::launch_residual_add(x, u, (size_t)B * c->layers[0].desc.d_model, c->stream);
+    return e == cudaSuccess ? PI_OK : fail(c, PI_ERR_CUDA, "residual add: %s", cudaGetErrorString(e));
+}
+
+pi_status pi_layer_shard(pi_ctx *c, int32_t layer, int32_t *shard, int32_t *nshards)
+{
+    if (!c) return PI_ERR_ARG;
+    pi_status st = check_layer(c, layer);
+    if (st) return st;
+    if (!shard || !nshards) return fail(c, PI_ERR_ARG, "shard/nshards NULL");
+    *shard = c->layers[layer].shard;
+    *nshards = c->layers[layer].nshards;
+    return PI_OK;
 }
 
 pi_status pi_set_trace(pi_ctx *c, float *x_trace, void *xhat_trace, int32_t *idx_trace, int32_t *count_trace)

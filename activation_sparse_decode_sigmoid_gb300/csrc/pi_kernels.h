@@ -42,6 +42,7 @@ enum : int {
     M_RESID = 32,    // merge into the fp32 residual x (else write y)
     M_COUNTS = 64,   // predictor: per-neuron selection counts over the tokens
     M_COMPACT = 128, // predictor: write the ascending idx list + count
+    M_YF32 = 256,    // merge: write the fp32 update to yf_out (x is only read, by the RMSNorm)
 };
 
 struct LayerDev {
@@ -75,6 +76,7 @@ struct StepParams {
     int32_t *count_out;
     uint16_t *y_out;        // [B][d]
     int32_t *counts_out;    // [n]
+    float *yf_out;          // [B][d] fp32 layer update (mode M_YF32: written instead of added into x)
     // workspace
     // Cross-SM exchanges that need no grid barrier: every 64-bit word holds
     // a value (low half) and the epoch of the layer that wrote it (high
@@ -265,7 +267,8 @@ cudaError_t launch_permute_rows(const void *src, void *dst, const int32_t *perm,
                                 cudaStream_t s, size_t dstStride = 0);
 cudaError_t launch_bias_tail(const uint16_t *b, uint8_t *up, int n, size_t rowB, size_t upB, cudaStream_t s);
 cudaError_t launch_transpose_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int d, int n,
-                                       cudaStream_t s);
+                                       int nsrc, cudaStream_t s);
+cudaError_t launch_residual_add(float *x, const float *u, size_t n, cudaStream_t s);
 cudaError_t launch_q4_split(const uint8_t *src, uint8_t *dst, const int32_t *perm, int n, int d, int scB,
                             cudaStream_t s, size_t dstStride = 0);
 cudaError_t launch_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int n, cudaStream_t s);

@@ -27,10 +27,11 @@ __global__ void permute_rows_kernel(const uint4 *__restrict__ src, uint4 *__rest
     }
 }
 
-// dst [n][d] (row i = physical neuron i) from src [d][n] (column o = original
-// neuron o): dst[i][j] = src[j][perm[i]].  32x32 tiles through shared memory.
+// dst [n][d] (row i = physical neuron i) from src [d][nsrc] (column o =
+// original neuron o): dst[i][j] = src[j][perm[i]] (n = nsrc, or fewer rows
+// for a shard of the neurons).  32x32 tiles through shared memory.
 __global__ void transpose_permute16_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
-                                           const int32_t *__restrict__ perm, int d, int n)
+                                           const int32_t *__restrict__ perm, int d, int n, int nsrc)
 {
     __shared__ uint16_t tile[32][33];
     const int i0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
@@ -39,7 +40,7 @@ __global__ void transpose_permute16_kernel(const uint16_t *__restrict__ src, uin
         const int i = i0 + tx, j = j0 + yy;
         if (i < n && j < d) {
             const int o = perm ? perm[i] : i;
-            tile[yy][tx] = src[(size_t)j * n + o];
+            tile[yy][tx] = src[(size_t)j * nsrc + o];
         }
     }
     __syncthreads();
@@ -106,10 +107,10 @@ cudaError_t launch_bias_tail(const uint16_t *b, uint8_t *up, int n, size_t rowB,
 }
 
 cudaError_t launch_transpose_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int d, int n,
-                                       cudaStream_t s)
+                                       int nsrc, cudaStream_t s)
 {
     dim3 grid((n + 31) / 32, (d + 31) / 32), block(32, 8);
-    transpose_permute16_kernel<<<grid, block, 0, s>>>(src, dst, perm, d, n);
+    transpose_permute16_kernel<<<grid, block, 0, s>>>(src, dst, perm, d, n, nsrc);
     return cudaGetLastError();
 }
 
@@ -177,6 +178,30 @@ cudaError_t launch_q4_to_f16_rows(const LayerDev &L, const LayerDev &to, const i
                                   int *status, int *abort_flag, cudaStream_t s)
 {
     return launch_pdl(q4_to_f16_rows_kernel, dim3(4 * 152), dim3(256), 0, s, L, to, idx, count, status, abort_flag);
+}
+
+// x[i] += u[i], i < n (fp32): a layer's update, reduced over the shards of a
+// neuron-sharded layer, added into the residual stream
+__global__ void residual_add_kernel(float *__restrict__ x, const float *__restrict__ u, size_t n)
+{
+    const size_t n4 = n / 4;
+    float4 *x4 = reinterpret_cast<float4 *>(x);
+    const float4 *u4 = reinterpret_cast<const float4 *>(u);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        float4 a = x4[i];
+        const float4 b = u4[i];
+        a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
+        x4[i] = a;
+    }
+    for (size_t i = 4 * n4 + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        x[i] += u[i];
+}
+
+cudaError_t launch_residual_add(float *x, const float *u, size_t n, cudaStream_t s)
+{
+    const size_t blocks = (n / 4 + 255) / 256;
+    residual_add_kernel<<<(unsigned)(blocks < 1 ? 1 : (blocks > 1024 ? 1024 : blocks)), 256, 0, s>>>(x, u, n);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int n, cudaStream_t s)

@@ -1285,6 +1285,8 @@ static __device__ void phase_d(const StepParams &p, const Shm &S, const LayerDev
                     st_tagged2(p.xx + 4 * (size_t)u, ep, __float_as_uint(xv.x), __float_as_uint(xv.y));
                     st_tagged2(p.xx + 4 * (size_t)u + 2, ep, __float_as_uint(xv.z), __float_as_uint(xv.w));
                 }
+            } else if (p.mode & M_YF32) {
+                reinterpret_cast<float4 *>(p.yf_out)[u] = acc;
             } else {
                 const uint32_t lo = (uint32_t)F::round(acc.x) | ((uint32_t)F::round(acc.y) << 16);
                 const uint32_t hi = (uint32_t)F::round(acc.z) | ((uint32_t)F::round(acc.w) << 16);

@@ -33,7 +33,8 @@ EXPORTS = ("pi_create", "pi_destroy", "pi_set_stream", "pi_load_layer", "pi_laye
            "pi_debug_set_wait_limit", "pi_debug_barrier_extra", "pi_debug_set_timeline",
            "pi_debug_set_tuning", "pi_debug_copy_hidden", "pi_debug_set_mma_min_batch",
            "pi_sparse_ffn_noalloc", "pi_set_hot_prefix", "pi_hot_prefix_crossover", "pi_choose_hot_prefix",
-           "pi_layerwise_min_batch")
+           "pi_layerwise_min_batch", "pi_load_layer_shard", "pi_layer_shard", "pi_layer_partial",
+           "pi_residual_add")
 
 
 class PiError(RuntimeError):
@@ -100,6 +101,11 @@ def load_library(path: str = LIB_PATH):
         "pi_layerwise_min_batch": (st, [P, I32, P]),
         "pi_hot_prefix_crossover": (st, [P, I32, I32, I32, ctypes.c_double, ctypes.c_double, P]),
         "pi_choose_hot_prefix": (st, [P, I32, P, I32, I32, P]),
+        "pi_load_layer_shard": (st, [P, I32, ctypes.POINTER(pi_layer_desc), ctypes.POINTER(pi_layer_weights), P,
+                                     I32, I32]),
+        "pi_layer_shard": (st, [P, I32, P, P]),
+        "pi_layer_partial": (st, [P, I32, P, I32, P]),
+        "pi_residual_add": (st, [P, P, P, I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -150,6 +156,28 @@ def pi_load_layer(ctx: int, layer: int, desc: pi_layer_desc, weights: pi_layer_w
     perm_arr = None if perm is None else np.ascontiguousarray(perm, dtype=np.int32)
     rc = load_library().pi_load_layer(ctx, layer, ctypes.byref(desc), ctypes.byref(weights), _ptr(perm_arr))
     _check(ctx, rc, "pi_load_layer")
+
+
+def pi_load_layer_shard(ctx: int, layer: int, desc: pi_layer_desc, weights: pi_layer_weights, perm, shard: int,
+                        nshards: int) -> None:
+    perm_arr = None if perm is None else np.ascontiguousarray(perm, dtype=np.int32)
+    rc = load_library().pi_load_layer_shard(ctx, layer, ctypes.byref(desc), ctypes.byref(weights), _ptr(perm_arr),
+                                            shard, nshards)
+    _check(ctx, rc, "pi_load_layer_shard")
+
+
+def pi_layer_shard(ctx: int, layer: int) -> tuple[int, int]:
+    v = np.zeros(2, np.int32)
+    _check(ctx, load_library().pi_layer_shard(ctx, layer, _ptr(v[0:1]), _ptr(v[1:2])), "pi_layer_shard")
+    return int(v[0]), int(v[1])
+
+
+def pi_layer_partial(ctx: int, layer: int, x, B: int, u) -> None:
+    _check(ctx, load_library().pi_layer_partial(ctx, layer, _ptr(x), B, _ptr(u)), "pi_layer_partial")
+
+
+def pi_residual_add(ctx: int, x, u, B: int) -> None:
+    _check(ctx, load_library().pi_residual_add(ctx, _ptr(x), _ptr(u), B), "pi_residual_add")
 
 
 def pi_layer_counts(ctx: int, layer: int, x_hat, T: int, counts) -> None:
@@ -309,6 +337,15 @@ class Context:
     def load_layer(self, layer: int, lw: dict, perm=None) -> None:
         """Load a layer dict as drawn by ``workload.make_layer`` (numpy, host)
         or ``workload.make_layer_device`` (torch, device)."""
+        desc, w, keep = self._weights(lw)
+        self._s()
+        pi_load_layer(self.handle, layer, desc, w, perm)
+        self.descs[layer] = desc
+        self.hot[layer] = 0
+        del keep
+
+    def _weights(self, lw: dict):
+        """(descriptor, weight pointers, the buffers they point into) of a layer dict."""
         desc = pi_layer_desc(lw["d"], lw["n"], lw["r"], lw["act"], lw["w_dtype"], lw["act_dtype"])
         keys = ("w_up", "w_gate", "b", "w_down", "b_down", "p_w1", "p_b1", "p_w2", "p_b2")
         vals = [lw.get(k) for k in keys]
@@ -330,10 +367,32 @@ class Context:
             keep.append(v)
             ptrs.append(_ptr(v))
         w = pi_layer_weights(*ptrs, 1 if on_dev else 0)
+        return desc, w, keep
+
+    def load_layer_shard(self, layer: int, lw: dict, shard: int, nshards: int, perm=None) -> None:
+        """Load shard `shard` of `nshards` of a layer dict (its physical
+        neurons shard, shard + nshards, ...)."""
+        desc, w, keep = self._weights(lw)
         self._s()
-        pi_load_layer(self.handle, layer, desc, w, perm)
+        pi_load_layer_shard(self.handle, layer, desc, w, perm, shard, nshards)
+        n = lw["n"]
+        desc.d_ffn = (n - shard + nshards - 1) // nshards
         self.descs[layer] = desc
         self.hot[layer] = 0
+        del keep
+
+    def layer_partial(self, layer: int, x, u=None):
+        """The layer's fp32 update of the residual x ([B][d]), not added."""
+        import torch
+        if u is None:
+            u = torch.empty_like(x)
+        self._s()
+        pi_layer_partial(self.handle, layer, x, x.shape[0], u)
+        return u
+
+    def residual_add(self, x, u) -> None:
+        self._s()
+        pi_residual_add(self.handle, x, u, x.shape[0])
 
     def layer_counts(self, layer: int, x_hat):
         import torch

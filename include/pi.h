@@ -133,6 +133,45 @@ pi_status pi_set_stream(pi_ctx *ctx, void *stream);
 pi_status pi_load_layer(pi_ctx *ctx, int32_t layer, const pi_layer_desc *desc,
                         const pi_layer_weights *w, const int32_t *perm);
 
+/* Neuron-sharded layer, for splitting one layer's neurons over several GPUs
+ * (multi-GPU support is listed as future work on the de.news.hada.io
+ * summary, "Jüngste Updates und Pläne").  Like pi_load_layer, but slot
+ * `layer` keeps only the neurons of shard `shard` of `nshards`, round-robin
+ * over the physical order: physical neuron i (after `perm`) belongs to shard
+ * i mod nshards, so every shard gets the same mix of hot and cold neurons.
+ * The slot holds the whole predictor hidden layer (W1, b1: every shard
+ * computes h), the W2 rows and b2 of its neurons, their FFN rows and biases,
+ * and b_down on shard 0 only (zeros elsewhere), so that the shards' updates
+ * add up to the unsplit layer's.  Local neuron j of the slot is physical
+ * neuron shard + j * nshards; lists of the slot (pi_predict, traces) hold
+ * local ids, and its d_ffn is the number of neurons it holds.  The other
+ * rules (arguments, ownership, errors) are pi_load_layer's; PI_ERR_ARG for
+ * nshards < 1, shard outside [0, nshards) or nshards > d_ffn. */
+pi_status pi_load_layer_shard(pi_ctx *ctx, int32_t layer, const pi_layer_desc *desc, const pi_layer_weights *w,
+                              const int32_t *perm, int32_t shard, int32_t nshards);
+
+/* *shard, *nshards of slot `layer` (0 and 1 for a layer loaded whole). */
+pi_status pi_layer_shard(pi_ctx *ctx, int32_t layer, int32_t *shard, int32_t *nshards);
+
+/* One layer's update of the residual stream, written instead of added
+ * (the merge step of the "CPU/GPU混合推理设计" section, left to the caller
+ * when the layer is split over devices): for x (dev fp32 [B][d], read only)
+ *   x_hat = act_dtype(x / sqrt(mean(x^2) + 1e-5)),
+ *   list  = the predicted union over the B tokens (as pi_predict),
+ *   u     = sparse FFN of x_hat on the list, in fp32 (as pi_sparse_ffn)
+ * into u (dev fp32 [B][d]).  For a shard layer, u is the shard's part: the
+ * sum of u over the shards equals the unsplit layer's update, so a caller
+ * that reduces u over its devices (one all-reduce of B * d floats per layer)
+ * and adds it with pi_residual_add takes the same step as pi_decode_step.
+ * x and u 16-byte aligned.  The trace set by pi_set_trace, if any, gets this
+ * layer's x, x_hat, list and count in its slot 0. */
+pi_status pi_layer_partial(pi_ctx *ctx, int32_t layer, const float *x, int32_t B, float *u);
+
+/* x += u, element by element in fp32, for B tokens of the stack's d_model
+ * (x, u dev fp32 [B][d], 16-byte aligned): adds a reduced layer update from
+ * pi_layer_partial into the residual stream. */
+pi_status pi_residual_add(pi_ctx *ctx, float *x, const float *u, int32_t B);
+
 /* Offline activation profile ("稀疏激活带来的推理局部性": count how often
  * each neuron is activated over general inputs).  For T calibration inputs
  * x_hat (dev [T][d], act_dtype), counts[i] (dev int32 [n]) is set to the
