@@ -57,8 +57,8 @@ struct Shm {
     unsigned *swords; // [wcap] predicted-mask words of this CTA's rows
     uint16_t *pb1s, *pb2s; // this CTA's b1 / b2 slices, as copied (16-byte-rounded ranges)
     uint64_t *bias_full;   // completes when a layer's bias slices have landed
-    uint64_t *act_full;    // [nsd] completes when a stage's owner warp has written its activations
-    float *red;     // [2][warps][kMaxNeuronsPerStage][TGF][2] cross-warp dot sums
+    uint64_t *act_full;    // [nsd] completes when a stage's P owner warps have written their partial sums
+    float *red;     // partial dot sums of the FFN stages: [nsd][kMaxNeuronsPerStage][P][TGF][2] (nsd * P <= 16)
 };
 
 enum { INFO_FLAG = 0, INFO_NCNT = 1, INFO_FAIL = 2, INFO_M = 3, INFO_REGION = 4 };
@@ -893,14 +893,19 @@ static __device__ bool resolve_list(const StepParams &p, const Shm &S, const Lay
 
 // ------------------------------------------------------------------ phase C: gather FFN
 // The ring delivers stages (npd whole neurons each) in list order.  Stage k
-// has an owner warp, k mod 16, which computes the dot products of its
-// neurons over the whole row (W_up, W_gate) and the activations, writes them
-// to shared memory and arrives on the stage's act_full barrier; no other warp
-// takes part, so there is no cross-warp reduction and no CTA barrier per
-// stage.  Every warp then adds the stage's down-projection rows into the
-// output columns its threads own and releases the stage (empty_d counts the
-// 16 warps).  Owners compute ahead, up to `ahead` stages past the stage
-// being merged, on stages that have already landed.
+// is owned by a group of P warps (P = 4, 2 or 1 for rings of up to 4, 8 or 16
+// stages), group k mod (16 / P); each of them computes its slice of the
+// dot products of the stage's neurons over the rows (W_up, W_gate), writes
+// the partial sums to shared memory and arrives on the stage's act_full
+// barrier (P arrivals); no other warp takes part, so there is no cross-warp
+// reduction and no CTA barrier per stage.  Every warp then forms the
+// activations from the P partial sums (in part order), adds the stage's
+// down-projection rows into the output columns its threads own and releases
+// the stage (empty_d counts the 16 warps).  Owners compute ahead, up to
+// `ahead` stages past the stage being merged, on stages that have already
+// landed.  With few stages of big neurons one warp's pass over a whole row
+// was the longest step of a stage's turn (1.8 us for a LLaMA-70B-shaped
+// ReGLU neuron), and owners busy with it delayed every stage's release.
 // Output columns of thread `tid`: 16-bit rows -> chunks of 8 columns ch = tid
 // and tid + 512 (kYSlots = 16 columns); Q4_0 -> half-block hb = tid (16
 // columns of block hb/2).
@@ -936,23 +941,29 @@ static __device__ __forceinline__ void q4_pairs(const uint4 v, bool high, uint32
     }
 }
 
-// One warp: the dot products of one neuron's W_up row (at a) and, for ReGLU,
-// its W_gate row (at a + upB) with the nt tokens' x_hat in xs (16-bit [t][d]),
-// over the whole row; full sums in every lane.
+// Warps that share the dot products of one stage: with few ring stages (big
+// neurons) one warp's pass over a whole row is the longest step of a stage's
+// turn, so the rows are split between P warps, each taking a contiguous
+// slice of every row; the stage's act_full barrier counts their P arrivals.
+static __device__ __forceinline__ int owner_parts(int nsd) { return nsd <= 4 ? 4 : (nsd <= 8 ? 2 : 1); }
+
+// One warp: its slice [c0, c1) (16-bit: chunks of 8 elements; Q4_0:
+// half-blocks of 16) of the dot products of one neuron's W_up row (at a)
+// and, for ReGLU, its W_gate row (at a + upB) with the nt tokens' x_hat in xs
+// (16-bit [t][d]); the slice's sums in every lane.
 template <typename T, bool Q4, int TGF, bool REGLU>
 static __device__ __forceinline__ void row_dots(const LayerDev &L, uint32_t a, uint32_t upB, uint32_t xs, int d,
-                                                int nt, int lane, float (&au)[TGF], float (&ag)[TGF])
+                                                int nt, int lane, int c0, int c1, float (&au)[TGF], float (&ag)[TGF])
 {
 #pragma unroll
     for (int t = 0; t < TGF; ++t) au[t] = ag[t] = 0.f;
     if constexpr (!Q4) {
-        const int nch = d >> 3;
         // two chains per token (alternate chunks) halve the dependent fma run
         float bu[TGF], bg[TGF];
 #pragma unroll
         for (int t = 0; t < TGF; ++t) bu[t] = bg[t] = 0.f;
-        for (int ch = lane; ch < nch; ch += 64) {
-            const bool two = ch + 32 < nch;
+        for (int ch = c0 + lane; ch < c1; ch += 64) {
+            const bool two = ch + 32 < c1;
             const uint4 w0 = ld_shared_v4(a + (uint32_t)ch * 16);
             const uint4 w1 = two ? ld_shared_v4(a + (uint32_t)(ch + 32) * 16) : make_uint4(0, 0, 0, 0);
             uint4 g0 = make_uint4(0, 0, 0, 0), g1 = make_uint4(0, 0, 0, 0);
@@ -980,8 +991,7 @@ static __device__ __forceinline__ void row_dots(const LayerDev &L, uint32_t a, u
     } else {
         // (Q4_0 layers take f16 activations: x_hat pairs and the q - 8 pairs
         // meet in the mixed-precision fma, an exact product rounded once)
-        const int nhb = d >> 4;
-        for (int hb = lane; hb < nhb; hb += 32) {
+        for (int hb = c0 + lane; hb < c1; hb += 32) {
             const int blk = hb >> 1;
             const bool high = (hb & 1) != 0;
             uint32_t qu[8], qg[8];
@@ -1037,7 +1047,16 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
     const uint32_t dnoff = upB + (REGLU ? rowB : 0u); // offset of the W_down^T row
     const uint32_t ring = smem_u32(S.ring);
     const uint32_t xs = smem_u32(S.xs);
-    float *act = S.red; // [nsd][kMaxNeuronsPerStage][TGF] activations of the stages in the ring
+    const int P = owner_parts(p.nsd);  // warps sharing a stage's dot products
+    const int G16 = kConsumerWarps / P; // owner groups: group g owns stages g, g + G16, ...
+    const int part = warp % P;
+    const int units = Q4 ? nhb : nch;  // this warp's slice of every row it computes
+    const int c0 = units * part / P, c1 = units * (part + 1) / P;
+    // [nsd][kMaxNeuronsPerStage][P][TGF][2] partial dot sums (up, gate) of the stages in the ring
+    float *red = S.red;
+    const auto red_at = [&](uint32_t os, int j, int q, int t) {
+        return red + ((((int)os * kMaxNeuronsPerStage + j) * P + q) * TGF + t) * 2;
+    };
     bool ok = true;
     for (int g = 0; g < ngf; ++g) {
         const int t0 = g * p.tg, nt = min(p.tg, p.B - t0);
@@ -1050,9 +1069,9 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
             for (int e = 0; e < kYSlots; ++e) y[t][e] = 0.f;
 
         uint32_t slot = sd % p.nsd, par = (sd / p.nsd) & 1; // ring position of stage k
-        int own = warp;                                      // next stage this warp owns
+        int own = warp / P;                                  // next stage this warp's group owns
         for (int k = 0; k < nst; ++k) {
-            // ---- owned stages up to k + ahead: their activations
+            // ---- owned stages up to k + ahead: this warp's part of their dot products
             while (own < nst && own <= k + ahead) {
                 const uint32_t sa = sd + (uint32_t)own;
                 const uint32_t os = sa % p.nsd, op = (sa / p.nsd) & 1;
@@ -1062,34 +1081,46 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
                     const uint32_t base = ring + os * (uint32_t)p.dslotB;
                     const int nn = min(npd, ncnt - own * npd);
                     for (int j = 0; j < nn; ++j) {
-                        const int pos = own * npd + j;
-                        const int id = S.slist[pos];
                         float au[TGF], ag[TGF];
-                        row_dots<T, Q4, TGF, REGLU>(L, base + (uint32_t)(j * nb), upB, xs, d, nt, lane, au, ag);
+                        row_dots<T, Q4, TGF, REGLU>(L, base + (uint32_t)(j * nb), upB, xs, d, nt, lane, c0, c1, au, ag);
                         if (lane == 0) {
-                            const float bias = L.bias_tail ? F::one(ld_shared_u16(base + (uint32_t)(j * nb) + rowB))
-                                                           : S.sbias[pos];
 #pragma unroll
                             for (int t = 0; t < TGF; ++t) {
-                                const float r = fmaxf((REGLU ? ag[t] : au[t]) + bias, 0.f);
-                                const float av = REGLU ? r * au[t] : (SQ ? r * r : r);
-                                act[(os * kMaxNeuronsPerStage + j) * TGF + t] = id >= 0 && t < nt ? av : 0.f;
+                                float *r = red_at(os, j, part, t);
+                                r[0] = au[t];
+                                r[1] = ag[t];
                             }
                         }
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(S.act_full + os);
                 }
-                own += kConsumerWarps;
+                own += G16;
             }
             // ---- stage k: its down-projection rows into this thread's columns
             if (wait_cta(S.full_d + slot, par, p, fail_word(S), ok) && wait_cta(S.act_full + slot, par, p, fail_word(S), ok)) {
                 const uint32_t base = ring + slot * (uint32_t)p.dslotB;
                 const int nn = min(npd, ncnt - k * npd);
                 for (int j = 0; j < nn; ++j) {
+                    // the neuron's activation from its P partial sums, added in part order
+                    const int pos = k * npd + j;
+                    const float bias = L.bias_tail ? F::one(ld_shared_u16(base + (uint32_t)(j * nb) + rowB)) : S.sbias[pos];
+                    const bool live = S.slist[pos] >= 0;
                     float a[TGF];
 #pragma unroll
-                    for (int t = 0; t < TGF; ++t) a[t] = act[(slot * kMaxNeuronsPerStage + j) * TGF + t];
+                    for (int t = 0; t < TGF; ++t) {
+                        float su = 0.f, sg = 0.f;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (q < P) {
+                                const float *r = red_at(slot, j, q, t);
+                                su += r[0];
+                                sg += r[1];
+                            }
+                        const float rl = fmaxf((REGLU ? sg : su) + bias, 0.f);
+                        const float av = REGLU ? rl * su : (SQ ? rl * rl : rl);
+                        a[t] = live && t < nt ? av : 0.f;
+                    }
                     const uint32_t dn = base + (uint32_t)(j * nb) + dnoff;
                     if (!Q4) {
 #pragma unroll
@@ -1315,7 +1346,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
         mbar_init(S.lst_full, 1);
         mbar_init(S.lst_free, 1);
         mbar_init(S.bias_full, 1);
-        for (int i = 0; i < p.nsd; ++i) mbar_init(S.act_full + i, 1);
+        for (int i = 0; i < p.nsd; ++i) mbar_init(S.act_full + i, owner_parts(p.nsd));
         fence_barrier_init();
         S.info[INFO_FAIL] = 0;
         S.info[INFO_REGION] = 0;
