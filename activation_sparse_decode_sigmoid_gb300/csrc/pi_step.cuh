@@ -941,11 +941,13 @@ static __device__ __forceinline__ void q4_pairs(const uint4 v, bool high, uint32
     }
 }
 
-// Warps that share the dot products of one stage: with few ring stages (big
-// neurons) one warp's pass over a whole row is the longest step of a stage's
-// turn, so the rows are split between P warps, each taking a contiguous
-// slice of every row; the stage's act_full barrier counts their P arrivals.
-static __device__ __forceinline__ int owner_parts(int nsd) { return nsd <= 4 ? 4 : (nsd <= 8 ? 2 : 1); }
+// Warps that share the dot products of one stage: one warp's pass over a
+// whole row is the longest step of a stage's turn, so the rows are split
+// between P warps, each taking a contiguous slice of every row; the stage's
+// act_full barrier counts their P arrivals.  (Measured: 4 pays with rings of
+// up to 4 stages, 2 with more; partial sums of nsd * P <= 32 stage-parts fit
+// the shared buffer.)
+static __device__ __forceinline__ int owner_parts(int nsd) { return nsd <= 4 ? 4 : 2; }
 
 // One warp: its slice [c0, c1) (16-bit: chunks of 8 elements; Q4_0:
 // half-blocks of 16) of the dot products of one neuron's W_up row (at a)

@@ -50,9 +50,10 @@ def parse_args():
     ap.add_argument("--hot-prefix", action="store_true",
                     help="give every layer its always-active prefix at the byte crossover for the batch")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
-    ap.add_argument("--mode", choices=["step", "ffn"], default="step",
+    ap.add_argument("--mode", choices=["step", "ffn", "sequence"], default="step",
                     help="step: the decode step over the stack (the headline); ffn: the sparse FFN of one "
-                         "full-size layer alone, for per-kernel numbers")
+                         "full-size layer alone, for per-kernel numbers; sequence: the workload's prompt "
+                         "(one step of its prompt length) followed by its decode tokens one at a time")
     return ap.parse_args()
 
 
@@ -522,6 +523,69 @@ def run_ffn(args, world, rank, local):
             "gpu_launches": K * ((4 if cfg.w_dtype == W.Q4_0 else 3) if tc else 1)}), flush=True)
 
 
+def run_sequence(args, world, rank, local):
+    """A prompt of cfg.prompt tokens (one batched step through the stack, the
+    union of their predicted neurons) followed by cfg.tokens one-token decode
+    steps, as the Falcon-40B-shaped Q4_0 workload defines it; each timed
+    sequence is that whole run.  Tokens/s counts prompt and decode tokens."""
+    import torch
+    from activation_sparse_decode_sigmoid_gb300 import build as libbuild
+    from activation_sparse_decode_sigmoid_gb300 import workload as W
+    from activation_sparse_decode_sigmoid_gb300.calibrate import load_synthetic_stack
+
+    libbuild.build()
+    torch.cuda.set_device(local)
+    cfg = W.CONFIGS[args.config]
+    if cfg.prompt < 1:
+        raise SystemExit(f"{cfg.name} has no prompt phase")
+    L = args.layers or cfg.L
+    P, T, K, Wm = cfg.prompt, cfg.tokens, args.steps, args.warmup
+    ctx, _ = load_synthetic_stack(cfg, L, args.seed, local, P)
+    d = cfg.d
+    xp = torch.from_numpy(W.decode_inputs(cfg, (K + Wm) * P, args.seed)).cuda(local).view(K + Wm, P, d)
+    xd = torch.from_numpy(W.decode_inputs(cfg, (K + Wm) * T, args.seed + 1)).cuda(local).view(K + Wm, T, 1, d)
+    stream = torch.cuda.current_stream(local)
+
+    def sequence(i, ev=None):
+        ctx.decode_step(xp[i])
+        if ev is not None:
+            ev.record(stream)
+        for t in range(T):
+            ctx.decode_step(xd[i, t])
+
+    for i in range(Wm):
+        sequence(i)
+    ctx.check()
+    e = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    torch.cuda.synchronize(local)
+    barrier(world)
+    for k in range(K):
+        e[k][0].record(stream)
+        sequence(Wm + k, e[k][1])
+        e[k][2].record(stream)
+    torch.cuda.synchronize(local)
+    ctx.check()
+    ms = sum(a.elapsed_time(c) for a, _, c in e)
+    ms_prompt = sum(a.elapsed_time(b) for a, b, _ in e) / K
+    ms = allreduce_max(world, ms, torch.device("cuda", local))
+    from activation_sparse_decode_sigmoid_gb300 import pi
+    mb = pi.pi_layerwise_min_batch(ctx.handle, 0)
+    per_prompt = ((8 if cfg.w_dtype == W.Q4_0 else 7) * L) if 0 < mb <= P else 1
+    ctx.close()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "prompt + decode tokens/s of the workload's sequence", "value": world * K * (P + T) / (ms / 1e3),
+            "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": W.DTYPE_NAMES[cfg.w_dtype],
+            "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: {L} layers, a {P}-token prompt step then {T} one-token steps",
+                       "seq_len": P + T},
+            "prompt_ms": ms_prompt, "prompt_tokens_per_s": P / (ms_prompt / 1e3),
+            "decode_ms_per_token": (ms / K - ms_prompt) / T,
+            "decode_tokens_per_s": T / ((ms / K - ms_prompt) / 1e3),
+            "gpu_launches": K * (per_prompt + T)}), flush=True)
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_init(args)
@@ -529,6 +593,8 @@ def main():
         run_reference(args, world, rank)
     elif args.mode == "ffn":
         run_ffn(args, world, rank, local)
+    elif args.mode == "sequence":
+        run_sequence(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:
