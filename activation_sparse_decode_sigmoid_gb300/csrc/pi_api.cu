@@ -73,11 +73,6 @@ struct pi_ctx {
     float *hbuf = nullptr;       // [max_batch][kMaxRank] predictor hidden layer of large batches
     uint32_t *mbits = nullptr;   // [kMaxN / 32] union mask words of large batches
     bool h_batched = false;      // the last predictor pass was the batched one (h in hbuf)
-    // Q4_0 layers on the tensor cores: the listed rows are dequantised into these
-    // 16-bit rows first (sized for the largest Q4_0 layer loaded; one layer at a time)
-    uint8_t *q4s_up = nullptr, *q4s_gate = nullptr, *q4s_dn = nullptr;
-    size_t q4s_cap_up = 0, q4s_cap_gate = 0, q4s_cap_dn = 0; // bytes
-    LayerDev *q4s_layers = nullptr; // device [max_layers]: each Q4_0 layer's 16-bit view of those rows
     // Batches of at least this many tokens run layer by layer: batched predictor launches and the
     // tensor-core FFN (0: never; -1: by layer kind, see layerwise_min_b).
     int mma_min_b = -1;
@@ -350,11 +345,6 @@ pi_status pi_create(pi_ctx **out, int32_t device, void *stream, int32_t max_laye
     c->mpart = (float *)ptrs[10];
     c->hbuf = (float *)ptrs[11];
     c->mbits = (uint32_t *)ptrs[12];
-    if (cudaMalloc(&c->q4s_layers, sizeof(LayerDev) * (size_t)max_layers) != cudaSuccess) {
-        for (void *p : ptrs) cudaFree(p);
-        delete c;
-        return PI_ERR_OOM;
-    }
     *out = c;
     return PI_OK;
 }
@@ -379,10 +369,6 @@ pi_status pi_destroy(pi_ctx *c)
         cudaFree(c->mpart);
         cudaFree(c->hbuf);
         cudaFree(c->mbits);
-        cudaFree(c->q4s_up);
-        cudaFree(c->q4s_gate);
-        cudaFree(c->q4s_dn);
-        cudaFree(c->q4s_layers);
     }
     delete c;
     return PI_OK;
@@ -392,60 +378,6 @@ pi_status pi_set_stream(pi_ctx *c, void *stream)
 {
     if (!c) return PI_ERR_ARG;
     c->stream = (cudaStream_t)stream;
-    return PI_OK;
-}
-
-// The 16-bit view of a Q4_0 layer's dequantised rows in the context's
-// scratch: the layer's shape and biases, W_up rows with a bias tail.
-static LayerDev q4_view(const pi_ctx *c, const LayerDev &L)
-{
-    LayerDev v = L;
-    v.q4 = 0;
-    v.scB = 0;
-    v.rowB = 2 * L.d;
-    v.upB = 2 * L.d + 16;
-    v.bias_tail = 1;
-    v.up = c->q4s_up;
-    v.gate = L.gate ? c->q4s_gate : nullptr;
-    v.dn = c->q4s_dn;
-    return v;
-}
-
-// Room in the scratch for Q4_0 layer `layer`, then the views and tensor maps
-// of every loaded Q4_0 layer (the scratch may have moved).
-static pi_status q4_scratch(pi_ctx *c, int layer)
-{
-    const LayerDev &L = c->layers[layer].dev;
-    const size_t up = (size_t)L.n * (2 * L.d + 16), row = (size_t)L.n * 2 * L.d;
-    const auto grow = [&](uint8_t *&p, size_t &cap, size_t need) {
-        if (need <= cap) return cudaSuccess;
-        cudaFree(p);
-        p = nullptr;
-        cap = 0;
-        const cudaError_t e = cudaMalloc(&p, need);
-        if (e == cudaSuccess) cap = need;
-        return e;
-    };
-    cudaError_t e = grow(c->q4s_up, c->q4s_cap_up, up);
-    if (e == cudaSuccess && L.gate) e = grow(c->q4s_gate, c->q4s_cap_gate, row);
-    if (e == cudaSuccess) e = grow(c->q4s_dn, c->q4s_cap_dn, row);
-    if (e != cudaSuccess) { // no room: the layer keeps the CUDA-core path for batches too
-        cudaGetLastError();
-        c->layers[layer].maps = false;
-        return PI_OK;
-    }
-    // the scratch only grows, so every loaded Q4_0 layer fits it
-    for (int l = 0; l < c->max_layers; ++l) {
-        LayerSlot &s = c->layers[l];
-        if (!s.loaded || s.desc.w_dtype != PI_Q4_0) continue;
-        const LayerDev v = q4_view(c, s.dev);
-        e = cudaMemcpy(c->q4s_layers + l, &v, sizeof(LayerDev), cudaMemcpyHostToDevice);
-        if (e == cudaSuccess) e = pi::encode_map(&s.tm_up, v.up, (uint64_t)v.d, (uint64_t)v.n, (uint64_t)v.upB, 1);
-        if (e == cudaSuccess && v.gate)
-            e = pi::encode_map(&s.tm_gate, v.gate, (uint64_t)v.d, (uint64_t)v.n, (uint64_t)v.rowB, 1);
-        if (e == cudaSuccess) e = pi::encode_map(&s.tm_dn, v.dn, (uint64_t)v.d, (uint64_t)v.n, (uint64_t)v.rowB, 1);
-        s.maps = e == cudaSuccess; // without maps the layer keeps the CUDA-core path
-    }
     return PI_OK;
 }
 
@@ -642,8 +574,9 @@ static pi_status load_rows(pi_ctx *c, int32_t layer, const pi_layer_desc *desc, 
     s.desc.d_ffn = n; // the neurons this slot holds
     s.loaded = true;
     s.maps = false;
-    if (q4 && c->max_batch >= 2) return q4_scratch(c, layer); // batches reach the tensor cores dequantised
-    if (!q4) {
+    if (q4) {
+        s.maps = true; // batches dequantise the rows in the tensor-core kernels' shared memory
+    } else {
         cudaError_t me = pi::encode_map(&s.tm_up, pup, (uint64_t)d, (uint64_t)n, (uint64_t)rowB + 16, 1);
         if (me == cudaSuccess && reglu) me = pi::encode_map(&s.tm_gate, pgate, (uint64_t)d, (uint64_t)n, (uint64_t)rowB, 1);
         if (me == cudaSuccess) me = pi::encode_map(&s.tm_dn, pdn, (uint64_t)d, (uint64_t)n, (uint64_t)rowB, 1);
@@ -729,7 +662,7 @@ pi_status pi_layer_counts(pi_ctx *c, int32_t layer, const void *x_hat, int32_t T
 }
 
 // Batches of at least mma_min_b tokens take the tensor-core gather-GEMM
-// (pi_mma.cu; Q4_0 rows dequantised to f16 first); smaller ones the step kernel.
+// (pi_mma.cu; Q4_0 layers pi_mma_q4.cu); smaller ones the step kernel.
 // A layer without tensor maps (none could be made) stays on the step kernel.
 // The smallest batch that runs layer by layer.  Unless set, 2 tokens for
 // 16-bit layers and 3 for Q4_0 ones: at 2 tokens the persistent kernel's
@@ -768,15 +701,6 @@ static pi_status mma_ffn(pi_ctx *c, int layer, const uint16_t *xhat, int B, cons
         me = pi::encode_map(&q.tm_act_lo, actL, (uint64_t)pi::kMaxN, (uint64_t)B, (uint64_t)pi::kMaxN * 2, np);
     if (me != cudaSuccess) return fail(c, PI_ERR_CUDA, "tensor map: %s", cudaGetErrorString(me));
     q.layer = c->d_layers + layer;
-    if (dsc.w_dtype == PI_Q4_0) {
-        // the listed rows, dequantised to f16 at their list positions: the
-        // tensor-core kernels then read rows 0 .. m-1 of that 16-bit view
-        const cudaError_t de = pi::launch_q4_to_f16_rows(ls.dev, q4_view(c, ls.dev), idx, count, c->ctl + 2,
-                                                         c->ctl + 3, c->stream);
-        if (de != cudaSuccess) return fail(c, PI_ERR_CUDA, "Q4_0 rows: %s", cudaGetErrorString(de));
-        q.layer = c->q4s_layers + layer;
-        idx = nullptr;
-    }
     q.xhat = xhat;
     q.B = B;
     q.Npad = (B + 15) / 16 * 16;
@@ -792,7 +716,9 @@ static pi_status mma_ffn(pi_ctx *c, int layer, const uint16_t *xhat, int B, cons
     q.status = c->ctl + 2;
     q.abort_flag = c->ctl + 3;
     q.wait_ns = c->wait_ns;
-    const cudaError_t e = pi::launch_ffn_mma(q, dsc.act_dtype == PI_BF16, dsc.act == PI_REGLU, c->G, c->stream);
+    const cudaError_t e = dsc.w_dtype == PI_Q4_0
+                              ? pi::launch_ffn_mma_q4(q, dsc.act == PI_REGLU, c->G, c->stream)
+                              : pi::launch_ffn_mma(q, dsc.act_dtype == PI_BF16, dsc.act == PI_REGLU, c->G, c->stream);
     if (e != cudaSuccess) return fail(c, PI_ERR_CUDA, "tensor-core FFN launch: %s", cudaGetErrorString(e));
     return PI_OK;
 }

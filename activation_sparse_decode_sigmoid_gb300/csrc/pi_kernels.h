@@ -196,6 +196,10 @@ cudaError_t launch_step_bf16(const StepParams &p, int tgf, int grid, cudaStream_
 cudaError_t launch_step_q4(const StepParams &p, int tgf, int grid, cudaStream_t s);
 // the union-mask FFN on tcgen05: up/gate kernel on `grid` SMs, then the down kernel
 cudaError_t launch_ffn_mma(const MmaParams &p, bool bf16, bool reglu, int grid, cudaStream_t s);
+// the same for a Q4_0 layer (f16 activations): the rows are dequantised in shared memory
+cudaError_t launch_ffn_mma_q4(const MmaParams &p, bool reglu, int grid, cudaStream_t s);
+// y (or x +=) = the down kernel's nks share partials added in share order, + b_down
+cudaError_t launch_ffn_merge(const MmaParams &p, bool bf16, int nks, int grid, cudaStream_t s);
 
 // Programmatic dependent launch for the layer-by-layer path: each kernel is
 // launched so that it may be scheduled while its predecessor in the stream
@@ -272,12 +276,4 @@ cudaError_t launch_residual_add(float *x, const float *u, size_t n, cudaStream_t
 cudaError_t launch_q4_split(const uint8_t *src, uint8_t *dst, const int32_t *perm, int n, int d, int scB,
                             cudaStream_t s, size_t dstStride = 0);
 cudaError_t launch_permute16(const uint16_t *src, uint16_t *dst, const int32_t *perm, int n, cudaStream_t s);
-// The rows of the listed neurons of a Q4_0 layer L (idx NULL: every neuron;
-// count NULL: n) dequantised to f16 at list position k -> row k of `to`, a
-// 16-bit layer of the same shape (W_up rows with their bias tail), for the
-// tensor-core FFN.  An id outside [0, n) is flagged in *status and its rows
-// are zero.
-cudaError_t launch_q4_to_f16_rows(const LayerDev &L, const LayerDev &to, const int32_t *idx, const int32_t *count,
-                                  int *status, int *abort_flag, cudaStream_t s);
-
 } // namespace pi

@@ -125,61 +125,6 @@ cudaError_t launch_q4_split(const uint8_t *src, uint8_t *dst, const int32_t *per
     return cudaGetLastError();
 }
 
-// Thread = one half-block (16 columns) of list position k: its 16 nibbles (the
-// low or the high halves of the block's 16 bytes) and the block's fp16 scale
-// give w = (q - 8) * s, rounded to f16 (|w| <= 8 |s|), for W_up, W_gate and
-// W_down^T alike; the thread of half-block 0 also writes W_up's bias tail.
-__global__ void q4_to_f16_rows_kernel(const LayerDev L, const LayerDev to, const int32_t *__restrict__ idx,
-                                      const int32_t *__restrict__ count, int *status, int *abort_flag)
-{
-    pdl_enter();
-    if (*(volatile int *)abort_flag) return;
-    int m = count ? *count : L.n;
-    if (m < 0 || m > L.n) m = 0; // (the FFN kernels flag it)
-    const int nhb = L.d / 16;
-    const size_t total = (size_t)m * nhb;
-    for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (size_t)gridDim.x * blockDim.x) {
-        const int k = (int)(q / nhb), hb = (int)(q % nhb);
-        int id = idx ? idx[k] : k;
-        const bool ok = id >= 0 && id < L.n;
-        if (!ok) {
-            atomicCAS(status, 0, PI_DEV_FLAG);
-            atomicExch(abort_flag, 1);
-            id = 0;
-        }
-        const int blk = hb >> 1, sh = (hb & 1) * 4;
-        const auto one = [&](const uint8_t *src, size_t srcB, uint8_t *dst, size_t dstB) {
-            const uint8_t *row = src + (size_t)id * srcB;
-            const float s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(row + 2 * blk)));
-            const uint4 v = *reinterpret_cast<const uint4 *>(row + L.scB + (size_t)blk * 16);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o[8];
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-                const float a = ok ? (float)((int)((w[e >> 2] >> (8 * (e & 3) + sh)) & 15u) - 8) * s : 0.f;
-                const float b = ok ? (float)((int)((w[(e + 1) >> 2] >> (8 * ((e + 1) & 3) + sh)) & 15u) - 8) * s : 0.f;
-                o[e >> 1] = (uint32_t)__half_as_ushort(__float2half_rn(a)) |
-                            ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
-            }
-            uint4 *out = reinterpret_cast<uint4 *>(dst + (size_t)k * dstB + (size_t)hb * 32);
-            out[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            out[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        };
-        one(L.up, (size_t)L.upB, const_cast<uint8_t *>(to.up), (size_t)to.upB);
-        if (L.gate) one(L.gate, (size_t)L.rowB, const_cast<uint8_t *>(to.gate), (size_t)to.rowB);
-        one(L.dn, (size_t)L.rowB, const_cast<uint8_t *>(to.dn), (size_t)to.rowB);
-        if (hb == 0) // the bias tail after the W_up row
-            *reinterpret_cast<uint4 *>(const_cast<uint8_t *>(to.up) + (size_t)k * to.upB + to.rowB) =
-                make_uint4(ok ? (uint32_t)L.b[id] : 0u, 0u, 0u, 0u);
-    }
-}
-
-cudaError_t launch_q4_to_f16_rows(const LayerDev &L, const LayerDev &to, const int32_t *idx, const int32_t *count,
-                                  int *status, int *abort_flag, cudaStream_t s)
-{
-    return launch_pdl(q4_to_f16_rows_kernel, dim3(4 * 152), dim3(256), 0, s, L, to, idx, count, status, abort_flag);
-}
-
 // x[i] += u[i], i < n (fp32): a layer's update, reduced over the shards of a
 // neuron-sharded layer, added into the residual stream
 __global__ void residual_add_kernel(float *__restrict__ x, const float *__restrict__ u, size_t n)

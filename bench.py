@@ -389,18 +389,17 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_hbm()
     value = world * K * B / (ms / 1e3)
     # batches from the library's layer-by-layer threshold on run per layer: RMSNorm, the
-    # predictor's hidden layer, output layer and compaction, (Q4_0: the listed rows to f16,)
-    # the FFN's up and down kernels and the share merge; smaller ones are one persistent
-    # launch per step
+    # predictor's hidden layer, output layer and compaction, the FFN's up and down kernels
+    # (Q4_0: with the rows dequantised in shared memory) and the share merge; smaller ones
+    # are one persistent launch per step
     mb = pi.pi_layerwise_min_batch(ctx.handle, 0)
     layerwise = 0 < mb <= B
     q4 = cfg.w_dtype == W.Q4_0
-    ffn = ("FFN up/gate (whole rows on the CUDA cores up to 4 tokens, else tcgen05), down (tcgen05), "
-           "share merge")
-    kernel = (f"per-layer launches: RMSNorm, batched predictor (3), Q4_0 rows to f16, {ffn}" if layerwise and q4
-              else f"per-layer launches: RMSNorm, batched predictor (3), {ffn}" if layerwise
+    ffn = ("FFN up/gate and down (tcgen05, Q4_0 rows dequantised in shared memory), share merge" if q4 else
+           "FFN up/gate (whole rows on the CUDA cores up to 4 tokens, else tcgen05), down (tcgen05), share merge")
+    kernel = (f"per-layer launches: RMSNorm, batched predictor (3), {ffn}" if layerwise
               else "step_kernel (one persistent launch per step)")
-    launches_per_step = (8 if q4 else 7) * L if layerwise else 1
+    launches_per_step = 7 * L if layerwise else 1
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
@@ -503,7 +502,7 @@ def run_ffn(args, world, rank, local):
     ms = allreduce_max(world, e0.elapsed_time(e1) / K, dev)
     m = int(cnt.item())
     mb = pi.pi_layerwise_min_batch(ctx.handle, 0)
-    tc = 0 < mb <= B  # the tensor-core FFN: (Q4_0: rows to f16,) up, down, merge
+    tc = 0 < mb <= B  # the tensor-core FFN: up, down, merge
     rows = 3 if cfg.act == W.REGLU else 2
     row = cfg.d * 18 / 32 if cfg.w_dtype == W.Q4_0 else cfg.d * 2
     byts = m * (rows * row + 2) + B * cfg.d * 4
@@ -520,7 +519,7 @@ def run_ffn(args, world, rank, local):
                        "path": "tensor cores (tcgen05)" if tc else "step kernel"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "peak_source": f"{kind} copy bandwidth (hbm_gbs)", "traffic": None},
-            "gpu_launches": K * ((4 if cfg.w_dtype == W.Q4_0 else 3) if tc else 1)}), flush=True)
+            "gpu_launches": K * (3 if tc else 1)}), flush=True)
 
 
 def run_sequence(args, world, rank, local):
@@ -570,7 +569,7 @@ def run_sequence(args, world, rank, local):
     ms = allreduce_max(world, ms, torch.device("cuda", local))
     from activation_sparse_decode_sigmoid_gb300 import pi
     mb = pi.pi_layerwise_min_batch(ctx.handle, 0)
-    per_prompt = ((8 if cfg.w_dtype == W.Q4_0 else 7) * L) if 0 < mb <= P else 1
+    per_prompt = 7 * L if 0 < mb <= P else 1
     ctx.close()
     if rank == 0:
         print(json.dumps({

@@ -124,11 +124,6 @@ pi_status pi_set_stream(pi_ctx *ctx, void *stream);
  * WdT (one contiguous row per neuron) and splitting Q4_0 rows into separate
  * scale and nibble arrays.  This is the offline placement step of the
  * "CPU/GPU混合推理设计" section, mapped to one device: hot neurons first.
- * In a context with max_batch >= 2, a Q4_0 layer also sizes the context's
- * 16-bit scratch, into which batches dequantise their listed rows for the
- * tensor cores (n * (4 d + 16) bytes, plus n * 2 d for ReGLU, for the
- * largest Q4_0 layer loaded); if it cannot be allocated, that layer's
- * batches stay on the CUDA cores.
  * Synchronous: returns when the copy is done; the caller keeps its buffers. */
 pi_status pi_load_layer(pi_ctx *ctx, int32_t layer, const pi_layer_desc *desc,
                         const pi_layer_weights *w, const int32_t *perm);
@@ -374,10 +369,10 @@ pi_status pi_debug_set_tuning(pi_ctx *ctx, int32_t prefetch, int32_t prefetch_ns
 pi_status pi_debug_copy_hidden(pi_ctx *ctx, float *dst, int32_t count);
 
 /* Smallest batch (tokens) that runs layer by layer: the predictor as
- * batched launches and the FFN as a gather-GEMM (up to 4 tokens the up/gate
- * rows stream whole through the CUDA cores, else tcgen05; the down
- * projection on tcgen05; Q4_0 rows dequantised to f16 into a context scratch
- * first).  Smaller
+ * batched launches and the FFN as a gather-GEMM (up to 4 tokens the 16-bit
+ * up/gate rows stream whole through the CUDA cores, else tcgen05; the down
+ * projection on tcgen05; Q4_0 rows dequantised to f16 in the tensor-core
+ * kernels' shared memory).  Smaller
  * batches run in the persistent step kernel (CUDA cores).  -1 (the default)
  * chooses by weight type: 2 tokens for 16-bit layers, 3 for Q4_0 layers.  0
  * keeps every batch on the step kernel.  For comparing the two paths.

@@ -31,6 +31,8 @@ CFGS = {
     "ring_wrap": W.LayerConfig("ring_wrap", 4096, 12000, 2048, 2, W.RELU, W.F16, W.F16, alpha=0.9, cfg_id=205),
     # wide ReGLU rows: the few-token row kernel's ring holds only 4 to 6 neurons
     "reglu_wide": W.LayerConfig("reglu_wide", 8192, 16384, 64, 1, W.REGLU, W.BF16, W.BF16, alpha=0.7, cfg_id=207),
+    # ReGLU with Q4_0 rows; d not a multiple of 256: a partial last super-stage of 8 blocks
+    "reglu_q4": W.LayerConfig("reglu_q4", 416, 700, 32, 3, W.REGLU, W.Q4_0, W.F16, alpha=0.7, cfg_id=208),
 }
 
 
@@ -58,7 +60,7 @@ def test_predict_and_sparse_ffn(c64, name, B):
     G.ffn_checked(c64, 0, layer, x, idx, cnt, oidx)
 
 
-@pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4", "sqrelu_bf16"])
+@pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4", "reglu_q4", "sqrelu_bf16"])
 @pytest.mark.parametrize("B", [1, 2, 3, 4, 7, 9, 64])
 @pytest.mark.parametrize("path", ["default", "step kernel"], indirect=True)
 def test_batch_sizes(c64, name, B, path):
@@ -101,7 +103,7 @@ def test_few_token_row_kernel_wraps_its_ring(c64, name, B):
         pi.pi_debug_set_mma_min_batch(c64.handle, AUTO)
 
 
-@pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4", "sqrelu_bf16"])
+@pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "relu_q4", "reglu_q4", "sqrelu_bf16"])
 @pytest.mark.parametrize("path", ["default", "step kernel"], indirect=True)
 def test_dense_ffn(c64, name, path):
     cfg, layer = _layer(name)
@@ -320,6 +322,36 @@ def test_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
     got_d, want_d = G.y_to_f64(yd, cfg.act_dtype), O.masked_ffn(layer, x, every)
     assert max_rel_err(got_d, want_d) <= G.tol(layer)
     assert np.all(np.abs(got_d - want_d) <= G.tc_error_bound(layer, x, every))
+
+
+@pytest.mark.parametrize("name", ["relu_q4", "reglu_q4"])
+@pytest.mark.parametrize("B", [3, 8, 64])
+def test_q4_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
+    """Q4_0 batches dequantise their listed rows in the tensor-core kernels'
+    shared memory, w = (q - 8) * s rounded to f16 on its way to the MMA (no
+    dequantised copy goes back to HBM); the FFN must match the oracle (exact
+    fp64 dequantisation) within the Q4_0 tolerance and the step kernel's
+    CUDA-core path (fp32 products) within twice it, sparse and dense."""
+    cfg, layer = _layer(name)
+    c64.load_layer(0, layer)
+    x = W.xhat_inputs(cfg, B, 81 + B)
+    xd = G.dev16(x)
+    idx, cnt, oidx = G.predict_checked(c64, 0, layer, x)
+    y_tc = c64.sparse_ffn(0, xd, idx, cnt)
+    c64.check()
+    pi.pi_debug_set_mma_min_batch(c64.handle, 0)
+    y_cc = c64.sparse_ffn(0, xd, idx, cnt)
+    yd_cc = c64.dense_ffn(0, xd)
+    c64.check()
+    pi.pi_debug_set_mma_min_batch(c64.handle, AUTO)
+    got = G.y_to_f64(y_tc, cfg.act_dtype)
+    assert max_rel_err(got, O.masked_ffn(layer, x, oidx)) <= G.tol(layer)
+    assert max_rel_err(got, G.y_to_f64(y_cc, cfg.act_dtype)) <= 2 * G.tol(layer)
+    yd = c64.dense_ffn(0, xd)
+    c64.check()
+    got_d = G.y_to_f64(yd, cfg.act_dtype)
+    assert max_rel_err(got_d, O.masked_ffn(layer, x, np.arange(cfg.n, dtype=np.int32))) <= G.tol(layer)
+    assert max_rel_err(got_d, G.y_to_f64(yd_cc, cfg.act_dtype)) <= 2 * G.tol(layer)
 
 
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "ring_wrap", "opt_1layer"])
