@@ -934,8 +934,14 @@ static __device__ __forceinline__ void q4_pairs(const uint4 v, bool high, uint32
             uint32_t m = (t & (high ? 0x00F000F0u : 0x000F000Fu)) | 0x64006400u;
             __half2 x;
             memcpy(&x, &m, 4);
-            x = high ? __hfma2(x, __float2half2_rn(0.0625f), __float2half2_rn(-72.f)) // (1024 + 16q)/16 - 72
-                     : __hsub2(x, __float2half2_rn(1032.f));                           // 1024 + q - 1032
+            // the constants by their f16 bits: 1/16 = 0x2C00, -72 = 0xD480, 1032 = 0x6408
+            uint32_t c0 = 0x2C002C00u, c1 = 0xD480D480u, c2 = 0x64086408u;
+            __half2 k0, k1, k2;
+            memcpy(&k0, &c0, 4);
+            memcpy(&k1, &c1, 4);
+            memcpy(&k2, &c2, 4);
+            x = high ? __hfma2(x, k0, k1) // (1024 + 16q)/16 - 72
+                     : __hsub2(x, k2);    // 1024 + q - 1032
             memcpy(&h[2 * i + j], &x, 4);
         }
     }
