@@ -22,9 +22,10 @@
 //                 to about twice that precision).
 //   ffn_down_mma  column blocks of 256 x shares of the list: D = W_down^T
 //                 (M = 128 columns per tile, MN-major: 512-byte segments of
-//                 the gathered rows, by gather4) x A^T (N = B rounded up to 16, K-major),
-//                 once with the hi and once with the lo part into the same
-//                 fp32 accumulator, K = the share of the list in steps of 64 neurons; the
+//                 the gathered rows, by gather4) x A^T (K-major: the hi rows,
+//                 then the lo rows, N = 2 x B rounded up to 16, so each stage
+//                 of rows is read once; the epilogue adds the two products),
+//                 K = the share of the list in steps of 64 neurons; the
 //                 epilogue adds b_down and writes y (16-bit) or adds into the
 //                 fp32 residual x, or, when a block has several shares, fp32
 //                 partials that ffn_merge adds in share order.
@@ -68,6 +69,8 @@ constexpr int kIssuers = 11;                // TMA producer warps
 constexpr int kMT = 32 * (kIssuers + 1);  // + the MMA warp; warps 0..3 (TMEM lanes 0..127) run the epilogues
 constexpr uint32_t kTileA = 16384; // 128 rows x 128 bytes
 constexpr uint32_t kTileX = 8192;  // up to 64 rows x 128 bytes
+constexpr int kUpMaxSt = 9;        // stages of the up kernel, at most
+constexpr uint32_t kUpArena = 9 * (kTileA + kTileX); // its stages: 216 KB (the same for ReGLU's 3 x 72 KB)
 
 // TMA issue is split over the producer warps (one lane each): warp 0 and
 // warps 2.. take every kIssuers-th load of a stage and each posts its own
@@ -77,41 +80,31 @@ constexpr uint32_t kTileX = 8192;  // up to 64 rows x 128 bytes
 __device__ __forceinline__ int issuer_index(int warp) { return warp == 0 ? 0 : (warp >= 2 ? warp - 1 : -1); }
 
 // ------------------------------------------------------------------ up / gate kernel
-// Rows of the SM's slice are taken up to RP = 128 at a time (one MMA tile;
-// RP = 256 would let two tiles share each K step).  Small stages leave room
-// for more of them in shared memory: nine for ReLU, five for ReGLU, whose
-// stages carry two matrices; more stages keep more bytes in flight.
+// Rows of the SM's slice are taken up to RP = 128 at a time (one MMA tile),
+// or up to 256 (two tiles sharing each K step) when the slice holds more than
+// 128: a second pass over all of K for a few rows would cost nearly as much
+// as the first.  Small stages leave room for more of them in shared memory:
+// nine for ReLU, five for ReGLU, whose stages carry two matrices (five and
+// three of 256 rows); more stages keep more bytes in flight.
 // Warp 0 (one lane) produces: per stage, gather4 loads of the rows' next 64
 // columns (W_up, W_gate) and a tile load of x_hat; warp 1 (one lane) issues
 // the MMAs and commits each stage back to the producer; all four warps run
 // the epilogue.  Rows past the slice are gathered from row n (out of range:
 // zeros) or left stale; their accumulator rows are never read.
-template <typename T, bool REGLU, int STAGES, int RP>
-__global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ MmaParams p)
+//
+// up_passes: the passes of one CTA's slice with RP rows per pass (128 or 256)
+// and as many stages as the arena holds.
+template <typename T, bool REGLU, int RP>
+__device__ __forceinline__ void up_passes(const MmaParams &p, uint8_t *smem, uint64_t *full, uint64_t *empty,
+                                          uint64_t *done, int *sid, int *pub, uint32_t tmem, int m, int s0, int s1)
 {
-    extern __shared__ __align__(1024) uint8_t smem[];
     using H = H16<T>;
     const LayerDev &L = *p.layer;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = L.d, n = L.n, B = p.B, Np = p.Npad;
     constexpr uint32_t kW = RP / 128 * kTileA; // RP rows x 128 bytes of one weight matrix
     constexpr uint32_t kStage = kW * (REGLU ? 2 : 1) + kTileX;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * kStage); // one arrival per producer
-    uint64_t *empty = full + STAGES;
-    uint64_t *done = empty + STAGES;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
-    int *sid = reinterpret_cast<int *>(tslot + 4); // [RP] row ids of the current pass
-    int *pub = sid + RP;                           // [kIssuers] stages each producer issued
-    if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) mbar_init(full + s, kIssuers), mbar_init1(empty + s);
-        mbar_init1(done);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    // TMEM: tile j (0, 1) of U at columns [j Np, (j+1) Np), of the gate at [(2+j) Np, ...)
-    const uint32_t tmem = tmem_alloc(tslot, 256);
-    pdl_enter(); // (the barriers and tensor memory above were set up while the list was finished)
-    const int m = list_len(p, n);
-    const int s0 = slice_at(m, blockIdx.x, gridDim.x), s1 = slice_at(m, blockIdx.x + 1, gridDim.x);
+    constexpr uint32_t nst = kUpArena / kStage < (uint32_t)kUpMaxSt ? kUpArena / kStage : (uint32_t)kUpMaxSt;
     const int KT = (d + kBK - 1) / kBK;
     const uint32_t base = smem_addr(smem);
     const uint32_t id_up = idesc(H::fmt, 0, 0, 128, (uint32_t)Np);
@@ -138,9 +131,10 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
             const int nq = (rows + 3) / 4;
             const int mine = (nq - iss + kIssuers - 1) / kIssuers; // gathers q = iss, iss + kIssuers, ...
             const uint32_t bytes = (uint32_t)mine * 512u * (REGLU ? 2u : 1u) + (iss == 0 ? (uint32_t)Np * 128u : 0u);
-            for (int kt = 0; kt < KT && ok; ++kt, ++gp) {
-                const uint32_t st = gp % STAGES;
-                if (gp >= STAGES && !mbar_wait_bounded(empty + st, ((gp / STAGES) - 1) & 1, p)) {
+            Cur cp(gp, nst);
+            for (int kt = 0; kt < KT && ok; ++kt, ++gp, cp.next(nst)) {
+                const uint32_t st = cp.s;
+                if (gp >= nst && !mbar_wait_bounded(empty + st, cp.ph ^ 1u, p)) {
                     ok = false; // (nothing issued for this stage)
                     break;
                 }
@@ -156,27 +150,27 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
                 if (iss == 0) tile_load(sb + kW * (REGLU ? 2 : 1), &p.tm_x, kt * kBK, 0, fb);
             }
         } else if (warp == 1 && lane == 0) {
-            for (int kt = 0; kt < KT && ok; ++kt, ++gc) {
-                const uint32_t st = gc % STAGES;
-                if (!mbar_wait_bounded(full + st, (gc / STAGES) & 1, p)) {
+            // descriptors of stage 0; a byte offset o adds o / 16 (the start address field)
+            const uint64_t d0 = sdesc(base, 16, 1024);
+            Cur cc(gc, nst);
+            for (int kt = 0; kt < KT && ok; ++kt, ++gc, cc.next(nst)) {
+                if (!mbar_wait_bounded(full + cc.s, cc.ph, p)) {
                     ok = false;
                     break;
                 }
                 tc_after();
-                const uint32_t sb = base + st * kStage;
-                const uint32_t xb = sb + kW * (REGLU ? 2 : 1);
+                const uint64_t ds = d0 + ((cc.s * kStage) >> 4);
+                const uint64_t bx0 = ds + ((kW * (REGLU ? 2u : 1u)) >> 4);
 #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k) {
-                    const uint64_t bx = sdesc(xb + k * 32, 16, 1024);
                     for (int j = 0; j < ntile; ++j) {
-                        mma(tmem + (uint32_t)(j * Np), sdesc(sb + j * kTileA + k * 32, 16, 1024), bx, id_up,
-                            (kt | k) != 0);
+                        const uint64_t a = ds + ((j * kTileA) >> 4) + 2 * k;
+                        mma(tmem + (uint32_t)(j * Np), a, bx0 + 2 * k, id_up, (kt | k) != 0);
                         if (REGLU)
-                            mma(tmem + (uint32_t)((2 + j) * Np), sdesc(sb + kW + j * kTileA + k * 32, 16, 1024), bx,
-                                id_up, (kt | k) != 0);
+                            mma(tmem + (uint32_t)((2 + j) * Np), a + (kW >> 4), bx0 + 2 * k, id_up, (kt | k) != 0);
                     }
                 }
-                mma_commit(empty + st);
+                mma_commit(empty + cc.s);
             }
             mma_commit(done); // always: the MMAs issued so far complete before `done` flips
         }
@@ -227,7 +221,37 @@ __global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ Mma
         }
     }
     // no copy of this CTA may be in flight when it exits
-    settle_producers<kIssuers>(full, STAGES, pub, iss, lane, gp);
+    settle_producers<kIssuers>(full, (int)nst, pub, iss, lane, gp);
+}
+
+template <typename T, bool REGLU>
+__global__ void __launch_bounds__(kMT, 1) ffn_up_mma(const __grid_constant__ MmaParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const LayerDev &L = *p.layer;
+    const int tid = threadIdx.x;
+    const int n = L.n;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kUpArena); // [kUpMaxSt], one arrival per producer
+    uint64_t *empty = full + kUpMaxSt;
+    uint64_t *done = empty + kUpMaxSt;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
+    int *sid = reinterpret_cast<int *>(tslot + 4); // [256] row ids of the current pass
+    int *pub = sid + 256;                          // [kIssuers] stages each producer issued
+    if (tid == 0) {
+        for (int s = 0; s < kUpMaxSt; ++s) mbar_init(full + s, kIssuers), mbar_init1(empty + s);
+        mbar_init1(done);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // TMEM: tile j (0, 1) of U at columns [j Np, (j+1) Np), of the gate at [(2+j) Np, ...)
+    const uint32_t tmem = tmem_alloc(tslot, 256);
+    pdl_enter(); // (the barriers and tensor memory above were set up while the list was finished)
+    const int m = list_len(p, n);
+    const int s0 = slice_at(m, blockIdx.x, gridDim.x), s1 = slice_at(m, blockIdx.x + 1, gridDim.x);
+    // a slice of more than 128 rows runs in passes of up to 256 (two MMA tiles
+    // per K step) rather than a second pass of a few rows; its stages are
+    // twice as large, so fewer of them fit in the arena
+    if (s1 - s0 > 128) up_passes<T, REGLU, 256>(p, smem, full, empty, done, sid, pub, tmem, m, s0, s1);
+    else up_passes<T, REGLU, 128>(p, smem, full, empty, done, sid, pub, tmem, m, s0, s1);
     tmem_free(tmem, 256);
 }
 
@@ -431,8 +455,9 @@ __global__ void __launch_bounds__(kRowT, 1) ffn_up_rows(const __grid_constant__ 
 // Work unit u = (256-column block cb, share ks of the list).  For each of the
 // block's two 128-column tiles, D[128 columns x Np tokens] = W_down^T (MN-
 // major A: per stage 64 neurons x 256 columns, four 64-column atoms filled by
-// gather4) x A^T (K-major B: tile loads of tokens x 64 neurons, the hi and the
-// lo part, each multiplied into the same accumulator).  When the list is
+// gather4) x A^T (K-major B: tile loads of tokens x 64 neurons, the hi part
+// then the lo part, one operand of 2 Np rows; the epilogue adds the two
+// halves of the accumulator).  When the list is
 // split over several shares, the units write fp32 partials that ffn_merge
 // adds in share order; with one share the unit writes y or x.  A stage holds
 // 32 KB of rows and 2 x Np x 128 bytes of A^T: nst stages, as many as fit.
@@ -466,13 +491,16 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
         mbar_init1(done);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    const uint32_t tmem = tmem_alloc(tslot, 128); // tile j at columns [j Np, (j+1) Np)
+    // tile j at columns [2 j Np, 2 (j+1) Np): the product with the hi rows, then with the lo rows
+    const uint32_t tmem = tmem_alloc(tslot, 256);
     pdl_enter(); // (the barriers and tensor memory above were set up while the up kernel finished)
     const int m = list_len(p, n);
     const int KTall = (m + kBK - 1) / kBK;
     const int ncb = (d + 255) / 256;
     const uint32_t base = smem_addr(smem);
-    const uint32_t id_dn = idesc(H::fmt, 1, 0, 128, (uint32_t)Np);
+    // one MMA per (k, tile) against the hi and lo rows together (N = 2 Np, the
+    // lo part follows the hi part in the stage), so the rows are read once
+    const uint32_t id_dn = idesc(H::fmt, 1, 0, 128, 2u * (uint32_t)Np);
     const int iss = issuer_index(warp);
     // 64 gathers per stage (4 column atoms x 16 groups of 4 neurons): g = iss, iss + kIssuers, ...
     const uint32_t bytes = (uint32_t)((64 - iss + kIssuers - 1) / kIssuers) * 512u + (iss == 0 ? 2u * kX : 0u);
@@ -494,8 +522,9 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
             int f0[2], f1[2], f2[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) f0[h] = fetch(0, h), f1[h] = fetch(1, h), f2[h] = fetch(2, h);
+            Cur cp(gp, nst);
             for (int kt = 0; kt < KT; ++kt) {
-                const uint32_t st = gp % (uint32_t)nst;
+                const uint32_t st = cp.s;
                 const int k0 = (k_lo + kt) * kBK;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -508,7 +537,7 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
                 }
                 __syncwarp();
                 if (lane == 0 && ok) {
-                    if (gp >= (uint32_t)nst && !mbar_wait_bounded(empty + st, ((gp / nst) - 1) & 1, p)) ok = false;
+                    if (gp >= (uint32_t)nst && !mbar_wait_bounded(empty + st, cp.ph ^ 1u, p)) ok = false;
                     if (ok) {
                         const uint32_t sb = base + st * kStage;
                         uint64_t *fb = full + st;
@@ -523,32 +552,32 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
                             tile_load(sb + kDnW + kX, &p.tm_act_lo, k0, 0, fb);
                         }
                         ++gp; // (lane 0 counts the stages it issued)
+                        cp.next(nst);
                     }
                 }
                 __syncwarp(); // myids is rewritten for the next stage
             }
         }
         if (warp == 1 && lane == 0) {
-            for (int kt = 0; kt < KT && ok; ++kt, ++gc) {
-                const uint32_t st = gc % (uint32_t)nst;
-                if (!mbar_wait_bounded(full + st, (gc / nst) & 1, p)) {
+            // descriptors of stage 0; a byte offset o adds o / 16 (the start address field)
+            const uint64_t dA = sdesc(base, kDnAtom, 1024), dB = sdesc(base + kDnW, 16, 1024);
+            Cur cc(gc, nst);
+            for (int kt = 0; kt < KT && ok; ++kt, ++gc, cc.next(nst)) {
+                if (!mbar_wait_bounded(full + cc.s, cc.ph, p)) {
                     ok = false;
                     break;
                 }
                 tc_after();
-                const uint32_t sb = base + st * kStage;
+                const uint64_t a0 = dA + ((cc.s * kStage) >> 4), b0 = dB + ((cc.s * kStage) >> 4);
 #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k) {
-                    const uint64_t bh = sdesc(sb + kDnW + k * 32, 16, 1024);
-                    const uint64_t bl = sdesc(sb + kDnW + kX + k * 32, 16, 1024);
 #pragma unroll
                     for (int j = 0; j < 2; ++j) { // atoms 2j, 2j+1: LBO steps from one 64-column atom to the next
-                        const uint64_t a = sdesc(sb + (uint32_t)(2 * j) * kDnAtom + k * 16 * 128, kDnAtom, 1024);
-                        mma(tmem + (uint32_t)(j * Np), a, bh, id_dn, (kt | k) != 0);
-                        mma(tmem + (uint32_t)(j * Np), a, bl, id_dn, 1u);
+                        const uint64_t a = a0 + (uint64_t)((2 * j * kDnAtom + k * 16 * 128) >> 4);
+                        mma(tmem + (uint32_t)(2 * j * Np), a, b0 + 2 * k, id_dn, (kt | k) != 0);
                     }
                 }
-                mma_commit(empty + st);
+                mma_commit(empty + cc.s);
             }
             mma_commit(done); // always: the MMAs issued so far complete before `done` flips
         }
@@ -561,9 +590,13 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
             const int c = c0 + j * 128 + warp * 32 + lane;
             const float bd = c < d ? H::one(L.bdown[c]) : 0.f;
             for (int t0 = 0; t0 < Np; t0 += 16) {
-                float v[16];
-                if (KT > 0) tmem_ld16(lane_addr + (uint32_t)(j * Np + t0), v);
-                else
+                float v[16], vl[16];
+                if (KT > 0) {
+                    tmem_ld16(lane_addr + (uint32_t)(2 * j * Np + t0), v);
+                    tmem_ld16(lane_addr + (uint32_t)(2 * j * Np + Np + t0), vl);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] += vl[i];
+                } else
                     for (int i = 0; i < 16; ++i) v[i] = 0.f;
                 if (c < d && live) {
 #pragma unroll
@@ -584,7 +617,7 @@ __global__ void __launch_bounds__(kMT, 1) ffn_down_mma(const __grid_constant__ M
     }
     // no copy of this CTA may be in flight when it exits
     settle_producers<kIssuers>(full, nst, pub, iss, lane, gp);
-    tmem_free(tmem, 128);
+    tmem_free(tmem, 256);
 }
 
 // y (or x +=) = the shares' partials added in share order, + b_down
@@ -608,12 +641,12 @@ __global__ void ffn_merge(const __grid_constant__ MmaParams p, int nks)
 template <typename T, bool REGLU>
 cudaError_t launch_up(const MmaParams &p, int grid, cudaStream_t s)
 {
-    constexpr int st = REGLU ? 5 : 9, rp = 128;
-    // stages, then full[st], empty[st], done, the TMEM slot (16 bytes), the row ids [rp] and the
-    // producers' stage counts [kIssuers]
-    const int smem = st * (int)(rp / 128 * kTileA * (REGLU ? 2 : 1) + kTileX) + (2 * st + 1) * 8 + 16 + rp * 4 +
-                     kIssuers * 4;
-    auto kern = ffn_up_mma<T, REGLU, st, rp>;
+    // the stage arena: nine 128-row stages for ReLU, five for ReGLU (whose
+    // stages carry two matrices), or five / three of 256 rows; then
+    // full[kUpMaxSt], empty[kUpMaxSt], done, the TMEM slot (16 bytes), the row
+    // ids [256] and the producers' stage counts [kIssuers]
+    const int smem = (int)kUpArena + (2 * kUpMaxSt + 1) * 8 + 16 + 256 * 4 + kIssuers * 4;
+    auto kern = ffn_up_mma<T, REGLU>;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kMT), smem, s, p);

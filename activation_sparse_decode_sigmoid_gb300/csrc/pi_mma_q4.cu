@@ -162,18 +162,6 @@ __device__ __forceinline__ void warp_arrive(uint64_t *b, bool wrote, int lane)
 }
 
 
-// Position in a ring of n slots: slot s, and the parity ph of the slot's
-// current round.  Advancing is an add and a compare; the role loops need no
-// division per step.
-struct Cur {
-    uint32_t s, ph;
-    __device__ __forceinline__ Cur(uint32_t g, uint32_t n) : s(g % n), ph((g / n) & 1u) {}
-    __device__ __forceinline__ void next(uint32_t n)
-    {
-        if (++s == n) s = 0, ph ^= 1u;
-    }
-};
-
 // The raw Q4_0 data a converting thread needs for one 256-column super-stage
 // S of its row (two 128-column K steps): the nibbles of blocks 8 S + 4 j +
 // 2 h and 8 S + 4 j + 2 h + 1 for j = 0, 1 (its half h of each step) and the

@@ -139,6 +139,18 @@ __device__ __forceinline__ void split16(float a, uint16_t &hi, uint16_t &lo)
     lo = H::round(a - H::one(hi));
 }
 
+// Position in a ring of n slots: slot s, and the parity ph of the slot's
+// current round.  Advancing is an add and a compare; the role loops need no
+// division per step.
+struct Cur {
+    uint32_t s, ph;
+    __device__ __forceinline__ Cur(uint32_t g, uint32_t n) : s(g % n), ph((g / n) & 1u) {}
+    __device__ __forceinline__ void next(uint32_t n)
+    {
+        if (++s == n) s = 0, ph ^= 1u;
+    }
+};
+
 // shared-memory matrix descriptor, 128-byte swizzle
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo)
 {
