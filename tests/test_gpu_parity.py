@@ -354,6 +354,43 @@ def test_q4_tensor_core_ffn_matches_oracle_and_cuda_core_path(c64, name, B):
     assert max_rel_err(got_d, G.y_to_f64(yd_cc, cfg.act_dtype)) <= 2 * G.tol(layer)
 
 
+# tall layers: so many neurons that a CTA of the tensor-core up kernel makes
+# more than one pass over K on 152 SMs (16-bit rows: 263 rows per SM, a
+# 256-row pass then a short one; Q4_0 ReLU, two CTAs per SM: 132 rows per CTA,
+# two 128-row passes; Q4_0 ReGLU, one CTA per SM: 132 rows)
+TALL = {
+    "tall_relu_f16": W.LayerConfig("tall_relu_f16", 128, 40000, 32, 1, W.RELU, W.F16, W.F16, alpha=0.8, cfg_id=211),
+    "tall_reglu_bf16": W.LayerConfig("tall_reglu_bf16", 128, 40000, 32, 1, W.REGLU, W.BF16, W.BF16, alpha=0.7,
+                                     cfg_id=212),
+    "tall_relu_q4": W.LayerConfig("tall_relu_q4", 160, 40000, 32, 1, W.RELU, W.Q4_0, W.F16, alpha=0.8, cfg_id=213),
+    "tall_reglu_q4": W.LayerConfig("tall_reglu_q4", 96, 20000, 32, 1, W.REGLU, W.Q4_0, W.F16, alpha=0.7, cfg_id=214),
+}
+
+
+@pytest.mark.parametrize("name", list(TALL))
+@pytest.mark.parametrize("B", [8, 64])
+def test_tensor_core_ffn_several_passes_per_cta(c64, name, B):
+    """Dense FFN of a tall layer on the tensor cores (every neuron listed, so
+    each up-kernel CTA runs more than one pass over K): the oracle within the
+    stated tolerance, the step kernel's CUDA-core path within twice it."""
+    cfg = TALL[name]
+    layer = W.make_layer(cfg, 0, 0, random_b1=True, random_bdown=True)
+    c64.load_layer(0, layer)
+    x = W.xhat_inputs(cfg, B, 91 + B)
+    xd = G.dev16(x)
+    y_tc = c64.dense_ffn(0, xd)
+    c64.check()
+    try:
+        pi.pi_debug_set_mma_min_batch(c64.handle, 0)
+        y_cc = c64.dense_ffn(0, xd)
+        c64.check()
+    finally:
+        pi.pi_debug_set_mma_min_batch(c64.handle, AUTO)
+    got = G.y_to_f64(y_tc, cfg.act_dtype)
+    assert max_rel_err(got, O.masked_ffn(layer, x, np.arange(cfg.n, dtype=np.int32))) <= G.tol(layer)
+    assert max_rel_err(got, G.y_to_f64(y_cc, cfg.act_dtype)) <= 2 * G.tol(layer)
+
+
 @pytest.mark.parametrize("name", ["relu_f16", "reglu_bf16", "ring_wrap", "opt_1layer"])
 @pytest.mark.parametrize("B", [2, 5, 8, 9, 16, 17, 40, 64])
 def test_batched_predictor_matches_oracle_and_step_kernel(c64, name, B):
