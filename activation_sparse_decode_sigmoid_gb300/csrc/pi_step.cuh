@@ -58,10 +58,10 @@ struct Shm {
     uint16_t *pb1s, *pb2s; // this CTA's b1 / b2 slices, as copied (16-byte-rounded ranges)
     uint64_t *bias_full;   // completes when a layer's bias slices have landed
     uint64_t *act_full;    // [nsd] completes when a stage's P owner warps have written their partial sums
-    float *red;     // partial dot sums of the FFN stages: [nsd][kMaxNeuronsPerStage][P][TGF][2] (nsd * P <= 16)
+    float *red;     // partial dot sums of the FFN stages: [nsd][npd][P][TGF][2] (nsd * npd * P <= 2 * 16 * 8)
 };
 
-enum { INFO_FLAG = 0, INFO_NCNT = 1, INFO_FAIL = 2, INFO_M = 3, INFO_REGION = 4 };
+enum { INFO_FLAG = 0, INFO_NCNT = 1, INFO_FAIL = 2, INFO_M = 3, INFO_REGION = 4, INFO_OWNP = 5 };
 
 static __device__ __forceinline__ volatile int *fail_word(const Shm &S) { return S.info + INFO_FAIL; }
 
@@ -950,10 +950,18 @@ static __device__ __forceinline__ void q4_pairs(const uint4 v, bool high, uint32
 // Warps that share the dot products of one stage: one warp's pass over a
 // whole row is the longest step of a stage's turn, so the rows are split
 // between P warps, each taking a contiguous slice of every row; the stage's
-// act_full barrier counts their P arrivals.  (Measured: 4 pays with rings of
-// up to 4 stages, 2 with more; partial sums of nsd * P <= 32 stage-parts fit
-// the shared buffer.)
-static __device__ __forceinline__ int owner_parts(int nsd) { return nsd <= 4 ? 4 : 2; }
+// act_full barrier counts their P arrivals.  P = 4 whenever the partial sums
+// of every stage's neurons and parts fit the shared buffer (nsd x neurons per
+// stage x P <= 2 x 16 x 8), else 2; the same P for every layer of the launch
+// (the barriers are set up once).  Measured at one token, 12-layer stacks, P
+// = 4 against 2: Falcon-40B f16 52.1 -> 50.4 us a layer, Q4_0 52.8 -> 52.4,
+// OPT-30B 44.8 -> 44.7; P = 8 was slower everywhere (56.4, 48.1, 54.4).
+static __device__ __forceinline__ int owner_parts(const StepParams &p)
+{
+    int npd = 1;
+    for (int l = 0; l < p.L; ++l) npd = max(npd, neurons_per_stage(p.layers[l], p));
+    return p.nsd * npd * 4 <= 2 * kConsumerWarps * kMaxNeuronsPerStage ? 4 : 2;
+}
 
 // One warp: its slice [c0, c1) (16-bit: chunks of 8 elements; Q4_0:
 // half-blocks of 16) of the dot products of one neuron's W_up row (at a)
@@ -1055,15 +1063,15 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
     const uint32_t dnoff = upB + (REGLU ? rowB : 0u); // offset of the W_down^T row
     const uint32_t ring = smem_u32(S.ring);
     const uint32_t xs = smem_u32(S.xs);
-    const int P = owner_parts(p.nsd);  // warps sharing a stage's dot products
+    const int P = S.info[INFO_OWNP];    // warps sharing a stage's dot products
     const int G16 = kConsumerWarps / P; // owner groups: group g owns stages g, g + G16, ...
     const int part = warp % P;
     const int units = Q4 ? nhb : nch;  // this warp's slice of every row it computes
     const int c0 = units * part / P, c1 = units * (part + 1) / P;
-    // [nsd][kMaxNeuronsPerStage][P][TGF][2] partial dot sums (up, gate) of the stages in the ring
+    // [nsd][npd][P][TGF][2] partial dot sums (up, gate) of the stages in the ring
     float *red = S.red;
     const auto red_at = [&](uint32_t os, int j, int q, int t) {
-        return red + ((((int)os * kMaxNeuronsPerStage + j) * P + q) * TGF + t) * 2;
+        return red + ((((int)os * npd + j) * P + q) * TGF + t) * 2;
     };
     bool ok = true;
     for (int g = 0; g < ngf; ++g) {
@@ -1354,7 +1362,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const StepParams p)
         mbar_init(S.lst_full, 1);
         mbar_init(S.lst_free, 1);
         mbar_init(S.bias_full, 1);
-        for (int i = 0; i < p.nsd; ++i) mbar_init(S.act_full + i, owner_parts(p.nsd));
+        const int P = p.nsd > 0 ? owner_parts(p) : 1;
+        S.info[INFO_OWNP] = P;
+        for (int i = 0; i < p.nsd; ++i) mbar_init(S.act_full + i, P);
         fence_barrier_init();
         S.info[INFO_FAIL] = 0;
         S.info[INFO_REGION] = 0;
