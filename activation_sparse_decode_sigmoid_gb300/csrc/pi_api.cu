@@ -201,11 +201,13 @@ pi_status plan(pi_ctx *c, StepParams &p, int l0, int L, int B, int mode, int *tg
     p.slotB = 16384;
     p.nss = pred ? std::min(pi::kConsumerWarps, ringB / p.slotB) : 0; // one consumer warp per slot
     if (pred && p.nss < 2) return fail(c, PI_ERR_UNSUPPORTED, "predictor ring does not fit shared memory");
-    // FFN stages: as many as the ring holds, up to 16 (one owner warp each),
-    // each at least one neuron and at most 24 KB of them: small neurons
-    // (Q4_0 rows, narrow layers) share a stage only when 16 stages of one
-    // neuron would leave the ring mostly empty
-    p.dslotB = ffn ? round_up(std::max(nbmax, std::min(24576, ringB / 16 / 128 * 128)), 128) : 0;
+    // FFN stages: as many as the ring holds, up to 16, each of up to three
+    // whole neurons within about 28 KB: a 16-bit neuron of 24 KB or more takes
+    // a stage of its own, three Q4_0 neurons share one.  Measured at one token
+    // (Falcon-40B-shaped Q4_0, 12-layer stack, us a layer): one neuron a stage
+    // 53.5, two 50.3, three 49.6, four 52.0
+    const int per_stage = std::min(3, std::max(1, 28672 / std::max(1, nbmax)));
+    p.dslotB = ffn ? round_up(per_stage * nbmax, 128) : 0;
     p.nsd = ffn ? std::min(16, ringB / p.dslotB) : 0;
     if (ffn && p.nsd < 2)
         return fail(c, PI_ERR_UNSUPPORTED, "a neuron (%d bytes) does not fit two pipeline stages", nbmax);
