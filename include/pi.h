@@ -349,8 +349,9 @@ pi_status pi_debug_set_timeline(pi_ctx *ctx, uint64_t *stamps, int32_t per_cta);
 
 /* Tuning knobs of the step kernel (also read from PI_PREFETCH, PI_PREFETCH_NS,
  * PI_LOOKAHEAD and PI_ROWS_AHEAD at pi_create): prefetch = L2 prefetch of the
- * predictor weights: 0 none (default); the next layer's slice during the FFN
- * phase, 1 all at once or 2 paced at one 16 KB chunk per prefetch_ns per SM;
+ * predictor weights: 0 none (the default for 16-bit stacks); the next layer's
+ * slice during the FFN phase, 1 all at once or 2 paced at one 16 KB chunk per
+ * prefetch_ns per SM (the default for Q4_0 stacks, prefetch_ns 800);
  * 3 each layer's W2 slice in one burst as soon as the previous layer's FFN
  * phase is over.  lookahead = how many ring stages past the one being merged
  * an owner warp may compute activations for in the FFN phase (capped at the
