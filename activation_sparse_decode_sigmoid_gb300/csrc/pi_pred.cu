@@ -562,9 +562,11 @@ cudaError_t launch_all(const PredParams &p, int sms, cudaStream_t s)
 {
     const int B = p.B;
     // hidden layer: token tiles of 2, 4 (two blocks up to 8 tokens: twice the CTAs) or 8;
-    // one row per warp up to 8 tokens, else two
-    cudaError_t e = B <= 2   ? launch_hidden<T, 1, 8, 2>(p, sms, s)
-                    : B <= 8 ? launch_hidden<T, 1, 8, 4>(p, sms, s)
+    // one row per warp up to 8 tokens, else two; row chunks in flight per lane: 16 for 2
+    // tokens, 12 for 4 (measured, pred_hidden at 2 / 3 / 8 tokens, us: 8 in flight 17.2 /
+    // 14.1 / 15.1, 12: 15.9 / 13.7 / 14.6, 16: 14.0 / 12.6 / 19.0)
+    cudaError_t e = B <= 2   ? launch_hidden<T, 1, 16, 2>(p, sms, s)
+                    : B <= 8 ? launch_hidden<T, 1, 12, 4>(p, sms, s)
                              : launch_hidden<T, 2, 4, 8>(p, sms, s);
     if (e != cudaSuccess) return e;
     // output layer (the tile stays within shared memory): beyond r = 1024, 2 rows per
