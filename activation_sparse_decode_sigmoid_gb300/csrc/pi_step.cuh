@@ -1158,17 +1158,21 @@ static __device__ bool phase_c_impl(const StepParams &p, const Shm &S, const Lay
                             uint32_t qh[8];
                             q4_pairs(ld_shared_v4(dn + L.scB + blk * 16), (hb & 1) != 0, qh);
                             const float s = __half2float(__ushort_as_half(ld_shared_u16(dn + blk * 2)));
-                            float qf[16];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float2 f2 = F16T<__half>::pair(qh[e]);
-                                qf[2 * e] = f2.x, qf[2 * e + 1] = f2.y;
-                            }
+                            // a * s rounded to f16 (relative error <= 2^-12), then
+                            // its exact products with q - 8 in the mixed-precision
+                            // fma: no conversion of the nibble pairs to fp32
 #pragma unroll
                             for (int t = 0; t < TGF; ++t) {
-                                const float as = a[t] * s;
+                                const uint16_t ab = __half_as_ushort(__float2half_rn(a[t] * s));
 #pragma unroll
-                                for (int e = 0; e < 16; ++e) y[t][e] = fmaf(as, qf[e], y[t][e]);
+                                for (int e = 0; e < 8; ++e) {
+                                    float lo = y[t][2 * e], hi = y[t][2 * e + 1];
+                                    asm("{ .reg .b16 ql, qh, ha; mov.b32 {ql, qh}, %2; mov.b16 ha, %3;"
+                                        " fma.rn.f32.f16 %0, ql, ha, %0; fma.rn.f32.f16 %1, qh, ha, %1; }"
+                                        : "+f"(lo), "+f"(hi)
+                                        : "r"(qh[e]), "h"(ab));
+                                    y[t][2 * e] = lo, y[t][2 * e + 1] = hi;
+                                }
                             }
                         }
                     }
