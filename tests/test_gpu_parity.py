@@ -373,7 +373,33 @@ def test_tensor_core_ffn_several_passes_per_cta(c64, name, B):
     """Dense FFN of a tall layer on the tensor cores (every neuron listed, so
     each up-kernel CTA runs more than one pass over K): the oracle within the
     stated tolerance, the step kernel's CUDA-core path within twice it."""
-    cfg = TALL[name]
+    _dense_tc_matches(c64, TALL[name], B)
+
+
+# wide layers: the down-projection splits each 256-column block's list into
+# shares, 24 blocks x 6 shares at d = 6144 (a d that is no power of two),
+# 32 x 4 at d = 8192; with 200 neurons (4 K steps of 64) most shares hold
+# one step
+WIDE = {
+    "wide_relu_f16": W.LayerConfig("wide_relu_f16", 6144, 2000, 32, 1, W.RELU, W.F16, W.F16, alpha=0.8, cfg_id=215),
+    "wide_reglu_bf16": W.LayerConfig("wide_reglu_bf16", 8192, 1500, 32, 1, W.REGLU, W.BF16, W.BF16, alpha=0.7,
+                                     cfg_id=216),
+    "wide_relu_q4": W.LayerConfig("wide_relu_q4", 8192, 1200, 32, 1, W.RELU, W.Q4_0, W.F16, alpha=0.8, cfg_id=217),
+    "wide_short_bf16": W.LayerConfig("wide_short_bf16", 8192, 200, 32, 1, W.RELU, W.BF16, W.BF16, alpha=0.8,
+                                     cfg_id=218),
+}
+
+
+@pytest.mark.parametrize("name", list(WIDE))
+@pytest.mark.parametrize("B", [8, 24])
+def test_tensor_core_ffn_wide_layers(c64, name, B):
+    """Dense FFN of a wide layer on the tensor cores, the down-projection's
+    share partials merged in order: the oracle within the stated tolerance,
+    the CUDA-core path within twice it."""
+    _dense_tc_matches(c64, WIDE[name], B)
+
+
+def _dense_tc_matches(c64, cfg, B):
     layer = W.make_layer(cfg, 0, 0, random_b1=True, random_bdown=True)
     c64.load_layer(0, layer)
     x = W.xhat_inputs(cfg, B, 91 + B)
